@@ -1,0 +1,166 @@
+/*
+ * mbrs_softmax.h -- C ABI of the GB300 (sm_103a) fused row softmax.
+ *
+ * The operation (page "Dissecting Memory Bandwidth & SRAM Tiling in Triton:
+ * From GEMM to FlashAttention-3", section "The Mathematical Remedy: Online
+ * Softmax Tiling"; page "I Wrote My First GPU Kernel", section "What Fusion
+ * Actually Does"):
+ *
+ *     y[r, c] = exp(x[r, c] - m_r) / sum_k exp(x[r, k] - m_r),  m_r = max_k x[r, k]
+ *
+ * for every row r < rows and column c < cols, each element read from memory
+ * once and written once (page "fused-softmax-roofline": one read and one
+ * write per element; page "Kernel Fusion": 128 MB instead of 512 MB for a
+ * 4096 x 4096 fp32 matrix).
+ *
+ * Layout (page "GPU Kernels - Implementing and optimizing Softmax", section
+ * "Baseline & Triton Softmax kernel": rows addressed as base + row * stride):
+ *   - row-major; element (r, c) of `in` is at in + r * row_stride + c and the
+ *     result goes to out + r * row_stride + c (strides in ELEMENTS, one stride
+ *     for both buffers, row_stride >= cols);
+ *   - in and out hold the same dtype: IEEE binary32, binary16 or bfloat16;
+ *   - columns cols .. row_stride-1 of each row are neither read nor written;
+ *   - arithmetic is fp32 (one exp per element); the result is rounded once
+ *     to the output dtype, round-to-nearest-even.
+ *
+ * Values: -inf entries are masked entries (they get 0).  A row with no finite
+ * max -- every entry -inf -- or with a NaN or +inf entry comes out all NaN.
+ *
+ * Ownership: the caller owns both device buffers and the stream.  `out` is
+ * never pre-initialised (page "I Wrote My First GPU Kernel", section "The
+ * Honest Part": empty_like instead of zeros_like).  in == out (exact
+ * aliasing) is allowed; any other overlap of the two byte ranges is rejected.
+ * Calls are asynchronous on `stream`; nothing is synchronised.
+ *
+ * Errors: arguments are checked on the host before any launch and a status
+ * code is returned (no launch happens unless the status is SOFTMAX_OK).
+ * Asynchronous device faults surface at the caller's next synchronisation as
+ * with any CUDA library.  Bounded waits inside the kernels that run out set a
+ * device error word; softmax_check_device_error() reads it.
+ */
+#ifndef MBRS_SOFTMAX_H
+#define MBRS_SOFTMAX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream handle, declared here when its headers are absent. */
+#if !defined(__DRIVER_TYPES_H__)
+struct CUstream_st;
+typedef struct CUstream_st *cudaStream_t;
+#endif
+
+typedef enum {
+    SOFTMAX_F32 = 0,  /* IEEE binary32 */
+    SOFTMAX_F16 = 1,  /* IEEE binary16 */
+    SOFTMAX_BF16 = 2  /* bfloat16 (top half of a binary32) */
+} softmax_dtype_t;
+
+typedef enum {
+    SOFTMAX_OK = 0,
+    SOFTMAX_ERR_NULL = 1,        /* in or out is NULL while rows > 0 */
+    SOFTMAX_ERR_SHAPE = 2,       /* rows < 0, cols < 1, or the extent overflows int64 */
+    SOFTMAX_ERR_STRIDE = 3,      /* row_stride < cols */
+    SOFTMAX_ERR_DTYPE = 4,       /* dtype not a softmax_dtype_t */
+    SOFTMAX_ERR_OVERLAP = 5,     /* in and out overlap without being equal */
+    SOFTMAX_ERR_UNSUPPORTED = 6, /* a forced path that cannot take this shape */
+    SOFTMAX_ERR_CUDA = 7,        /* a CUDA runtime call or launch failed */
+    SOFTMAX_ERR_TIMEOUT = 8,     /* a bounded device wait ran out (device error word) */
+    SOFTMAX_ERR_ALIGN = 9,       /* in or out not aligned to its element size */
+    SOFTMAX_ERR_ARG = 10         /* a bad argument to a diagnostic call */
+} softmax_status_t;
+
+/* Kernel paths the dispatcher chooses between. */
+typedef enum {
+    SOFTMAX_PATH_AUTO = 0,    /* width-based choice (default) */
+    SOFTMAX_PATH_WARP = 1,    /* a warp (or 2..16 lanes) per row, cols <= 1024 */
+    SOFTMAX_PATH_CTA = 2,     /* a thread block per row, row held in registers */
+    SOFTMAX_PATH_CLUSTER = 3, /* a thread-block cluster per row: TMA bulk loads,
+                                 (max, sum) exchanged through distributed shared memory */
+    SOFTMAX_PATH_SPLIT = 4    /* rows split across the whole grid: pass 1 writes
+                                 per-chunk (max, sum), pass 2 merges them, re-reads and writes */
+} softmax_path_t;
+
+/*
+ * softmax_fwd -- the fused row softmax described above.
+ *   in, out     device pointers (element-aligned); may be NULL only if rows == 0
+ *   rows        number of rows (>= 0); rows == 0 returns SOFTMAX_OK and launches nothing
+ *   cols        valid columns per row (>= 1)
+ *   row_stride  distance between row starts in elements (>= cols), both buffers
+ *   dtype       a softmax_dtype_t
+ *   stream      the CUDA stream to launch on (0 = legacy default stream)
+ * The SPLIT path (very long rows, or few long rows) needs rows * chunks * 8
+ * bytes of scratch; softmax_fwd takes it stream-ordered from a pool the
+ * library keeps per device and returns it on the same stream.
+ * Returns a softmax_status_t.
+ */
+int softmax_fwd(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride,
+                int dtype, cudaStream_t stream);
+
+/* A static English string for a status code (never NULL). */
+const char *softmax_status_string(int status);
+
+/* The path (softmax_path_t) that the last successful softmax_fwd on any thread took. */
+int softmax_last_path(void);
+
+/*
+ * Test and tuning hook: force every following call onto `path` (0 = automatic).
+ * threads / vpt / group override the launch shape where > 0 (threads per block,
+ * 16-byte vectors per thread, and lanes per row / cluster size / chunks per
+ * row for paths 1 / 3 / 4).  A forced shape that cannot cover the row makes
+ * softmax_fwd return SOFTMAX_ERR_UNSUPPORTED.  Process-wide, not thread-safe.
+ */
+int softmax_set_force_path(int path, int threads, int vpt, int group);
+
+/* Description of the launch softmax_fwd would make (host only, no GPU work). */
+typedef struct {
+    int path;              /* softmax_path_t actually chosen */
+    int threads;           /* threads per block */
+    int vpt;               /* 16-byte vectors per thread per tile */
+    int group;             /* lanes per row (1), cluster size (3), chunks per row (4), else 1 */
+    int launches;          /* kernels per call: 1, or 2 for the SPLIT path */
+    int vec_store;         /* 1 if out has in's 16-byte phase (vector stores) */
+    int64_t grid;          /* blocks of the (first) kernel */
+    int64_t smem_bytes;    /* dynamic shared memory per block */
+    int64_t scratch_bytes; /* device scratch the call needs (SPLIT only) */
+    int64_t hbm_bytes;     /* algorithmic bytes: 2 * rows * cols * elem (3x for SPLIT) */
+} softmax_plan_t;
+
+/*
+ * softmax_plan -- fill *plan with the launch softmax_fwd would make for these
+ * arguments (pointer alignment given by in_addr / out_addr, which are only
+ * inspected, never dereferenced).  num_sms > 0 plans for a GPU with that many
+ * SMs without touching CUDA; num_sms == 0 queries the current device.
+ * Honours softmax_set_force_path.  Returns a softmax_status_t.
+ */
+int softmax_plan(uint64_t in_addr, uint64_t out_addr, int64_t rows, int64_t cols,
+                 int64_t row_stride, int dtype, int num_sms, softmax_plan_t *plan);
+
+/*
+ * Synchronise `stream`, then read and clear this device's error word.
+ * Returns SOFTMAX_ERR_TIMEOUT if a bounded wait ran out in any kernel since the
+ * last check, SOFTMAX_ERR_CUDA if the synchronisation failed, else SOFTMAX_OK.
+ */
+int softmax_check_device_error(cudaStream_t stream);
+
+/*
+ * Test hooks for the bounded waits of the CLUSTER path.  wait_limit_ns bounds
+ * each wait on a TMA completion barrier (default 1 s; <= 0 restores it).
+ * starve != 0 makes the next launches skip arming that barrier, so the wait
+ * can only run out: the kernel records SOFTMAX_ERR_TIMEOUT, skips its stores
+ * and returns normally.  Process-wide, not thread-safe.
+ */
+int softmax_set_wait_test(int64_t wait_limit_ns, int starve);
+
+/* Version of this ABI: major * 10000 + minor * 100 + patch. */
+int softmax_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MBRS_SOFTMAX_H */

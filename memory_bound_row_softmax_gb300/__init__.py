@@ -1,14 +1,16 @@
 """GB300-native fused row softmax.
 
-``softmax_fwd`` (and the diagnostics next to it) are thin ctypes bindings over
-the C-ABI library built from ``csrc/``; the library is loaded on first use and
+``softmax_fwd`` and the diagnostics beside it are thin ctypes bindings over the
+C-ABI library built from ``csrc/``.  The library is loaded on first use, and
 its absence is an error, never a fallback.
 """
-from .workloads import CONFIGS  # noqa: F401
+import importlib
+
+_BINDING_NAMES = ("softmax_fwd", "softmax_fwd_ptr", "plan", "set_force_path", "last_path",
+                  "check_device_error", "set_wait_test", "abi_version", "status_string", "SoftmaxError")
 
 
 def __getattr__(name):
-    from . import binding
-    if hasattr(binding, name):
-        return getattr(binding, name)
-    raise AttributeError(name)
+    if name in _BINDING_NAMES:
+        return getattr(importlib.import_module(".binding", __name__), name)
+    raise AttributeError(f"module {__name__!r} has no attribute {name!r}")

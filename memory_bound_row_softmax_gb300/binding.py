@@ -1,0 +1,160 @@
+"""ctypes binding over the C ABI in ``include/mbrs_softmax.h``.
+
+Argument marshalling only: every step of the softmax runs in the CUDA kernels
+of ``_build/libmbrs_softmax.so``.  If that library has not been built, the
+first call raises -- there is no other implementation to fall back to.
+PyTorch supplies device memory and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libmbrs_softmax.so")
+
+OK, ERR_NULL, ERR_SHAPE, ERR_STRIDE, ERR_DTYPE, ERR_OVERLAP, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_ALIGN, \
+    ERR_ARG = range(11)
+PATH_AUTO, PATH_WARP, PATH_CTA, PATH_CLUSTER, PATH_SPLIT = range(5)
+PATH_NAMES = {PATH_WARP: "warp", PATH_CTA: "cta", PATH_CLUSTER: "cluster", PATH_SPLIT: "split"}
+DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
+
+_i64, _u64, _int, _vp = ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("path", _int), ("threads", _int), ("vpt", _int), ("group", _int), ("launches", _int),
+                ("vec_store", _int), ("grid", _i64), ("smem_bytes", _i64), ("scratch_bytes", _i64),
+                ("hbm_bytes", _i64)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+# Every function the header declares, with its ctypes signature.
+SIGNATURES = {
+    "softmax_fwd": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp]),
+    "softmax_status_string": (ctypes.c_char_p, [_int]),
+    "softmax_last_path": (_int, []),
+    "softmax_set_force_path": (_int, [_int, _int, _int, _int]),
+    "softmax_plan": (_int, [_u64, _u64, _i64, _i64, _i64, _int, _int, ctypes.POINTER(Plan)]),
+    "softmax_check_device_error": (_int, [_vp]),
+    "softmax_set_wait_test": (_int, [_i64, _int]),
+    "softmax_abi_version": (_int, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class SoftmaxError(RuntimeError):
+    def __init__(self, status: int, what: str = "softmax_fwd"):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C-ABI library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"CUDA library {_LIB_PATH} is missing: build it with "
+                    "`python -m memory_bound_row_softmax_gb300.build` (there is no fallback path)")
+            handle = ctypes.CDLL(_LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().softmax_status_string(status).decode()
+
+
+def _torch_dtype_code(t) -> int:
+    import torch
+    codes = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+    if t.dtype not in codes:
+        raise TypeError(f"softmax_fwd takes float32, float16 or bfloat16, not {t.dtype}")
+    return codes[t.dtype]
+
+
+def softmax_fwd_ptr(in_ptr: int, out_ptr: int, rows: int, cols: int, row_stride: int, dtype: int,
+                    stream: int = 0) -> int:
+    """Raw call: device addresses and sizes in, status out (no exception)."""
+    return lib().softmax_fwd(in_ptr, out_ptr, rows, cols, row_stride, dtype, stream)
+
+
+def softmax_fwd(x, out=None, stream=None):
+    """Row softmax of a 2-D CUDA tensor (last dimension contiguous).
+
+    ``out`` (optional) must have x's shape, dtype, device and row stride; it
+    may be ``x`` itself.  Launches on ``stream`` (default: the current stream of
+    x's device) and returns ``out``.
+    """
+    import torch
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise TypeError("softmax_fwd needs a CUDA tensor")
+    if x.dim() != 2:
+        raise ValueError(f"softmax_fwd needs a 2-D tensor, got {tuple(x.shape)}")
+    rows, cols = x.shape
+    if cols > 1 and x.stride(1) != 1:
+        raise ValueError("the last dimension must be contiguous (stride 1)")
+    row_stride = x.stride(0) if rows > 1 else max(cols, x.stride(0))
+    code = _torch_dtype_code(x)
+    if out is None:
+        out = torch.empty_strided((rows, cols), (row_stride, 1), dtype=x.dtype, device=x.device)
+    else:
+        if out.shape != x.shape or out.dtype != x.dtype or out.device != x.device:
+            raise ValueError("out must match x in shape, dtype and device")
+        o_stride = out.stride(0) if rows > 1 else row_stride
+        if (cols > 1 and out.stride(1) != 1) or o_stride != row_stride:
+            raise ValueError("out must have x's row stride")
+    with torch.cuda.device(x.device):
+        s = stream if stream is not None else torch.cuda.current_stream(x.device)
+        handle = s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
+        st = lib().softmax_fwd(x.data_ptr(), out.data_ptr(), rows, cols, row_stride, code, handle)
+    if st != OK:
+        raise SoftmaxError(st)
+    return out
+
+
+def plan(in_addr: int, out_addr: int, rows: int, cols: int, row_stride: int, dtype,
+         num_sms: int = 0) -> dict:
+    """The launch softmax_fwd would make (host only when num_sms > 0)."""
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else dtype
+    p = Plan()
+    st = lib().softmax_plan(in_addr, out_addr, rows, cols, row_stride, code, num_sms, ctypes.byref(p))
+    if st != OK:
+        raise SoftmaxError(st, "softmax_plan")
+    return p.as_dict()
+
+
+def set_force_path(path: int, threads: int = 0, vpt: int = 0, group: int = 0) -> None:
+    st = lib().softmax_set_force_path(path, threads, vpt, group)
+    if st != OK:
+        raise SoftmaxError(st, "softmax_set_force_path")
+
+
+def last_path() -> int:
+    return lib().softmax_last_path()
+
+
+def check_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    handle = s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
+    return lib().softmax_check_device_error(handle)
+
+
+def set_wait_test(wait_limit_ns: int = 0, starve: bool = False) -> None:
+    lib().softmax_set_wait_test(wait_limit_ns, 1 if starve else 0)
+
+
+def abi_version() -> int:
+    return lib().softmax_abi_version()

@@ -1,0 +1,350 @@
+// abi.cu -- the C ABI: argument checks, the width-based dispatcher, launch
+// planning and the diagnostics declared in include/mbrs_softmax.h.
+//
+// Dispatch (page "fused-softmax-roofline", section on the shapes where the
+// fused kernel loses: the fixed per-row costs must be paid per lane group, not
+// per block, for short rows; page "GPU Kernels - Implementing and optimizing
+// Softmax", sections "CUDA optimized for block per row" and "CUDA scaling
+// threads": wide rows need more threads per row so that enough loads are in
+// flight):
+//   cols <= 1024                    path 1, 2..32 lanes per row
+//   row fits one block's registers  path 2, a block per row
+//   row fits a cluster (<= 16 CTAs) path 3, a cluster per row, if the clusters
+//                                   fill the GPU
+//   otherwise                       path 4, rows split over the grid (2 passes)
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mbrs_softmax.h"
+#include "launch.h"
+
+using namespace mbrs;
+
+namespace {
+
+constexpr int kAbiVersion = 10000;  // 1.0.0
+constexpr int kVecBytes = 16;
+constexpr int kMaxDevices = 64;
+constexpr int64_t kDefaultWaitNs = 1000000000;  // 1 s
+constexpr int64_t kMaxGrid = 0x7fffffff;
+
+std::atomic<int> g_last_path{0};
+std::atomic<int> g_force_path{0}, g_force_threads{0}, g_force_vpt{0}, g_force_group{0};
+std::atomic<int64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_starve{0};
+
+struct Plan {
+    int path = 0, threads = 0, vpt = 0, group = 1, launches = 0, vec_store = 0;
+    int64_t grid = 0, smem = 0, scratch = 0, hbm = 0, chunks = 1, chunk_vecs = 0;
+};
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int next_pow2(int64_t v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+int elem_bytes(int dtype) { return dtype == SOFTMAX_F32 ? 4 : 2; }
+
+// Host-side argument checks, in the order the header documents.
+int check_args(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row_stride, int dtype,
+               int64_t *extent_bytes) {
+    if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_F16 && dtype != SOFTMAX_BF16) return SOFTMAX_ERR_DTYPE;
+    if (rows < 0 || cols < 1) return SOFTMAX_ERR_SHAPE;
+    if (row_stride < cols) return SOFTMAX_ERR_STRIDE;
+    const int es = elem_bytes(dtype);
+    // extent = (rows - 1) * row_stride + cols elements must fit in int64 bytes
+    if (rows > 0) {
+        if (rows - 1 > (INT64_MAX - cols) / row_stride) return SOFTMAX_ERR_SHAPE;
+        const int64_t ext = (rows - 1) * row_stride + cols;
+        if (ext > INT64_MAX / es) return SOFTMAX_ERR_SHAPE;
+        *extent_bytes = ext * es;
+    } else {
+        *extent_bytes = 0;
+        return SOFTMAX_OK;
+    }
+    if (in == 0 || out == 0) return SOFTMAX_ERR_NULL;
+    if (in % es != 0 || out % es != 0) return SOFTMAX_ERR_ALIGN;
+    if (in != out) {
+        const uint64_t n = (uint64_t)*extent_bytes;
+        const bool disjoint = (in + n <= out) || (out + n <= in);
+        if (!disjoint) return SOFTMAX_ERR_OVERLAP;
+    }
+    return SOFTMAX_OK;
+}
+
+int device_sms(int *sms) {
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SOFTMAX_ERR_CUDA;
+    const int slot = dev & (kMaxDevices - 1);
+    int v = cache[slot].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SOFTMAX_ERR_CUDA;
+        cache[slot].store(v, std::memory_order_relaxed);
+    }
+    *sms = v;
+    return SOFTMAX_OK;
+}
+
+// The launch for one call.  nv bounds the vectors any row needs: rows whose
+// byte stride is a multiple of 16 share the first row's phase; otherwise a row
+// may start up to V-1 elements into its first vector.
+int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row_stride, int dtype, int sms,
+              Plan *p) {
+    const int es = elem_bytes(dtype), V = kVecBytes / es;
+    const bool uniform = ((row_stride * es) % kVecBytes) == 0;
+    const int64_t head = (int64_t)((in % kVecBytes) / es);
+    const int64_t nv = uniform ? cdiv(head + cols, V) : cdiv(cols + V - 1, V);
+    p->vec_store = (in % kVecBytes) == (out % kVecBytes);
+    p->hbm = 2 * rows * cols * es;
+
+    const int fpath = g_force_path.load(), fth = g_force_threads.load(), fvpt = g_force_vpt.load(),
+              fgrp = g_force_group.load();
+    int path = fpath;
+    if (path == SOFTMAX_PATH_AUTO) {
+        if (cols <= 1024 && nv <= 32 * 9) {
+            path = SOFTMAX_PATH_WARP;
+        } else if (nv <= 1024 * 4) {
+            path = SOFTMAX_PATH_CTA;
+        } else {
+            const int64_t csize = cdiv(nv, nv <= 16 * 512 * 4 ? 512 * 4 : 1024 * 4);
+            const bool fits = csize <= 16 && rows * csize <= kMaxGrid;
+            path = (fits && rows * csize >= sms) ? SOFTMAX_PATH_CLUSTER : SOFTMAX_PATH_SPLIT;
+        }
+    }
+    p->path = path;
+    p->launches = 1;
+    switch (path) {
+        case SOFTMAX_PATH_WARP: {
+            int g, vpt;
+            if (fgrp > 0) {
+                g = fgrp;
+                vpt = fvpt > 0 ? fvpt : (int)cdiv(nv, g);
+            } else if (nv <= 16) {
+                g = std::max(2, next_pow2(nv));
+                vpt = 1;
+            } else {
+                g = 32;
+                vpt = fvpt > 0 ? fvpt : (int)cdiv(nv, 32);
+            }
+            if (!warp_shape_ok(g, vpt) || (int64_t)g * vpt < nv) return SOFTMAX_ERR_UNSUPPORTED;
+            int threads = fth > 0 ? fth : 128;
+            if (fth <= 0)  // spread small problems over more SMs
+                while (threads > 32 && cdiv(rows * g, threads) < sms) threads /= 2;
+            if (threads < 32 || threads > 256 || threads % 32 != 0 || threads % g != 0)
+                return SOFTMAX_ERR_UNSUPPORTED;
+            p->threads = threads;
+            p->vpt = vpt;
+            p->group = g;
+            p->grid = std::min<int64_t>(cdiv(rows * g, threads), kMaxGrid);
+            break;
+        }
+        case SOFTMAX_PATH_CTA: {
+            int vpt = fvpt > 0 ? fvpt : 4;
+            int threads = fth > 0 ? fth : std::min(1024, std::max(64, next_pow2(cdiv(nv, vpt))));
+            if (!cta_shape_ok(threads, vpt) || (int64_t)threads * vpt < nv) return SOFTMAX_ERR_UNSUPPORTED;
+            p->threads = threads;
+            p->vpt = vpt;
+            p->grid = std::min(rows, kMaxGrid);
+            break;
+        }
+        case SOFTMAX_PATH_CLUSTER: {
+            int threads = fth > 0 ? fth : (nv <= 16 * 512 * 4 ? 512 : 1024);
+            int vpt = fvpt > 0 ? fvpt : 4;
+            int64_t csize = fgrp > 0 ? fgrp : cdiv(nv, (int64_t)threads * vpt);
+            if (!cluster_shape_ok(threads, vpt) || csize < 1 || csize > 16) return SOFTMAX_ERR_UNSUPPORTED;
+            if (cdiv(nv, csize) > (int64_t)threads * vpt) return SOFTMAX_ERR_UNSUPPORTED;
+            if (rows * csize > kMaxGrid) return SOFTMAX_ERR_UNSUPPORTED;
+            p->threads = threads;
+            p->vpt = vpt;
+            p->group = (int)csize;
+            p->grid = rows * csize;
+            p->smem = cluster_smem_bytes(threads, vpt);
+            break;
+        }
+        case SOFTMAX_PATH_SPLIT: {
+            const int threads = fth > 0 ? fth : 256;
+            const int vpt = fvpt > 0 ? fvpt : 4;
+            if (!split_shape_ok(threads, vpt)) return SOFTMAX_ERR_UNSUPPORTED;
+            const int64_t tile = (int64_t)threads * vpt;
+            const int64_t per_sm = 2048 / threads;
+            int64_t k;
+            if (fgrp > 0) {
+                k = std::min<int64_t>(fgrp, nv);
+            } else {
+                const int64_t target = (int64_t)sms * per_sm * 2;
+                k = std::max<int64_t>(1, std::min(cdiv(target, rows), cdiv(nv, tile)));
+            }
+            const int64_t chunk_vecs = cdiv(cdiv(nv, k), tile) * tile;
+            k = cdiv(nv, chunk_vecs);
+            if (rows > INT64_MAX / k / 8) return SOFTMAX_ERR_UNSUPPORTED;
+            p->threads = threads;
+            p->vpt = vpt;
+            p->group = (int)std::min<int64_t>(k, 0x7fffffff);
+            p->chunks = k;
+            p->chunk_vecs = chunk_vecs;
+            p->grid = std::min<int64_t>(rows * k, (int64_t)sms * per_sm * 4);
+            p->scratch = rows * k * 8;
+            p->launches = 2;
+            p->hbm = 3 * rows * cols * es;
+            break;
+        }
+        default:
+            return SOFTMAX_ERR_UNSUPPORTED;
+    }
+    return SOFTMAX_OK;
+}
+
+// Stream-ordered scratch for the split path: one pool per device that keeps
+// its memory (release threshold = max), so steady-state calls do not reach
+// the driver's allocator.
+cudaError_t scratch_pool(int dev, cudaMemPool_t *pool) {
+    static std::mutex mu;
+    static cudaMemPool_t pools[kMaxDevices] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    cudaMemPool_t &slot = pools[dev & (kMaxDevices - 1)];
+    if (!slot) {
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaError_t e = cudaMemPoolCreate(&slot, &props);
+        if (e != cudaSuccess) {
+            slot = nullptr;
+            return e;
+        }
+        uint64_t keep = UINT64_MAX;
+        e = cudaMemPoolSetAttribute(slot, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) return e;
+    }
+    *pool = slot;
+    return cudaSuccess;
+}
+
+int run(const Plan &p, const LaunchArgs &a) {
+    cudaError_t e = cudaSuccess;
+    switch (p.path) {
+        case SOFTMAX_PATH_WARP: e = launch_warp(a, p.threads, p.group, p.vpt, p.grid); break;
+        case SOFTMAX_PATH_CTA: e = launch_cta(a, p.threads, p.vpt, p.grid); break;
+        case SOFTMAX_PATH_CLUSTER:
+            e = launch_cluster(a, p.threads, p.vpt, p.group, g_wait_ns.load(), g_starve.load());
+            break;
+        case SOFTMAX_PATH_SPLIT: {
+            int dev = 0;
+            cudaMemPool_t pool;
+            void *scratch = nullptr;
+            e = cudaGetDevice(&dev);
+            if (e == cudaSuccess) e = scratch_pool(dev, &pool);
+            if (e == cudaSuccess) e = cudaMallocFromPoolAsync(&scratch, (size_t)p.scratch, pool, a.stream);
+            if (e == cudaSuccess) {
+                e = launch_split(a, p.threads, p.vpt, p.chunks, p.chunk_vecs, p.grid, scratch);
+                cudaError_t f = cudaFreeAsync(scratch, a.stream);
+                if (e == cudaSuccess) e = f;
+            }
+            break;
+        }
+        default: return SOFTMAX_ERR_UNSUPPORTED;
+    }
+    if (e == cudaErrorInvalidValue) return SOFTMAX_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? SOFTMAX_OK : SOFTMAX_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int softmax_fwd(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride, int dtype,
+                cudaStream_t stream) {
+    int64_t ext = 0;
+    const uint64_t ia = (uint64_t)(uintptr_t)in, oa = (uint64_t)(uintptr_t)out;
+    int st = check_args(ia, oa, rows, cols, row_stride, dtype, &ext);
+    if (st != SOFTMAX_OK || rows == 0) return st;
+    int sms = 0;
+    st = device_sms(&sms);
+    if (st != SOFTMAX_OK) return st;
+    Plan p;
+    st = make_plan(ia, oa, rows, cols, row_stride, dtype, sms, &p);
+    if (st != SOFTMAX_OK) return st;
+    LaunchArgs a{in, out, rows, cols, row_stride, dtype, p.vec_store, stream};
+    st = run(p, a);
+    if (st == SOFTMAX_OK) g_last_path.store(p.path);
+    return st;
+}
+
+const char *softmax_status_string(int status) {
+    switch (status) {
+        case SOFTMAX_OK: return "ok";
+        case SOFTMAX_ERR_NULL: return "null pointer with rows > 0";
+        case SOFTMAX_ERR_SHAPE: return "bad shape (rows < 0, cols < 1, or extent overflows int64)";
+        case SOFTMAX_ERR_STRIDE: return "row_stride < cols";
+        case SOFTMAX_ERR_DTYPE: return "unknown dtype";
+        case SOFTMAX_ERR_OVERLAP: return "in and out overlap without being equal";
+        case SOFTMAX_ERR_UNSUPPORTED: return "forced path or shape cannot take these arguments";
+        case SOFTMAX_ERR_CUDA: return "CUDA runtime error";
+        case SOFTMAX_ERR_TIMEOUT: return "a bounded device wait ran out";
+        case SOFTMAX_ERR_ALIGN: return "pointer not aligned to its element size";
+        case SOFTMAX_ERR_ARG: return "bad argument to a diagnostic call";
+        default: return "unknown status";
+    }
+}
+
+int softmax_last_path(void) { return g_last_path.load(); }
+
+int softmax_set_force_path(int path, int threads, int vpt, int group) {
+    if (path < SOFTMAX_PATH_AUTO || path > SOFTMAX_PATH_SPLIT) return SOFTMAX_ERR_ARG;
+    g_force_path.store(path);
+    g_force_threads.store(threads > 0 ? threads : 0);
+    g_force_vpt.store(vpt > 0 ? vpt : 0);
+    g_force_group.store(group > 0 ? group : 0);
+    return SOFTMAX_OK;
+}
+
+int softmax_plan(uint64_t in_addr, uint64_t out_addr, int64_t rows, int64_t cols, int64_t row_stride, int dtype,
+                 int num_sms, softmax_plan_t *plan) {
+    if (!plan || num_sms < 0) return SOFTMAX_ERR_ARG;
+    std::memset(plan, 0, sizeof(*plan));
+    int64_t ext = 0;
+    int st = check_args(in_addr, out_addr, rows, cols, row_stride, dtype, &ext);
+    if (st != SOFTMAX_OK || rows == 0) return st;
+    int sms = num_sms;
+    if (sms == 0) {
+        st = device_sms(&sms);
+        if (st != SOFTMAX_OK) return st;
+    }
+    Plan p;
+    st = make_plan(in_addr, out_addr, rows, cols, row_stride, dtype, sms, &p);
+    if (st != SOFTMAX_OK) return st;
+    plan->path = p.path;
+    plan->threads = p.threads;
+    plan->vpt = p.vpt;
+    plan->group = p.group;
+    plan->launches = p.launches;
+    plan->vec_store = p.vec_store;
+    plan->grid = p.grid;
+    plan->smem_bytes = p.smem;
+    plan->scratch_bytes = p.scratch;
+    plan->hbm_bytes = p.hbm;
+    return SOFTMAX_OK;
+}
+
+int softmax_check_device_error(cudaStream_t stream) {
+    unsigned int word = 0;
+    if (read_clear_error_word(stream, &word) != cudaSuccess) return SOFTMAX_ERR_CUDA;
+    return word ? SOFTMAX_ERR_TIMEOUT : SOFTMAX_OK;
+}
+
+int softmax_set_wait_test(int64_t wait_limit_ns, int starve) {
+    g_wait_ns.store(wait_limit_ns > 0 ? wait_limit_ns : kDefaultWaitNs);
+    g_starve.store(starve ? 1 : 0);
+    return SOFTMAX_OK;
+}
+
+int softmax_abi_version(void) { return kAbiVersion; }
+
+}  // extern "C"

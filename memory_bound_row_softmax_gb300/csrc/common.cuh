@@ -1,0 +1,346 @@
+// common.cuh -- device building blocks shared by the row-softmax kernels.
+//
+// Every kernel computes, per row, the numerically stable softmax
+//     y_c = exp(x_c - m) / l,   m = max_c x_c,   l = sum_c exp(x_c - m)
+// (page "Dissecting Memory Bandwidth & SRAM Tiling in Triton", section "The
+// Mathematical Remedy: Online Softmax Tiling") with one read and one write of
+// each element (page "fused-softmax-roofline").
+//
+// Per-thread state.  A thread holds its elements in registers, takes its own
+// max m_t, turns its elements into e_c = exp(x_c - m_t) at once and sums them
+// into l_t.  The (m_t, l_t) pairs of all threads of a row are then combined
+// with the two-state merge rule of the same section,
+//     m = max(m1, m2),   l = l1 exp(m1 - m) + l2 exp(m2 - m),
+// and each thread finally scales its e_c by exp(m_t - m) / l.  This needs one
+// exp per element and ONE cross-thread reduction per row (instead of a max
+// reduction followed by a sum reduction), which matters most where the row
+// spans the warps of a block or the blocks of a cluster.
+//
+// exp is computed as 2^(x log2 e - m log2 e) with the PTX instruction
+// ex2.approx.ftz.f32 (relative error about 2^-22); the shift m log2 e is the
+// same for the whole row, so its rounding cancels in the ratio.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mbrs {
+
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
+constexpr int kVecBytes = 16;                  // one 128-bit access
+
+// ---------------------------------------------------------------------------
+// element types
+// ---------------------------------------------------------------------------
+template <typename T> struct Elem;
+
+template <> struct Elem<float> {
+    static constexpr int kVec = 4;  // elements per 16-byte vector
+    __device__ static __forceinline__ float to_f(float v) { return v; }
+    __device__ static __forceinline__ float from_f(float v) { return v; }
+    __device__ static __forceinline__ void unpack(const uint4 &r, float *x) {
+        x[0] = __uint_as_float(r.x);
+        x[1] = __uint_as_float(r.y);
+        x[2] = __uint_as_float(r.z);
+        x[3] = __uint_as_float(r.w);
+    }
+    __device__ static __forceinline__ uint4 pack(const float *y) {
+        return make_uint4(__float_as_uint(y[0]), __float_as_uint(y[1]), __float_as_uint(y[2]),
+                          __float_as_uint(y[3]));
+    }
+};
+
+template <> struct Elem<__half> {
+    static constexpr int kVec = 8;
+    __device__ static __forceinline__ float to_f(__half v) { return __half2float(v); }
+    __device__ static __forceinline__ __half from_f(float v) { return __float2half_rn(v); }
+    __device__ static __forceinline__ float2 pair(uint32_t w) {
+        __half2 h = *reinterpret_cast<const __half2 *>(&w);
+        return __half22float2(h);
+    }
+    __device__ static __forceinline__ uint32_t unpair(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
+    __device__ static __forceinline__ void unpack(const uint4 &r, float *x) {
+        float2 p;
+        p = pair(r.x); x[0] = p.x; x[1] = p.y;
+        p = pair(r.y); x[2] = p.x; x[3] = p.y;
+        p = pair(r.z); x[4] = p.x; x[5] = p.y;
+        p = pair(r.w); x[6] = p.x; x[7] = p.y;
+    }
+    __device__ static __forceinline__ uint4 pack(const float *y) {
+        return make_uint4(unpair(y[0], y[1]), unpair(y[2], y[3]), unpair(y[4], y[5]),
+                          unpair(y[6], y[7]));
+    }
+};
+
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+    __device__ static __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+    __device__ static __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+    __device__ static __forceinline__ float2 pair(uint32_t w) {
+        // bf16 -> f32 is exact: the bf16 bits are the top half of the f32
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    __device__ static __forceinline__ uint32_t unpair(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
+    __device__ static __forceinline__ void unpack(const uint4 &r, float *x) {
+        float2 p;
+        p = pair(r.x); x[0] = p.x; x[1] = p.y;
+        p = pair(r.y); x[2] = p.x; x[3] = p.y;
+        p = pair(r.z); x[4] = p.x; x[5] = p.y;
+        p = pair(r.w); x[6] = p.x; x[7] = p.y;
+    }
+    __device__ static __forceinline__ uint4 pack(const float *y) {
+        return make_uint4(unpair(y[0], y[1]), unpair(y[2], y[3]), unpair(y[4], y[5]),
+                          unpair(y[6], y[7]));
+    }
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// mbarrier (shared::cta) -- arrival/transaction barrier the TMA engine completes.
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for phase `parity` of an mbarrier: gives up after limit_ns of
+// global time and returns false.  Never spins without a bound.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0; it < (1u << 30); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((int64_t)(global_timer_ns() - t0) > limit_ns) return false;
+    }
+    return false;
+}
+
+// 1-D TMA bulk copy global -> this CTA's shared memory, completing on `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// thread-block cluster
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f2(uint32_t addr, float a, float b) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+
+// device error word bit: a bounded wait ran out
+constexpr unsigned int kErrWaitTimeout = 1u;
+
+// ---------------------------------------------------------------------------
+// (max, sum) states
+// ---------------------------------------------------------------------------
+// The shift a state with max m uses: an empty state (m = -inf) shifts by 0 so
+// that its (all -inf) entries give exp = 0 instead of NaN.
+__device__ __forceinline__ float safe_shift(float m) { return m == -INFINITY ? 0.f : m; }
+
+// l scaled from max m to max M >= m (0 for an empty state).
+__device__ __forceinline__ float rescale(float l, float m, float M) {
+    return m == -INFINITY ? 0.f : l * ex2((m - M) * kLog2e);
+}
+
+// Merge the states of the `width` lanes of each aligned lane group (width a
+// power of two <= 32).  All 32 lanes must call it.
+template <int WIDTH>
+__device__ __forceinline__ void group_merge(float &m, float &l) {
+    float M = m;
+#pragma unroll
+    for (int o = WIDTH / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = rescale(l, m, M);
+#pragma unroll
+    for (int o = WIDTH / 2; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    m = M;
+    l = L;
+}
+
+// The final per-thread factor: e_c * factor = exp(x_c - M) / L.  A row with no
+// finite max (every entry -inf) gives NaN, as does a NaN or +inf entry (L NaN).
+__device__ __forceinline__ float out_factor(float m_t, float M, float L) {
+    if (M == -INFINITY) return __int_as_float(0x7fc00000);
+    return rescale(1.f, m_t, M) * (1.f / L);
+}
+
+// ---------------------------------------------------------------------------
+// row geometry: a row is covered by 16-byte aligned vectors
+// ---------------------------------------------------------------------------
+// A row starting at element pointer p has `head` = (address mod 16) / elem
+// elements in front of it inside its first aligned vector.  Vector v covers
+// the row's columns [v*V - head, v*V - head + V); the row needs
+// nvec = ceil((head + cols) / V) vectors.  Only the first and the last vector
+// can be partial; those are read and written element by element so that no
+// access leaves the row.
+template <typename T>
+struct RowView {
+    static constexpr int V = Elem<T>::kVec;
+    const T *in;   // row start (input)
+    T *out;        // row start (output)
+    int head;      // elements before the row start in its first vector
+    int64_t cols;
+    int64_t nvec;
+    bool vec_store;  // out has the same 16-byte phase as in
+
+    __device__ __forceinline__ RowView(const T *in_row, T *out_row, int64_t cols_, bool vec_store_)
+        : in(in_row), out(out_row), cols(cols_), vec_store(vec_store_) {
+        head = (int)((reinterpret_cast<uintptr_t>(in_row) & (kVecBytes - 1)) / sizeof(T));
+        nvec = (head + cols + V - 1) / V;
+    }
+    __device__ __forceinline__ bool full(int64_t v) const {
+        const int64_t p = v * V;
+        return p >= head && p + V <= head + cols;
+    }
+    // Load vector v (must be < nvec) as floats; columns outside the row read -inf.
+    __device__ __forceinline__ void load(int64_t v, float *x) const {
+        const int64_t c0 = v * V - head;
+        if (full(v)) {
+            Elem<T>::unpack(*reinterpret_cast<const uint4 *>(in + c0), x);
+        } else {
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int64_t c = c0 + i;
+                x[i] = (c >= 0 && c < cols) ? Elem<T>::to_f(in[c]) : -INFINITY;
+            }
+        }
+    }
+    // Store vector v's results; only columns inside the row are written.
+    __device__ __forceinline__ void store(int64_t v, const float *y) const {
+        const int64_t c0 = v * V - head;
+        if (vec_store && full(v)) {
+            *reinterpret_cast<uint4 *>(out + c0) = Elem<T>::pack(y);
+        } else {
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int64_t c = c0 + i;
+                if (c >= 0 && c < cols) out[c] = Elem<T>::from_f(y[i]);
+            }
+        }
+    }
+};
+
+// A thread's tile of VPT vectors (VPT * V floats in registers).
+template <typename T, int VPT>
+struct Tile {
+    static constexpr int V = Elem<T>::kVec;
+    float x[VPT][V];
+
+    // load vectors first + j*step (j < VPT) of a row, -inf past `end`
+    __device__ __forceinline__ void load(const RowView<T> &row, int64_t first, int64_t step, int64_t end) {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t v = first + j * step;
+            if (v < end) {
+                row.load(v, x[j]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < V; ++i) x[j][i] = -INFINITY;
+            }
+        }
+    }
+    // Replace x by e = exp(x - m_t) with the tile's own max; return (m_t, l_t).
+    __device__ __forceinline__ float2 exp_in_place() {
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+#pragma unroll
+            for (int i = 0; i < V; ++i) m = fmaxf(m, x[j][i]);
+        const float shift = safe_shift(m) * kLog2e;
+        float l = 0.f;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            float lj = 0.f;
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                x[j][i] = ex2(fmaf(x[j][i], kLog2e, -shift));
+                lj += x[j][i];
+            }
+            l += lj;
+        }
+        return make_float2(m, l);
+    }
+    __device__ __forceinline__ void scale_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
+                                                float f) {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t v = first + j * step;
+            if (v < end) {
+                float y[V];
+#pragma unroll
+                for (int i = 0; i < V; ++i) y[i] = x[j][i] * f;
+                row.store(v, y);
+            }
+        }
+    }
+};
+
+}  // namespace mbrs

@@ -1,0 +1,100 @@
+// k_cluster.cu -- path 3 instantiations: a thread-block cluster per row, TMA
+// bulk loads into each block's shared memory and a (max, sum) exchange through
+// distributed shared memory.  Also reads and clears the device error word.
+#include <atomic>
+
+#include "kernels.cuh"
+#include "launch.h"
+
+namespace mbrs {
+
+namespace {
+constexpr int kMaxDevices = 64;
+
+template <typename T, int THREADS, int VPT>
+cudaError_t prepare(int device) {
+    // per-device, once: opt in to large dynamic shared memory and clusters of 16
+    static std::atomic<unsigned long long> done{0};
+    const unsigned long long bit = 1ull << (device & (kMaxDevices - 1));
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    auto fn = k_cluster_rows<T, THREADS, VPT>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         ClusterSmem<THREADS, VPT>::kBytes);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+template <typename T, int THREADS, int VPT>
+cudaError_t go(const LaunchArgs &a, int csize, int64_t wait_ns, int starve) {
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return e;
+    e = prepare<T, THREADS, VPT>(device);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.rows * csize), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = ClusterSmem<THREADS, VPT>::kBytes;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_cluster_rows<T, THREADS, VPT>, static_cast<const T *>(a.in),
+                           static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store, wait_ns, starve);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <typename T, int THREADS>
+cudaError_t by_vpt(const LaunchArgs &a, int vpt, int csize, int64_t wait_ns, int starve) {
+    switch (vpt) {
+        case 2: return go<T, THREADS, 2>(a, csize, wait_ns, starve);
+        case 4: return go<T, THREADS, 4>(a, csize, wait_ns, starve);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t by_shape(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns, int starve) {
+    switch (threads) {
+        case 256: return by_vpt<T, 256>(a, vpt, csize, wait_ns, starve);
+        case 512: return by_vpt<T, 512>(a, vpt, csize, wait_ns, starve);
+        case 1024: return by_vpt<T, 1024>(a, vpt, csize, wait_ns, starve);
+        default: return cudaErrorInvalidValue;
+    }
+}
+}  // namespace
+
+bool cluster_shape_ok(int threads, int vpt) {
+    return (threads == 256 || threads == 512 || threads == 1024) && (vpt == 2 || vpt == 4);
+}
+
+int64_t cluster_smem_bytes(int threads, int vpt) {
+    return (int64_t)threads * vpt * kVecBytes + 16 + (threads / 32) * 8 + kMaxCluster * 8;
+}
+
+cudaError_t launch_cluster(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns, int starve) {
+    if (csize < 1 || csize > kMaxCluster) return cudaErrorInvalidValue;
+    switch (a.dtype) {
+        case 0: return by_shape<float>(a, threads, vpt, csize, wait_ns, starve);
+        case 1: return by_shape<__half>(a, threads, vpt, csize, wait_ns, starve);
+        case 2: return by_shape<__nv_bfloat16>(a, threads, vpt, csize, wait_ns, starve);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t read_clear_error_word(cudaStream_t stream, unsigned int *word) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(word, g_error_word, sizeof(unsigned int), 0, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(unsigned int), 0, cudaMemcpyHostToDevice);
+}
+
+}  // namespace mbrs

@@ -1,0 +1,57 @@
+// k_warp.cu -- path 1 instantiations: a lane group (2..32 lanes) per row.
+#include "kernels.cuh"
+#include "launch.h"
+
+namespace mbrs {
+
+namespace {
+template <typename T, int G, int VPT>
+cudaError_t go(const LaunchArgs &a, int threads, int64_t grid) {
+    k_warp_rows<T, G, VPT><<<(unsigned)grid, threads, 0, a.stream>>>(
+        static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t by_shape(const LaunchArgs &a, int threads, int group, int vpt, int64_t grid) {
+    if (group < 32) {
+        if (vpt != 1) return cudaErrorInvalidValue;
+        switch (group) {
+            case 2: return go<T, 2, 1>(a, threads, grid);
+            case 4: return go<T, 4, 1>(a, threads, grid);
+            case 8: return go<T, 8, 1>(a, threads, grid);
+            case 16: return go<T, 16, 1>(a, threads, grid);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (vpt) {
+        case 1: return go<T, 32, 1>(a, threads, grid);
+        case 2: return go<T, 32, 2>(a, threads, grid);
+        case 3: return go<T, 32, 3>(a, threads, grid);
+        case 4: return go<T, 32, 4>(a, threads, grid);
+        case 5: return go<T, 32, 5>(a, threads, grid);
+        case 6: return go<T, 32, 6>(a, threads, grid);
+        case 7: return go<T, 32, 7>(a, threads, grid);
+        case 8: return go<T, 32, 8>(a, threads, grid);
+        case 9: return go<T, 32, 9>(a, threads, grid);
+        default: return cudaErrorInvalidValue;
+    }
+}
+}  // namespace
+
+bool warp_shape_ok(int group, int vpt) {
+    if (group == 2 || group == 4 || group == 8 || group == 16) return vpt == 1;
+    return group == 32 && vpt >= 1 && vpt <= 9;
+}
+
+cudaError_t launch_warp(const LaunchArgs &a, int threads, int group, int vpt, int64_t grid) {
+    if (threads < 32 || threads > 256 || threads % 32 != 0) return cudaErrorInvalidValue;
+    switch (a.dtype) {
+        case 0: return by_shape<float>(a, threads, group, vpt, grid);
+        case 1: return by_shape<__half>(a, threads, group, vpt, grid);
+        case 2: return by_shape<__nv_bfloat16>(a, threads, group, vpt, grid);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace mbrs

@@ -1,0 +1,37 @@
+// launch.h -- host-side interface between the C ABI (abi.cu) and the per-path
+// translation units that hold the kernel instantiations.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mbrs {
+
+struct LaunchArgs {
+    const void *in;
+    void *out;
+    int64_t rows, cols, stride;
+    int dtype;      // 0 f32, 1 f16, 2 bf16
+    int vec_store;  // out shares in's 16-byte phase
+    cudaStream_t stream;
+};
+
+// Each launcher returns cudaErrorInvalidValue when no instantiation matches
+// the requested shape (the planner only asks for shapes that exist).
+bool warp_shape_ok(int group, int vpt);
+cudaError_t launch_warp(const LaunchArgs &a, int threads, int group, int vpt, int64_t grid);
+
+bool cta_shape_ok(int threads, int vpt);
+cudaError_t launch_cta(const LaunchArgs &a, int threads, int vpt, int64_t grid);
+
+bool cluster_shape_ok(int threads, int vpt);
+int64_t cluster_smem_bytes(int threads, int vpt);
+cudaError_t launch_cluster(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns, int starve);
+// read this device's error word after synchronising `stream`, then clear it
+cudaError_t read_clear_error_word(cudaStream_t stream, unsigned int *word);
+
+bool split_shape_ok(int threads, int vpt);
+cudaError_t launch_split(const LaunchArgs &a, int threads, int vpt, int64_t chunks, int64_t chunk_vecs,
+                         int64_t grid, void *scratch);
+
+}  // namespace mbrs

@@ -1,0 +1,266 @@
+"""GPU parity: the sm_103a kernels, called through the C ABI, against the CPU
+oracle, element by element, on seeded inputs.
+
+Covers every path (automatic and forced), ragged row counts, widths around
+every vector / warp / block / cluster boundary, misaligned base pointers and
+strides, padding that must stay untouched, in-place calls, the special values
+(-inf masks, NaN, +inf, spikes), the workloads of the pages at full size, and
+the bounded-wait error path.
+"""
+import numpy as np
+import pytest
+import torch
+
+from memory_bound_row_softmax_gb300 import binding as B
+from memory_bound_row_softmax_gb300 import build as build_mod
+from memory_bound_row_softmax_gb300 import workloads as W
+
+from gpu_harness import DeviceCase, compare, decode, run_and_compare
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ["f32", "f16", "bf16"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build_mod.build()
+    torch.cuda.init()
+    yield
+    B.set_force_path(0)
+    B.set_wait_test(0, False)
+
+
+def rnd(rows, cols, dtype, seed, stride=0, sigma=2.0):
+    return W.make_random(rows, cols, dtype, seed, row_stride=stride, sigma=sigma)
+
+
+# -- automatic dispatch across widths -----------------------------------------------
+
+WIDTHS = [1, 2, 3, 5, 7, 8, 9, 16, 31, 33, 63, 100, 255, 257, 1000, 1023, 1024, 1025, 2047, 2048, 2055,
+          4096, 4103, 8192, 8199, 16391, 32768, 32775, 65536, 131079]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("cols", WIDTHS)
+def test_auto_widths(dtype, cols):
+    rows = 5 if cols > 10000 else 7
+    res = run_and_compare(rnd(rows, cols, dtype, seed=cols), dtype)
+    assert res["path"] in (B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_SPLIT)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("rows", [1, 2, 3, 31, 33, 257, 1000])
+@pytest.mark.parametrize("cols", [40, 700, 3000])
+def test_ragged_row_counts(dtype, rows, cols):
+    run_and_compare(rnd(rows, cols, dtype, seed=rows * 7 + cols), dtype)
+
+
+def test_zero_rows_is_a_no_op():
+    assert B.softmax_fwd_ptr(0, 0, 0, 5, 5, 0) == B.OK
+
+
+# -- every path forced onto the widths it can take ---------------------------------------
+
+FORCED = {
+    B.PATH_WARP: [1, 2, 3, 7, 9, 17, 31, 33, 100, 255, 256, 257, 1000, 1024],
+    B.PATH_CTA: [1, 9, 100, 1025, 2047, 4096, 4103, 8199, 16384],
+    B.PATH_CLUSTER: [1, 100, 2048, 9000, 16391, 65536, 131079],
+    B.PATH_SPLIT: [1, 100, 4103, 65536, 262147],
+}
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("path,cols", [(p, c) for p, cs in FORCED.items() for c in cs])
+def test_forced_path(dtype, path, cols):
+    res = run_and_compare(rnd(3, cols, dtype, seed=100 + cols), dtype, path=path)
+    assert res["path"] == path
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("group", [1, 2, 3, 5, 8, 16])
+def test_cluster_sizes(dtype, group):
+    res = run_and_compare(rnd(4, 3001, dtype, seed=group), dtype, path=B.PATH_CLUSTER, threads=256, vpt=2,
+                          group=group)
+    assert res["path"] == B.PATH_CLUSTER
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("threads,vpt", [(64, 8), (128, 2), (512, 4), (1024, 2)])
+def test_cta_shapes(dtype, threads, vpt):
+    cols = {"f32": 4 * threads * vpt - 5, "f16": 8 * threads * vpt - 9, "bf16": 8 * threads * vpt - 9}[dtype]
+    res = run_and_compare(rnd(3, cols, dtype, seed=threads + vpt), dtype, path=B.PATH_CTA, threads=threads, vpt=vpt)
+    assert res["path"] == B.PATH_CTA
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("chunks", [1, 2, 7, 64])
+def test_split_chunk_counts(dtype, chunks):
+    res = run_and_compare(rnd(3, 50001, dtype, seed=chunks), dtype, path=B.PATH_SPLIT, group=chunks)
+    assert res["path"] == B.PATH_SPLIT
+
+
+def test_forced_shape_that_cannot_cover_the_row_is_rejected():
+    case = DeviceCase(rnd(2, 5000, "f32", 1), "f32")
+    assert case.run(5000, path=B.PATH_WARP) == B.ERR_UNSUPPORTED
+    assert case.run(5000, path=B.PATH_CLUSTER, threads=256, vpt=2, group=2) == B.ERR_UNSUPPORTED
+
+
+# -- alignment, strides, aliasing ------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("in_off,out_off", [(1, 1), (2, 2), (3, 3), (1, 0), (0, 3), (5, 2)])
+@pytest.mark.parametrize("cols", [7, 100, 1000, 3001, 20011])
+def test_misaligned_pointers(dtype, in_off, out_off, cols):
+    run_and_compare(rnd(4, cols, dtype, seed=cols + in_off), dtype, in_off=in_off, out_off=out_off)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("cols,extra", [(31, 1), (100, 3), (1000, 8), (2048, 5), (4096, 8), (20000, 7)])
+def test_padded_strides(dtype, cols, extra):
+    x = rnd(9, cols, dtype, seed=cols, stride=cols + extra)
+    run_and_compare(x, dtype, cols)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("path", [0, B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_SPLIT])
+def test_in_place(dtype, path):
+    cols = 1000 if path in (0, B.PATH_WARP) else 6007
+    run_and_compare(rnd(6, cols, dtype, seed=path), dtype, inplace=True, in_off=1, path=path)
+
+
+def test_partial_overlap_is_rejected():
+    d = torch.zeros(1000, device="cuda")
+    p = d.data_ptr()
+    assert B.softmax_fwd_ptr(p, p + 16, 10, 10, 10, 0) == B.ERR_OVERLAP
+
+
+# -- special values ------------------------------------------------------------------
+
+def special_rows(dtype, cols):
+    """Rows 0..6: fully masked, one-hot, a NaN, a +inf, constant, a +100 spike, half masked."""
+    x = W.make_random(8, cols, dtype, seed=77, sigma=1.0)
+
+    def put(row, idx, v):
+        x[row, idx] = W.quantise(np.asarray([v], dtype=np.float64), dtype)[0]
+
+    put(0, slice(None), -np.inf)
+    put(1, slice(None), -np.inf)
+    put(1, cols // 2, 1.5)
+    put(2, cols - 1, np.nan)
+    put(3, 0, np.inf)
+    put(4, slice(None), 0.375)
+    put(5, cols // 3, float(decode(x[5], dtype).max()) + 100.0)
+    put(6, slice(0, None, 2), -np.inf)
+    return x
+
+
+def _result_bits(x, dtype, path):
+    c = DeviceCase(x, dtype)
+    assert c.run(x.shape[1], path=path) == B.OK
+    return c.result(x.shape[1])
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("path,cols", [(B.PATH_WARP, 33), (B.PATH_WARP, 1000), (B.PATH_CTA, 3000),
+                                       (B.PATH_CLUSTER, 20000), (B.PATH_SPLIT, 20000)])
+def test_special_values(dtype, path, cols):
+    x = special_rows(dtype, cols)
+    run_and_compare(x, dtype, path=path)
+    y = decode(_result_bits(x, dtype, path), dtype)
+    assert np.isnan(y[0]).all() and np.isnan(y[2]).all() and np.isnan(y[3]).all()
+    assert y[1, cols // 2] == 1.0 and (np.delete(y[1], cols // 2) == 0).all()
+    assert np.isfinite(y[5]).all() and abs(y[5, cols // 3] - 1.0) < 1e-3
+    assert (y[6, ::2] == 0).all()
+
+
+def test_constant_rows_are_exactly_one_over_n():
+    for cols in (1, 2, 4, 1024, 4096, 131072):
+        x = np.full((2, cols), 0.5, dtype=np.float32)
+        c = DeviceCase(x, "f32")
+        assert c.run(cols) == B.OK
+        y = decode(c.result(cols), "f32")
+        assert np.abs(y - 1.0 / cols).max() <= 1e-6 * (1.0 / cols) + 1e-12
+
+
+# -- the pages' workloads at full size ----------------------------------------------------
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
+def test_config_full_size(name):
+    w = W.CONFIGS[name]
+    x = W.make_input(w)
+    res = run_and_compare(x, w.dtype, w.cols)
+    if name == "c3":  # the spike rows: the spiked entry carries almost all the mass
+        rows, cols = W.spike_plan(w)
+        c = DeviceCase(x, "f32")
+        assert c.run(w.cols) == B.OK
+        y = decode(c.result(w.cols), "f32")
+        assert np.isfinite(y[rows]).all()
+        assert (np.abs(y[rows, cols] - 1.0) < 1e-6).all()
+    print(name, res)
+
+
+@pytest.mark.parametrize("cols", W.SWEEP_WIDTHS)
+def test_sweep_width_full_size(cols):
+    w = W.sweep_workload(cols)
+    x = W.make_input(w)
+    rng = np.random.default_rng(cols)
+    sample = np.unique(np.concatenate([[0, 1, 2, w.rows - 1], rng.integers(0, w.rows, 61)]))
+    run_and_compare(x, "f32", rows=sample)
+
+
+def test_offsets_beyond_int32():
+    # 65539 rows x 32768 fp16: element offsets pass 2^31; tile 64 seeded rows
+    rows, cols = 65539, 32768
+    block = W.make_random(64, cols, "f16", seed=31, sigma=3.0)
+    d_in = torch.from_numpy(block.view(np.int16)).cuda().repeat((rows + 63) // 64, 1)[:rows].contiguous()
+    d_out = torch.empty_like(d_in)
+    st = B.softmax_fwd_ptr(d_in.data_ptr(), d_out.data_ptr(), rows, cols, cols, 1,
+                           torch.cuda.current_stream().cuda_stream)
+    assert st == B.OK
+    torch.cuda.synchronize()
+    check = [0, 63, 64, 65535, 65536, 65538]
+    got = d_out[check].cpu().numpy().view(np.uint16)
+    compare(got, np.ascontiguousarray(block[[r % 64 for r in check]]), "f16", cols)
+    del d_in, d_out
+    torch.cuda.empty_cache()
+
+
+# -- the bounded wait and the device error word ------------------------------------------
+
+def test_wait_timeout_is_reported_and_recoverable():
+    x = rnd(4, 20000, "bf16", seed=5)
+    c = DeviceCase(x, "bf16")
+    B.set_wait_test(1_000_000, starve=True)  # 1 ms, and the TMA barrier is never armed
+    try:
+        assert c.run(20000, path=B.PATH_CLUSTER) == B.OK
+        assert B.check_device_error() == B.ERR_TIMEOUT
+    finally:
+        B.set_wait_test(0, False)
+    assert B.check_device_error() == B.OK
+    # outputs were skipped, the context is still usable and the next call is exact
+    run_and_compare(x, "bf16", path=B.PATH_CLUSTER)
+
+
+# -- the tensor-level binding --------------------------------------------------------------
+
+@pytest.mark.parametrize("tdtype,name", [(torch.float32, "f32"), (torch.float16, "f16"), (torch.bfloat16, "bf16")])
+def test_torch_binding(tdtype, name):
+    g = torch.Generator(device="cpu").manual_seed(3)
+    x = (torch.randn(37, 3001, generator=g) * 3).to(tdtype).cuda()
+    y = B.softmax_fwd(x)
+    ref = torch.softmax(x.double(), dim=1)
+    assert (y.double() - ref).abs().max().item() <= {"f32": 1e-6, "f16": 1e-3, "bf16": 4e-3}[name]
+    out = torch.empty_like(x)
+    assert B.softmax_fwd(x, out) is out
+    assert torch.equal(out, y)
+    z = x.clone()
+    B.softmax_fwd(z, z)
+    assert torch.equal(z, y)
+    big = torch.randn(8, 4000, device="cuda").to(tdtype)
+    view = big[:, 100:3100]  # a strided view: row stride 4000
+    assert torch.equal(B.softmax_fwd(view), B.softmax_fwd(view.contiguous()))
+    with pytest.raises(ValueError):
+        B.softmax_fwd(x.t())
