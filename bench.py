@@ -1,0 +1,487 @@
+"""Benchmark of the fused row softmax on GB300.
+
+One step = one softmax_fwd call (the whole hot path: load, row max, exp and
+sum, normalise and store, dispatch) over the fp16 4096 x 2048 workload the
+pages quote (x ~ N(0, 9), seed 1).  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload c1..c5] [--no-per-shape] [--sweep]
+
+Timing: W warm-up steps, then exactly K steps bracketed by a barrier and a
+device synchronisation; every launch is bracketed by CUDA events on the
+launching stream.  Each step reads a different buffer set; the sets together
+are larger than 2.5x the L2, so every step's input comes from HBM.
+`value` is whole-job throughput (algorithmic bytes 2*rows*cols*elem of all
+ranks / max-over-ranks time of the K steps); the roofline block uses the
+mean per-launch device time.  Under torchrun every rank runs its own copy of
+the workload (weak scaling, rows are independent: no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s and % of GB300 roofline (2×bytes/peak) per shape; µs/call"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# multi-rank plumbing (host side; tested on CPU with gloo)
+# ---------------------------------------------------------------------------
+
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_max_seconds(seconds: float, world: int) -> float:
+    """Max of a per-rank duration over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return seconds
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate_gbs(bytes_per_rank_step: int, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: all ranks' bytes over the slowest rank's time."""
+    return bytes_per_rank_step * steps * world / max_seconds / 1e9
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.t0 = self.t1 = 0.0
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._reader = threading.Thread(target=self._read, daemon=True)
+            self._reader.start()
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        self.t1 = time.time()
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._reader.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() in ("active", "1"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None,
+                "window_ms": round((self.t1 - self.t0) * 1e3, 1)}
+
+
+def rotating_sets(x_dev, n_bytes_per_set: int, l2_bytes: int, min_sets: int = 2):
+    """Buffer sets (in, out) totalling > 2.5x L2; the inputs are copies of x."""
+    import torch
+    sets = max(min_sets, -(-int(2.5 * l2_bytes) // max(1, n_bytes_per_set)))
+    out = []
+    for _ in range(sets):
+        out.append((x_dev.clone(), torch.empty_like(x_dev)))
+    return out
+
+
+def time_steps(launch, sets, steps: int, warmup: int, world: int = 1, preroll_ms: float = 0.0):
+    """Run warmup + steps launches over rotating sets; returns (per-launch ms list, total ms)."""
+    import torch
+    for i in range(warmup):
+        launch(*sets[i % len(sets)])
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if preroll_ms > 0:  # keep the GPU busy while the host queues the launches ahead
+        torch.cuda._sleep(int(preroll_ms * 1e6))
+    t0.record()
+    for i in range(steps):
+        a, b = sets[i % len(sets)]
+        starts[i].record()
+        launch(a, b)
+        ends[i].record()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return per, t0.elapsed_time(t1)
+
+
+def traffic_record(workload: str):
+    """ncu DRAM bytes per launch for this workload's dominant kernel, if the
+    kernel sources are unchanged since the capture (else None)."""
+    from memory_bound_row_softmax_gb300 import build as build_mod
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("sources_digest") != build_mod.sources_digest():
+        return None
+    return rec
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args) -> dict | None:
+    import numpy as np
+    import torch
+
+    from memory_bound_row_softmax_gb300 import binding as B
+    from memory_bound_row_softmax_gb300 import build as build_mod
+    from memory_bound_row_softmax_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    build_mod.build()
+    B.lib()
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    peaks = measured_peaks()
+
+    w = W.CONFIGS[args.workload]
+    x = W.make_input(w)
+    bits = x.view(np.int32 if w.dtype == "f32" else np.int16)
+    x_dev = torch.from_numpy(bits).to(dev)
+    code = B.DTYPE_CODES[w.dtype]
+    stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream
+    lib = B.lib()
+
+    def launch(a, b):
+        st = lib.softmax_fwd(a.data_ptr(), b.data_ptr(), w.rows, w.cols, w.stride, code, handle)
+        if st != 0:
+            raise B.SoftmaxError(st)
+
+    plan = B.plan(x_dev.data_ptr(), x_dev.data_ptr() + (1 << 40), w.rows, w.cols, w.stride, code)
+    set_bytes = 2 * x_dev.numel() * x_dev.element_size()
+    sets = rotating_sets(x_dev, set_bytes, l2)
+
+    if args.only_kernel:  # the command the ncu captures run: launches only
+        per, total_ms = time_steps(launch, sets, args.steps, args.warmup, world)
+        if rank == 0:
+            print(json.dumps({"workload": w.name, "steps": args.steps, "us_mean": statistics.fmean(per) * 1e3,
+                              "plan": plan}))
+        return None
+
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local)
+    clocks.start()
+    # untimed pre-load so that the clock samples see this kernel's steady state
+    t_end = time.time() + 0.4
+    while time.time() < t_end:
+        for i in range(200):
+            launch(*sets[i % len(sets)])
+        torch.cuda.synchronize()
+    per, total_ms = time_steps(launch, sets, args.steps, args.warmup, world,
+                               preroll_ms=min(200.0, 0.004 * args.steps))
+    clk = clocks.stop()
+
+    max_s = reduce_max_seconds(total_ms / 1e3, world)
+    alg = w.algorithmic_bytes
+    value = aggregate_gbs(alg, args.steps, world, max_s)
+    mean_launch_ms = statistics.fmean(per)
+    achieved = plan["hbm_bytes"] / (mean_launch_ms / 1e3) / 1e9
+    traffic = traffic_record(w.name)
+    result = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_s * 1e3 / args.steps, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name, "rows": w.rows, "cols": w.cols, "row_stride": w.stride,
+            "storage_dtype": w.dtype, "arithmetic": "f32 (one exp per element)",
+            "per_rank_rows": w.rows, "parallelism": f"replicas x{world} (rows independent)",
+            "l2": f"inputs larger than L2: {len(sets)} rotating buffer sets, "
+                  f"{len(sets) * set_bytes / 1e6:.0f} MB > 2.5 x L2 ({l2 / 1e6:.0f} MB)",
+            "path": B.PATH_NAMES.get(plan["path"]), "threads": plan["threads"], "vpt": plan["vpt"],
+            "group": plan["group"],
+        },
+        "us_per_call": {"mean": round(mean_launch_ms * 1e3, 3), "median": round(statistics.median(per) * 1e3, 3)},
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
+            "traffic": traffic["bytes_per_launch"] if traffic else None,
+            "algorithmic_bytes": plan["hbm_bytes"],
+        },
+        "clocks": clk,
+        "gpu_launches": args.steps * plan["launches"],
+    }
+    if rank == 0:
+        result["e2e"] = e2e_measure(launch, x, w, dev, min(args.steps, 2000))
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(x, w)
+    if rank == 0 and world == 1 and not args.no_per_shape:
+        result["per_shape"] = per_shape(args, peaks, l2, dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+def e2e_measure(launch, x, w, dev, steps: int) -> dict:
+    """Same metric through the C ABI with host buffers: H2D of the input from
+    pinned memory, the call, D2H of the output, every step, all timed."""
+    import numpy as np
+    import torch
+    bits = x.view(np.int32 if w.dtype == "f32" else np.int16)
+    h_in = torch.from_numpy(bits).pin_memory()
+    h_out = torch.empty_like(h_in).pin_memory()
+    d_in = torch.empty_like(h_in, device=dev)
+    d_out = torch.empty_like(d_in)
+    for _ in range(3):
+        d_in.copy_(h_in, non_blocking=True)
+        launch(d_in, d_out)
+        h_out.copy_(d_out, non_blocking=True)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        d_in.copy_(h_in, non_blocking=True)
+        launch(d_in, d_out)
+        h_out.copy_(d_out, non_blocking=True)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    nbytes = h_in.numel() * h_in.element_size()
+    return {"value": round(w.algorithmic_bytes * steps / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "steps": steps,
+            "ms_per_step": round(ms / steps, 4)}
+
+
+def cpu_baseline(x, w, min_seconds: float = 3.0) -> dict:
+    """The CPU oracle (untuned) over the whole workload on all host cores."""
+    import oracle
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.softmax(x, w.dtype, cols=w.cols, threads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    return {"value": round(w.algorithmic_bytes * reps / el / 1e9, 3), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{reps} full pass(es) over all {w.rows} rows of {w.name} ({el:.1f} s wall, "
+                      f"double-precision C, rows split over {cores} threads)"}
+
+
+def per_shape(args, peaks, l2, dev) -> dict:
+    """Every workload of the pages: median us/call of 200 timed launches after
+    50 warm-up (the harness of the pages), GB/s, fraction of the measured HBM
+    peak and of a device-to-device copy of the same bytes timed the same way."""
+    import numpy as np
+    import torch
+
+    from memory_bound_row_softmax_gb300 import binding as B
+    from memory_bound_row_softmax_gb300 import workloads as W
+
+    lib = B.lib()
+    handle = torch.cuda.current_stream(dev).cuda_stream
+    todo = [W.CONFIGS[k] for k in ("c1", "c2", "c3", "c4", "c5")]
+    if args.sweep:
+        todo += [W.sweep_workload(c) for c in W.SWEEP_WIDTHS]
+    table = {}
+    for w in todo:
+        if w.kind == "uniform":  # sweep matrices: seeded on the device (timing only)
+            g = torch.Generator(device=dev).manual_seed(w.seed)
+            xd = (torch.rand((w.rows, w.stride), generator=g, device=dev, dtype=torch.float32) * 200 - 100)
+            xd = xd.view(torch.int32)
+        else:
+            x = W.make_input(w)
+            xd = torch.from_numpy(x.view(np.int32 if w.dtype == "f32" else np.int16)).to(dev)
+        code = B.DTYPE_CODES[w.dtype]
+
+        def launch(a, b, w=w, code=code):
+            st = lib.softmax_fwd(a.data_ptr(), b.data_ptr(), w.rows, w.cols, w.stride, code, handle)
+            if st != 0:
+                raise B.SoftmaxError(st)
+
+        plan = B.plan(xd.data_ptr(), xd.data_ptr() + (1 << 40), w.rows, w.cols, w.stride, code)
+        set_bytes = 2 * xd.numel() * xd.element_size()
+        sets = rotating_sets(xd, set_bytes, l2)
+        per, _ = time_steps(launch, sets, 200, 50)
+        med = statistics.median(per)
+        # the copy ceiling: rows*cols*elem bytes, device to device, same rotation
+        nbytes = w.rows * w.cols * w.elem_bytes
+        csets = [(torch.empty(nbytes, dtype=torch.uint8, device=dev), torch.empty(nbytes, dtype=torch.uint8, device=dev))
+                 for _ in range(max(2, -(-int(2.5 * l2) // (2 * nbytes))))]
+        cper, _ = time_steps(lambda a, b: b.copy_(a), csets, 200, 50)
+        cmed = statistics.median(cper)
+        gbs = plan["hbm_bytes"] / (med / 1e3) / 1e9
+        alg = w.algorithmic_bytes / (med / 1e3) / 1e9
+        copy_gbs = 2 * nbytes / (cmed / 1e3) / 1e9
+        table[w.name] = {
+            "path": B.PATH_NAMES.get(plan["path"]), "us_median": round(med * 1e3, 2),
+            "us_p10": round(float(np.percentile(per, 10)) * 1e3, 2),
+            "us_p90": round(float(np.percentile(per, 90)) * 1e3, 2),
+            "gbs": round(alg, 1), "frac_of_measured_hbm": round(alg / peaks["hbm_gbs"], 4),
+            "frac_of_nominal_8tbs": round(alg / 8000.0, 4),
+            "copy_us": round(cmed * 1e3, 2), "copy_gbs": round(copy_gbs, 1),
+            "frac_of_copy": round(alg / copy_gbs, 4), "time_vs_copy": round(med / cmed, 3),
+            "moved_gbs": round(gbs, 1),
+        }
+        del sets, csets, xd
+        torch.cuda.empty_cache()
+    return table
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle, as it stands
+# ---------------------------------------------------------------------------
+
+def run_reference(args) -> dict | None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    from memory_bound_row_softmax_gb300 import workloads as W
+    oracle.build()
+    w = W.CONFIGS[args.workload]
+    x = W.make_input(w)
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.softmax(x, w.dtype, cols=w.cols, threads=cores)
+    t_full = time.perf_counter() - t0
+    budget_s = 90.0
+    rows_per_step = int(max(1, min(w.rows, w.rows * budget_s / max(1, args.steps + args.warmup) / t_full)))
+    for i in range(args.warmup):
+        r0 = (i * rows_per_step) % max(1, w.rows - rows_per_step + 1)
+        oracle.softmax(x[r0:r0 + rows_per_step], w.dtype, cols=w.cols, threads=cores)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        r0 = (i * rows_per_step) % max(1, w.rows - rows_per_step + 1)
+        oracle.softmax(x[r0:r0 + rows_per_step], w.dtype, cols=w.cols, threads=cores)
+    el = time.perf_counter() - t0
+    step_bytes = 2 * rows_per_step * w.cols * w.elem_bytes
+    value = step_bytes * args.steps / el / 1e9
+    sample = (f"each step: rows [r0, r0+{rows_per_step}) of {w.name} ({rows_per_step} of {w.rows} rows), "
+              f"double-precision C oracle over {cores} threads")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "row_stride": w.stride,
+                   "storage_dtype": w.dtype, "rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="c2", choices=("c1", "c2", "c3", "c4", "c5"))
+    ap.add_argument("--no-per-shape", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="add the fp32 width sweep to the per-shape table")
+    ap.add_argument("--only-kernel", action="store_true",
+                    help="warm-up and timed launches only (the command profiled with ncu)")
+    ap.add_argument("--json-out", default="")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        line = json.dumps(res)
+        print(line, flush=True)
+        if args.json_out:
+            with open(args.json_out, "w") as f:
+                f.write(line + "\n")
+
+
+if __name__ == "__main__":
+    main()
