@@ -151,31 +151,49 @@ def rotating_sets(x_dev, n_bytes_per_set: int, l2_bytes: int, min_sets: int = 2)
     return out
 
 
-def time_steps(launch, sets, steps: int, warmup: int, world: int = 1, preroll_ms: float = 0.0):
-    """Run warmup + steps launches over rotating sets; returns (per-launch ms list, total ms)."""
+def time_steps(launch, sets, steps: int, warmup: int, world: int = 1, graph: bool = True):
+    """W warm-up launches, then exactly `steps` launches over the rotating sets.
+
+    With graph=True the timed launches are captured once into a CUDA graph and
+    replayed, so the host's per-call cost (Python, ctypes, launch) cannot leave
+    the GPU idle between steps; events bracket the replay on the launching
+    stream.  Returns (mean ms per launch, total ms, per-launch ms or None)."""
     import torch
     for i in range(warmup):
         launch(*sets[i % len(sets)])
     torch.cuda.synchronize()
+    g = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(steps):
+                launch(*sets[i % len(sets)])
+        torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    if preroll_ms > 0:  # keep the GPU busy while the host queues the launches ahead
-        torch.cuda._sleep(int(preroll_ms * 1e6))
-    t0.record()
-    for i in range(steps):
-        a, b = sets[i % len(sets)]
-        starts[i].record()
-        launch(a, b)
-        ends[i].record()
-    t1.record()
+    per = None
+    if g is not None:
+        t0.record()
+        g.replay()
+        t1.record()
+    else:
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        t0.record()
+        for i in range(steps):
+            starts[i].record()
+            launch(*sets[i % len(sets)])
+            ends[i].record()
+        t1.record()
     torch.cuda.synchronize()
     barrier(world)
-    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    return per, t0.elapsed_time(t1)
+    total = t0.elapsed_time(t1)
+    if g is None:
+        per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    del g
+    return total / steps, total, per
 
 
 def traffic_record(workload: str):
@@ -227,7 +245,8 @@ def run_ours(args) -> dict | None:
     lib = B.lib()
 
     def launch(a, b):
-        st = lib.softmax_fwd(a.data_ptr(), b.data_ptr(), w.rows, w.cols, w.stride, code, handle)
+        st = lib.softmax_fwd(a.data_ptr(), b.data_ptr(), w.rows, w.cols, w.stride, code,
+                             torch.cuda.current_stream().cuda_stream)
         if st != 0:
             raise B.SoftmaxError(st)
 
@@ -235,11 +254,10 @@ def run_ours(args) -> dict | None:
     set_bytes = 2 * x_dev.numel() * x_dev.element_size()
     sets = rotating_sets(x_dev, set_bytes, l2)
 
-    if args.only_kernel:  # the command the ncu captures run: launches only
-        per, total_ms = time_steps(launch, sets, args.steps, args.warmup, world)
+    if args.only_kernel:  # the command the ncu captures run: eager launches only
+        mean_ms, total_ms, _ = time_steps(launch, sets, args.steps, args.warmup, world, graph=False)
         if rank == 0:
-            print(json.dumps({"workload": w.name, "steps": args.steps, "us_mean": statistics.fmean(per) * 1e3,
-                              "plan": plan}))
+            print(json.dumps({"workload": w.name, "steps": args.steps, "us_mean": mean_ms * 1e3, "plan": plan}))
         return None
 
     clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
@@ -251,14 +269,12 @@ def run_ours(args) -> dict | None:
         for i in range(200):
             launch(*sets[i % len(sets)])
         torch.cuda.synchronize()
-    per, total_ms = time_steps(launch, sets, args.steps, args.warmup, world,
-                               preroll_ms=min(200.0, 0.004 * args.steps))
+    mean_launch_ms, total_ms, _ = time_steps(launch, sets, args.steps, args.warmup, world)
     clk = clocks.stop()
 
     max_s = reduce_max_seconds(total_ms / 1e3, world)
     alg = w.algorithmic_bytes
     value = aggregate_gbs(alg, args.steps, world, max_s)
-    mean_launch_ms = statistics.fmean(per)
     achieved = plan["hbm_bytes"] / (mean_launch_ms / 1e3) / 1e9
     traffic = traffic_record(w.name)
     result = {
@@ -280,10 +296,11 @@ def run_ours(args) -> dict | None:
             "per_rank_rows": w.rows, "parallelism": f"replicas x{world} (rows independent)",
             "l2": f"inputs larger than L2: {len(sets)} rotating buffer sets, "
                   f"{len(sets) * set_bytes / 1e6:.0f} MB > 2.5 x L2 ({l2 / 1e6:.0f} MB)",
+            "timing": "K launches captured in one CUDA graph, replayed between CUDA events",
             "path": B.PATH_NAMES.get(plan["path"]), "threads": plan["threads"], "vpt": plan["vpt"],
             "group": plan["group"],
         },
-        "us_per_call": {"mean": round(mean_launch_ms * 1e3, 3), "median": round(statistics.median(per) * 1e3, 3)},
+        "us_per_call": round(mean_launch_ms * 1e3, 3),
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
@@ -355,9 +372,10 @@ def cpu_baseline(x, w, min_seconds: float = 3.0) -> dict:
 
 
 def per_shape(args, peaks, l2, dev) -> dict:
-    """Every workload of the pages: median us/call of 200 timed launches after
-    50 warm-up (the harness of the pages), GB/s, fraction of the measured HBM
-    peak and of a device-to-device copy of the same bytes timed the same way."""
+    """Every workload of the pages: mean us/call over 200 timed launches after
+    50 warm-up (the harness of the pages; replayed from a CUDA graph), GB/s,
+    fraction of the measured HBM peak and of a device-to-device copy of the
+    same bytes timed the same way."""
     import numpy as np
     import torch
 
@@ -381,28 +399,25 @@ def per_shape(args, peaks, l2, dev) -> dict:
         code = B.DTYPE_CODES[w.dtype]
 
         def launch(a, b, w=w, code=code):
-            st = lib.softmax_fwd(a.data_ptr(), b.data_ptr(), w.rows, w.cols, w.stride, code, handle)
+            st = lib.softmax_fwd(a.data_ptr(), b.data_ptr(), w.rows, w.cols, w.stride, code,
+                                 torch.cuda.current_stream().cuda_stream)
             if st != 0:
                 raise B.SoftmaxError(st)
 
         plan = B.plan(xd.data_ptr(), xd.data_ptr() + (1 << 40), w.rows, w.cols, w.stride, code)
         set_bytes = 2 * xd.numel() * xd.element_size()
         sets = rotating_sets(xd, set_bytes, l2)
-        per, _ = time_steps(launch, sets, 200, 50)
-        med = statistics.median(per)
+        med, _, _ = time_steps(launch, sets, 200, 50)
         # the copy ceiling: rows*cols*elem bytes, device to device, same rotation
         nbytes = w.rows * w.cols * w.elem_bytes
         csets = [(torch.empty(nbytes, dtype=torch.uint8, device=dev), torch.empty(nbytes, dtype=torch.uint8, device=dev))
                  for _ in range(max(2, -(-int(2.5 * l2) // (2 * nbytes))))]
-        cper, _ = time_steps(lambda a, b: b.copy_(a), csets, 200, 50)
-        cmed = statistics.median(cper)
+        cmed, _, _ = time_steps(lambda a, b: b.copy_(a), csets, 200, 50)
         gbs = plan["hbm_bytes"] / (med / 1e3) / 1e9
         alg = w.algorithmic_bytes / (med / 1e3) / 1e9
         copy_gbs = 2 * nbytes / (cmed / 1e3) / 1e9
         table[w.name] = {
-            "path": B.PATH_NAMES.get(plan["path"]), "us_median": round(med * 1e3, 2),
-            "us_p10": round(float(np.percentile(per, 10)) * 1e3, 2),
-            "us_p90": round(float(np.percentile(per, 90)) * 1e3, 2),
+            "path": B.PATH_NAMES.get(plan["path"]), "us_per_call": round(med * 1e3, 2),
             "gbs": round(alg, 1), "frac_of_measured_hbm": round(alg / peaks["hbm_gbs"], 4),
             "frac_of_nominal_8tbs": round(alg / 8000.0, 4),
             "copy_us": round(cmed * 1e3, 2), "copy_gbs": round(copy_gbs, 1),

@@ -16,9 +16,14 @@
 // reduction followed by a sum reduction), which matters most where the row
 // spans the warps of a block or the blocks of a cluster.
 //
-// exp is computed as 2^(x log2 e - m log2 e) with the PTX instruction
-// ex2.approx.ftz.f32 (relative error about 2^-22); the shift m log2 e is the
-// same for the whole row, so its rounding cancels in the ratio.
+// exp is computed as 2^(x log2 e - s) with the PTX instruction
+// ex2.approx.ftz.f32 (relative error about 2^-22), where s = fl(m log2 e) is
+// the shift rounded once to fp32.  States are carried in that base-2 form,
+// (s, l) with l = sum 2^(x log2 e - s), and merged as
+//     S = max(s1, s2),   l = l1 2^(s1 - S) + l2 2^(s2 - S),
+// so every element of a row ends up scaled by the same 2^(-S): the rounding
+// of the shift cancels in the ratio instead of differing from thread to thread
+// (with |m| near 100 a per-thread rounding would cost ~5e-6 relative).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -200,15 +205,15 @@ __device__ __forceinline__ void st_cluster_f2(uint32_t addr, float a, float b) {
 constexpr unsigned int kErrWaitTimeout = 1u;
 
 // ---------------------------------------------------------------------------
-// (max, sum) states
+// (s, l) states, s = fl(max * log2 e)
 // ---------------------------------------------------------------------------
-// The shift a state with max m uses: an empty state (m = -inf) shifts by 0 so
-// that its (all -inf) entries give exp = 0 instead of NaN.
-__device__ __forceinline__ float safe_shift(float m) { return m == -INFINITY ? 0.f : m; }
+// The shift an element uses: an empty state (s = -inf) shifts by 0 so that
+// its (all -inf) entries give 2^-inf = 0 instead of NaN.
+__device__ __forceinline__ float safe_shift(float s) { return s == -INFINITY ? 0.f : s; }
 
-// l scaled from max m to max M >= m (0 for an empty state).
-__device__ __forceinline__ float rescale(float l, float m, float M) {
-    return m == -INFINITY ? 0.f : l * ex2((m - M) * kLog2e);
+// l taken from shift s to shift S >= s (0 for an empty state).
+__device__ __forceinline__ float rescale(float l, float s, float S) {
+    return s == -INFINITY ? 0.f : l * ex2(s - S);
 }
 
 // Merge the states of the `width` lanes of each aligned lane group (width a
@@ -225,11 +230,12 @@ __device__ __forceinline__ void group_merge(float &m, float &l) {
     l = L;
 }
 
-// The final per-thread factor: e_c * factor = exp(x_c - M) / L.  A row with no
-// finite max (every entry -inf) gives NaN, as does a NaN or +inf entry (L NaN).
-__device__ __forceinline__ float out_factor(float m_t, float M, float L) {
-    if (M == -INFINITY) return __int_as_float(0x7fc00000);
-    return rescale(1.f, m_t, M) * (1.f / L);
+// The final per-thread factor: e_c * factor = 2^(x_c log2 e - S) / L.  A row
+// with no finite max (every entry -inf) gives NaN, as does a NaN or +inf
+// entry (L NaN).
+__device__ __forceinline__ float out_factor(float s_t, float S, float L) {
+    if (S == -INFINITY) return __int_as_float(0x7fc00000);
+    return rescale(1.f, s_t, S) * (1.f / L);
 }
 
 // ---------------------------------------------------------------------------
@@ -307,14 +313,16 @@ struct Tile {
             }
         }
     }
-    // Replace x by e = exp(x - m_t) with the tile's own max; return (m_t, l_t).
+    // Replace x by e = 2^(x log2 e - s_t) with the tile's own max m_t and
+    // s_t = fl(m_t log2 e); return the state (s_t, l_t).
     __device__ __forceinline__ float2 exp_in_place() {
         float m = -INFINITY;
 #pragma unroll
         for (int j = 0; j < VPT; ++j)
 #pragma unroll
             for (int i = 0; i < V; ++i) m = fmaxf(m, x[j][i]);
-        const float shift = safe_shift(m) * kLog2e;
+        const float s = m * kLog2e;  // -inf stays -inf, +inf stays +inf
+        const float shift = safe_shift(s);
         float l = 0.f;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
@@ -326,7 +334,7 @@ struct Tile {
             }
             l += lj;
         }
-        return make_float2(m, l);
+        return make_float2(s, l);
     }
     __device__ __forceinline__ void scale_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
                                                 float f) {

@@ -17,8 +17,9 @@
 //                           reduction spanning many blocks needs: page
 //                           "Kernel Fusion", section "What fusion cannot fix").
 //
-// All paths keep the per-thread (m_t, l_t) scheme of common.cuh: one exp per
-// element, one merge round per row.
+// All paths keep the per-thread (s_t, l_t) scheme of common.cuh: one exp per
+// element, one merge round per row.  Variables named m / M below hold the
+// base-2 shifts s / S of those states.
 #pragma once
 
 #include "common.cuh"
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(THREADS)
             m = M;
         }
         block_merge<NW>(m, l, red[parity]);
-        const float shift = m * kLog2e;
+        const float shift = m;  // states are (s, l): m here is the row's S
         const float inv = m == -INFINITY ? __int_as_float(0x7fc00000) : 1.f / l;
         for (int64_t t0 = c0; t0 < c1; t0 += kTile) {
             if (t0 != c0) tile.load(rv, t0 + threadIdx.x, THREADS, c1);
