@@ -78,11 +78,14 @@ typedef enum {
 typedef enum {
     SOFTMAX_PATH_AUTO = 0,    /* width-based choice (default) */
     SOFTMAX_PATH_WARP = 1,    /* a warp (or 2..16 lanes) per row, cols <= 1024 */
-    SOFTMAX_PATH_CTA = 2,     /* a thread block per row, row held in registers */
-    SOFTMAX_PATH_CLUSTER = 3, /* a thread-block cluster per row: TMA bulk loads,
-                                 (max, sum) exchanged through distributed shared memory */
-    SOFTMAX_PATH_SPLIT = 4    /* rows split across the whole grid: pass 1 writes
+    SOFTMAX_PATH_CTA = 2,     /* a thread block per row, row held in registers (any alignment) */
+    SOFTMAX_PATH_CLUSTER = 3, /* a thread-block cluster per row: TMA bulk loads of the aligned
+                                 part, (max, sum) exchanged through distributed shared memory */
+    SOFTMAX_PATH_SPLIT = 4,   /* rows split across the whole grid: pass 1 writes
                                  per-chunk (max, sum), pass 2 merges them, re-reads and writes */
+    SOFTMAX_PATH_RING = 5     /* persistent blocks or clusters (<= 16 blocks per row) looping over
+                                 rows, fed by a ring of shared-memory stages that TMA bulk copies
+                                 keep full; rows of whole aligned 16-byte vectors only */
 } softmax_path_t;
 
 /*
@@ -111,7 +114,7 @@ int softmax_last_path(void);
  * Test and tuning hook: force every following call onto `path` (0 = automatic).
  * threads / vpt / group override the launch shape where > 0 (threads per block,
  * 16-byte vectors per thread, and lanes per row / cluster size / chunks per
- * row for paths 1 / 3 / 4).  A forced shape that cannot cover the row makes
+ * row for paths 1 / 3 and 5 / 4).  A forced shape that cannot cover the row makes
  * softmax_fwd return SOFTMAX_ERR_UNSUPPORTED.  Process-wide, not thread-safe.
  */
 int softmax_set_force_path(int path, int threads, int vpt, int group);
@@ -121,13 +124,14 @@ typedef struct {
     int path;              /* softmax_path_t actually chosen */
     int threads;           /* threads per block */
     int vpt;               /* 16-byte vectors per thread per tile */
-    int group;             /* lanes per row (1), cluster size (3), chunks per row (4), else 1 */
+    int group;             /* lanes per row (1), cluster size (3, 5), chunks per row (4), else 1 */
     int launches;          /* kernels per call: 1, or 2 for the SPLIT path */
     int vec_store;         /* 1 if out has in's 16-byte phase (vector stores) */
     int64_t grid;          /* blocks of the (first) kernel */
     int64_t smem_bytes;    /* dynamic shared memory per block */
     int64_t scratch_bytes; /* device scratch the call needs (SPLIT only) */
     int64_t hbm_bytes;     /* algorithmic bytes: 2 * rows * cols * elem (3x for SPLIT) */
+    int stages;            /* shared-memory ring stages per block (RING), else 0 */
 } softmax_plan_t;
 
 /*
@@ -148,15 +152,15 @@ int softmax_plan(uint64_t in_addr, uint64_t out_addr, int64_t rows, int64_t cols
 int softmax_check_device_error(cudaStream_t stream);
 
 /*
- * Test hooks for the bounded waits of the CLUSTER path.  wait_limit_ns bounds
- * each wait on a TMA completion barrier (default 1 s; <= 0 restores it).
+ * Test hooks for the bounded waits of the CLUSTER and RING paths.  wait_limit_ns
+ * bounds each wait on a TMA completion barrier (default 1 s; <= 0 restores it).
  * starve != 0 makes the next launches skip arming that barrier, so the wait
  * can only run out: the kernel records SOFTMAX_ERR_TIMEOUT, skips its stores
  * and returns normally.  Process-wide, not thread-safe.
  */
 int softmax_set_wait_test(int64_t wait_limit_ns, int starve);
 
-/* Version of this ABI: major * 10000 + minor * 100 + patch. */
+/* Version of this ABI: major * 10000 + minor * 100 + patch (1.1.0 adds the RING path). */
 int softmax_abi_version(void);
 
 #ifdef __cplusplus

@@ -15,8 +15,8 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "
 
 OK, ERR_NULL, ERR_SHAPE, ERR_STRIDE, ERR_DTYPE, ERR_OVERLAP, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_ALIGN, \
     ERR_ARG = range(11)
-PATH_AUTO, PATH_WARP, PATH_CTA, PATH_CLUSTER, PATH_SPLIT = range(5)
-PATH_NAMES = {PATH_WARP: "warp", PATH_CTA: "cta", PATH_CLUSTER: "cluster", PATH_SPLIT: "split"}
+PATH_AUTO, PATH_WARP, PATH_CTA, PATH_CLUSTER, PATH_SPLIT, PATH_RING = range(6)
+PATH_NAMES = {PATH_WARP: "warp", PATH_CTA: "cta", PATH_CLUSTER: "cluster", PATH_SPLIT: "split", PATH_RING: "ring"}
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
 
 _i64, _u64, _int, _vp = ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p
@@ -25,7 +25,7 @@ _i64, _u64, _int, _vp = ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_
 class Plan(ctypes.Structure):
     _fields_ = [("path", _int), ("threads", _int), ("vpt", _int), ("group", _int), ("launches", _int),
                 ("vec_store", _int), ("grid", _i64), ("smem_bytes", _i64), ("scratch_bytes", _i64),
-                ("hbm_bytes", _i64)]
+                ("hbm_bytes", _i64), ("stages", _int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

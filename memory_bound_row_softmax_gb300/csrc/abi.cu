@@ -7,11 +7,13 @@
 // Softmax", sections "CUDA optimized for block per row" and "CUDA scaling
 // threads": wide rows need more threads per row so that enough loads are in
 // flight):
-//   cols <= 1024                    path 1, 2..32 lanes per row
-//   row fits one block's registers  path 2, a block per row
-//   row fits a cluster (<= 16 CTAs) path 3, a cluster per row, if the clusters
-//                                   fill the GPU
-//   otherwise                       path 4, rows split over the grid (2 passes)
+//   cols <= 1024                       path 1, 2..32 lanes per row
+//   rows of whole aligned 16-B vectors path 5, persistent blocks / clusters fed
+//                                      by a TMA ring (cluster size grows with
+//                                      the row), if they can fill the GPU
+//   other rows fitting a block         path 2, a block per row in registers
+//   other rows fitting a cluster       path 3, a cluster per row
+//   otherwise                          path 4, rows split over the grid (2 passes)
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
@@ -25,7 +27,7 @@ using namespace mbrs;
 
 namespace {
 
-constexpr int kAbiVersion = 10000;  // 1.0.0
+constexpr int kAbiVersion = 10100;  // 1.1.0
 constexpr int kVecBytes = 16;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDefaultWaitNs = 1000000000;  // 1 s
@@ -37,9 +39,15 @@ std::atomic<int64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int> g_starve{0};
 
 struct Plan {
-    int path = 0, threads = 0, vpt = 0, group = 1, launches = 0, vec_store = 0;
-    int64_t grid = 0, smem = 0, scratch = 0, hbm = 0, chunks = 1, chunk_vecs = 0;
+    int path = 0, threads = 0, vpt = 0, group = 1, launches = 0, vec_store = 0, stages = 0;
+    int64_t grid = 0, smem = 0, scratch = 0, hbm = 0, chunks = 1, chunk_vecs = 0, slice_vecs = 0;
 };
+
+// Ring sizing: shared memory a block may fill with stages (of the ~228 KB an
+// SM has, leaving room for the per-block reserve), and the blocks per SM that
+// the ring aims for.
+constexpr int64_t kRingSmemPerSm = 220 * 1024;
+constexpr int kRingMaxStages = 32;
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int next_pow2(int64_t v) {
@@ -105,11 +113,16 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
 
     const int fpath = g_force_path.load(), fth = g_force_threads.load(), fvpt = g_force_vpt.load(),
               fgrp = g_force_group.load();
+    // the ring moves whole aligned vectors only: every row start and row end on 16 bytes
+    const bool ring_ok = (in % kVecBytes) == 0 && (out % kVecBytes) == 0 && uniform &&
+                         ((cols * es) % kVecBytes) == 0;
     int path = fpath;
     if (path == SOFTMAX_PATH_AUTO) {
         if (cols <= 1024 && nv <= 32 * 9) {
             path = SOFTMAX_PATH_WARP;
-        } else if (nv <= 1024 * 4) {
+        } else if (ring_ok && cdiv(nv, 16) <= 4096 && rows * 16 * 2 >= sms) {
+            path = SOFTMAX_PATH_RING;
+        } else if (nv <= 1024 * 5) {
             path = SOFTMAX_PATH_CTA;
         } else {
             const int64_t csize = cdiv(nv, nv <= 16 * 512 * 4 ? 512 * 4 : 1024 * 4);
@@ -125,9 +138,9 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             if (fgrp > 0) {
                 g = fgrp;
                 vpt = fvpt > 0 ? fvpt : (int)cdiv(nv, g);
-            } else if (nv <= 16) {
-                g = std::max(2, next_pow2(nv));
-                vpt = 1;
+            } else if (nv <= 16 * 4) {  // several rows per warp, up to 4 vectors per lane
+                g = std::max(2, next_pow2(cdiv(nv, 4)));
+                vpt = fvpt > 0 ? fvpt : (int)cdiv(nv, g);
             } else {
                 g = 32;
                 vpt = fvpt > 0 ? fvpt : (int)cdiv(nv, 32);
@@ -145,8 +158,14 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             break;
         }
         case SOFTMAX_PATH_CTA: {
-            int vpt = fvpt > 0 ? fvpt : 4;
-            int threads = fth > 0 ? fth : std::min(1024, std::max(64, next_pow2(cdiv(nv, vpt))));
+            // the fewest threads (a power of two) that need at most 4 vectors each
+            // (5 at 1024 threads); vpt = what the row then needs, not a rounded-up 4
+            int threads = fth;
+            if (threads <= 0) {
+                threads = 64;
+                while (threads < 1024 && cdiv(nv, threads) > 4) threads *= 2;
+            }
+            int vpt = fvpt > 0 ? fvpt : std::max<int>(2, (int)cdiv(nv, threads));
             if (!cta_shape_ok(threads, vpt) || (int64_t)threads * vpt < nv) return SOFTMAX_ERR_UNSUPPORTED;
             p->threads = threads;
             p->vpt = vpt;
@@ -165,6 +184,43 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             p->group = (int)csize;
             p->grid = rows * csize;
             p->smem = cluster_smem_bytes(threads, vpt);
+            break;
+        }
+        case SOFTMAX_PATH_RING: {
+            if (!ring_ok) return SOFTMAX_ERR_UNSUPPORTED;
+            // cluster size: enough blocks for the row's registers (<= 4096 vectors
+            // each), more while the rows alone cannot occupy every SM
+            int64_t csize = fgrp > 0 ? fgrp : std::max<int64_t>(1, cdiv(nv, 4096));
+            if (fgrp <= 0)
+                while (csize < 16 && rows * csize < sms && cdiv(nv, csize * 2) >= 256) csize *= 2;
+            if (csize < 1 || csize > 16) return SOFTMAX_ERR_UNSUPPORTED;
+            const int64_t slice = cdiv(nv, csize);
+            int vpt = fvpt > 0 ? fvpt : (slice <= 1024 ? 2 : 4);
+            int threads = fth > 0 ? fth : std::max(64, next_pow2(cdiv(slice, vpt)));
+            if (fth <= 0 && threads > 1024) {
+                vpt = 4;
+                threads = next_pow2(cdiv(slice, 4));
+            }
+            if (!ring_shape_ok(threads, vpt) || (int64_t)threads * vpt < slice) return SOFTMAX_ERR_UNSUPPORTED;
+            const int64_t stage_bytes = slice * kVecBytes;
+            int per_sm = std::max(1, std::min(4, 2048 / threads));
+            int64_t stages = 0;
+            for (; per_sm >= 1; --per_sm) {
+                stages = (kRingSmemPerSm / per_sm - 1024) / stage_bytes;
+                if (stages >= 2) break;
+            }
+            if (stages < 2) return SOFTMAX_ERR_UNSUPPORTED;
+            stages = std::min<int64_t>(stages, kRingMaxStages);
+            // no more stages than a block has rows to prefetch
+            const int64_t units = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)sms * per_sm / csize));
+            stages = std::max<int64_t>(2, std::min<int64_t>(stages, cdiv(rows, units)));
+            p->threads = threads;
+            p->vpt = vpt;
+            p->group = (int)csize;
+            p->stages = (int)stages;
+            p->slice_vecs = slice;
+            p->smem = ring_smem_bytes((int)stages, (int)slice, threads);
+            p->grid = units * csize;  // estimate; the launch sizes it from occupancy
             break;
         }
         case SOFTMAX_PATH_SPLIT: {
@@ -235,6 +291,11 @@ int run(const Plan &p, const LaunchArgs &a) {
         case SOFTMAX_PATH_CLUSTER:
             e = launch_cluster(a, p.threads, p.vpt, p.group, g_wait_ns.load(), g_starve.load());
             break;
+        case SOFTMAX_PATH_RING: {
+            RingCfg c{p.threads, p.vpt, p.group, p.stages, (int)p.slice_vecs, p.smem};
+            e = launch_ring(a, c, g_wait_ns.load(), g_starve.load(), nullptr);
+            break;
+        }
         case SOFTMAX_PATH_SPLIT: {
             int dev = 0;
             cudaMemPool_t pool;
@@ -297,7 +358,7 @@ const char *softmax_status_string(int status) {
 int softmax_last_path(void) { return g_last_path.load(); }
 
 int softmax_set_force_path(int path, int threads, int vpt, int group) {
-    if (path < SOFTMAX_PATH_AUTO || path > SOFTMAX_PATH_SPLIT) return SOFTMAX_ERR_ARG;
+    if (path < SOFTMAX_PATH_AUTO || path > SOFTMAX_PATH_RING) return SOFTMAX_ERR_ARG;
     g_force_path.store(path);
     g_force_threads.store(threads > 0 ? threads : 0);
     g_force_vpt.store(vpt > 0 ? vpt : 0);
@@ -330,13 +391,22 @@ int softmax_plan(uint64_t in_addr, uint64_t out_addr, int64_t rows, int64_t cols
     plan->smem_bytes = p.smem;
     plan->scratch_bytes = p.scratch;
     plan->hbm_bytes = p.hbm;
+    plan->stages = p.stages;
+    if (p.path == SOFTMAX_PATH_RING && num_sms == 0) {  // the persistent grid the launch will use
+        RingCfg c{p.threads, p.vpt, p.group, p.stages, (int)p.slice_vecs, p.smem};
+        LaunchArgs a{nullptr, nullptr, rows, cols, row_stride, dtype, p.vec_store, nullptr};
+        int64_t grid = 0;
+        if (launch_ring(a, c, 0, 0, &grid) != cudaSuccess) return SOFTMAX_ERR_CUDA;
+        plan->grid = grid;
+    }
     return SOFTMAX_OK;
 }
 
 int softmax_check_device_error(cudaStream_t stream) {
-    unsigned int word = 0;
+    unsigned int word = 0, ring_word = 0;
     if (read_clear_error_word(stream, &word) != cudaSuccess) return SOFTMAX_ERR_CUDA;
-    return word ? SOFTMAX_ERR_TIMEOUT : SOFTMAX_OK;
+    if (read_clear_ring_error_word(&ring_word) != cudaSuccess) return SOFTMAX_ERR_CUDA;
+    return (word | ring_word) ? SOFTMAX_ERR_TIMEOUT : SOFTMAX_OK;
 }
 
 int softmax_set_wait_test(int64_t wait_limit_ns, int starve) {

@@ -172,6 +172,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// Order this thread's earlier generic-proxy accesses to shared memory before
+// later async-proxy (TMA) accesses to it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // thread-block cluster
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;

@@ -16,7 +16,9 @@ template <typename T, int THREADS>
 cudaError_t by_vpt(const LaunchArgs &a, int vpt, int64_t grid) {
     switch (vpt) {
         case 2: return go<T, THREADS, 2>(a, grid);
+        case 3: return go<T, THREADS, 3>(a, grid);
         case 4: return go<T, THREADS, 4>(a, grid);
+        case 5: return go<T, THREADS, 5>(a, grid);
         case 8:
             if constexpr (THREADS < 1024) return go<T, THREADS, 8>(a, grid);  // 1024 x 8 spills
             return cudaErrorInvalidValue;
@@ -39,7 +41,7 @@ cudaError_t by_shape(const LaunchArgs &a, int threads, int vpt, int64_t grid) {
 
 bool cta_shape_ok(int threads, int vpt) {
     const bool t = threads == 64 || threads == 128 || threads == 256 || threads == 512 || threads == 1024;
-    return t && (vpt == 2 || vpt == 4 || (vpt == 8 && threads < 1024));
+    return t && ((vpt >= 2 && vpt <= 5) || (vpt == 8 && threads < 1024));
 }
 
 cudaError_t launch_cta(const LaunchArgs &a, int threads, int vpt, int64_t grid) {

@@ -12,17 +12,26 @@ cudaError_t go(const LaunchArgs &a, int threads, int64_t grid) {
     return cudaGetLastError();
 }
 
+template <typename T, int G>
+cudaError_t small_vpt(const LaunchArgs &a, int threads, int vpt, int64_t grid) {
+    switch (vpt) {
+        case 1: return go<T, G, 1>(a, threads, grid);
+        case 2: return go<T, G, 2>(a, threads, grid);
+        case 3: return go<T, G, 3>(a, threads, grid);
+        case 4: return go<T, G, 4>(a, threads, grid);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 template <typename T>
 cudaError_t by_shape(const LaunchArgs &a, int threads, int group, int vpt, int64_t grid) {
-    if (group < 32) {
-        if (vpt != 1) return cudaErrorInvalidValue;
-        switch (group) {
-            case 2: return go<T, 2, 1>(a, threads, grid);
-            case 4: return go<T, 4, 1>(a, threads, grid);
-            case 8: return go<T, 8, 1>(a, threads, grid);
-            case 16: return go<T, 16, 1>(a, threads, grid);
-            default: return cudaErrorInvalidValue;
-        }
+    switch (group) {
+        case 2: return small_vpt<T, 2>(a, threads, vpt, grid);
+        case 4: return small_vpt<T, 4>(a, threads, vpt, grid);
+        case 8: return small_vpt<T, 8>(a, threads, vpt, grid);
+        case 16: return small_vpt<T, 16>(a, threads, vpt, grid);
+        case 32: break;
+        default: return cudaErrorInvalidValue;
     }
     switch (vpt) {
         case 1: return go<T, 32, 1>(a, threads, grid);
@@ -40,7 +49,7 @@ cudaError_t by_shape(const LaunchArgs &a, int threads, int group, int vpt, int64
 }  // namespace
 
 bool warp_shape_ok(int group, int vpt) {
-    if (group == 2 || group == 4 || group == 8 || group == 16) return vpt == 1;
+    if (group == 2 || group == 4 || group == 8 || group == 16) return vpt >= 1 && vpt <= 4;
     return group == 32 && vpt >= 1 && vpt <= 9;
 }
 

@@ -9,6 +9,13 @@
 //                           its slice with a TMA bulk copy, and the blocks
 //                           exchange their (max, sum) through distributed
 //                           shared memory -- still one read, one write.
+//   path 5  k_ring_rows     persistent blocks (or clusters of up to 16 blocks,
+//                           each owning a slice of the row) loop over their
+//                           rows; one thread keeps a ring of shared-memory
+//                           stages filled with 1-D TMA bulk copies, so the
+//                           loads of the next rows are in flight while the
+//                           current row is reduced and stored.  Rows must be
+//                           made of whole aligned 16-byte vectors.
 //   path 4  k_split_stats / k_split_apply
 //                           rows cut into chunks spread over the whole grid;
 //                           pass 1 streams each chunk into a (max, sum) state
@@ -194,6 +201,142 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     l = w.y;
     group_merge<32>(m, l);
     if (ok) tile.scale_store(rv, s0 + tid, THREADS, s1, out_factor(s.x, m, l));
+}
+
+// ---------------------------------------------------------------------------
+// path 5: persistent TMA ring (a block or a cluster per row, many rows each)
+// ---------------------------------------------------------------------------
+// Shared memory: `stages` slots of slice_vecs 16-byte vectors, one mbarrier
+// per slot, the block-merge scratch (2 x NW states) and the cluster exchange
+// slots (2 x 16 states); the last two are double-buffered by row parity.
+struct RingLayout {
+    int64_t stage_bytes, bar_off, red_off, slot_off, bytes;
+    __host__ __device__ RingLayout(int stages, int slice_vecs, int threads) {
+        stage_bytes = (int64_t)slice_vecs * kVecBytes;
+        bar_off = stage_bytes * stages;
+        red_off = bar_off + 8 * stages;
+        red_off = (red_off + 15) & ~int64_t(15);
+        slot_off = red_off + 2 * (threads / 32) * 8;
+        bytes = slot_off + 2 * kMaxCluster * 8;
+    }
+};
+
+template <typename T, int THREADS, int VPT>
+__global__ void __launch_bounds__(THREADS, (THREADS >= 512 ? 1 : 512 / THREADS))
+    k_ring_rows(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int stages, int slice_vecs,
+                int64_t wait_ns, int starve) {
+    constexpr int V = Elem<T>::kVec;
+    constexpr int NW = THREADS / 32;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const RingLayout L(stages, slice_vecs, THREADS);
+    const uint32_t stage_base = smem_addr(smem);
+    const uint32_t bar_base = smem_addr(smem + L.bar_off);
+    float2 *red = reinterpret_cast<float2 *>(smem + L.red_off);
+    float2 *slots = reinterpret_cast<float2 *>(smem + L.slot_off);
+    const int tid = threadIdx.x, lane = tid & 31;
+
+    const uint32_t rank = cluster_rank(), csize = cluster_size();
+    const int64_t cid = blockIdx.x / csize, ncl = gridDim.x / csize;
+    // every row is nvec whole vectors; this block owns vectors [s0, s1) of each
+    const int64_t nvec = cols / V;
+    const int64_t per = (nvec + csize - 1) / csize;
+    const int64_t s0 = min((int64_t)rank * per, nvec), s1 = min(s0 + per, nvec);
+    const int nmine = (int)(s1 - s0);
+    const uint32_t bytes = (uint32_t)nmine * kVecBytes;
+    // rows cid, cid + ncl, ... (the same count for every block of a cluster)
+    const int64_t nrows = rows > cid ? (rows - cid + ncl - 1) / ncl : 0;
+
+    if (tid == 0) {
+        for (int st = 0; st < stages; ++st) mbar_init(bar_base + 8 * st, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // producer (thread 0): load this block's slice of local row i into slot i % stages
+    auto issue = [&](int64_t i) {
+        const int st = (int)(i % stages);
+        const uint32_t bar = bar_base + 8 * st;
+        if (starve) return;  // test hook: the slot is never armed
+        if (bytes == 0) {
+            mbar_arrive(bar);
+            return;
+        }
+        mbar_arrive_expect_tx(bar, bytes);
+        const char *src = reinterpret_cast<const char *>(in + (cid + i * ncl) * stride + s0 * V);
+        const uint32_t dst = stage_base + (uint32_t)(st * L.stage_bytes);
+        for (uint32_t off = 0; off < bytes; off += kBulkPiece)
+            bulk_g2s(dst + off, src + off, min(kBulkPiece, bytes - off), bar);
+    };
+    if (tid == 0)
+        for (int64_t i = 0; i < min((int64_t)stages, nrows); ++i) issue(i);
+    if (csize > 1) {  // this block runs: peers may push into its slots once they waited
+        __syncwarp();
+        cluster_arrive_relaxed();
+    }
+
+    bool timed_out = false;
+    for (int64_t i = 0; i < nrows; ++i) {
+        const int st = (int)(i % stages);
+        const bool ok = mbar_wait_bounded(bar_base + 8 * st, (uint32_t)((i / stages) & 1), wait_ns);
+        if (!ok) {
+            atomicOr(&g_error_word, kErrWaitTimeout);
+            timed_out = true;
+        }
+        const uint4 *slot = reinterpret_cast<const uint4 *>(smem + st * L.stage_bytes);
+        Tile<T, VPT> tile;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = tid + j * THREADS;
+            if (v < nmine) {
+                Elem<T>::unpack(slot[v], tile.x[j]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < V; ++k) tile.x[j][k] = -INFINITY;
+            }
+        }
+        const float2 s = tile.exp_in_place();
+        float m = s.x, l = s.y;
+        block_merge<NW>(m, l, red + (i & 1) * NW);  // its barrier also frees slot st
+        if (tid == 0 && i + stages < nrows) {
+            fence_proxy_async_smem();
+            issue(i + stages);
+        }
+        if (csize > 1) {
+            if (i == 0) cluster_wait_acquire();
+            float2 *sl = slots + (i & 1) * kMaxCluster;
+            if (tid == 0) {
+                const uint32_t mine = smem_addr(sl + rank);
+                for (uint32_t q = 0; q < csize; ++q) st_cluster_f2(map_to_rank(mine, q), m, l);
+            }
+            __syncwarp();
+            cluster_arrive_release();
+            cluster_wait_acquire();
+            const float2 w = lane < (int)csize ? sl[lane] : make_float2(-INFINITY, 0.f);
+            m = w.x;
+            l = w.y;
+            group_merge<32>(m, l);
+        }
+        if (ok) {
+            const float f = out_factor(s.x, m, l);
+            T *orow = out + (cid + i * ncl) * stride + s0 * V;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int v = tid + j * THREADS;
+                if (v < nmine) {
+                    float y[V];
+#pragma unroll
+                    for (int k = 0; k < V; ++k) y[k] = tile.x[j][k] * f;
+                    *reinterpret_cast<uint4 *>(orow + (int64_t)v * V) = Elem<T>::pack(y);
+                }
+            }
+        }
+    }
+    // after a wait that ran out, copies may still be landing: wait for them
+    // (bounded) before the block's shared memory is released
+    if (timed_out && !starve && tid == 0) {
+        for (int64_t i = max((int64_t)0, nrows - stages); i < nrows; ++i)
+            mbar_wait_bounded(bar_base + 8 * (int)(i % stages), (uint32_t)((i / stages) & 1), wait_ns);
+    }
 }
 
 // ---------------------------------------------------------------------------

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 namespace mbrs {
 
 struct LaunchArgs {
@@ -29,6 +31,18 @@ int64_t cluster_smem_bytes(int threads, int vpt);
 cudaError_t launch_cluster(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns, int starve);
 // read this device's error word after synchronising `stream`, then clear it
 cudaError_t read_clear_error_word(cudaStream_t stream, unsigned int *word);
+
+// path 5: persistent TMA ring.  grid (out) is the persistent grid actually
+// used; with a.in == nullptr nothing is launched (grid query only).
+struct RingCfg {
+    int threads, vpt, csize, stages, slice_vecs;
+    int64_t smem;
+};
+bool ring_shape_ok(int threads, int vpt);
+int64_t ring_smem_bytes(int stages, int slice_vecs, int threads);
+cudaError_t launch_ring(const LaunchArgs &a, const RingCfg &c, int64_t wait_ns, int starve, int64_t *grid);
+// read this translation unit's device error word (after a stream sync), then clear it
+cudaError_t read_clear_ring_error_word(unsigned int *word);
 
 bool split_shape_ok(int threads, int vpt);
 cudaError_t launch_split(const LaunchArgs &a, int threads, int vpt, int64_t chunks, int64_t chunk_vecs,

@@ -45,7 +45,7 @@ def test_status_strings():
     for s in range(11):
         assert B.status_string(s) and B.status_string(s) != "unknown status"
     assert B.status_string(99) == "unknown status"
-    assert B.abi_version() == 10000
+    assert B.abi_version() == 10100
 
 
 @pytest.mark.parametrize("args,expect", [
@@ -97,6 +97,12 @@ def test_plans_cover_every_row(rows, cols, stride, dt, in_off):
         assert p["grid"] * p["threads"] // p["group"] >= min(rows, p["grid"] * p["threads"] // p["group"])
     elif path == B.PATH_CTA:
         assert p["threads"] * p["vpt"] >= nv and p["grid"] == rows
+    elif path == B.PATH_RING:
+        assert (stride * es) % 16 == 0 and (cols * es) % 16 == 0 and in_off == 0
+        slice_ = -(-nv // p["group"])
+        assert 1 <= p["group"] <= 16 and p["threads"] * p["vpt"] >= slice_
+        assert p["stages"] >= 2 and p["smem_bytes"] >= p["stages"] * slice_ * 16
+        assert p["smem_bytes"] <= 227 * 1024 and p["grid"] % p["group"] == 0
     elif path == B.PATH_CLUSTER:
         assert 1 <= p["group"] <= 16 and -(-nv // p["group"]) <= p["threads"] * p["vpt"]
         assert p["grid"] == rows * p["group"] and p["smem_bytes"] <= 227 * 1024
@@ -110,9 +116,12 @@ def test_dispatch_follows_width_rule():
     plan = lambda r, c, dt="f32": B.plan(1 << 24, 1 << 40, r, c, c, dt, num_sms=152)["path"]
     assert plan(64, 1000) == B.PATH_WARP          # cols <= 1024: a warp per row
     assert plan(64, 1024) == B.PATH_WARP
-    assert plan(64, 1025) == B.PATH_CTA           # medium rows: a block per row
-    assert plan(4096, 16384) == B.PATH_CTA
-    assert plan(512, 131072, "bf16") == B.PATH_CLUSTER   # long rows, enough of them
+    assert plan(64, 1025) == B.PATH_CTA           # misaligned medium rows: a block per row
+    assert plan(4096, 16391) == B.PATH_CTA
+    assert plan(4096, 2048, "f16") == B.PATH_RING        # aligned rows: the TMA ring
+    assert plan(4096, 16384) == B.PATH_RING
+    assert plan(512, 131072, "bf16") == B.PATH_RING      # long rows: ring of clusters
+    assert plan(512, 131079, "bf16") == B.PATH_CLUSTER   # long misaligned rows, enough of them
     assert plan(4, 131072, "bf16") == B.PATH_SPLIT       # too few rows to fill the GPU
     assert plan(64, 1 << 22) == B.PATH_SPLIT             # too long for a cluster
 
@@ -128,6 +137,11 @@ def test_forced_paths_and_rejections():
         B.set_force_path(B.PATH_CLUSTER, 256, 2, 2)
         with pytest.raises(B.SoftmaxError):
             B.plan(1 << 24, 1 << 40, 64, 5000, 5000, "f32", num_sms=152)
+        B.set_force_path(B.PATH_RING)
+        with pytest.raises(B.SoftmaxError):   # misaligned rows cannot ride the ring
+            B.plan(1 << 24, 1 << 40, 64, 5001, 5001, "f32", num_sms=152)
+        with pytest.raises(B.SoftmaxError):   # nor can an out with another 16-byte phase
+            B.plan(1 << 24, (1 << 40) + 4, 64, 5000, 5000, "f32", num_sms=152)
         with pytest.raises(B.SoftmaxError):
             B.set_force_path(9)
     finally:

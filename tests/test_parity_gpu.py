@@ -69,6 +69,7 @@ FORCED = {
     B.PATH_CTA: [1, 9, 100, 1025, 2047, 4096, 4103, 8199, 16384],
     B.PATH_CLUSTER: [1, 100, 2048, 9000, 16391, 65536, 131079],
     B.PATH_SPLIT: [1, 100, 4103, 65536, 262147],
+    B.PATH_RING: [8, 1024, 2048, 4096, 8192, 65536, 131072],
 }
 
 
@@ -89,7 +90,36 @@ def test_cluster_sizes(dtype, group):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("threads,vpt", [(64, 8), (128, 2), (512, 4), (1024, 2)])
+@pytest.mark.parametrize("group", [1, 2, 3, 5, 8, 16])
+@pytest.mark.parametrize("rows", [3, 700])
+def test_ring_cluster_sizes(dtype, group, rows):
+    # 700 rows: every block walks its ring of stages many times (slot reuse,
+    # mbarrier phase flips, double-buffered exchange slots)
+    res = run_and_compare(rnd(rows, 4096, dtype, seed=group + rows), dtype, path=B.PATH_RING, group=group)
+    assert res["path"] == B.PATH_RING
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("threads,vpt", [(64, 1), (128, 4), (1024, 4), (256, 2), (512, 1)])
+@pytest.mark.parametrize("fill", ["full", "one_vector_short"])
+def test_ring_shapes(dtype, threads, vpt, fill):
+    V = 4 if dtype == "f32" else 8
+    cols = threads * vpt * V - (V if fill == "one_vector_short" else 0)
+    res = run_and_compare(rnd(1500, cols, dtype, seed=threads + cols), dtype, path=B.PATH_RING, threads=threads,
+                          vpt=vpt)
+    assert res["path"] == B.PATH_RING
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_ring_rejects_misaligned_rows(dtype):
+    case = DeviceCase(rnd(4, 4096, dtype, 2), dtype, in_off=1)
+    assert case.run(4096, path=B.PATH_RING) == B.ERR_UNSUPPORTED
+    case = DeviceCase(rnd(4, 4096, dtype, 2), dtype, out_off=1)
+    assert case.run(4096, path=B.PATH_RING) == B.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("threads,vpt", [(64, 8), (128, 2), (512, 4), (1024, 2), (256, 3), (1024, 5)])
 def test_cta_shapes(dtype, threads, vpt):
     cols = {"f32": 4 * threads * vpt - 5, "f16": 8 * threads * vpt - 9, "bf16": 8 * threads * vpt - 9}[dtype]
     res = run_and_compare(rnd(3, cols, dtype, seed=threads + vpt), dtype, path=B.PATH_CTA, threads=threads, vpt=vpt)
@@ -126,10 +156,13 @@ def test_padded_strides(dtype, cols, extra):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("path", [0, B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_SPLIT])
+@pytest.mark.parametrize("path", [0, B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_SPLIT, B.PATH_RING])
 def test_in_place(dtype, path):
     cols = 1000 if path in (0, B.PATH_WARP) else 6007
-    run_and_compare(rnd(6, cols, dtype, seed=path), dtype, inplace=True, in_off=1, path=path)
+    off = 1
+    if path == B.PATH_RING:
+        cols, off = 6016, 0
+    run_and_compare(rnd(300, cols, dtype, seed=path), dtype, inplace=True, in_off=off, path=path)
 
 
 def test_partial_overlap_is_rejected():
@@ -166,7 +199,8 @@ def _result_bits(x, dtype, path):
 
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("path,cols", [(B.PATH_WARP, 33), (B.PATH_WARP, 1000), (B.PATH_CTA, 3000),
-                                       (B.PATH_CLUSTER, 20000), (B.PATH_SPLIT, 20000)])
+                                       (B.PATH_CLUSTER, 20000), (B.PATH_SPLIT, 20000), (B.PATH_RING, 4096),
+                                       (B.PATH_RING, 65536)])
 def test_special_values(dtype, path, cols):
     x = special_rows(dtype, cols)
     run_and_compare(x, dtype, path=path)
@@ -231,18 +265,19 @@ def test_offsets_beyond_int32():
 
 # -- the bounded wait and the device error word ------------------------------------------
 
-def test_wait_timeout_is_reported_and_recoverable():
+@pytest.mark.parametrize("path,group", [(B.PATH_CLUSTER, 0), (B.PATH_RING, 1), (B.PATH_RING, 4)])
+def test_wait_timeout_is_reported_and_recoverable(path, group):
     x = rnd(4, 20000, "bf16", seed=5)
     c = DeviceCase(x, "bf16")
-    B.set_wait_test(1_000_000, starve=True)  # 1 ms, and the TMA barrier is never armed
+    B.set_wait_test(1_000_000, starve=True)  # 1 ms, and the TMA barriers are never armed
     try:
-        assert c.run(20000, path=B.PATH_CLUSTER) == B.OK
+        assert c.run(20000, path=path, group=group) == B.OK
         assert B.check_device_error() == B.ERR_TIMEOUT
     finally:
         B.set_wait_test(0, False)
     assert B.check_device_error() == B.OK
     # outputs were skipped, the context is still usable and the next call is exact
-    run_and_compare(x, "bf16", path=B.PATH_CLUSTER)
+    run_and_compare(x, "bf16", path=path, group=group)
 
 
 # -- the tensor-level binding --------------------------------------------------------------
@@ -261,7 +296,10 @@ def test_torch_binding(tdtype, name):
     B.softmax_fwd(z, z)
     assert torch.equal(z, y)
     big = torch.randn(8, 4000, device="cuda").to(tdtype)
-    view = big[:, 100:3100]  # a strided view: row stride 4000
-    assert torch.equal(B.softmax_fwd(view), B.softmax_fwd(view.contiguous()))
+    view = big[:, 100:3100]  # a strided, differently aligned view: row stride 4000
+    tol = {"f32": 1e-6, "f16": 1e-3, "bf16": 4e-3}[name]
+    vref = torch.softmax(view.double(), dim=1)
+    assert (B.softmax_fwd(view).double() - vref).abs().max().item() <= tol
+    assert (B.softmax_fwd(view.contiguous()).double() - vref).abs().max().item() <= tol
     with pytest.raises(ValueError):
         B.softmax_fwd(x.t())
