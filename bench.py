@@ -250,6 +250,8 @@ def run_ours(args) -> dict | None:
         if st != 0:
             raise B.SoftmaxError(st)
 
+    if args.force:
+        B.set_force_path(*[int(v) for v in args.force.split(",")])
     plan = B.plan(x_dev.data_ptr(), x_dev.data_ptr() + (1 << 40), w.rows, w.cols, w.stride, code)
     set_bytes = 2 * x_dev.numel() * x_dev.element_size()
     sets = rotating_sets(x_dev, set_bytes, l2)
@@ -408,10 +410,12 @@ def per_shape(args, peaks, l2, dev) -> dict:
         set_bytes = 2 * xd.numel() * xd.element_size()
         sets = rotating_sets(xd, set_bytes, l2)
         med, _, _ = time_steps(launch, sets, 200, 50)
-        # the copy ceiling: rows*cols*elem bytes, device to device, same rotation
+        # the copy ceiling: rows*cols*elem bytes (as 4-byte words), device to
+        # device, same rotation
         nbytes = w.rows * w.cols * w.elem_bytes
-        csets = [(torch.empty(nbytes, dtype=torch.uint8, device=dev), torch.empty(nbytes, dtype=torch.uint8, device=dev))
-                 for _ in range(max(2, -(-int(2.5 * l2) // (2 * nbytes))))]
+        nwords = -(-nbytes // 4)
+        csets = [(torch.empty(nwords, dtype=torch.int32, device=dev), torch.empty(nwords, dtype=torch.int32, device=dev))
+                 for _ in range(max(2, -(-int(2.5 * l2) // (8 * nwords))))]
         cmed, _, _ = time_steps(lambda a, b: b.copy_(a), csets, 200, 50)
         gbs = plan["hbm_bytes"] / (med / 1e3) / 1e9
         alg = w.algorithmic_bytes / (med / 1e3) / 1e9
@@ -483,6 +487,8 @@ def main(argv=None):
     ap.add_argument("--no-per-shape", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="add the fp32 width sweep to the per-shape table")
+    ap.add_argument("--force", default="",
+                    help="path[,threads,vpt,group]: force a kernel path and launch shape (profiling, tuning)")
     ap.add_argument("--only-kernel", action="store_true",
                     help="warm-up and timed launches only (the command profiled with ncu)")
     ap.add_argument("--json-out", default="")

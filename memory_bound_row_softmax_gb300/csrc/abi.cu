@@ -188,22 +188,22 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
         }
         case SOFTMAX_PATH_RING: {
             if (!ring_ok) return SOFTMAX_ERR_UNSUPPORTED;
-            // cluster size: enough blocks for the row's registers (<= 4096 vectors
-            // each), more while the rows alone cannot occupy every SM
-            int64_t csize = fgrp > 0 ? fgrp : std::max<int64_t>(1, cdiv(nv, 4096));
+            // cluster size: slices of at most 512 x 4 vectors (1024 x 4 if a row
+            // needs more than 16 such slices), more blocks while the rows alone
+            // cannot occupy every SM
+            int64_t csize = fgrp > 0 ? fgrp : std::max<int64_t>(1, cdiv(nv, cdiv(nv, 2048) <= 16 ? 2048 : 4096));
             if (fgrp <= 0)
                 while (csize < 16 && rows * csize < sms && cdiv(nv, csize * 2) >= 256) csize *= 2;
             if (csize < 1 || csize > 16) return SOFTMAX_ERR_UNSUPPORTED;
             const int64_t slice = cdiv(nv, csize);
-            int vpt = fvpt > 0 ? fvpt : (slice <= 1024 ? 2 : 4);
+            // 4 vectors per thread (fewer only for slices under 256 vectors)
+            int vpt = fvpt > 0 ? fvpt : (int)std::min<int64_t>(4, cdiv(slice, 64));
+            if (vpt == 3) vpt = 4;
             int threads = fth > 0 ? fth : std::max(64, next_pow2(cdiv(slice, vpt)));
-            if (fth <= 0 && threads > 1024) {
-                vpt = 4;
-                threads = next_pow2(cdiv(slice, 4));
-            }
             if (!ring_shape_ok(threads, vpt) || (int64_t)threads * vpt < slice) return SOFTMAX_ERR_UNSUPPORTED;
             const int64_t stage_bytes = slice * kVecBytes;
-            int per_sm = std::max(1, std::min(4, 2048 / threads));
+            // blocks per SM the ring aims for: 1024 threads' worth (<= 64 registers each)
+            int per_sm = std::max(1, std::min(8, 1024 / threads));
             int64_t stages = 0;
             for (; per_sm >= 1; --per_sm) {
                 stages = (kRingSmemPerSm / per_sm - 1024) / stage_bytes;

@@ -81,6 +81,31 @@ cudaError_t per_wave(int device, int csize, int64_t smem, int64_t *out) {
     return cudaSuccess;
 }
 
+int sms_of(int device) {
+    int sms = 1;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    return sms > 0 ? sms : 1;
+}
+
+// Persistent units (blocks, or clusters) for `rows` rows given that at most
+// `wave` fit at once.  Each unit walks ceil(rows / U) rows and the call lasts
+// about as long as its busiest unit, so take the U in [wave/2, wave] with the
+// least ceil(rows/U) * U (the most even split), the larger on ties.  Single
+// blocks are counted in whole SMs (`step` = SMs) so every SM gets as many.
+int64_t balanced_units(int64_t rows, int64_t wave, int64_t step) {
+    if (rows <= wave) return rows;
+    int64_t best = wave, best_cost = INT64_MAX;
+    const int64_t lo = std::max<int64_t>(step, wave / 2);
+    for (int64_t u = (wave / step) * step; u >= lo; u -= step) {
+        const int64_t cost = ((rows + u - 1) / u) * u;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = u;
+        }
+    }
+    return best;
+}
+
 template <typename T, int THREADS, int VPT>
 cudaError_t go(const LaunchArgs &a, const RingCfg &c, int64_t wait_ns, int starve, int64_t *grid_out) {
     int device = 0;
@@ -89,7 +114,7 @@ cudaError_t go(const LaunchArgs &a, const RingCfg &c, int64_t wait_ns, int starv
     int64_t wave = 0;
     if (e == cudaSuccess) e = per_wave<T, THREADS, VPT>(device, c.csize, c.smem, &wave);
     if (e != cudaSuccess) return e;
-    const int64_t units = std::min<int64_t>(a.rows, wave);  // blocks (or clusters), each >= 1 row
+    const int64_t units = balanced_units(a.rows, wave, c.csize == 1 ? sms_of(device) : 1);
     const int64_t grid = units * c.csize;
     if (grid_out) *grid_out = grid;
     if (!a.in) return cudaSuccess;  // grid query only

@@ -48,7 +48,7 @@ WIDTHS = [1, 2, 3, 5, 7, 8, 9, 16, 31, 33, 63, 100, 255, 257, 1000, 1023, 1024, 
 def test_auto_widths(dtype, cols):
     rows = 5 if cols > 10000 else 7
     res = run_and_compare(rnd(rows, cols, dtype, seed=cols), dtype)
-    assert res["path"] in (B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_SPLIT)
+    assert res["path"] in (B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_SPLIT, B.PATH_RING)
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
