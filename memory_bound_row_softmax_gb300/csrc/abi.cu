@@ -56,6 +56,27 @@ int next_pow2(int64_t v) {
     return p;
 }
 
+// Threads of the block-per-row register kernel: the fewest (a power of two)
+// that need at most 4 vectors each.
+int cta_threads(int64_t nv) {
+    int threads = 64;
+    while (threads < 1024 && cdiv(nv, threads) > 4) threads *= 2;
+    return threads;
+}
+
+// Row bytes the block-per-row register kernel keeps in flight per SM: rows
+// resident at once (registers: the row widened to fp32 plus ~24 per thread)
+// times the row's bytes.  When this reaches ~96 KB the kernel already runs at
+// copy speed (measured: fp32 4096-wide rows); below it the shared-memory ring,
+// whose prefetch does not cost registers, keeps more bytes in flight.
+constexpr int64_t kRegInFlightEnough = 96 * 1024;
+int64_t cta_bytes_in_flight(int64_t nv, int es) {
+    const int threads = cta_threads(nv);
+    const int64_t regs = cdiv(nv, threads) * (kVecBytes / es) + 24;
+    const int64_t rows_per_sm = std::min<int64_t>(2048 / threads, 65536 / (threads * regs));
+    return rows_per_sm * nv * kVecBytes;
+}
+
 int elem_bytes(int dtype) { return dtype == SOFTMAX_F32 ? 4 : 2; }
 
 // Host-side argument checks, in the order the header documents.
@@ -120,7 +141,8 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
     if (path == SOFTMAX_PATH_AUTO) {
         if (cols <= 1024 && nv <= 32 * 9) {
             path = SOFTMAX_PATH_WARP;
-        } else if (ring_ok && cdiv(nv, 16) <= 4096 && rows * 16 * 2 >= sms) {
+        } else if (ring_ok && cdiv(nv, 16) <= 4096 && rows * 16 * 2 >= sms &&
+                   (nv > 4096 || cta_bytes_in_flight(nv, es) < kRegInFlightEnough)) {
             path = SOFTMAX_PATH_RING;
         } else if (nv <= 1024 * 5) {
             path = SOFTMAX_PATH_CTA;
@@ -160,11 +182,7 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
         case SOFTMAX_PATH_CTA: {
             // the fewest threads (a power of two) that need at most 4 vectors each
             // (5 at 1024 threads); vpt = what the row then needs, not a rounded-up 4
-            int threads = fth;
-            if (threads <= 0) {
-                threads = 64;
-                while (threads < 1024 && cdiv(nv, threads) > 4) threads *= 2;
-            }
+            int threads = fth > 0 ? fth : cta_threads(nv);
             int vpt = fvpt > 0 ? fvpt : std::max<int>(2, (int)cdiv(nv, threads));
             if (!cta_shape_ok(threads, vpt) || (int64_t)threads * vpt < nv) return SOFTMAX_ERR_UNSUPPORTED;
             p->threads = threads;
@@ -188,10 +206,11 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
         }
         case SOFTMAX_PATH_RING: {
             if (!ring_ok) return SOFTMAX_ERR_UNSUPPORTED;
-            // cluster size: slices of at most 512 x 4 vectors (1024 x 4 if a row
-            // needs more than 16 such slices), more blocks while the rows alone
-            // cannot occupy every SM
-            int64_t csize = fgrp > 0 ? fgrp : std::max<int64_t>(1, cdiv(nv, cdiv(nv, 2048) <= 16 ? 2048 : 4096));
+            // cluster size: slices of at most 1024 x 4 vectors for fp32 and 512 x 4
+            // for 16-bit data (whose 1024-thread ring would spill at 64 registers),
+            // more blocks while the rows alone cannot occupy every SM
+            const int64_t max_slice = (es == 4 || cdiv(nv, 2048) > 16) ? 4096 : 2048;
+            int64_t csize = fgrp > 0 ? fgrp : std::max<int64_t>(1, cdiv(nv, max_slice));
             if (fgrp <= 0)
                 while (csize < 16 && rows * csize < sms && cdiv(nv, csize * 2) >= 256) csize *= 2;
             if (csize < 1 || csize > 16) return SOFTMAX_ERR_UNSUPPORTED;

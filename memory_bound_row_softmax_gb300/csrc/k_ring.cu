@@ -114,7 +114,9 @@ cudaError_t go(const LaunchArgs &a, const RingCfg &c, int64_t wait_ns, int starv
     int64_t wave = 0;
     if (e == cudaSuccess) e = per_wave<T, THREADS, VPT>(device, c.csize, c.smem, &wave);
     if (e != cudaSuccess) return e;
-    const int64_t units = balanced_units(a.rows, wave, c.csize == 1 ? sms_of(device) : 1);
+    // single blocks: an even split of rows over whole SMs; clusters: the full
+    // wave, so that their blocks sit evenly on the SMs
+    const int64_t units = c.csize == 1 ? balanced_units(a.rows, wave, sms_of(device)) : std::min(a.rows, wave);
     const int64_t grid = units * c.csize;
     if (grid_out) *grid_out = grid;
     if (!a.in) return cudaSuccess;  // grid query only

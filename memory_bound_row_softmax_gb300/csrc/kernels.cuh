@@ -207,14 +207,16 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
 // path 5: persistent TMA ring (a block or a cluster per row, many rows each)
 // ---------------------------------------------------------------------------
 // Shared memory: `stages` slots of slice_vecs 16-byte vectors, one mbarrier
-// per slot, the block-merge scratch (2 x NW states) and the cluster exchange
-// slots (2 x 16 states); the last two are double-buffered by row parity.
+// per slot, two exchange mbarriers, the block-merge scratch (2 x NW states)
+// and the cluster exchange slots (2 x 16 states); the last three are
+// double-buffered by row parity.
 struct RingLayout {
-    int64_t stage_bytes, bar_off, red_off, slot_off, bytes;
+    int64_t stage_bytes, bar_off, xbar_off, red_off, slot_off, bytes;
     __host__ __device__ RingLayout(int stages, int slice_vecs, int threads) {
         stage_bytes = (int64_t)slice_vecs * kVecBytes;
         bar_off = stage_bytes * stages;
-        red_off = bar_off + 8 * stages;
+        xbar_off = bar_off + 8 * stages;
+        red_off = xbar_off + 16;
         red_off = (red_off + 15) & ~int64_t(15);
         slot_off = red_off + 2 * (threads / 32) * 8;
         bytes = slot_off + 2 * kMaxCluster * 8;
@@ -246,8 +248,11 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 512 ? 1 : 512 / THREADS))
     // rows cid, cid + ncl, ... (the same count for every block of a cluster)
     const int64_t nrows = rows > cid ? (rows - cid + ncl - 1) / ncl : 0;
 
+    const uint32_t xbar_base = smem_addr(smem + L.xbar_off);
     if (tid == 0) {
         for (int st = 0; st < stages; ++st) mbar_init(bar_base + 8 * st, 1);
+        mbar_init(xbar_base, 1);
+        mbar_init(xbar_base + 8, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -269,9 +274,10 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 512 ? 1 : 512 / THREADS))
     };
     if (tid == 0)
         for (int64_t i = 0; i < min((int64_t)stages, nrows); ++i) issue(i);
-    if (csize > 1) {  // this block runs: peers may push into its slots once they waited
+    if (csize > 1) {  // every block's exchange barriers are initialised before any peer sends
         __syncwarp();
-        cluster_arrive_relaxed();
+        cluster_arrive_release();
+        cluster_wait_acquire();
     }
 
     bool timed_out = false;
@@ -301,22 +307,33 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 512 ? 1 : 512 / THREADS))
             fence_proxy_async_smem();
             issue(i + stages);
         }
+        bool xok = true;
         if (csize > 1) {
-            if (i == 0) cluster_wait_acquire();
+            // Exchange without a cluster barrier: every block sends its state into
+            // slot `rank` of every peer (itself included) with st.async, which
+            // completes on the receiver's exchange barrier for this row's parity;
+            // each block then waits for its own barrier to have seen csize states.
+            // Slots and barriers alternate by row parity: a peer can only send
+            // row i+2's state after it received ours for row i+1, which we send
+            // after reading row i's slots.
             float2 *sl = slots + (i & 1) * kMaxCluster;
+            const uint32_t xbar = xbar_base + 8 * (uint32_t)(i & 1);
             if (tid == 0) {
+                mbar_arrive_expect_tx(xbar, csize * 8u);
                 const uint32_t mine = smem_addr(sl + rank);
-                for (uint32_t q = 0; q < csize; ++q) st_cluster_f2(map_to_rank(mine, q), m, l);
+                for (uint32_t q = 0; q < csize; ++q) st_async_f2(map_to_rank(mine, q), m, l, map_to_rank(xbar, q));
             }
-            __syncwarp();
-            cluster_arrive_release();
-            cluster_wait_acquire();
+            xok = mbar_wait_bounded(xbar, (uint32_t)((i >> 1) & 1), wait_ns);
+            if (!xok) {
+                atomicOr(&g_error_word, kErrWaitTimeout);
+                timed_out = true;
+            }
             const float2 w = lane < (int)csize ? sl[lane] : make_float2(-INFINITY, 0.f);
             m = w.x;
             l = w.y;
             group_merge<32>(m, l);
         }
-        if (ok) {
+        if (ok && xok) {
             const float f = out_factor(s.x, m, l);
             T *orow = out + (cid + i * ncl) * stride + s0 * V;
 #pragma unroll
@@ -336,6 +353,11 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 512 ? 1 : 512 / THREADS))
     if (timed_out && !starve && tid == 0) {
         for (int64_t i = max((int64_t)0, nrows - stages); i < nrows; ++i)
             mbar_wait_bounded(bar_base + 8 * (int)(i % stages), (uint32_t)((i / stages) & 1), wait_ns);
+    }
+    if (csize > 1) {  // no block leaves while a peer may still address its shared memory
+        __syncwarp();
+        cluster_arrive_release();
+        cluster_wait_acquire();
     }
 }
 
