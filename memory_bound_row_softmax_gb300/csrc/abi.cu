@@ -219,7 +219,13 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             int vpt = fvpt > 0 ? fvpt : (int)std::min<int64_t>(4, cdiv(slice, 64));
             if (vpt == 3) vpt = 4;
             int threads = fth > 0 ? fth : std::max(64, next_pow2(cdiv(slice, vpt)));
-            if (!ring_shape_ok(threads, vpt) || (int64_t)threads * vpt < slice) return SOFTMAX_ERR_UNSUPPORTED;
+            if (csize > 1 && fth <= 0 && threads < 256) {  // cluster rings start at 256 threads
+                threads = 256;
+                vpt = (int)std::max<int64_t>(2, cdiv(slice, 256));
+                if (vpt == 3) vpt = 4;
+            }
+            if (!ring_shape_ok(threads, vpt, (int)csize) || (int64_t)threads * vpt < slice)
+                return SOFTMAX_ERR_UNSUPPORTED;
             const int64_t stage_bytes = slice * kVecBytes;
             // blocks per SM the ring aims for: 1024 threads' worth (<= 64 registers each)
             int per_sm = std::max(1, std::min(8, 1024 / threads));

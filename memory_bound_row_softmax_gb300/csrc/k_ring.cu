@@ -13,14 +13,14 @@ namespace mbrs {
 namespace {
 constexpr int kMaxDevices = 64;
 
-template <typename T, int THREADS, int VPT>
+template <typename T, int THREADS, int VPT, bool CL>
 cudaError_t prepare(int device) {
     static std::atomic<unsigned long long> done{0};
     const unsigned long long bit = 1ull << (device & (kMaxDevices - 1));
     if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
     int optin = 0;
     cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
-    auto fn = k_ring_rows<T, THREADS, VPT>;
+    auto fn = k_ring_rows<T, THREADS, VPT, CL>;
     if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
@@ -36,11 +36,11 @@ struct GridKey {
 };
 
 // Co-resident blocks (or clusters) of this kernel on the current device.
-template <typename T, int THREADS, int VPT>
+template <typename T, int THREADS, int VPT, bool CL>
 cudaError_t per_wave(int device, int csize, int64_t smem, int64_t *out) {
     static std::mutex mu;
     static std::vector<GridKey> cache;
-    const void *fn = reinterpret_cast<const void *>(k_ring_rows<T, THREADS, VPT>);
+    const void *fn = reinterpret_cast<const void *>(k_ring_rows<T, THREADS, VPT, CL>);
     {
         std::lock_guard<std::mutex> lock(mu);
         for (const auto &k : cache)
@@ -52,7 +52,7 @@ cudaError_t per_wave(int device, int csize, int64_t smem, int64_t *out) {
     int64_t n = 0;
     if (csize == 1) {
         int per_sm = 0, sms = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_ring_rows<T, THREADS, VPT>,
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_ring_rows<T, THREADS, VPT, CL>,
                                                                       THREADS, (size_t)smem);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
         if (e != cudaSuccess) return e;
@@ -70,7 +70,7 @@ cudaError_t per_wave(int device, int csize, int64_t smem, int64_t *out) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int clusters = 0;
-        cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, k_ring_rows<T, THREADS, VPT>, &cfg);
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, k_ring_rows<T, THREADS, VPT, CL>, &cfg);
         if (e != cudaSuccess) return e;
         n = clusters;
     }
@@ -106,13 +106,13 @@ int64_t balanced_units(int64_t rows, int64_t wave, int64_t step) {
     return best;
 }
 
-template <typename T, int THREADS, int VPT>
+template <typename T, int THREADS, int VPT, bool CL>
 cudaError_t go(const LaunchArgs &a, const RingCfg &c, int64_t wait_ns, int starve, int64_t *grid_out) {
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
-    if (e == cudaSuccess) e = prepare<T, THREADS, VPT>(device);
+    if (e == cudaSuccess) e = prepare<T, THREADS, VPT, CL>(device);
     int64_t wave = 0;
-    if (e == cudaSuccess) e = per_wave<T, THREADS, VPT>(device, c.csize, c.smem, &wave);
+    if (e == cudaSuccess) e = per_wave<T, THREADS, VPT, CL>(device, c.csize, c.smem, &wave);
     if (e != cudaSuccess) return e;
     // single blocks: an even split of rows over whole SMs; clusters: the full
     // wave, so that their blocks sit evenly on the SMs
@@ -132,7 +132,7 @@ cudaError_t go(const LaunchArgs &a, const RingCfg &c, int64_t wait_ns, int starv
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = c.csize > 1 ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, k_ring_rows<T, THREADS, VPT>, static_cast<const T *>(a.in),
+    e = cudaLaunchKernelEx(&cfg, k_ring_rows<T, THREADS, VPT, CL>, static_cast<const T *>(a.in),
                            static_cast<T *>(a.out), a.rows, a.cols, a.stride, c.stages, c.slice_vecs, wait_ns,
                            starve);
     if (e != cudaSuccess) return e;
@@ -141,10 +141,17 @@ cudaError_t go(const LaunchArgs &a, const RingCfg &c, int64_t wait_ns, int starv
 
 template <typename T, int THREADS>
 cudaError_t by_vpt(const LaunchArgs &a, const RingCfg &c, int64_t w, int s, int64_t *g) {
+    if (c.csize > 1) {  // cluster rings: 256..1024 threads, 2 or 4 vectors each
+        if constexpr (THREADS >= 256) {
+            if (c.vpt == 2) return go<T, THREADS, 2, true>(a, c, w, s, g);
+            if (c.vpt == 4) return go<T, THREADS, 4, true>(a, c, w, s, g);
+        }
+        return cudaErrorInvalidValue;
+    }
     switch (c.vpt) {
-        case 1: return go<T, THREADS, 1>(a, c, w, s, g);
-        case 2: return go<T, THREADS, 2>(a, c, w, s, g);
-        case 4: return go<T, THREADS, 4>(a, c, w, s, g);
+        case 1: return go<T, THREADS, 1, false>(a, c, w, s, g);
+        case 2: return go<T, THREADS, 2, false>(a, c, w, s, g);
+        case 4: return go<T, THREADS, 4, false>(a, c, w, s, g);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -162,8 +169,9 @@ cudaError_t by_shape(const LaunchArgs &a, const RingCfg &c, int64_t w, int s, in
 }
 }  // namespace
 
-bool ring_shape_ok(int threads, int vpt) {
+bool ring_shape_ok(int threads, int vpt, int csize) {
     const bool t = threads == 64 || threads == 128 || threads == 256 || threads == 512 || threads == 1024;
+    if (csize > 1) return threads >= 256 && t && (vpt == 2 || vpt == 4);
     return t && (vpt == 1 || vpt == 2 || vpt == 4);
 }
 

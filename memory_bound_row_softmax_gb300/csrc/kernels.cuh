@@ -223,8 +223,12 @@ struct RingLayout {
     }
 };
 
-template <typename T, int THREADS, int VPT>
-__global__ void __launch_bounds__(THREADS, (THREADS >= 512 ? 1 : 512 / THREADS))
+// CLUSTER = false: one block per row (no exchange code, fewer registers);
+// CLUSTER = true: launched with clusters of csize blocks, each owning a slice,
+// bounded to 64 registers so two 512-thread blocks fit on an SM.
+template <typename T, int THREADS, int VPT, bool CLUSTER>
+__global__ void __launch_bounds__(THREADS, CLUSTER ? (THREADS >= 1024 ? 1 : 1024 / THREADS)
+                                                   : (THREADS >= 512 ? 1 : 512 / THREADS))
     k_ring_rows(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int stages, int slice_vecs,
                 int64_t wait_ns, int starve) {
     constexpr int V = Elem<T>::kVec;
@@ -237,7 +241,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 512 ? 1 : 512 / THREADS))
     float2 *slots = reinterpret_cast<float2 *>(smem + L.slot_off);
     const int tid = threadIdx.x, lane = tid & 31;
 
-    const uint32_t rank = cluster_rank(), csize = cluster_size();
+    const uint32_t rank = CLUSTER ? cluster_rank() : 0u, csize = CLUSTER ? cluster_size() : 1u;
     const int64_t cid = blockIdx.x / csize, ncl = gridDim.x / csize;
     // every row is nvec whole vectors; this block owns vectors [s0, s1) of each
     const int64_t nvec = cols / V;
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 512 ? 1 : 512 / THREADS))
     };
     if (tid == 0)
         for (int64_t i = 0; i < min((int64_t)stages, nrows); ++i) issue(i);
-    if (csize > 1) {  // every block's exchange barriers are initialised before any peer sends
+    if (CLUSTER) {  // every block's exchange barriers are initialised before any peer sends
         __syncwarp();
         cluster_arrive_release();
         cluster_wait_acquire();
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 512 ? 1 : 512 / THREADS))
             issue(i + stages);
         }
         bool xok = true;
-        if (csize > 1) {
+        if (CLUSTER) {
             // Exchange without a cluster barrier: every block sends its state into
             // slot `rank` of every peer (itself included) with st.async, which
             // completes on the receiver's exchange barrier for this row's parity;
@@ -354,7 +358,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 512 ? 1 : 512 / THREADS))
         for (int64_t i = max((int64_t)0, nrows - stages); i < nrows; ++i)
             mbar_wait_bounded(bar_base + 8 * (int)(i % stages), (uint32_t)((i / stages) & 1), wait_ns);
     }
-    if (csize > 1) {  // no block leaves while a peer may still address its shared memory
+    if (CLUSTER) {  // no block leaves while a peer may still address its shared memory
         __syncwarp();
         cluster_arrive_release();
         cluster_wait_acquire();

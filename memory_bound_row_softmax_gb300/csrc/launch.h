@@ -38,7 +38,7 @@ struct RingCfg {
     int threads, vpt, csize, stages, slice_vecs;
     int64_t smem;
 };
-bool ring_shape_ok(int threads, int vpt);
+bool ring_shape_ok(int threads, int vpt, int csize);
 int64_t ring_smem_bytes(int stages, int slice_vecs, int threads);
 cudaError_t launch_ring(const LaunchArgs &a, const RingCfg &c, int64_t wait_ns, int starve, int64_t *grid);
 // read this translation unit's device error word (after a stream sync), then clear it
