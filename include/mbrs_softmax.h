@@ -71,7 +71,8 @@ typedef enum {
     SOFTMAX_ERR_CUDA = 7,        /* a CUDA runtime call or launch failed */
     SOFTMAX_ERR_TIMEOUT = 8,     /* a bounded device wait ran out (device error word) */
     SOFTMAX_ERR_ALIGN = 9,       /* in or out not aligned to its element size */
-    SOFTMAX_ERR_ARG = 10         /* a bad argument to a diagnostic call */
+    SOFTMAX_ERR_ARG = 10,        /* a bad argument to a diagnostic call */
+    SOFTMAX_ERR_SCRATCH_LIMIT = 11 /* softmax_fwd_noalloc: rows exceed its fixed scratch array */
 } softmax_status_t;
 
 /* Kernel paths the dispatcher chooses between. */
@@ -159,6 +160,38 @@ int softmax_check_device_error(cudaStream_t stream);
  * and returns normally.  Process-wide, not thread-safe.
  */
 int softmax_set_wait_test(int64_t wait_limit_ns, int starve);
+
+/*
+ * softmax_fwd_noalloc -- the same softmax for callers that cannot allocate
+ * device memory.  (The pages have no counterpart: this entry point answers a
+ * deployment constraint, not a step of the method.)
+ *
+ * softmax_fwd's split path takes a little scratch per call from a stream-
+ * ordered memory pool.  Some callers cannot allow that: code running under an
+ * allocator that a host framework owns exclusively, real-time loops where an
+ * allocation's latency or failure is not acceptable, or processes that must
+ * not grow their device footprint after start-up.  This entry point always
+ * runs the split path (two passes, 3 element crossings) with its per-chunk
+ * states in a fixed array of SOFTMAX_NOALLOC_MAX_STATES (s, l) pairs
+ * (512 KiB) compiled into the library; every GPU that loads the library holds
+ * that array until the process exits.  It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *   - Arguments, layout and status codes are those of softmax_fwd.  rows may
+ *     be at most SOFTMAX_NOALLOC_MAX_STATES; larger calls return
+ *     SOFTMAX_ERR_SCRATCH_LIMIT before any launch (each row needs at least one
+ *     state; chunks per row are reduced to fit).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the array and leaves its states there.
+ *     Nothing in it needs to start at zero: the second pass reads only states
+ *     the first pass of the same call wrote.  Calls whose kernels overlap on
+ *     the GPU (different streams, or graphs launched concurrently) race on the
+ *     array: serialise them.
+ */
+#define SOFTMAX_NOALLOC_MAX_STATES 65536
+int softmax_fwd_noalloc(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride,
+                        int dtype, cudaStream_t stream);
 
 /* Version of this ABI: major * 10000 + minor * 100 + patch (1.1.0 adds the RING path). */
 int softmax_abi_version(void);

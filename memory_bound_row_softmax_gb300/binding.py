@@ -14,7 +14,7 @@ import threading
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libmbrs_softmax.so")
 
 OK, ERR_NULL, ERR_SHAPE, ERR_STRIDE, ERR_DTYPE, ERR_OVERLAP, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_ALIGN, \
-    ERR_ARG = range(11)
+    ERR_ARG, ERR_SCRATCH_LIMIT = range(12)
 PATH_AUTO, PATH_WARP, PATH_CTA, PATH_CLUSTER, PATH_SPLIT, PATH_RING = range(6)
 PATH_NAMES = {PATH_WARP: "warp", PATH_CTA: "cta", PATH_CLUSTER: "cluster", PATH_SPLIT: "split", PATH_RING: "ring"}
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
@@ -41,6 +41,7 @@ SIGNATURES = {
     "softmax_check_device_error": (_int, [_vp]),
     "softmax_set_wait_test": (_int, [_i64, _int]),
     "softmax_abi_version": (_int, []),
+    "softmax_fwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp]),
 }
 
 _lib = None
@@ -87,6 +88,14 @@ def softmax_fwd_ptr(in_ptr: int, out_ptr: int, rows: int, cols: int, row_stride:
                     stream: int = 0) -> int:
     """Raw call: device addresses and sizes in, status out (no exception)."""
     return lib().softmax_fwd(in_ptr, out_ptr, rows, cols, row_stride, dtype, stream)
+
+
+def softmax_fwd_noalloc_ptr(in_ptr: int, out_ptr: int, rows: int, cols: int, row_stride: int, dtype: int,
+                            stream: int = 0) -> int:
+    """Raw call of the entry point that allocates nothing (for callers that
+    cannot allocate device memory; its scratch is a fixed array in the
+    library).  Status out, no exception."""
+    return lib().softmax_fwd_noalloc(in_ptr, out_ptr, rows, cols, row_stride, dtype, stream)
 
 
 def softmax_fwd(x, out=None, stream=None):

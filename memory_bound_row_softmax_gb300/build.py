@@ -20,7 +20,7 @@ LIB = os.path.join(BUILD, "libmbrs_softmax.so")
 ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["abi.cu", "k_warp.cu", "k_cta.cu", "k_cluster.cu", "k_split.cu", "k_ring.cu"]
+SOURCES = ["abi.cu", "k_warp.cu", "k_cta.cu", "k_cluster.cu", "k_split.cu", "k_ring.cu", "k_noalloc.cu"]
 HEADERS = ["common.cuh", "kernels.cuh", "launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -341,6 +341,26 @@ int run(const Plan &p, const LaunchArgs &a) {
     return e == cudaSuccess ? SOFTMAX_OK : SOFTMAX_ERR_CUDA;
 }
 
+// Split-path shape for softmax_fwd_noalloc: as the split path's own choice,
+// with chunks per row capped so that rows * chunks fits the fixed array.
+int plan_noalloc(uint64_t in, int64_t rows, int64_t cols, int64_t row_stride, int dtype, int sms, int64_t *chunks,
+                 int64_t *chunk_vecs, int64_t *grid) {
+    if (rows > kNoAllocMaxStates) return SOFTMAX_ERR_SCRATCH_LIMIT;
+    const int es = elem_bytes(dtype), V = kVecBytes / es;
+    const bool uniform = ((row_stride * es) % kVecBytes) == 0;
+    const int64_t head = (int64_t)((in % kVecBytes) / es);
+    const int64_t nv = uniform ? cdiv(head + cols, V) : cdiv(cols + V - 1, V);
+    const int64_t tile = (int64_t)kNoAllocThreads * kNoAllocVpt;
+    const int64_t per_sm = 2048 / kNoAllocThreads;
+    int64_t k = std::max<int64_t>(1, std::min(cdiv((int64_t)sms * per_sm * 2, rows), cdiv(nv, tile)));
+    k = std::max<int64_t>(1, std::min(k, kNoAllocMaxStates / rows));
+    const int64_t cv = cdiv(cdiv(nv, k), tile) * tile;
+    *chunk_vecs = cv;
+    *chunks = cdiv(nv, cv);
+    *grid = std::min<int64_t>(rows * *chunks, (int64_t)sms * per_sm * 4);
+    return SOFTMAX_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -363,6 +383,25 @@ int softmax_fwd(const void *in, void *out, int64_t rows, int64_t cols, int64_t r
     return st;
 }
 
+int softmax_fwd_noalloc(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride, int dtype,
+                        cudaStream_t stream) {
+    int64_t ext = 0;
+    const uint64_t ia = (uint64_t)(uintptr_t)in, oa = (uint64_t)(uintptr_t)out;
+    int st = check_args(ia, oa, rows, cols, row_stride, dtype, &ext);
+    if (st != SOFTMAX_OK || rows == 0) return st;
+    int sms = 0;
+    st = device_sms(&sms);
+    if (st != SOFTMAX_OK) return st;
+    int64_t chunks = 0, chunk_vecs = 0, grid = 0;
+    st = plan_noalloc(ia, rows, cols, row_stride, dtype, sms, &chunks, &chunk_vecs, &grid);
+    if (st != SOFTMAX_OK) return st;
+    const int vec_store = (ia % kVecBytes) == (oa % kVecBytes);
+    LaunchArgs a{in, out, rows, cols, row_stride, dtype, vec_store, stream};
+    const cudaError_t e = launch_split_noalloc(a, chunks, chunk_vecs, grid);
+    if (e == cudaErrorInvalidValue) return SOFTMAX_ERR_SCRATCH_LIMIT;
+    return e == cudaSuccess ? SOFTMAX_OK : SOFTMAX_ERR_CUDA;
+}
+
 const char *softmax_status_string(int status) {
     switch (status) {
         case SOFTMAX_OK: return "ok";
@@ -376,6 +415,8 @@ const char *softmax_status_string(int status) {
         case SOFTMAX_ERR_TIMEOUT: return "a bounded device wait ran out";
         case SOFTMAX_ERR_ALIGN: return "pointer not aligned to its element size";
         case SOFTMAX_ERR_ARG: return "bad argument to a diagnostic call";
+        case SOFTMAX_ERR_SCRATCH_LIMIT:
+            return "softmax_fwd_noalloc: more rows than its fixed device scratch array holds states for";
         default: return "unknown status";
     }
 }

@@ -44,6 +44,13 @@ cudaError_t launch_ring(const LaunchArgs &a, const RingCfg &c, int64_t wait_ns, 
 // read this translation unit's device error word (after a stream sync), then clear it
 cudaError_t read_clear_ring_error_word(unsigned int *word);
 
+// softmax_fwd_noalloc: the split path with its per-chunk states in a fixed
+// device array of kNoAllocMaxStates float2 (k_noalloc.cu); rows * chunks must
+// not exceed it.  Launch shape: 256 threads, 4 vectors per thread.
+constexpr int64_t kNoAllocMaxStates = 65536;
+constexpr int kNoAllocThreads = 256, kNoAllocVpt = 4;
+cudaError_t launch_split_noalloc(const LaunchArgs &a, int64_t chunks, int64_t chunk_vecs, int64_t grid);
+
 bool split_shape_ok(int threads, int vpt);
 cudaError_t launch_split(const LaunchArgs &a, int threads, int vpt, int64_t chunks, int64_t chunk_vecs,
                          int64_t grid, void *scratch);
