@@ -65,14 +65,14 @@ int cta_threads(int64_t nv) {
 }
 
 // Row bytes the block-per-row register kernel keeps in flight per SM: rows
-// resident at once (registers: the row widened to fp32 plus ~24 per thread)
-// times the row's bytes.  When this reaches ~96 KB the kernel already runs at
+// resident at once (registers: 4 per 16-byte vector -- fp32 values, or
+// 16-bit data kept packed -- plus ~24 per thread) times the row's bytes.  When this reaches ~96 KB the kernel already runs at
 // copy speed (measured: fp32 4096-wide rows); below it the shared-memory ring,
 // whose prefetch does not cost registers, keeps more bytes in flight.
 constexpr int64_t kRegInFlightEnough = 96 * 1024;
-int64_t cta_bytes_in_flight(int64_t nv, int es) {
+int64_t cta_bytes_in_flight(int64_t nv) {
     const int threads = cta_threads(nv);
-    const int64_t regs = cdiv(nv, threads) * (kVecBytes / es) + 24;
+    const int64_t regs = cdiv(nv, threads) * 4 + 24;
     const int64_t rows_per_sm = std::min<int64_t>(2048 / threads, 65536 / (threads * regs));
     return rows_per_sm * nv * kVecBytes;
 }
@@ -142,7 +142,7 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
         if (cols <= 1024 && nv <= 32 * 9) {
             path = SOFTMAX_PATH_WARP;
         } else if (ring_ok && cdiv(nv, 16) <= 4096 && rows * 16 * 2 >= sms &&
-                   (nv > 4096 || cta_bytes_in_flight(nv, es) < kRegInFlightEnough)) {
+                   (nv > 4096 || cta_bytes_in_flight(nv) < kRegInFlightEnough)) {
             path = SOFTMAX_PATH_RING;
         } else if (nv <= 1024 * 5) {
             path = SOFTMAX_PATH_CTA;

@@ -43,6 +43,7 @@ template <typename T> struct Elem;
 
 template <> struct Elem<float> {
     static constexpr int kVec = 4;  // elements per 16-byte vector
+    static constexpr uint32_t kNegInfBits = 0xff800000u;
     __device__ static __forceinline__ float to_f(float v) { return v; }
     __device__ static __forceinline__ float from_f(float v) { return v; }
     __device__ static __forceinline__ void unpack(const uint4 &r, float *x) {
@@ -59,6 +60,7 @@ template <> struct Elem<float> {
 
 template <> struct Elem<__half> {
     static constexpr int kVec = 8;
+    static constexpr uint16_t kNegInfBits = 0xfc00;
     __device__ static __forceinline__ float to_f(__half v) { return __half2float(v); }
     __device__ static __forceinline__ __half from_f(float v) { return __float2half_rn(v); }
     __device__ static __forceinline__ float2 pair(uint32_t w) {
@@ -68,6 +70,10 @@ template <> struct Elem<__half> {
     __device__ static __forceinline__ uint32_t unpair(float a, float b) {
         __half2 h = __floats2half2_rn(a, b);
         return *reinterpret_cast<const uint32_t *>(&h);
+    }
+    __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+        __half2 r = __hmax2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
+        return *reinterpret_cast<const uint32_t *>(&r);
     }
     __device__ static __forceinline__ void unpack(const uint4 &r, float *x) {
         float2 p;
@@ -84,6 +90,7 @@ template <> struct Elem<__half> {
 
 template <> struct Elem<__nv_bfloat16> {
     static constexpr int kVec = 8;
+    static constexpr uint16_t kNegInfBits = 0xff80;
     __device__ static __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
     __device__ static __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
     __device__ static __forceinline__ float2 pair(uint32_t w) {
@@ -93,6 +100,11 @@ template <> struct Elem<__nv_bfloat16> {
     __device__ static __forceinline__ uint32_t unpair(float a, float b) {
         __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
         return *reinterpret_cast<const uint32_t *>(&h);
+    }
+    __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+        __nv_bfloat162 r = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&a),
+                                   *reinterpret_cast<const __nv_bfloat162 *>(&b));
+        return *reinterpret_cast<const uint32_t *>(&r);
     }
     __device__ static __forceinline__ void unpack(const uint4 &r, float *x) {
         float2 p;
@@ -293,6 +305,24 @@ struct RowView {
             }
         }
     }
+    // Load vector v as raw 16-byte storage; for 16-bit types, columns outside
+    // the row hold the -inf bit pattern.
+    __device__ __forceinline__ uint4 load_raw(int64_t v) const {
+        const int64_t c0 = v * V - head;
+        if (full(v)) return *reinterpret_cast<const uint4 *>(in + c0);
+        static_assert(sizeof(T) == 2, "raw partial vectors are for 16-bit types");
+        const uint16_t ninf = Elem<T>::kNegInfBits;
+        const uint16_t *src = reinterpret_cast<const uint16_t *>(in);
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t ca = c0 + 2 * k, cb = ca + 1;
+            const uint32_t a = (ca >= 0 && ca < cols) ? src[ca] : ninf;
+            const uint32_t b = (cb >= 0 && cb < cols) ? src[cb] : ninf;
+            w[k] = a | (b << 16);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
     // Store vector v's results; only columns inside the row are written.
     __device__ __forceinline__ void store(int64_t v, const float *y) const {
         const int64_t c0 = v * V - head;
@@ -308,28 +338,43 @@ struct RowView {
     }
 };
 
-// A thread's tile of VPT vectors (VPT * V floats in registers).
+// A thread's tile of VPT vectors.  Two forms share one interface:
+//   FloatTile   the elements widened to fp32 (fp32 data: no extra registers);
+//               stats() overwrites them with e = 2^(x log2 e - s_t).
+//   PackedTile  the raw 16-bit storage (half the registers of FloatTile for
+//               fp16/bf16); stats() only accumulates, and the exponentials are
+//               computed again, with the same shift, when the results are
+//               formed -- the same bits, two exps per element instead of one.
+// Interface: set(j, raw) / set_empty(j) / load_one(j, row, v) /
+// load(row, first, step, end);
+// stats() -> (s_t, l_t); values(j, f, y): y = e * f for vector j;
+// values_shift(j, shift, f, y): y = 2^(x log2 e - shift) * f (inputs only,
+// before stats()); scale_store(row, first, step, end, f).
 template <typename T, int VPT>
-struct Tile {
+struct FloatTile {
     static constexpr int V = Elem<T>::kVec;
     float x[VPT][V];
 
+    __device__ __forceinline__ void set(int j, const uint4 &raw) { Elem<T>::unpack(raw, x[j]); }
+    __device__ __forceinline__ void load_one(int j, const RowView<T> &row, int64_t v) { row.load(v, x[j]); }
+    __device__ __forceinline__ void set_empty(int j) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) x[j][i] = -INFINITY;
+    }
     // load vectors first + j*step (j < VPT) of a row, -inf past `end`
     __device__ __forceinline__ void load(const RowView<T> &row, int64_t first, int64_t step, int64_t end) {
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int64_t v = first + j * step;
-            if (v < end) {
+            if (v < end)
                 row.load(v, x[j]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < V; ++i) x[j][i] = -INFINITY;
-            }
+            else
+                set_empty(j);
         }
     }
     // Replace x by e = 2^(x log2 e - s_t) with the tile's own max m_t and
     // s_t = fl(m_t log2 e); return the state (s_t, l_t).
-    __device__ __forceinline__ float2 exp_in_place() {
+    __device__ __forceinline__ float2 stats() {
         float m = -INFINITY;
 #pragma unroll
         for (int j = 0; j < VPT; ++j)
@@ -350,19 +395,107 @@ struct Tile {
         }
         return make_float2(s, l);
     }
+    __device__ __forceinline__ void values(int j, float f, float *y) const {
+#pragma unroll
+        for (int i = 0; i < V; ++i) y[i] = x[j][i] * f;
+    }
+    __device__ __forceinline__ void values_shift(int j, float shift, float f, float *y) const {
+#pragma unroll
+        for (int i = 0; i < V; ++i) y[i] = ex2(fmaf(x[j][i], kLog2e, -shift)) * f;
+    }
     __device__ __forceinline__ void scale_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
-                                                float f) {
+                                                float f) const {
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int64_t v = first + j * step;
             if (v < end) {
                 float y[V];
-#pragma unroll
-                for (int i = 0; i < V; ++i) y[i] = x[j][i] * f;
+                values(j, f, y);
                 row.store(v, y);
             }
         }
     }
 };
+
+template <typename T, int VPT>
+struct PackedTile {
+    static_assert(sizeof(T) == 2, "packed tiles hold 16-bit data");
+    static constexpr int V = Elem<T>::kVec;
+    uint4 raw[VPT];
+    float shift;  // the shift stats() used
+
+    __device__ __forceinline__ void set(int j, const uint4 &r) { raw[j] = r; }
+    __device__ __forceinline__ void load_one(int j, const RowView<T> &row, int64_t v) { raw[j] = row.load_raw(v); }
+    __device__ __forceinline__ void set_empty(int j) {
+        const uint32_t w = (uint32_t)Elem<T>::kNegInfBits * 0x10001u;
+        raw[j] = make_uint4(w, w, w, w);
+    }
+    __device__ __forceinline__ void load(const RowView<T> &row, int64_t first, int64_t step, int64_t end) {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t v = first + j * step;
+            if (v < end)
+                raw[j] = row.load_raw(v);
+            else
+                set_empty(j);
+        }
+    }
+    __device__ __forceinline__ float2 stats() {
+        // the max on the packed pairs (a NaN never wins, as with fmaxf)
+        uint32_t mw = (uint32_t)Elem<T>::kNegInfBits * 0x10001u;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            mw = Elem<T>::max2(mw, raw[j].x);
+            mw = Elem<T>::max2(mw, raw[j].y);
+            mw = Elem<T>::max2(mw, raw[j].z);
+            mw = Elem<T>::max2(mw, raw[j].w);
+        }
+        const float2 mp = Elem<T>::pair(mw);
+        const float m = fmaxf(mp.x, mp.y);
+        const float s = m * kLog2e;
+        shift = safe_shift(s);
+        float l = 0.f;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            float x[V];
+            Elem<T>::unpack(raw[j], x);
+            float lj = 0.f;
+#pragma unroll
+            for (int i = 0; i < V; ++i) lj += ex2(fmaf(x[i], kLog2e, -shift));
+            l += lj;
+        }
+        // The results are formed later from the packed words again: hide the
+        // words' values from the compiler so that it recomputes the
+        // exponentials there instead of keeping 8 fp32 values per vector live.
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+            asm volatile("" : "+r"(raw[j].x), "+r"(raw[j].y), "+r"(raw[j].z), "+r"(raw[j].w));
+        return make_float2(s, l);
+    }
+    __device__ __forceinline__ void values_shift(int j, float sh, float f, float *y) const {
+        float x[V];
+        Elem<T>::unpack(raw[j], x);
+#pragma unroll
+        for (int i = 0; i < V; ++i) y[i] = ex2(fmaf(x[i], kLog2e, -sh)) * f;
+    }
+    __device__ __forceinline__ void values(int j, float f, float *y) const { values_shift(j, shift, f, y); }
+    __device__ __forceinline__ void scale_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
+                                                float f) const {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t v = first + j * step;
+            if (v < end) {
+                float y[V];
+                values(j, f, y);
+                row.store(v, y);
+            }
+        }
+    }
+};
+
+// fp32 rows keep their exponentials; 16-bit rows stay packed.
+template <typename T, int VPT> struct TileSel { using type = PackedTile<T, VPT>; };
+template <int VPT> struct TileSel<float, VPT> { using type = FloatTile<float, VPT>; };
+template <typename T, int VPT> using Tile = typename TileSel<T, VPT>::type;
 
 }  // namespace mbrs

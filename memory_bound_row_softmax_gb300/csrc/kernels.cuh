@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(256) k_warp_rows(const T *in, T *out, int64_t 
                       vec_store != 0);
         Tile<T, VPT> tile;
         tile.load(rv, t, G, active ? rv.nvec : 0);
-        const float2 s = tile.exp_in_place();
+        const float2 s = tile.stats();
         float m = s.x, l = s.y;
         group_merge<G>(m, l);
         if (active) tile.scale_store(rv, t, G, rv.nvec, out_factor(s.x, m, l));
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(THREADS) k_cta_rows(const T *in, T *out, int64
         RowView<T> rv(in + row * stride, out + row * stride, cols, vec_store != 0);
         Tile<T, VPT> tile;
         tile.load(rv, threadIdx.x, THREADS, rv.nvec);
-        const float2 s = tile.exp_in_place();
+        const float2 s = tile.stats();
         float m = s.x, l = s.y;
         block_merge<NW>(m, l, red[parity]);
         tile.scale_store(rv, threadIdx.x, THREADS, rv.nvec, out_factor(s.x, m, l));
@@ -175,15 +175,14 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
         const int64_t v = s0 + j * THREADS + tid;
         if (v < s1) {
             if (v >= f0 && v < f1)
-                Elem<T>::unpack(stage[v - s0], tile.x[j]);
+                tile.set(j, stage[v - s0]);
             else
-                rv.load(v, tile.x[j]);  // a partial vector at the row's edge
+                tile.load_one(j, rv, v);  // a partial vector at the row's edge
         } else {
-#pragma unroll
-            for (int i = 0; i < V; ++i) tile.x[j][i] = -INFINITY;
+            tile.set_empty(j);
         }
     }
-    const float2 s = tile.exp_in_place();
+    const float2 s = tile.stats();
     float m = s.x, l = s.y;
     block_merge<NW>(m, l, red);
 
@@ -297,14 +296,12 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? (THREADS >= 1024 ? 1 : 1024
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int v = tid + j * THREADS;
-            if (v < nmine) {
-                Elem<T>::unpack(slot[v], tile.x[j]);
-            } else {
-#pragma unroll
-                for (int k = 0; k < V; ++k) tile.x[j][k] = -INFINITY;
-            }
+            if (v < nmine)
+                tile.set(j, slot[v]);
+            else
+                tile.set_empty(j);
         }
-        const float2 s = tile.exp_in_place();
+        const float2 s = tile.stats();
         float m = s.x, l = s.y;
         block_merge<NW>(m, l, red + (i & 1) * NW);  // its barrier also frees slot st
         if (tid == 0 && i + stages < nrows) {
@@ -345,8 +342,7 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? (THREADS >= 1024 ? 1 : 1024
                 const int v = tid + j * THREADS;
                 if (v < nmine) {
                     float y[V];
-#pragma unroll
-                    for (int k = 0; k < V; ++k) y[k] = tile.x[j][k] * f;
+                    tile.values(j, f, y);
                     *reinterpret_cast<uint4 *>(orow + (int64_t)v * V) = Elem<T>::pack(y);
                 }
             }
@@ -384,7 +380,7 @@ __global__ void __launch_bounds__(THREADS) k_split_stats(const T *in, int64_t ro
         for (int64_t t0 = c0; t0 < c1; t0 += kTile) {
             Tile<T, VPT> tile;
             tile.load(rv, t0 + threadIdx.x, THREADS, c1);
-            const float2 s = tile.exp_in_place();
+            const float2 s = tile.stats();
             const float M = fmaxf(m, s.x);
             l = rescale(l, m, M) + rescale(s.y, s.x, M);
             m = M;
@@ -423,10 +419,14 @@ __global__ void __launch_bounds__(THREADS)
         for (int64_t t0 = c0; t0 < c1; t0 += kTile) {
             if (t0 != c0) tile.load(rv, t0 + threadIdx.x, THREADS, c1);
 #pragma unroll
-            for (int j = 0; j < VPT; ++j)
-#pragma unroll
-                for (int i = 0; i < V; ++i) tile.x[j][i] = ex2(fmaf(tile.x[j][i], kLog2e, -shift)) * inv;
-            tile.scale_store(rv, t0 + threadIdx.x, THREADS, c1, 1.f);
+            for (int j = 0; j < VPT; ++j) {
+                const int64_t v = t0 + threadIdx.x + (int64_t)j * THREADS;
+                if (v < c1) {
+                    float y[V];
+                    tile.values_shift(j, shift, inv, y);
+                    rv.store(v, y);
+                }
+            }
         }
     }
 }
