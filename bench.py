@@ -235,10 +235,16 @@ def run_ours(args) -> dict | None:
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     peaks = measured_peaks()
 
-    w = W.CONFIGS[args.workload]
-    x = W.make_input(w)
-    bits = x.view(np.int32 if w.dtype == "f32" else np.int16)
-    x_dev = torch.from_numpy(bits).to(dev)
+    if args.workload.startswith("w"):  # a width of the fp32 sweep, seeded on the device
+        w = W.sweep_workload(int(args.workload[1:]))
+        x = None
+        g = torch.Generator(device=dev).manual_seed(w.seed)
+        x_dev = (torch.rand((w.rows, w.stride), generator=g, device=dev) * 200 - 100).view(torch.int32)
+    else:
+        w = W.CONFIGS[args.workload]
+        x = W.make_input(w)
+        bits = x.view(np.int32 if w.dtype == "f32" else np.int16)
+        x_dev = torch.from_numpy(bits).to(dev)
     code = B.DTYPE_CODES[w.dtype]
     stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream
@@ -312,9 +318,9 @@ def run_ours(args) -> dict | None:
         "clocks": clk,
         "gpu_launches": args.steps * plan["launches"],
     }
-    if rank == 0:
+    if rank == 0 and x is not None:
         result["e2e"] = e2e_measure(launch, x, w, dev, min(args.steps, 2000))
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and x is not None:
         result["cpu_baseline"] = cpu_baseline(x, w)
     if rank == 0 and world == 1 and not args.no_per_shape:
         result["per_shape"] = per_shape(args, peaks, l2, dev)
@@ -483,7 +489,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="c2", choices=("c1", "c2", "c3", "c4", "c5"))
+    ap.add_argument("--workload", default="c2",
+                    help="c1..c5 (the pages' workloads) or wN (fp32 width-sweep matrix of width N)")
     ap.add_argument("--no-per-shape", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="add the fp32 width sweep to the per-shape table")
