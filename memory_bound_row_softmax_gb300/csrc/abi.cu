@@ -20,7 +20,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "mbrs_softmax.h"
+#include "../../include/mbrs_softmax.h"
 #include "launch.h"
 
 using namespace mbrs;

@@ -14,9 +14,8 @@
 //                           rows; one thread keeps a ring of shared-memory
 //                           stages filled with 1-D TMA bulk copies, so the
 //                           loads of the next rows are in flight while the
-//                           current row is reduced; results go back into the
-//                           stage and leave by TMA bulk stores, one per warp.
-//                           Rows must be made of whole aligned 16-byte vectors.
+//                           current row is reduced and stored.  Rows must be
+//                           made of whole aligned 16-byte vectors.
 //   path 4  k_split_stats / k_split_apply
 //                           rows cut into chunks spread over the whole grid;
 //                           pass 1 streams each chunk into a (max, sum) state
@@ -243,19 +242,14 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? (THREADS >= 1024 ? 1 : 1024
 
     const uint32_t rank = CLUSTER ? cluster_rank() : 0u, csize = CLUSTER ? cluster_size() : 1u;
     const int64_t cid = blockIdx.x / csize, ncl = gridDim.x / csize;
-    // every row is nvec whole vectors; this block owns vectors [s0, s0 + nmine) of each
+    // every row is nvec whole vectors; this block owns vectors [s0, s1) of each
     const int64_t nvec = cols / V;
     const int64_t per = (nvec + csize - 1) / csize;
-    const int64_t s0 = min((int64_t)rank * per, nvec);
-    const int nmine = (int)(min(s0 + per, nvec) - s0);
+    const int64_t s0 = min((int64_t)rank * per, nvec), s1 = min(s0 + per, nvec);
+    const int nmine = (int)(s1 - s0);
     const uint32_t bytes = (uint32_t)nmine * kVecBytes;
     // rows cid, cid + ncl, ... (the same count for every block of a cluster)
     const int64_t nrows = rows > cid ? (rows - cid + ncl - 1) / ncl : 0;
-    // warp w owns the contiguous vectors [w * 32 * VPT, (w + 1) * 32 * VPT) of the
-    // slice: its lanes read them from the stage in 16-byte steps, and it writes
-    // the results back as one contiguous piece for its bulk store
-    const int warp = tid >> 5;
-    const int wv0 = warp * 32 * VPT, wv1 = min(wv0 + 32 * VPT, nmine);
 
     const uint32_t xbar_base = smem_addr(smem + L.xbar_off);
     if (tid == 0) {
@@ -297,11 +291,11 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? (THREADS >= 1024 ? 1 : 1024
             atomicOr(&g_error_word, kErrWaitTimeout);
             timed_out = true;
         }
-        uint4 *slot = reinterpret_cast<uint4 *>(smem + st * L.stage_bytes);
+        const uint4 *slot = reinterpret_cast<const uint4 *>(smem + st * L.stage_bytes);
         Tile<T, VPT> tile;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
-            const int v = wv0 + j * 32 + lane;
+            const int v = tid + j * THREADS;
             if (v < nmine)
                 tile.set(j, slot[v]);
             else
@@ -309,13 +303,10 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? (THREADS >= 1024 ? 1 : 1024
         }
         const float2 s = tile.stats();
         float m = s.x, l = s.y;
-        // the previous row's bulk store must have read its stage before the
-        // barrier below lets thread 0 refill that stage
-        if (lane == 0) bulk_wait_read_all();
-        block_merge<NW>(m, l, red + (i & 1) * NW);
-        if (tid == 0 && i >= 1 && i - 1 + stages < nrows) {
+        block_merge<NW>(m, l, red + (i & 1) * NW);  // its barrier also frees slot st
+        if (tid == 0 && i + stages < nrows) {
             fence_proxy_async_smem();
-            issue(i - 1 + stages);  // into the slot of row i - 1
+            issue(i + stages);
         }
         bool xok = true;
         if (CLUSTER) {
@@ -343,29 +334,20 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? (THREADS >= 1024 ? 1 : 1024
             l = w.y;
             group_merge<32>(m, l);
         }
-        // results back into this row's stage, then one bulk store per warp
-        if (__all_sync(0xffffffffu, ok && xok)) {
+        if (ok && xok) {
             const float f = out_factor(s.x, m, l);
+            T *orow = out + (cid + i * ncl) * stride + s0 * V;
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
-                const int v = wv0 + j * 32 + lane;
+                const int v = tid + j * THREADS;
                 if (v < nmine) {
                     float y[V];
                     tile.values(j, f, y);
-                    slot[v] = Elem<T>::pack(y);
+                    *reinterpret_cast<uint4 *>(orow + (int64_t)v * V) = Elem<T>::pack(y);
                 }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && wv1 > wv0) {
-                T *orow = out + (cid + i * ncl) * stride + (s0 + wv0) * V;
-                bulk_s2g(orow, smem_addr(slot + wv0), (uint32_t)(wv1 - wv0) * kVecBytes);
-                bulk_commit();
             }
         }
     }
-    // the bulk stores have completed before the block (and its shared memory) goes
-    if (lane == 0) bulk_wait_all();
     // after a wait that ran out, copies may still be landing: wait for them
     // (bounded) before the block's shared memory is released
     if (timed_out && !starve && tid == 0) {
