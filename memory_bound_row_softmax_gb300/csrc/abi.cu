@@ -20,7 +20,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/mbrs_softmax.h"
+#include "mbrs_softmax.h"
 #include "launch.h"
 
 using namespace mbrs;
@@ -56,13 +56,24 @@ int next_pow2(int64_t v) {
     return p;
 }
 
-// Threads of the block-per-row register kernel: the fewest (a power of two)
-// that need at most 4 vectors each.
-int cta_threads(int64_t nv) {
+// Shape of the block-per-row register kernel: the fewest threads (a power of
+// two) that need at most 4 vectors each -- except that a row needing 1024
+// threads takes 512 threads with up to 10 vectors each instead, so that two
+// rows (not one) are in flight per SM.  vpt is rounded up to an instantiated
+// count (2..6, 8, 10).
+int cta_vpt_round(int64_t v) {
+    if (v <= 2) return 2;
+    if (v <= 6) return (int)v;
+    return v <= 8 ? 8 : 10;
+}
+void cta_shape(int64_t nv, int *threads_out, int *vpt_out) {
     int threads = 64;
     while (threads < 1024 && cdiv(nv, threads) > 4) threads *= 2;
-    return threads;
+    if (threads == 1024 && cdiv(nv, 512) <= 10) threads = 512;
+    *threads_out = threads;
+    *vpt_out = cta_vpt_round(cdiv(nv, threads));
 }
+
 
 // Row bytes the block-per-row register kernel keeps in flight per SM: rows
 // resident at once (registers: 4 per 16-byte vector -- fp32 values, or
@@ -71,8 +82,9 @@ int cta_threads(int64_t nv) {
 // whose prefetch does not cost registers, keeps more bytes in flight.
 constexpr int64_t kRegInFlightEnough = 96 * 1024;
 int64_t cta_bytes_in_flight(int64_t nv) {
-    const int threads = cta_threads(nv);
-    const int64_t regs = cdiv(nv, threads) * 4 + 24;
+    int threads, vpt;
+    cta_shape(nv, &threads, &vpt);
+    const int64_t regs = (int64_t)vpt * 4 + 24;
     const int64_t rows_per_sm = std::min<int64_t>(2048 / threads, 65536 / (threads * regs));
     return rows_per_sm * nv * kVecBytes;
 }
@@ -144,7 +156,7 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
         } else if (ring_ok && cdiv(nv, 16) <= 4096 && rows * 16 * 2 >= sms &&
                    (nv > 4096 || cta_bytes_in_flight(nv) < kRegInFlightEnough)) {
             path = SOFTMAX_PATH_RING;
-        } else if (nv <= 1024 * 5) {
+        } else if (nv <= 512 * 10) {
             path = SOFTMAX_PATH_CTA;
         } else {
             const int64_t csize = cdiv(nv, nv <= 16 * 512 * 4 ? 512 * 4 : 1024 * 4);
@@ -182,8 +194,13 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
         case SOFTMAX_PATH_CTA: {
             // the fewest threads (a power of two) that need at most 4 vectors each
             // (5 at 1024 threads); vpt = what the row then needs, not a rounded-up 4
-            int threads = fth > 0 ? fth : cta_threads(nv);
-            int vpt = fvpt > 0 ? fvpt : std::max<int>(2, (int)cdiv(nv, threads));
+            int threads = fth, vpt = fvpt;
+            if (threads <= 0) {
+                int v;
+                cta_shape(nv, &threads, &v);
+                if (vpt <= 0) vpt = v;
+            }
+            if (vpt <= 0) vpt = cta_vpt_round(cdiv(nv, threads));
             if (!cta_shape_ok(threads, vpt) || (int64_t)threads * vpt < nv) return SOFTMAX_ERR_UNSUPPORTED;
             p->threads = threads;
             p->vpt = vpt;

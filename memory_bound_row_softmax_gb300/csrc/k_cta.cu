@@ -19,11 +19,17 @@ cudaError_t by_vpt(const LaunchArgs &a, int vpt, int64_t grid) {
         case 3: return go<T, THREADS, 3>(a, grid);
         case 4: return go<T, THREADS, 4>(a, grid);
         case 5: return go<T, THREADS, 5>(a, grid);
-        case 8:
-            if constexpr (THREADS < 1024) return go<T, THREADS, 8>(a, grid);  // 1024 x 8 spills
-            return cudaErrorInvalidValue;
-        default: return cudaErrorInvalidValue;
+        default: break;
     }
+    if constexpr (THREADS < 1024) {  // 1024 threads x more than 5 vectors would spill
+        switch (vpt) {
+            case 6: return go<T, THREADS, 6>(a, grid);
+            case 8: return go<T, THREADS, 8>(a, grid);
+            case 10: return go<T, THREADS, 10>(a, grid);
+            default: break;
+        }
+    }
+    return cudaErrorInvalidValue;
 }
 
 template <typename T>
@@ -41,7 +47,7 @@ cudaError_t by_shape(const LaunchArgs &a, int threads, int vpt, int64_t grid) {
 
 bool cta_shape_ok(int threads, int vpt) {
     const bool t = threads == 64 || threads == 128 || threads == 256 || threads == 512 || threads == 1024;
-    return t && ((vpt >= 2 && vpt <= 5) || (vpt == 8 && threads < 1024));
+    return t && ((vpt >= 2 && vpt <= 5) || ((vpt == 6 || vpt == 8 || vpt == 10) && threads < 1024));
 }
 
 cudaError_t launch_cta(const LaunchArgs &a, int threads, int vpt, int64_t grid) {

@@ -76,9 +76,11 @@ __device__ __forceinline__ void block_merge(float &m, float &l, float2 *red) {
     group_merge<32>(m, l);
 }
 
+// With 6 or more vectors per thread the kernel is bounded to 64 registers
+// (1024 threads per SM), so that such wide rows still have two in flight per SM.
 template <typename T, int THREADS, int VPT>
-__global__ void __launch_bounds__(THREADS) k_cta_rows(const T *in, T *out, int64_t rows, int64_t cols,
-                                                      int64_t stride, int vec_store) {
+__global__ void __launch_bounds__(THREADS, (VPT >= 6 && THREADS < 1024) ? 1024 / THREADS : 1)
+    k_cta_rows(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store) {
     constexpr int NW = THREADS / 32;
     __shared__ float2 red[2][NW];
     int parity = 0;
