@@ -56,24 +56,38 @@ int next_pow2(int64_t v) {
     return p;
 }
 
-// Shape of the block-per-row register kernel: the fewest threads (a power of
-// two) that need at most 4 vectors each -- except that a row needing 1024
-// threads takes 512 threads with up to 10 vectors each instead, so that two
-// rows (not one) are in flight per SM.  vpt is rounded up to an instantiated
-// count (2..6, 8, 10).
+// Shape of the block-per-row register kernel.  For each thread count (a power
+// of two) the row needs vpt = ceil(nv / threads) vectors per thread, rounded
+// up to an instantiated count (2..6, 8, 10; at most 5 with 1024 threads).
+// Registers per thread: 4 per vector plus ~24, or the 64 the kernel is bounded
+// to from 6 vectors up.  The shape kept is the one with the most row bytes
+// resident per SM (rows per SM by threads and registers, times the row),
+// ties going to fewer threads -- measured, wide rows run best with 256 threads
+// x 8 vectors (8192-wide fp32: 59 us, against 68 us for 512 x 4).
 int cta_vpt_round(int64_t v) {
     if (v <= 2) return 2;
     if (v <= 6) return (int)v;
     return v <= 8 ? 8 : 10;
 }
-void cta_shape(int64_t nv, int *threads_out, int *vpt_out) {
-    int threads = 64;
-    while (threads < 1024 && cdiv(nv, threads) > 4) threads *= 2;
-    if (threads == 1024 && cdiv(nv, 512) <= 10) threads = 512;
-    *threads_out = threads;
-    *vpt_out = cta_vpt_round(cdiv(nv, threads));
+int64_t cta_rows_per_sm(int threads, int vpt) {
+    const int64_t regs = vpt >= 6 ? 64 : 4 * vpt + 24;
+    return std::min<int64_t>(std::min<int64_t>(2048 / threads, 65536 / (threads * regs)), 32);
 }
-
+bool cta_shape(int64_t nv, int *threads_out, int *vpt_out) {
+    int64_t best = -1;
+    for (int threads = 64; threads <= 1024; threads *= 2) {
+        const int64_t need = cdiv(nv, threads);
+        if (need > (threads == 1024 ? 5 : 10)) continue;
+        const int vpt = cta_vpt_round(need);
+        const int64_t resident = cta_rows_per_sm(threads, vpt);
+        if (resident > best) {
+            best = resident;
+            *threads_out = threads;
+            *vpt_out = vpt;
+        }
+    }
+    return best > 0;
+}
 
 // Row bytes the block-per-row register kernel keeps in flight per SM: rows
 // resident at once (registers: 4 per 16-byte vector -- fp32 values, or
@@ -82,11 +96,9 @@ void cta_shape(int64_t nv, int *threads_out, int *vpt_out) {
 // whose prefetch does not cost registers, keeps more bytes in flight.
 constexpr int64_t kRegInFlightEnough = 96 * 1024;
 int64_t cta_bytes_in_flight(int64_t nv) {
-    int threads, vpt;
-    cta_shape(nv, &threads, &vpt);
-    const int64_t regs = (int64_t)vpt * 4 + 24;
-    const int64_t rows_per_sm = std::min<int64_t>(2048 / threads, 65536 / (threads * regs));
-    return rows_per_sm * nv * kVecBytes;
+    int threads = 0, vpt = 0;
+    if (!cta_shape(nv, &threads, &vpt)) return 0;
+    return cta_rows_per_sm(threads, vpt) * nv * kVecBytes;
 }
 
 int elem_bytes(int dtype) { return dtype == SOFTMAX_F32 ? 4 : 2; }
@@ -154,7 +166,7 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
         if (cols <= 1024 && nv <= 32 * 9) {
             path = SOFTMAX_PATH_WARP;
         } else if (ring_ok && cdiv(nv, 16) <= 4096 && rows * 16 * 2 >= sms &&
-                   (nv > 4096 || cta_bytes_in_flight(nv) < kRegInFlightEnough)) {
+                   cta_bytes_in_flight(nv) < kRegInFlightEnough) {
             path = SOFTMAX_PATH_RING;
         } else if (nv <= 512 * 10) {
             path = SOFTMAX_PATH_CTA;
@@ -196,7 +208,8 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             // (5 at 1024 threads); vpt = what the row then needs, not a rounded-up 4
             int threads = fth, vpt = fvpt;
             if (threads <= 0) {
-                int v;
+                int v = 0;
+                threads = 1024;
                 cta_shape(nv, &threads, &v);
                 if (vpt <= 0) vpt = v;
             }

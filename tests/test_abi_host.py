@@ -119,7 +119,7 @@ def test_dispatch_follows_width_rule():
     assert plan(64, 1025) == B.PATH_CTA           # misaligned medium rows: a block per row
     assert plan(4096, 16391) == B.PATH_CTA
     assert plan(4096, 2048, "f16") in (B.PATH_RING, B.PATH_CTA)  # aligned: ring or registers
-    assert plan(4096, 16384) in (B.PATH_RING, B.PATH_CTA)
+    assert plan(4096, 16384) == B.PATH_CTA           # 512 x 8 keeps two 64 KB rows per SM
     assert plan(512, 131072, "bf16") == B.PATH_RING      # long rows: ring of clusters
     assert plan(512, 131079, "bf16") == B.PATH_CLUSTER   # long misaligned rows, enough of them
     assert plan(4, 131072, "bf16") == B.PATH_SPLIT       # too few rows to fill the GPU
