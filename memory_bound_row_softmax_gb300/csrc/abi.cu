@@ -184,12 +184,25 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             if (fgrp > 0) {
                 g = fgrp;
                 vpt = fvpt > 0 ? fvpt : (int)cdiv(nv, g);
-            } else if (nv <= 16 * 4) {  // several rows per warp, up to 4 vectors per lane
-                g = std::max(2, next_pow2(cdiv(nv, 4)));
-                vpt = fvpt > 0 ? fvpt : (int)cdiv(nv, g);
             } else {
+                // lanes per row: the group (2..32 lanes, up to 8 vectors each; 9
+                // for a whole warp) with the most row bytes resident per SM --
+                // warps per SM by registers (4 per vector + ~24) times rows per warp
+                int64_t best = -1;
                 g = 32;
-                vpt = fvpt > 0 ? fvpt : (int)cdiv(nv, 32);
+                vpt = (int)cdiv(nv, 32);
+                for (int gg = 2; gg <= 32; gg *= 2) {
+                    const int64_t v = cdiv(nv, gg);
+                    if (v > (gg == 32 ? 9 : 8)) continue;
+                    const int64_t warps = std::min<int64_t>(64, 65536 / (32 * (4 * v + 24)));
+                    const int64_t resident = warps * (32 / gg);
+                    if (resident > best) {
+                        best = resident;
+                        g = gg;
+                        vpt = (int)v;
+                    }
+                }
+                if (fvpt > 0) vpt = fvpt;
             }
             if (!warp_shape_ok(g, vpt) || (int64_t)g * vpt < nv) return SOFTMAX_ERR_UNSUPPORTED;
             int threads = fth > 0 ? fth : 128;
@@ -224,7 +237,7 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             int threads = fth > 0 ? fth : (nv <= 16 * 512 * 4 ? 512 : 1024);
             int vpt = fvpt > 0 ? fvpt : 4;
             int64_t csize = fgrp > 0 ? fgrp : cdiv(nv, (int64_t)threads * vpt);
-            if (!cluster_shape_ok(threads, vpt) || csize < 1 || csize > 16) return SOFTMAX_ERR_UNSUPPORTED;
+            if (!cluster_shape_ok(threads, vpt, es) || csize < 1 || csize > 16) return SOFTMAX_ERR_UNSUPPORTED;
             if (cdiv(nv, csize) > (int64_t)threads * vpt) return SOFTMAX_ERR_UNSUPPORTED;
             if (rows * csize > kMaxGrid) return SOFTMAX_ERR_UNSUPPORTED;
             p->threads = threads;

@@ -11,31 +11,36 @@ namespace mbrs {
 namespace {
 constexpr int kMaxDevices = 64;
 
-template <typename T, int THREADS, int VPT>
+template <int THREADS, int VPT, bool TMA>
+constexpr int cluster_smem() {
+    return TMA ? ClusterSmem<THREADS, VPT>::kBytes : ClusterSmem<THREADS, 0>::kBytes;
+}
+
+template <typename T, int THREADS, int VPT, bool TMA>
 cudaError_t prepare(int device) {
     // per-device, once: opt in to large dynamic shared memory and clusters of 16
     static std::atomic<unsigned long long> done{0};
     const unsigned long long bit = 1ull << (device & (kMaxDevices - 1));
     if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    auto fn = k_cluster_rows<T, THREADS, VPT>;
+    auto fn = k_cluster_rows<T, THREADS, VPT, TMA>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         ClusterSmem<THREADS, VPT>::kBytes);
+                                         cluster_smem<THREADS, VPT, TMA>());
     if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
     return e;
 }
 
-template <typename T, int THREADS, int VPT>
+template <typename T, int THREADS, int VPT, bool TMA>
 cudaError_t go(const LaunchArgs &a, int csize, int64_t wait_ns, int starve) {
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;
-    e = prepare<T, THREADS, VPT>(device);
+    e = prepare<T, THREADS, VPT, TMA>(device);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.rows * csize), 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = ClusterSmem<THREADS, VPT>::kBytes;
+    cfg.dynamicSmemBytes = cluster_smem<THREADS, VPT, TMA>();
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -44,17 +49,22 @@ cudaError_t go(const LaunchArgs &a, int csize, int64_t wait_ns, int starve) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k_cluster_rows<T, THREADS, VPT>, static_cast<const T *>(a.in),
+    e = cudaLaunchKernelEx(&cfg, k_cluster_rows<T, THREADS, VPT, TMA>, static_cast<const T *>(a.in),
                            static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store, wait_ns, starve);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
+// 2 or 4 vectors per thread: slices staged in shared memory by TMA; 8: slices
+// held in registers only.
 template <typename T, int THREADS>
 cudaError_t by_vpt(const LaunchArgs &a, int vpt, int csize, int64_t wait_ns, int starve) {
     switch (vpt) {
-        case 2: return go<T, THREADS, 2>(a, csize, wait_ns, starve);
-        case 4: return go<T, THREADS, 4>(a, csize, wait_ns, starve);
+        case 2: return go<T, THREADS, 2, true>(a, csize, wait_ns, starve);
+        case 4: return go<T, THREADS, 4, true>(a, csize, wait_ns, starve);
+        case 8:  // 16-bit data only: fp32 at 8 vectors would spill at 64 registers
+            if constexpr (THREADS <= 512 && sizeof(T) == 2) return go<T, THREADS, 8, false>(a, csize, wait_ns, starve);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
@@ -70,12 +80,14 @@ cudaError_t by_shape(const LaunchArgs &a, int threads, int vpt, int csize, int64
 }
 }  // namespace
 
-bool cluster_shape_ok(int threads, int vpt) {
-    return (threads == 256 || threads == 512 || threads == 1024) && (vpt == 2 || vpt == 4);
+bool cluster_shape_ok(int threads, int vpt, int elem_bytes) {
+    const bool t = threads == 256 || threads == 512 || threads == 1024;
+    return t && (vpt == 2 || vpt == 4 || (vpt == 8 && threads <= 512 && elem_bytes == 2));
 }
 
 int64_t cluster_smem_bytes(int threads, int vpt) {
-    return (int64_t)threads * vpt * kVecBytes + 16 + (threads / 32) * 8 + kMaxCluster * 8;
+    const int64_t stage = vpt == 8 ? 0 : (int64_t)threads * vpt * kVecBytes;
+    return stage + 16 + (threads / 32) * 8 + kMaxCluster * 8;
 }
 
 cudaError_t launch_cluster(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns, int starve) {

@@ -15,6 +15,7 @@ cudaError_t go(const LaunchArgs &a, int64_t grid) {
 template <typename T, int THREADS>
 cudaError_t by_vpt(const LaunchArgs &a, int vpt, int64_t grid) {
     switch (vpt) {
+        case 1: return go<T, THREADS, 1>(a, grid);
         case 2: return go<T, THREADS, 2>(a, grid);
         case 3: return go<T, THREADS, 3>(a, grid);
         case 4: return go<T, THREADS, 4>(a, grid);
@@ -47,7 +48,7 @@ cudaError_t by_shape(const LaunchArgs &a, int threads, int vpt, int64_t grid) {
 
 bool cta_shape_ok(int threads, int vpt) {
     const bool t = threads == 64 || threads == 128 || threads == 256 || threads == 512 || threads == 1024;
-    return t && ((vpt >= 2 && vpt <= 5) || ((vpt == 6 || vpt == 8 || vpt == 10) && threads < 1024));
+    return t && ((vpt >= 1 && vpt <= 5) || ((vpt == 6 || vpt == 8 || vpt == 10) && threads < 1024));
 }
 
 cudaError_t launch_cta(const LaunchArgs &a, int threads, int vpt, int64_t grid) {

@@ -19,6 +19,10 @@ cudaError_t small_vpt(const LaunchArgs &a, int threads, int vpt, int64_t grid) {
         case 2: return go<T, G, 2>(a, threads, grid);
         case 3: return go<T, G, 3>(a, threads, grid);
         case 4: return go<T, G, 4>(a, threads, grid);
+        case 5: return go<T, G, 5>(a, threads, grid);
+        case 6: return go<T, G, 6>(a, threads, grid);
+        case 7: return go<T, G, 7>(a, threads, grid);
+        case 8: return go<T, G, 8>(a, threads, grid);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -49,7 +53,7 @@ cudaError_t by_shape(const LaunchArgs &a, int threads, int group, int vpt, int64
 }  // namespace
 
 bool warp_shape_ok(int group, int vpt) {
-    if (group == 2 || group == 4 || group == 8 || group == 16) return vpt >= 1 && vpt <= 4;
+    if (group == 2 || group == 4 || group == 8 || group == 16) return vpt >= 1 && vpt <= 8;
     return group == 32 && vpt >= 1 && vpt <= 9;
 }
 

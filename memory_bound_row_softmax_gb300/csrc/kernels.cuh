@@ -115,13 +115,17 @@ struct ClusterSmem {
     static constexpr int kBytes = kSlotOff + kMaxCluster * 8;
 };
 
-template <typename T, int THREADS, int VPT>
+// TMA = true: each block pulls its slice into shared memory with bulk copies;
+// TMA = false: each block loads its slice straight into registers (no
+// staging, so occupancy is bounded by registers alone).
+template <typename T, int THREADS, int VPT, bool TMA>
 __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS))
     k_cluster_rows(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store,
                    int64_t wait_ns, int starve) {
     constexpr int V = Elem<T>::kVec;
     constexpr int NW = THREADS / 32;
-    using L = ClusterSmem<THREADS, VPT>;
+    // the layout the launch allocated: no staging area without TMA
+    using L = ClusterSmem<THREADS, TMA ? VPT : 0>;
     extern __shared__ __align__(128) unsigned char smem[];
     const uint4 *stage = reinterpret_cast<const uint4 *>(smem);
     float2 *red = reinterpret_cast<float2 *>(smem + L::kRedOff);
@@ -142,47 +146,52 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     const int64_t f0 = max(s0, first_full), f1 = min(s1, full_end);
     const uint32_t bytes = f1 > f0 ? (uint32_t)((f1 - f0) * kVecBytes) : 0u;
 
-    if (tid == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    if (tid == 0 && !starve) {
-        if (bytes > 0) {
-            mbar_arrive_expect_tx(bar, bytes);
-            const char *src = reinterpret_cast<const char *>(rv.in + (f0 * V - rv.head));
-            const uint32_t dst = smem_addr(stage + (f0 - s0));
-            for (uint32_t off = 0; off < bytes; off += kBulkPiece)
-                bulk_g2s(dst + off, src + off, min(kBulkPiece, bytes - off), bar);
-        } else {
-            mbar_arrive(bar);
-        }
-    }
-    // announce that this block runs: peers may write into its shared memory
-    // once they have waited on this arrival
-    __syncwarp();
-    cluster_arrive_relaxed();
-
-    bool ok = mbar_wait_bounded(bar, 0, wait_ns);
-    if (!ok) {
-        atomicOr(&g_error_word, kErrWaitTimeout);
-        // a copy may still be landing in this block's shared memory: give it
-        // one more bounded wait before the memory is reused or released
-        if (!starve) mbar_wait_bounded(bar, 0, wait_ns);
-    }
-
+    bool ok = true;
     Tile<T, VPT> tile;
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-        const int64_t v = s0 + j * THREADS + tid;
-        if (v < s1) {
-            if (v >= f0 && v < f1)
-                tile.set(j, stage[v - s0]);
-            else
-                tile.load_one(j, rv, v);  // a partial vector at the row's edge
-        } else {
-            tile.set_empty(j);
+    if constexpr (TMA) {
+        if (tid == 0) {
+            mbar_init(bar, 1);
+            fence_mbar_init();
         }
+        __syncthreads();
+        if (tid == 0 && !starve) {
+            if (bytes > 0) {
+                mbar_arrive_expect_tx(bar, bytes);
+                const char *src = reinterpret_cast<const char *>(rv.in + (f0 * V - rv.head));
+                const uint32_t dst = smem_addr(stage + (f0 - s0));
+                for (uint32_t off = 0; off < bytes; off += kBulkPiece)
+                    bulk_g2s(dst + off, src + off, min(kBulkPiece, bytes - off), bar);
+            } else {
+                mbar_arrive(bar);
+            }
+        }
+        // announce that this block runs: peers may write into its shared memory
+        // once they have waited on this arrival
+        __syncwarp();
+        cluster_arrive_relaxed();
+
+        ok = mbar_wait_bounded(bar, 0, wait_ns);
+        if (!ok) {
+            atomicOr(&g_error_word, kErrWaitTimeout);
+            // a copy may still be landing in this block's shared memory: give it
+            // one more bounded wait before the memory is reused or released
+            if (!starve) mbar_wait_bounded(bar, 0, wait_ns);
+        }
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t v = s0 + j * THREADS + tid;
+            if (v < s1) {
+                if (v >= f0 && v < f1)
+                    tile.set(j, stage[v - s0]);
+                else
+                    tile.load_one(j, rv, v);  // a partial vector at the row's edge
+            } else {
+                tile.set_empty(j);
+            }
+        }
+    } else {
+        cluster_arrive_relaxed();
+        tile.load(rv, s0 + tid, THREADS, s1);
     }
     const float2 s = tile.stats();
     float m = s.x, l = s.y;

@@ -26,7 +26,7 @@ cudaError_t launch_warp(const LaunchArgs &a, int threads, int group, int vpt, in
 bool cta_shape_ok(int threads, int vpt);
 cudaError_t launch_cta(const LaunchArgs &a, int threads, int vpt, int64_t grid);
 
-bool cluster_shape_ok(int threads, int vpt);
+bool cluster_shape_ok(int threads, int vpt, int elem_bytes);
 int64_t cluster_smem_bytes(int threads, int vpt);
 cudaError_t launch_cluster(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns, int starve);
 // read this device's error word after synchronising `stream`, then clear it

@@ -89,6 +89,23 @@ def test_cluster_sizes(dtype, group):
     assert res["path"] == B.PATH_CLUSTER
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("threads", [256, 512])
+@pytest.mark.parametrize("group", [1, 2, 3, 8, 16])
+def test_cluster_register_slices(dtype, threads, group):
+    # 8 vectors per thread: the cluster path's variant that holds its slice in
+    # registers instead of staging it in shared memory
+    cols = min(8 * threads * 8 * group - 13, 140001)
+    res = run_and_compare(rnd(5, cols, dtype, seed=group + threads), dtype, path=B.PATH_CLUSTER, threads=threads,
+                          vpt=8, group=group)
+    assert res["path"] == B.PATH_CLUSTER
+
+
+def test_cluster_register_slices_refuse_fp32():
+    case = DeviceCase(rnd(2, 4000, "f32", 1), "f32")
+    assert case.run(4000, path=B.PATH_CLUSTER, threads=256, vpt=8, group=2) == B.ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("group", [1, 2, 3, 5, 8, 16])
 @pytest.mark.parametrize("rows", [3, 700])
