@@ -165,6 +165,10 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
     if (path == SOFTMAX_PATH_AUTO) {
         if (cols <= 1024 && nv <= 32 * 9) {
             path = SOFTMAX_PATH_WARP;
+        } else if (nv > 512 * 10 && es == 2 && cdiv(nv, 2048) <= 16 && rows * cdiv(nv, 2048) >= sms) {
+            // 16-bit rows longer than a block's registers: a cluster holding the
+            // row in registers, 2048 vectors per block (c5: 52 us, ring 57 us)
+            path = SOFTMAX_PATH_CLUSTER;
         } else if (ring_ok && cdiv(nv, 16) <= 4096 && rows * 16 * 2 >= sms &&
                    cta_bytes_in_flight(nv) < kRegInFlightEnough) {
             path = SOFTMAX_PATH_RING;
@@ -191,9 +195,11 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
                 int64_t best = -1;
                 g = 32;
                 vpt = (int)cdiv(nv, 32);
+                // (measured: sub-warp groups with 6+ vectors per lane lose -- a
+                // 39-wide fp32 row ran 70 us on 2 x 6 against 62 us on 4 x 3)
                 for (int gg = 2; gg <= 32; gg *= 2) {
                     const int64_t v = cdiv(nv, gg);
-                    if (v > (gg == 32 ? 9 : 8)) continue;
+                    if (v > (gg == 32 ? 9 : 5)) continue;
                     const int64_t warps = std::min<int64_t>(64, 65536 / (32 * (4 * v + 24)));
                     const int64_t resident = warps * (32 / gg);
                     if (resident > best) {
@@ -234,8 +240,12 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             break;
         }
         case SOFTMAX_PATH_CLUSTER: {
-            int threads = fth > 0 ? fth : (nv <= 16 * 512 * 4 ? 512 : 1024);
-            int vpt = fvpt > 0 ? fvpt : 4;
+            // 16-bit rows: slices of 256 threads x 8 vectors held in registers;
+            // fp32 rows (which would spill there): TMA-staged slices of 512 or
+            // 1024 threads x 4 vectors
+            const bool regs = es == 2 && fth <= 0 && fvpt <= 0 && cdiv(nv, 2048) <= 16;
+            int threads = fth > 0 ? fth : (regs ? 256 : (nv <= 16 * 512 * 4 ? 512 : 1024));
+            int vpt = fvpt > 0 ? fvpt : (regs ? 8 : 4);
             int64_t csize = fgrp > 0 ? fgrp : cdiv(nv, (int64_t)threads * vpt);
             if (!cluster_shape_ok(threads, vpt, es) || csize < 1 || csize > 16) return SOFTMAX_ERR_UNSUPPORTED;
             if (cdiv(nv, csize) > (int64_t)threads * vpt) return SOFTMAX_ERR_UNSUPPORTED;

@@ -120,7 +120,8 @@ def test_dispatch_follows_width_rule():
     assert plan(4096, 16391) == B.PATH_CTA
     assert plan(4096, 2048, "f16") in (B.PATH_RING, B.PATH_CTA)  # aligned: ring or registers
     assert plan(4096, 16384) == B.PATH_CTA           # 512 x 8 keeps two 64 KB rows per SM
-    assert plan(512, 131072, "bf16") == B.PATH_RING      # long rows: ring of clusters
+    assert plan(512, 131072, "bf16") == B.PATH_CLUSTER   # long 16-bit rows: a cluster, registers
+    assert plan(512, 65536) == B.PATH_RING               # long aligned fp32 rows: ring of clusters
     assert plan(512, 131079, "bf16") == B.PATH_CLUSTER   # long misaligned rows, enough of them
     assert plan(4, 131072, "bf16") == B.PATH_SPLIT       # too few rows to fill the GPU
     assert plan(64, 1 << 22) == B.PATH_SPLIT             # too long for a cluster
