@@ -416,10 +416,12 @@ def per_shape(args, peaks, l2, dev) -> dict:
         set_bytes = 2 * xd.numel() * xd.element_size()
         sets = rotating_sets(xd, set_bytes, l2)
         med, _, _ = time_steps(launch, sets, 200, 50)
-        # the copy ceiling: rows*cols*elem bytes (as 4-byte words), device to
-        # device, same rotation
-        nbytes = w.rows * w.cols * w.elem_bytes
-        nwords = -(-nbytes // 4)
+        # the copy ceiling: rows*cols*elem bytes, device to device, same
+        # rotation; the size is rounded down to 64 KiB because the runtime's
+        # copy runs at half speed on sizes that are not (200,000,000 bytes:
+        # 131 us, 199,950,336 bytes: 60 us)
+        nbytes = max(65536, (w.rows * w.cols * w.elem_bytes) // 65536 * 65536)
+        nwords = nbytes // 4
         csets = [(torch.empty(nwords, dtype=torch.int32, device=dev), torch.empty(nwords, dtype=torch.int32, device=dev))
                  for _ in range(max(2, -(-int(2.5 * l2) // (8 * nwords))))]
         cmed, _, _ = time_steps(lambda a, b: b.copy_(a), csets, 200, 50)

@@ -7,8 +7,12 @@ namespace mbrs {
 namespace {
 template <typename T, int THREADS, int VPT>
 cudaError_t go(const LaunchArgs &a, int64_t grid) {
-    k_cta_rows<T, THREADS, VPT><<<(unsigned)grid, THREADS, 0, a.stream>>>(
-        static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store);
+    if constexpr (VPT >= 6)
+        k_cta_rows_wide<T, THREADS, VPT><<<(unsigned)grid, THREADS, 0, a.stream>>>(
+            static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store);
+    else
+        k_cta_rows<T, THREADS, VPT><<<(unsigned)grid, THREADS, 0, a.stream>>>(
+            static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store);
     return cudaGetLastError();
 }
 

@@ -76,11 +76,9 @@ __device__ __forceinline__ void block_merge(float &m, float &l, float2 *red) {
     group_merge<32>(m, l);
 }
 
-// With 6 or more vectors per thread the kernel is bounded to 64 registers
-// (1024 threads per SM), so that such wide rows still have two in flight per SM.
 template <typename T, int THREADS, int VPT>
-__global__ void __launch_bounds__(THREADS, (VPT >= 6 && THREADS < 1024) ? 1024 / THREADS : 1)
-    k_cta_rows(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store) {
+__device__ __forceinline__ void cta_rows_body(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride,
+                                              int vec_store) {
     constexpr int NW = THREADS / 32;
     __shared__ float2 red[2][NW];
     int parity = 0;
@@ -93,6 +91,23 @@ __global__ void __launch_bounds__(THREADS, (VPT >= 6 && THREADS < 1024) ? 1024 /
         block_merge<NW>(m, l, red[parity]);
         tile.scale_store(rv, threadIdx.x, THREADS, rv.nvec, out_factor(s.x, m, l));
     }
+}
+
+// Up to 5 vectors per thread: the compiler's own register choice (an explicit
+// minimum of one block per SM lets it take more: 64 instead of 40 registers
+// for 64 threads x 4 fp16 vectors).
+template <typename T, int THREADS, int VPT>
+__global__ void __launch_bounds__(THREADS) k_cta_rows(const T *in, T *out, int64_t rows, int64_t cols,
+                                                      int64_t stride, int vec_store) {
+    cta_rows_body<T, THREADS, VPT>(in, out, rows, cols, stride, vec_store);
+}
+
+// 6 or more vectors per thread: bounded to 64 registers (1024 threads per SM),
+// so that such wide rows still have two in flight per SM.
+template <typename T, int THREADS, int VPT>
+__global__ void __launch_bounds__(THREADS, 1024 / THREADS)
+    k_cta_rows_wide(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store) {
+    cta_rows_body<T, THREADS, VPT>(in, out, rows, cols, stride, vec_store);
 }
 
 // ---------------------------------------------------------------------------
