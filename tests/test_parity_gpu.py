@@ -282,19 +282,21 @@ def test_offsets_beyond_int32():
 
 # -- the bounded wait and the device error word ------------------------------------------
 
-@pytest.mark.parametrize("path,group", [(B.PATH_CLUSTER, 0), (B.PATH_RING, 1), (B.PATH_RING, 4)])
-def test_wait_timeout_is_reported_and_recoverable(path, group):
+@pytest.mark.parametrize("path,threads,vpt,group", [(B.PATH_CLUSTER, 512, 4, 0), (B.PATH_RING, 0, 0, 1),
+                                                    (B.PATH_RING, 0, 0, 4)])
+def test_wait_timeout_is_reported_and_recoverable(path, threads, vpt, group):
+    # the TMA-fed shapes (the cluster path's register-held slices have no waits)
     x = rnd(4, 20000, "bf16", seed=5)
     c = DeviceCase(x, "bf16")
     B.set_wait_test(1_000_000, starve=True)  # 1 ms, and the TMA barriers are never armed
     try:
-        assert c.run(20000, path=path, group=group) == B.OK
+        assert c.run(20000, path=path, threads=threads, vpt=vpt, group=group) == B.OK
         assert B.check_device_error() == B.ERR_TIMEOUT
     finally:
         B.set_wait_test(0, False)
     assert B.check_device_error() == B.OK
     # outputs were skipped, the context is still usable and the next call is exact
-    run_and_compare(x, "bf16", path=path, group=group)
+    run_and_compare(x, "bf16", path=path, threads=threads, vpt=vpt, group=group)
 
 
 # -- the tensor-level binding --------------------------------------------------------------
