@@ -154,7 +154,8 @@ int softmax_check_device_error(cudaStream_t stream);
 
 /*
  * Test hooks for the bounded waits of the CLUSTER and RING paths.  wait_limit_ns
- * bounds each wait on a TMA completion barrier (default 1 s; <= 0 restores it).
+ * bounds each wait on a TMA completion barrier (default 1 s; <= 0 restores it;
+ * values above 1 s are capped at 1 s, since the waits time 32-bit intervals).
  * starve != 0 makes the next launches skip arming that barrier, so the wait
  * can only run out: the kernel records SOFTMAX_ERR_TIMEOUT, skips its stores
  * and returns normally.  Process-wide, not thread-safe.

@@ -529,7 +529,8 @@ int softmax_check_device_error(cudaStream_t stream) {
 }
 
 int softmax_set_wait_test(int64_t wait_limit_ns, int starve) {
-    g_wait_ns.store(wait_limit_ns > 0 ? wait_limit_ns : kDefaultWaitNs);
+    // a drain wait lasts twice the limit and must stay under 2^31 ns
+    g_wait_ns.store(wait_limit_ns > 0 ? std::min(wait_limit_ns, kDefaultWaitNs) : kDefaultWaitNs);
     g_starve.store(starve ? 1 : 0);
     return SOFTMAX_OK;
 }

@@ -132,9 +132,11 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+// Low 32 bits of the global nanosecond timer (wraps every 4.29 s; differences
+// taken modulo 2^32 are right for intervals shorter than that).
+__device__ __forceinline__ uint32_t global_timer_lo() {
+    uint32_t t;
+    asm volatile("mov.u32 %0, %%globaltimer_lo;" : "=r"(t));
     return t;
 }
 
@@ -165,12 +167,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 // Bounded wait for phase `parity` of an mbarrier: gives up after limit_ns of
 // global time and returns false.  Never spins without a bound.
+// The timer is read 32 bits wide (two fewer live registers in the waits that
+// sit beside register-held tiles), so limit_ns is capped at 2^31 ns.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
+    const uint32_t limit = (uint32_t)min(limit_ns, (int64_t)0x7fffffff);
+    const uint32_t t0 = global_timer_lo();
     for (uint32_t it = 0; it < (1u << 30); ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((int64_t)(global_timer_ns() - t0) > limit_ns) return false;
+        if (global_timer_lo() - t0 > limit) return false;
     }
     return false;
 }

@@ -124,7 +124,8 @@ static __device__ unsigned int g_error_word = 0;
 template <int THREADS, int VPT>
 struct ClusterSmem {
     static constexpr int kStageBytes = THREADS * VPT * kVecBytes;
-    static constexpr int kBarOff = kStageBytes;
+    static constexpr int kBarOff = kStageBytes;      // TMA completion barrier
+    static constexpr int kXbarOff = kBarOff + 8;     // state exchange barrier
     static constexpr int kRedOff = kBarOff + 16;
     static constexpr int kSlotOff = kRedOff + (THREADS / 32) * 8;
     static constexpr int kBytes = kSlotOff + kMaxCluster * 8;
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     float2 *red = reinterpret_cast<float2 *>(smem + L::kRedOff);
     float2 *slots = reinterpret_cast<float2 *>(smem + L::kSlotOff);
     const uint32_t bar = smem_addr(smem + L::kBarOff);
+    const uint32_t xbar = smem_addr(smem + L::kXbarOff);
     const int tid = threadIdx.x, lane = tid & 31;
 
     const uint32_t rank = cluster_rank(), csize = cluster_size();
@@ -163,12 +165,14 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
 
     bool ok = true;
     Tile<T, VPT> tile;
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_init(xbar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(xbar, csize * 8u);  // csize states will arrive
+    }
+    __syncthreads();
     if constexpr (TMA) {
-        if (tid == 0) {
-            mbar_init(bar, 1);
-            fence_mbar_init();
-        }
-        __syncthreads();
         if (tid == 0 && !starve) {
             if (bytes > 0) {
                 mbar_arrive_expect_tx(bar, bytes);
@@ -212,15 +216,24 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     float m = s.x, l = s.y;
     block_merge<NW>(m, l, red);
 
-    // push this block's state into every block of the cluster, then gather
+    // Send this block's state into slot `rank` of every block of the cluster
+    // (itself included) with st.async, completing on the receiver's exchange
+    // barrier, and wait until this block has received all csize states.  The
+    // cluster wait first makes sure every peer runs and has initialised its
+    // barrier.  No block leaves before it has received every peer's state, so
+    // no store can target a block that has gone.
     cluster_wait_acquire();
     if (tid == 0) {
         const uint32_t my_slot = smem_addr(slots + rank);
-        for (uint32_t q = 0; q < csize; ++q) st_cluster_f2(map_to_rank(my_slot, q), m, l);
+        for (uint32_t q = 0; q < csize; ++q) st_async_f2(map_to_rank(my_slot, q), m, l, map_to_rank(xbar, q));
     }
-    __syncwarp();
-    cluster_arrive_release();
-    cluster_wait_acquire();
+    if (!mbar_wait_bounded(xbar, 0, wait_ns)) {
+        atomicOr(&g_error_word, kErrWaitTimeout);
+        ok = false;
+        // a late peer (one whose own copy wait ran out) may still send: stay
+        // resident for as long as its waits can last before leaving
+        mbar_wait_bounded(xbar, 0, 2 * wait_ns);
+    }
     const float2 w = lane < (int)csize ? slots[lane] : make_float2(-INFINITY, 0.f);
     m = w.x;
     l = w.y;
