@@ -258,6 +258,7 @@ def run_ours(args) -> dict | None:
 
     if args.force:
         B.set_force_path(*[int(v) for v in args.force.split(",")])
+    B.set_launch_overlap(not args.no_overlap)
     plan = B.plan(x_dev.data_ptr(), x_dev.data_ptr() + (1 << 40), w.rows, w.cols, w.stride, code)
     set_bytes = 2 * x_dev.numel() * x_dev.element_size()
     sets = rotating_sets(x_dev, set_bytes, l2)
@@ -305,6 +306,7 @@ def run_ours(args) -> dict | None:
             "l2": f"inputs larger than L2: {len(sets)} rotating buffer sets, "
                   f"{len(sets) * set_bytes / 1e6:.0f} MB > 2.5 x L2 ({l2 / 1e6:.0f} MB)",
             "timing": "K launches captured in one CUDA graph, replayed between CUDA events",
+            "launch_overlap": not args.no_overlap,
             "path": B.PATH_NAMES.get(plan["path"]), "threads": plan["threads"], "vpt": plan["vpt"],
             "group": plan["group"],
         },
@@ -416,6 +418,10 @@ def per_shape(args, peaks, l2, dev) -> dict:
         set_bytes = 2 * xd.numel() * xd.element_size()
         sets = rotating_sets(xd, set_bytes, l2)
         med, _, _ = time_steps(launch, sets, 200, 50)
+        # the same launches in plain stream order (no launch overlap)
+        B.set_launch_overlap(False)
+        med_plain, _, _ = time_steps(launch, sets, 200, 50)
+        B.set_launch_overlap(not args.no_overlap)
         # the copy ceiling: rows*cols*elem bytes, device to device, same
         # rotation; the size is rounded down to 64 KiB because the runtime's
         # copy runs at half speed on sizes that are not (200,000,000 bytes:
@@ -430,6 +436,7 @@ def per_shape(args, peaks, l2, dev) -> dict:
         copy_gbs = 2 * nbytes / (cmed / 1e3) / 1e9
         table[w.name] = {
             "path": B.PATH_NAMES.get(plan["path"]), "us_per_call": round(med * 1e3, 2),
+            "us_per_call_no_overlap": round(med_plain * 1e3, 2),
             "gbs": round(alg, 1), "frac_of_measured_hbm": round(alg / peaks["hbm_gbs"], 4),
             "frac_of_nominal_8tbs": round(alg / 8000.0, 4),
             "copy_us": round(cmed * 1e3, 2), "copy_gbs": round(copy_gbs, 1),
@@ -501,6 +508,8 @@ def main(argv=None):
     ap.add_argument("--only-kernel", action="store_true",
                     help="warm-up and timed launches only (the command profiled with ncu)")
     ap.add_argument("--json-out", default="")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="launch in plain stream order (no programmatic dependent launch)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -148,7 +148,9 @@ int softmax_plan(uint64_t in_addr, uint64_t out_addr, int64_t rows, int64_t cols
 /*
  * Synchronise `stream`, then read and clear this device's error word.
  * Returns SOFTMAX_ERR_TIMEOUT if a bounded wait ran out in any kernel since the
- * last check, SOFTMAX_ERR_CUDA if the synchronisation failed, else SOFTMAX_OK.
+ * last check, SOFTMAX_ERR_CUDA if the synchronisation failed or a cluster
+ * kernel found itself launched without clusters (it then did nothing), else
+ * SOFTMAX_OK.
  */
 int softmax_check_device_error(cudaStream_t stream);
 
@@ -161,6 +163,19 @@ int softmax_check_device_error(cudaStream_t stream);
  * and returns normally.  Process-wide, not thread-safe.
  */
 int softmax_set_wait_test(int64_t wait_limit_ns, int starve);
+
+/*
+ * Launch overlap (programmatic dependent launch), on by default.  With
+ * enable != 0 each kernel this library launches may be scheduled while the
+ * previous kernel in its stream is still finishing; before it reads or writes
+ * any global memory it waits on the device (griddepcontrol.wait) until that
+ * kernel has completed and its writes are visible, so the results are the
+ * same either way.  What overlaps is the launch latency and block placement,
+ * most visible for small inputs and for calls issued back to back.
+ * enable == 0 launches in plain stream order.  Process-wide; returns
+ * SOFTMAX_OK.
+ */
+int softmax_set_launch_overlap(int enable);
 
 /*
  * softmax_fwd_noalloc -- the same softmax for callers that cannot allocate
@@ -194,7 +209,8 @@ int softmax_set_wait_test(int64_t wait_limit_ns, int starve);
 int softmax_fwd_noalloc(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride,
                         int dtype, cudaStream_t stream);
 
-/* Version of this ABI: major * 10000 + minor * 100 + patch (1.1.0 adds the RING path). */
+/* Version of this ABI: major * 10000 + minor * 100 + patch (1.1.0 adds the RING
+ * path, 1.2.0 softmax_set_launch_overlap). */
 int softmax_abi_version(void);
 
 #ifdef __cplusplus

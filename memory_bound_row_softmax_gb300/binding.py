@@ -40,6 +40,7 @@ SIGNATURES = {
     "softmax_plan": (_int, [_u64, _u64, _i64, _i64, _i64, _int, _int, ctypes.POINTER(Plan)]),
     "softmax_check_device_error": (_int, [_vp]),
     "softmax_set_wait_test": (_int, [_i64, _int]),
+    "softmax_set_launch_overlap": (_int, [_int]),
     "softmax_abi_version": (_int, []),
     "softmax_fwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp]),
 }
@@ -163,6 +164,11 @@ def check_device_error(stream=None) -> int:
 
 def set_wait_test(wait_limit_ns: int = 0, starve: bool = False) -> None:
     lib().softmax_set_wait_test(wait_limit_ns, 1 if starve else 0)
+
+
+def set_launch_overlap(enable: bool = True) -> None:
+    """Programmatic dependent launch on (default) or off, process-wide."""
+    lib().softmax_set_launch_overlap(1 if enable else 0)
 
 
 def abi_version() -> int:

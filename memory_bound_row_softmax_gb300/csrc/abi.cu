@@ -27,7 +27,7 @@ using namespace mbrs;
 
 namespace {
 
-constexpr int kAbiVersion = 10100;  // 1.1.0
+constexpr int kAbiVersion = 10200;  // 1.2.0
 constexpr int kVecBytes = 16;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDefaultWaitNs = 1000000000;  // 1 s
@@ -37,6 +37,7 @@ std::atomic<int> g_last_path{0};
 std::atomic<int> g_force_path{0}, g_force_threads{0}, g_force_vpt{0}, g_force_group{0};
 std::atomic<int64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int> g_starve{0};
+std::atomic<int> g_overlap{1};
 
 struct Plan {
     int path = 0, threads = 0, vpt = 0, group = 1, launches = 0, vec_store = 0, stages = 0;
@@ -430,7 +431,7 @@ int softmax_fwd(const void *in, void *out, int64_t rows, int64_t cols, int64_t r
     Plan p;
     st = make_plan(ia, oa, rows, cols, row_stride, dtype, sms, &p);
     if (st != SOFTMAX_OK) return st;
-    LaunchArgs a{in, out, rows, cols, row_stride, dtype, p.vec_store, stream};
+    LaunchArgs a{in, out, rows, cols, row_stride, dtype, p.vec_store, stream, g_overlap.load()};
     st = run(p, a);
     if (st == SOFTMAX_OK) g_last_path.store(p.path);
     return st;
@@ -449,7 +450,7 @@ int softmax_fwd_noalloc(const void *in, void *out, int64_t rows, int64_t cols, i
     st = plan_noalloc(ia, rows, cols, row_stride, dtype, sms, &chunks, &chunk_vecs, &grid);
     if (st != SOFTMAX_OK) return st;
     const int vec_store = (ia % kVecBytes) == (oa % kVecBytes);
-    LaunchArgs a{in, out, rows, cols, row_stride, dtype, vec_store, stream};
+    LaunchArgs a{in, out, rows, cols, row_stride, dtype, vec_store, stream, g_overlap.load()};
     const cudaError_t e = launch_split_noalloc(a, chunks, chunk_vecs, grid);
     if (e == cudaErrorInvalidValue) return SOFTMAX_ERR_SCRATCH_LIMIT;
     return e == cudaSuccess ? SOFTMAX_OK : SOFTMAX_ERR_CUDA;
@@ -513,7 +514,7 @@ int softmax_plan(uint64_t in_addr, uint64_t out_addr, int64_t rows, int64_t cols
     plan->stages = p.stages;
     if (p.path == SOFTMAX_PATH_RING && num_sms == 0) {  // the persistent grid the launch will use
         RingCfg c{p.threads, p.vpt, p.group, p.stages, (int)p.slice_vecs, p.smem};
-        LaunchArgs a{nullptr, nullptr, rows, cols, row_stride, dtype, p.vec_store, nullptr};
+        LaunchArgs a{nullptr, nullptr, rows, cols, row_stride, dtype, p.vec_store, nullptr, 0};
         int64_t grid = 0;
         if (launch_ring(a, c, 0, 0, &grid) != cudaSuccess) return SOFTMAX_ERR_CUDA;
         plan->grid = grid;
@@ -525,6 +526,7 @@ int softmax_check_device_error(cudaStream_t stream) {
     unsigned int word = 0, ring_word = 0;
     if (read_clear_error_word(stream, &word) != cudaSuccess) return SOFTMAX_ERR_CUDA;
     if (read_clear_ring_error_word(&ring_word) != cudaSuccess) return SOFTMAX_ERR_CUDA;
+    if ((word | ring_word) & kErrNotCluster) return SOFTMAX_ERR_CUDA;
     return (word | ring_word) ? SOFTMAX_ERR_TIMEOUT : SOFTMAX_OK;
 }
 
@@ -532,6 +534,11 @@ int softmax_set_wait_test(int64_t wait_limit_ns, int starve) {
     // a drain wait lasts twice the limit and must stay under 2^31 ns
     g_wait_ns.store(wait_limit_ns > 0 ? std::min(wait_limit_ns, kDefaultWaitNs) : kDefaultWaitNs);
     g_starve.store(starve ? 1 : 0);
+    return SOFTMAX_OK;
+}
+
+int softmax_set_launch_overlap(int enable) {
+    g_overlap.store(enable ? 1 : 0);
     return SOFTMAX_OK;
 }
 

@@ -140,6 +140,17 @@ __device__ __forceinline__ uint32_t global_timer_lo() {
     return t;
 }
 
+// Programmatic dependent launch.  griddepcontrol.wait returns once the grid
+// this one depends on (the previous kernel in the stream, when this grid was
+// launched with programmatic stream serialisation; otherwise nothing) has
+// completed and its memory operations are visible.  Every kernel calls this
+// before its first global-memory access, then lets the next grid in the stream
+// be scheduled: that grid waits the same way before it touches memory.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // mbarrier (shared::cta) -- arrival/transaction barrier the TMA engine completes.
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -201,6 +212,14 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
 }
+// True when this grid was launched with explicit cluster dimensions.
+__device__ __forceinline__ bool explicit_cluster() {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmov.pred p, %%is_explicit_cluster;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r));
+    return r != 0;
+}
 __device__ __forceinline__ uint32_t cluster_size() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
@@ -232,8 +251,6 @@ __device__ __forceinline__ void st_cluster_f2(uint32_t addr, float a, float b) {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 
-// device error word bit: a bounded wait ran out
-constexpr unsigned int kErrWaitTimeout = 1u;
 
 // ---------------------------------------------------------------------------
 // (s, l) states, s = fl(max * log2 e)

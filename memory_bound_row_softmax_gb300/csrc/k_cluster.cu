@@ -37,22 +37,9 @@ cudaError_t go(const LaunchArgs &a, int csize, int64_t wait_ns, int starve) {
     if (e != cudaSuccess) return e;
     e = prepare<T, THREADS, VPT, TMA>(device);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.rows * csize), 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = cluster_smem<THREADS, VPT, TMA>();
-    cfg.stream = a.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k_cluster_rows<T, THREADS, VPT, TMA>, static_cast<const T *>(a.in),
-                           static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store, wait_ns, starve);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launch_kernel(k_cluster_rows<T, THREADS, VPT, TMA>, a, a.rows * csize, THREADS,
+                         cluster_smem<THREADS, VPT, TMA>(), csize, static_cast<const T *>(a.in),
+                         static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store, wait_ns, starve);
 }
 
 // 2 or 4 vectors per thread: slices staged in shared memory by TMA; 8: slices

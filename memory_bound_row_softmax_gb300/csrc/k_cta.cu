@@ -8,12 +8,12 @@ namespace {
 template <typename T, int THREADS, int VPT>
 cudaError_t go(const LaunchArgs &a, int64_t grid) {
     if constexpr (VPT >= 6)
-        k_cta_rows_wide<T, THREADS, VPT><<<(unsigned)grid, THREADS, 0, a.stream>>>(
-            static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store);
+        return launch_kernel(k_cta_rows_wide<T, THREADS, VPT>, a, grid, THREADS, 0, 0,
+                             static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride,
+                             a.vec_store);
     else
-        k_cta_rows<T, THREADS, VPT><<<(unsigned)grid, THREADS, 0, a.stream>>>(
-            static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store);
-    return cudaGetLastError();
+        return launch_kernel(k_cta_rows<T, THREADS, VPT>, a, grid, THREADS, 0, 0, static_cast<const T *>(a.in),
+                             static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store);
 }
 
 template <typename T, int THREADS>

@@ -43,14 +43,12 @@ cudaError_t states_address(int device, float2 **ptr) {
 template <typename T>
 cudaError_t go(const LaunchArgs &a, int64_t chunks, int64_t chunk_vecs, int64_t grid, float2 *states) {
     constexpr int kThreads = kNoAllocThreads, kVpt = kNoAllocVpt;
-    k_split_stats<T, kThreads, kVpt><<<(unsigned)grid, kThreads, 0, a.stream>>>(
-        static_cast<const T *>(a.in), a.rows, a.cols, a.stride, chunks, chunk_vecs, states);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_kernel(k_split_stats<T, kThreads, kVpt>, a, grid, kThreads, 0, 0,
+                                  static_cast<const T *>(a.in), a.rows, a.cols, a.stride, chunks, chunk_vecs, states);
     if (e != cudaSuccess) return e;
-    k_split_apply<T, kThreads, kVpt><<<(unsigned)grid, kThreads, 0, a.stream>>>(
-        static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride, chunks, chunk_vecs,
-        states, a.vec_store);
-    return cudaGetLastError();
+    return launch_kernel(k_split_apply<T, kThreads, kVpt>, a, grid, kThreads, 0, 0,
+                         static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride, chunks,
+                         chunk_vecs, states, a.vec_store);
 }
 }  // namespace
 

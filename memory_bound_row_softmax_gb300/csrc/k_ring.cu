@@ -120,23 +120,9 @@ cudaError_t go(const LaunchArgs &a, const RingCfg &c, int64_t wait_ns, int starv
     const int64_t grid = units * c.csize;
     if (grid_out) *grid_out = grid;
     if (!a.in) return cudaSuccess;  // grid query only
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)c.smem;
-    cfg.stream = a.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)c.csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = c.csize > 1 ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, k_ring_rows<T, THREADS, VPT, CL>, static_cast<const T *>(a.in),
-                           static_cast<T *>(a.out), a.rows, a.cols, a.stride, c.stages, c.slice_vecs, wait_ns,
-                           starve);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launch_kernel(k_ring_rows<T, THREADS, VPT, CL>, a, grid, THREADS, (size_t)c.smem, c.csize > 1 ? c.csize : 0,
+                         static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride, c.stages,
+                         c.slice_vecs, wait_ns, starve);
 }
 
 template <typename T, int THREADS>

@@ -8,14 +8,12 @@ namespace {
 template <typename T, int THREADS, int VPT>
 cudaError_t go(const LaunchArgs &a, int64_t chunks, int64_t chunk_vecs, int64_t grid, void *scratch) {
     float2 *part = static_cast<float2 *>(scratch);
-    k_split_stats<T, THREADS, VPT><<<(unsigned)grid, THREADS, 0, a.stream>>>(
-        static_cast<const T *>(a.in), a.rows, a.cols, a.stride, chunks, chunk_vecs, part);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_kernel(k_split_stats<T, THREADS, VPT>, a, grid, THREADS, 0, 0,
+                                  static_cast<const T *>(a.in), a.rows, a.cols, a.stride, chunks, chunk_vecs, part);
     if (e != cudaSuccess) return e;
-    k_split_apply<T, THREADS, VPT><<<(unsigned)grid, THREADS, 0, a.stream>>>(
-        static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride, chunks, chunk_vecs,
-        part, a.vec_store);
-    return cudaGetLastError();
+    return launch_kernel(k_split_apply<T, THREADS, VPT>, a, grid, THREADS, 0, 0,
+                         static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride, chunks,
+                         chunk_vecs, part, a.vec_store);
 }
 
 template <typename T>

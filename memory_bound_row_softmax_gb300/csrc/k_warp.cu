@@ -7,9 +7,8 @@ namespace mbrs {
 namespace {
 template <typename T, int G, int VPT>
 cudaError_t go(const LaunchArgs &a, int threads, int64_t grid) {
-    k_warp_rows<T, G, VPT><<<(unsigned)grid, threads, 0, a.stream>>>(
-        static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store);
-    return cudaGetLastError();
+    return launch_kernel(k_warp_rows<T, G, VPT>, a, grid, threads, 0, 0, static_cast<const T *>(a.in),
+                         static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store);
 }
 
 template <typename T, int G>

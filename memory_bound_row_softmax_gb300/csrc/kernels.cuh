@@ -30,6 +30,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "launch.h"
 
 namespace mbrs {
 
@@ -39,6 +40,7 @@ namespace mbrs {
 template <typename T, int G, int VPT>
 __global__ void __launch_bounds__(256) k_warp_rows(const T *in, T *out, int64_t rows, int64_t cols,
                                                    int64_t stride, int vec_store) {
+    pdl_enter();
     static_assert(G >= 2 && G <= 32 && (G & (G - 1)) == 0, "lane group is a power of two");
     const int t = threadIdx.x & (G - 1);
     const int64_t groups_per_block = blockDim.x / G;
@@ -99,6 +101,7 @@ __device__ __forceinline__ void cta_rows_body(const T *in, T *out, int64_t rows,
 template <typename T, int THREADS, int VPT>
 __global__ void __launch_bounds__(THREADS) k_cta_rows(const T *in, T *out, int64_t rows, int64_t cols,
                                                       int64_t stride, int vec_store) {
+    pdl_enter();
     cta_rows_body<T, THREADS, VPT>(in, out, rows, cols, stride, vec_store);
 }
 
@@ -107,6 +110,7 @@ __global__ void __launch_bounds__(THREADS) k_cta_rows(const T *in, T *out, int64
 template <typename T, int THREADS, int VPT>
 __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
     k_cta_rows_wide(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store) {
+    pdl_enter();
     cta_rows_body<T, THREADS, VPT>(in, out, rows, cols, stride, vec_store);
 }
 
@@ -138,6 +142,11 @@ template <typename T, int THREADS, int VPT, bool TMA>
 __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS))
     k_cluster_rows(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store,
                    int64_t wait_ns, int starve) {
+    pdl_enter();
+    if (!explicit_cluster()) {  // launched without clusters: touch no cluster state
+        if (threadIdx.x == 0) atomicOr(&g_error_word, kErrNotCluster);
+        return;
+    }
     constexpr int V = Elem<T>::kVec;
     constexpr int NW = THREADS / 32;
     // the layout the launch allocated: no staging area without TMA
@@ -269,6 +278,13 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? (THREADS >= 1024 ? 1 : 1024
                                                    : (THREADS >= 512 ? 1 : 512 / THREADS))
     k_ring_rows(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int stages, int slice_vecs,
                 int64_t wait_ns, int starve) {
+    pdl_enter();
+    if constexpr (CLUSTER) {
+        if (!explicit_cluster()) {  // launched without clusters: touch no cluster state
+            if (threadIdx.x == 0) atomicOr(&g_error_word, kErrNotCluster);
+            return;
+        }
+    }
     constexpr int V = Elem<T>::kVec;
     constexpr int NW = THREADS / 32;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -406,6 +422,7 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? (THREADS >= 1024 ? 1 : 1024
 template <typename T, int THREADS, int VPT>
 __global__ void __launch_bounds__(THREADS) k_split_stats(const T *in, int64_t rows, int64_t cols, int64_t stride,
                                                          int64_t chunks, int64_t chunk_vecs, float2 *part) {
+    pdl_enter();
     constexpr int NW = THREADS / 32;
     constexpr int64_t kTile = (int64_t)THREADS * VPT;
     __shared__ float2 red[2][NW];
@@ -433,6 +450,7 @@ template <typename T, int THREADS, int VPT>
 __global__ void __launch_bounds__(THREADS)
     k_split_apply(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int64_t chunks,
                   int64_t chunk_vecs, const float2 *part, int vec_store) {
+    pdl_enter();
     constexpr int V = Elem<T>::kVec;
     constexpr int NW = THREADS / 32;
     constexpr int64_t kTile = (int64_t)THREADS * VPT;

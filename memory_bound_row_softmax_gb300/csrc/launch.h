@@ -16,7 +16,53 @@ struct LaunchArgs {
     int dtype;      // 0 f32, 1 f16, 2 bf16
     int vec_store;  // out shares in's 16-byte phase
     cudaStream_t stream;
+    int overlap;    // launch with programmatic stream serialisation
 };
+
+// Device error word bits (k_cluster.cu / k_ring.cu each hold one word):
+// a bounded wait ran out; a cluster kernel found itself launched without a
+// cluster (it then returns before any cluster access).
+constexpr unsigned int kErrWaitTimeout = 1u;
+constexpr unsigned int kErrNotCluster = 2u;
+
+// Launch `kernel` on a.stream; csize >= 1 makes it a cluster launch with
+// clusters of csize blocks (kernels that use cluster instructions need it,
+// even for csize == 1), csize == 0 a plain launch.
+// With a.overlap set the launch allows programmatic dependent launch: the
+// grid may be scheduled while the previous kernel in the stream is still
+// finishing, so that its launch latency and block rasterisation overlap that
+// kernel's tail.  Every kernel of this library therefore starts with
+// griddepcontrol.wait (pdl_enter), which returns only once the previous grid
+// has completed and its memory operations are visible, before its first
+// global-memory access.
+template <typename... P, typename... A>
+cudaError_t launch_kernel(void (*kernel)(P...), const LaunchArgs &a, int64_t grid, int threads, size_t smem,
+                          int csize, A &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (csize >= 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)csize;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (a.overlap) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<A &&>(args)...);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
 
 // Each launcher returns cudaErrorInvalidValue when no instantiation matches
 // the requested shape (the planner only asks for shapes that exist).

@@ -322,3 +322,53 @@ def test_torch_binding(tdtype, name):
     assert (B.softmax_fwd(view.contiguous()).double() - vref).abs().max().item() <= tol
     with pytest.raises(ValueError):
         B.softmax_fwd(x.t())
+
+
+# -- launch overlap (programmatic dependent launch) ----------------------------------------
+
+def _bits_tensor(x: np.ndarray, dtype: str) -> torch.Tensor:
+    a = W.bits_view(np.ascontiguousarray(x), dtype)
+    return torch.from_numpy(a.view(np.int32) if dtype == "f32" else a.view(np.int16)).cuda()
+
+
+OVERLAP_CASES = [(B.PATH_WARP, 700), (B.PATH_CTA, 3000), (B.PATH_CLUSTER, 20011), (B.PATH_SPLIT, 20011),
+                 (B.PATH_RING, 16384), (0, 65536)]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("path,cols", OVERLAP_CASES)
+def test_launch_overlap_orders_against_neighbours(dtype, path, cols):
+    """Calls issued back to back on one stream, with the overlap on: before
+    each call a torch kernel rewrites the shared input buffer (the call must
+    read the new data, not the old) and right after it the next rewrite
+    follows (it must not land before the call has read).  Each output is
+    checked against the oracle, and a chain of in-place calls matches the
+    same chain run in plain stream order bit for bit."""
+    rows, k = 48, 5
+    xs = [rnd(rows, cols, dtype, 900 + i) for i in range(k)]
+    srcs = [_bits_tensor(x, dtype) for x in xs]
+    buf = torch.empty_like(srcs[0])
+    outs = [torch.empty_like(buf) for _ in range(k)]
+    code = W.DTYPES.index(dtype)
+    stream = torch.cuda.current_stream().cuda_stream
+    B.set_force_path(path)
+    try:
+        B.set_launch_overlap(True)
+        for i in range(k):
+            buf.copy_(srcs[i])
+            assert B.softmax_fwd_ptr(buf.data_ptr(), outs[i].data_ptr(), rows, cols, cols, code, stream) == B.OK
+        chains = {}
+        for overlap in (True, False):
+            B.set_launch_overlap(overlap)
+            z = srcs[0].clone()
+            for _ in range(4):
+                assert B.softmax_fwd_ptr(z.data_ptr(), z.data_ptr(), rows, cols, cols, code, stream) == B.OK
+            chains[overlap] = z
+        torch.cuda.synchronize()
+        assert B.check_device_error() == B.OK
+    finally:
+        B.set_launch_overlap(True)
+        B.set_force_path(0)
+    for i in range(k):
+        compare(outs[i].cpu().numpy().view(W.storage_dtype(dtype)), xs[i], dtype, cols)
+    assert torch.equal(chains[True], chains[False])
