@@ -151,6 +151,26 @@ __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// L2 prefetch hints.  A prefetch does not change what any later load
+// returns, so a kernel may issue them before griddepcontrol.wait: with launch
+// overlap its input starts moving from HBM into L2 while the previous kernel
+// is still finishing.  Only the 16-byte-aligned interior of elements
+// [e0, e1) of a row of `cols` elements (clipped to the row) is prefetched, so
+// no byte outside the row is named.
+constexpr uintptr_t kPrefetchPiece = 65536;
+__device__ __forceinline__ void prefetch_l2(uintptr_t addr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
+}
+template <typename T>
+__device__ __forceinline__ void prefetch_span_l2(const T *row, int64_t e0, int64_t e1, int64_t cols) {
+    e0 = max(e0, (int64_t)0);
+    e1 = min(e1, cols);
+    if (e1 <= e0) return;
+    const uintptr_t a = ((uintptr_t)(row + e0) + 15) & ~(uintptr_t)15;
+    const uintptr_t e = (uintptr_t)(row + e1) & ~(uintptr_t)15;
+    for (uintptr_t q = a; q < e; q += kPrefetchPiece) prefetch_l2(q, (uint32_t)min(e - q, kPrefetchPiece));
+}
+
 // mbarrier (shared::cta) -- arrival/transaction barrier the TMA engine completes.
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -40,7 +40,6 @@ namespace mbrs {
 template <typename T, int G, int VPT>
 __global__ void __launch_bounds__(256) k_warp_rows(const T *in, T *out, int64_t rows, int64_t cols,
                                                    int64_t stride, int vec_store) {
-    pdl_enter();
     static_assert(G >= 2 && G <= 32 && (G & (G - 1)) == 0, "lane group is a power of two");
     const int t = threadIdx.x & (G - 1);
     const int64_t groups_per_block = blockDim.x / G;
@@ -48,6 +47,9 @@ __global__ void __launch_bounds__(256) k_warp_rows(const T *in, T *out, int64_t 
     // rows of this warp's first group; the loop bound is warp-uniform so that
     // every lane reaches every shuffle
     const int64_t warp_row0 = (int64_t)blockIdx.x * groups_per_block + (threadIdx.x & ~31) / G;
+    if (t == 0 && warp_row0 + (threadIdx.x & 31) / G < rows)
+        prefetch_span_l2(in + (warp_row0 + (threadIdx.x & 31) / G) * stride, 0, cols, cols);
+    pdl_enter();
     for (int64_t base = warp_row0; base < rows; base += row_step) {
         const int64_t row = base + (threadIdx.x & 31) / G;
         const bool active = row < rows;
@@ -83,6 +85,8 @@ __device__ __forceinline__ void cta_rows_body(const T *in, T *out, int64_t rows,
                                               int vec_store) {
     constexpr int NW = THREADS / 32;
     __shared__ float2 red[2][NW];
+    if (threadIdx.x == 0 && blockIdx.x < rows) prefetch_span_l2(in + blockIdx.x * stride, 0, cols, cols);
+    pdl_enter();
     int parity = 0;
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
         RowView<T> rv(in + row * stride, out + row * stride, cols, vec_store != 0);
@@ -101,7 +105,6 @@ __device__ __forceinline__ void cta_rows_body(const T *in, T *out, int64_t rows,
 template <typename T, int THREADS, int VPT>
 __global__ void __launch_bounds__(THREADS) k_cta_rows(const T *in, T *out, int64_t rows, int64_t cols,
                                                       int64_t stride, int vec_store) {
-    pdl_enter();
     cta_rows_body<T, THREADS, VPT>(in, out, rows, cols, stride, vec_store);
 }
 
@@ -110,7 +113,6 @@ __global__ void __launch_bounds__(THREADS) k_cta_rows(const T *in, T *out, int64
 template <typename T, int THREADS, int VPT>
 __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
     k_cta_rows_wide(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store) {
-    pdl_enter();
     cta_rows_body<T, THREADS, VPT>(in, out, rows, cols, stride, vec_store);
 }
 
@@ -142,8 +144,8 @@ template <typename T, int THREADS, int VPT, bool TMA>
 __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS))
     k_cluster_rows(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store,
                    int64_t wait_ns, int starve) {
-    pdl_enter();
     if (!explicit_cluster()) {  // launched without clusters: touch no cluster state
+        pdl_enter();
         if (threadIdx.x == 0) atomicOr(&g_error_word, kErrNotCluster);
         return;
     }
@@ -171,6 +173,8 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     const int64_t full_end = ((rv.head + cols) % V) != 0 ? rv.nvec - 1 : rv.nvec;
     const int64_t f0 = max(s0, first_full), f1 = min(s1, full_end);
     const uint32_t bytes = f1 > f0 ? (uint32_t)((f1 - f0) * kVecBytes) : 0u;
+    if (tid == 0) prefetch_span_l2(in + row * stride, s0 * V - rv.head, s1 * V - rv.head, cols);
+    pdl_enter();
 
     bool ok = true;
     Tile<T, VPT> tile;
@@ -278,9 +282,9 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? (THREADS >= 1024 ? 1 : 1024
                                                    : (THREADS >= 512 ? 1 : 512 / THREADS))
     k_ring_rows(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int stages, int slice_vecs,
                 int64_t wait_ns, int starve) {
-    pdl_enter();
     if constexpr (CLUSTER) {
         if (!explicit_cluster()) {  // launched without clusters: touch no cluster state
+            pdl_enter();
             if (threadIdx.x == 0) atomicOr(&g_error_word, kErrNotCluster);
             return;
         }
@@ -312,7 +316,10 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? (THREADS >= 1024 ? 1 : 1024
         mbar_init(xbar_base, 1);
         mbar_init(xbar_base + 8, 1);
         fence_mbar_init();
+        for (int64_t i = 0; i < min((int64_t)stages, nrows); ++i)
+            prefetch_span_l2(in + (cid + i * ncl) * stride, s0 * V, s1 * V, cols);
     }
+    pdl_enter();
     __syncthreads();
 
     // producer (thread 0): load this block's slice of local row i into slot i % stages
@@ -419,9 +426,21 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? (THREADS >= 1024 ? 1 : 1024
 // ---------------------------------------------------------------------------
 // path 4: rows split over the grid (two passes, states in scratch)
 // ---------------------------------------------------------------------------
+// L2 prefetch of this block's first chunk (one thread), ahead of pdl_enter.
+template <typename T>
+__device__ __forceinline__ void prefetch_first_chunk(const T *in, int64_t rows, int64_t cols, int64_t stride,
+                                                     int64_t chunks, int64_t chunk_vecs) {
+    constexpr int V = Elem<T>::kVec;
+    if (threadIdx.x != 0 || (int64_t)blockIdx.x >= rows * chunks) return;
+    const int64_t row = blockIdx.x / chunks, k = blockIdx.x - row * chunks;
+    const RowView<T> rv(in + row * stride, nullptr, cols, false);
+    prefetch_span_l2(rv.in, k * chunk_vecs * V - rv.head, (k + 1) * chunk_vecs * V - rv.head, cols);
+}
+
 template <typename T, int THREADS, int VPT>
 __global__ void __launch_bounds__(THREADS) k_split_stats(const T *in, int64_t rows, int64_t cols, int64_t stride,
                                                          int64_t chunks, int64_t chunk_vecs, float2 *part) {
+    prefetch_first_chunk(in, rows, cols, stride, chunks, chunk_vecs);
     pdl_enter();
     constexpr int NW = THREADS / 32;
     constexpr int64_t kTile = (int64_t)THREADS * VPT;
@@ -450,6 +469,7 @@ template <typename T, int THREADS, int VPT>
 __global__ void __launch_bounds__(THREADS)
     k_split_apply(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int64_t chunks,
                   int64_t chunk_vecs, const float2 *part, int vec_store) {
+    prefetch_first_chunk(in, rows, cols, stride, chunks, chunk_vecs);
     pdl_enter();
     constexpr int V = Elem<T>::kVec;
     constexpr int NW = THREADS / 32;
