@@ -133,6 +133,9 @@ typedef struct {
     int64_t scratch_bytes; /* device scratch the call needs (SPLIT only) */
     int64_t hbm_bytes;     /* algorithmic bytes: 2 * rows * cols * elem (3x for SPLIT) */
     int stages;            /* shared-memory ring stages per block (RING), else 0 */
+    int whole_vectors;     /* 1 if every row is whole 16-byte vectors (in and out 16-byte
+                              aligned, row stride and width multiples of 16 bytes): the
+                              kernels then run their variants without edge tests */
 } softmax_plan_t;
 
 /*

@@ -25,7 +25,7 @@ _i64, _u64, _int, _vp = ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_
 class Plan(ctypes.Structure):
     _fields_ = [("path", _int), ("threads", _int), ("vpt", _int), ("group", _int), ("launches", _int),
                 ("vec_store", _int), ("grid", _i64), ("smem_bytes", _i64), ("scratch_bytes", _i64),
-                ("hbm_bytes", _i64), ("stages", _int)]
+                ("hbm_bytes", _i64), ("stages", _int), ("whole_vectors", _int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

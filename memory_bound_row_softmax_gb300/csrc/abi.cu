@@ -40,7 +40,7 @@ std::atomic<int> g_starve{0};
 std::atomic<int> g_overlap{1};
 
 struct Plan {
-    int path = 0, threads = 0, vpt = 0, group = 1, launches = 0, vec_store = 0, stages = 0;
+    int path = 0, threads = 0, vpt = 0, group = 1, launches = 0, vec_store = 0, stages = 0, whole = 0;
     int64_t grid = 0, smem = 0, scratch = 0, hbm = 0, chunks = 1, chunk_vecs = 0, slice_vecs = 0;
 };
 
@@ -155,6 +155,9 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
     const int64_t head = (int64_t)((in % kVecBytes) / es);
     const int64_t nv = uniform ? cdiv(head + cols, V) : cdiv(cols + V - 1, V);
     p->vec_store = (in % kVecBytes) == (out % kVecBytes);
+    // every row made of whole 16-byte vectors: the kernels' edge-free variants
+    p->whole = in % kVecBytes == 0 && out % kVecBytes == 0 && (row_stride * es) % kVecBytes == 0 &&
+               (cols * es) % kVecBytes == 0;
     p->hbm = 2 * rows * cols * es;
 
     const int fpath = g_force_path.load(), fth = g_force_threads.load(), fvpt = g_force_vpt.load(),
@@ -431,7 +434,7 @@ int softmax_fwd(const void *in, void *out, int64_t rows, int64_t cols, int64_t r
     Plan p;
     st = make_plan(ia, oa, rows, cols, row_stride, dtype, sms, &p);
     if (st != SOFTMAX_OK) return st;
-    LaunchArgs a{in, out, rows, cols, row_stride, dtype, p.vec_store, stream, g_overlap.load()};
+    LaunchArgs a{in, out, rows, cols, row_stride, dtype, p.vec_store, stream, g_overlap.load(), p.whole};
     st = run(p, a);
     if (st == SOFTMAX_OK) g_last_path.store(p.path);
     return st;
@@ -450,7 +453,7 @@ int softmax_fwd_noalloc(const void *in, void *out, int64_t rows, int64_t cols, i
     st = plan_noalloc(ia, rows, cols, row_stride, dtype, sms, &chunks, &chunk_vecs, &grid);
     if (st != SOFTMAX_OK) return st;
     const int vec_store = (ia % kVecBytes) == (oa % kVecBytes);
-    LaunchArgs a{in, out, rows, cols, row_stride, dtype, vec_store, stream, g_overlap.load()};
+    LaunchArgs a{in, out, rows, cols, row_stride, dtype, vec_store, stream, g_overlap.load(), 0};
     const cudaError_t e = launch_split_noalloc(a, chunks, chunk_vecs, grid);
     if (e == cudaErrorInvalidValue) return SOFTMAX_ERR_SCRATCH_LIMIT;
     return e == cudaSuccess ? SOFTMAX_OK : SOFTMAX_ERR_CUDA;
@@ -512,9 +515,10 @@ int softmax_plan(uint64_t in_addr, uint64_t out_addr, int64_t rows, int64_t cols
     plan->scratch_bytes = p.scratch;
     plan->hbm_bytes = p.hbm;
     plan->stages = p.stages;
+    plan->whole_vectors = p.whole;
     if (p.path == SOFTMAX_PATH_RING && num_sms == 0) {  // the persistent grid the launch will use
         RingCfg c{p.threads, p.vpt, p.group, p.stages, (int)p.slice_vecs, p.smem};
-        LaunchArgs a{nullptr, nullptr, rows, cols, row_stride, dtype, p.vec_store, nullptr, 0};
+        LaunchArgs a{nullptr, nullptr, rows, cols, row_stride, dtype, p.vec_store, nullptr, 0, p.whole};
         int64_t grid = 0;
         if (launch_ring(a, c, 0, 0, &grid) != cudaSuccess) return SOFTMAX_ERR_CUDA;
         plan->grid = grid;

@@ -380,6 +380,15 @@ struct RowView {
     }
 };
 
+// Tiles of rows made of whole 16-byte vectors only (WHOLE = true: in and out
+// 16-byte aligned, row stride and width multiples of 16 bytes, decided by the
+// host for the whole call): a thread's vectors first + j*step (j < VPT) move
+// as plain 16-byte accesses at constant offsets, with no edge test; those with
+// j*step >= whole_fit(first, end) lie past the tile's end.
+__device__ __forceinline__ int whole_fit(int64_t first, int64_t end) {
+    return (int)max(min(end - first, (int64_t)0x7fffffff), (int64_t)0);
+}
+
 // A thread's tile of VPT vectors.  Two forms share one interface:
 //   FloatTile   the elements widened to fp32 (fp32 data: no extra registers);
 //               stats() overwrites them with e = 2^(x log2 e - s_t).
@@ -388,10 +397,10 @@ struct RowView {
 //               computed again, with the same shift, when the results are
 //               formed -- the same bits, two exps per element instead of one.
 // Interface: set(j, raw) / set_empty(j) / load_one(j, row, v) /
-// load(row, first, step, end);
+// load<WHOLE>(row, first, step, end);
 // stats() -> (s_t, l_t); values(j, f, y): y = e * f for vector j;
 // values_shift(j, shift, f, y): y = 2^(x log2 e - shift) * f (inputs only,
-// before stats()); scale_store(row, first, step, end, f).
+// before stats()); scale_store<WHOLE>(row, first, step, end, f).
 template <typename T, int VPT>
 struct FloatTile {
     static constexpr int V = Elem<T>::kVec;
@@ -404,14 +413,27 @@ struct FloatTile {
         for (int i = 0; i < V; ++i) x[j][i] = -INFINITY;
     }
     // load vectors first + j*step (j < VPT) of a row, -inf past `end`
+    template <bool WHOLE = false>
     __device__ __forceinline__ void load(const RowView<T> &row, int64_t first, int64_t step, int64_t end) {
+        if constexpr (WHOLE) {
+            const uint4 *p = reinterpret_cast<const uint4 *>(row.in) + first;
+            const int fit = whole_fit(first, end);
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int64_t v = first + j * step;
-            if (v < end)
-                row.load(v, x[j]);
-            else
-                set_empty(j);
+            for (int j = 0; j < VPT; ++j) {
+                if (j * step < fit)
+                    Elem<T>::unpack(p[j * step], x[j]);
+                else
+                    set_empty(j);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int64_t v = first + j * step;
+                if (v < end)
+                    row.load(v, x[j]);
+                else
+                    set_empty(j);
+            }
         }
     }
     // Replace x by e = 2^(x log2 e - s_t) with the tile's own max m_t and
@@ -445,15 +467,29 @@ struct FloatTile {
 #pragma unroll
         for (int i = 0; i < V; ++i) y[i] = ex2(fmaf(x[j][i], kLog2e, -shift)) * f;
     }
+    template <bool WHOLE = false>
     __device__ __forceinline__ void scale_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
                                                 float f) const {
+        if constexpr (WHOLE) {
+            uint4 *q = reinterpret_cast<uint4 *>(row.out) + first;
+            const int fit = whole_fit(first, end);
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int64_t v = first + j * step;
-            if (v < end) {
-                float y[V];
-                values(j, f, y);
-                row.store(v, y);
+            for (int j = 0; j < VPT; ++j) {
+                if (j * step < fit) {
+                    float y[V];
+                    values(j, f, y);
+                    q[j * step] = Elem<T>::pack(y);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int64_t v = first + j * step;
+                if (v < end) {
+                    float y[V];
+                    values(j, f, y);
+                    row.store(v, y);
+                }
             }
         }
     }
@@ -472,14 +508,27 @@ struct PackedTile {
         const uint32_t w = (uint32_t)Elem<T>::kNegInfBits * 0x10001u;
         raw[j] = make_uint4(w, w, w, w);
     }
+    template <bool WHOLE = false>
     __device__ __forceinline__ void load(const RowView<T> &row, int64_t first, int64_t step, int64_t end) {
+        if constexpr (WHOLE) {
+            const uint4 *p = reinterpret_cast<const uint4 *>(row.in) + first;
+            const int fit = whole_fit(first, end);
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int64_t v = first + j * step;
-            if (v < end)
-                raw[j] = row.load_raw(v);
-            else
-                set_empty(j);
+            for (int j = 0; j < VPT; ++j) {
+                if (j * step < fit)
+                    raw[j] = p[j * step];
+                else
+                    set_empty(j);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int64_t v = first + j * step;
+                if (v < end)
+                    raw[j] = row.load_raw(v);
+                else
+                    set_empty(j);
+            }
         }
     }
     __device__ __forceinline__ float2 stats() {
@@ -521,15 +570,29 @@ struct PackedTile {
         for (int i = 0; i < V; ++i) y[i] = ex2(fmaf(x[i], kLog2e, -sh)) * f;
     }
     __device__ __forceinline__ void values(int j, float f, float *y) const { values_shift(j, shift, f, y); }
+    template <bool WHOLE = false>
     __device__ __forceinline__ void scale_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
                                                 float f) const {
+        if constexpr (WHOLE) {
+            uint4 *q = reinterpret_cast<uint4 *>(row.out) + first;
+            const int fit = whole_fit(first, end);
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int64_t v = first + j * step;
-            if (v < end) {
-                float y[V];
-                values(j, f, y);
-                row.store(v, y);
+            for (int j = 0; j < VPT; ++j) {
+                if (j * step < fit) {
+                    float y[V];
+                    values(j, f, y);
+                    q[j * step] = Elem<T>::pack(y);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int64_t v = first + j * step;
+                if (v < end) {
+                    float y[V];
+                    values(j, f, y);
+                    row.store(v, y);
+                }
             }
         }
     }

@@ -16,13 +16,13 @@ constexpr int cluster_smem() {
     return TMA ? ClusterSmem<THREADS, VPT>::kBytes : ClusterSmem<THREADS, 0>::kBytes;
 }
 
-template <typename T, int THREADS, int VPT, bool TMA>
+template <typename T, int THREADS, int VPT, bool TMA, bool WHOLE>
 cudaError_t prepare(int device) {
     // per-device, once: opt in to large dynamic shared memory and clusters of 16
     static std::atomic<unsigned long long> done{0};
     const unsigned long long bit = 1ull << (device & (kMaxDevices - 1));
     if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    auto fn = k_cluster_rows<T, THREADS, VPT, TMA>;
+    auto fn = k_cluster_rows<T, THREADS, VPT, TMA, WHOLE>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          cluster_smem<THREADS, VPT, TMA>());
     if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -30,16 +30,22 @@ cudaError_t prepare(int device) {
     return e;
 }
 
-template <typename T, int THREADS, int VPT, bool TMA>
-cudaError_t go(const LaunchArgs &a, int csize, int64_t wait_ns, int starve) {
+template <typename T, int THREADS, int VPT, bool TMA, bool WHOLE>
+cudaError_t go_as(const LaunchArgs &a, int csize, int64_t wait_ns, int starve) {
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;
-    e = prepare<T, THREADS, VPT, TMA>(device);
+    e = prepare<T, THREADS, VPT, TMA, WHOLE>(device);
     if (e != cudaSuccess) return e;
-    return launch_kernel(k_cluster_rows<T, THREADS, VPT, TMA>, a, a.rows * csize, THREADS,
+    return launch_kernel(k_cluster_rows<T, THREADS, VPT, TMA, WHOLE>, a, a.rows * csize, THREADS,
                          cluster_smem<THREADS, VPT, TMA>(), csize, static_cast<const T *>(a.in),
                          static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store, wait_ns, starve);
+}
+
+template <typename T, int THREADS, int VPT, bool TMA>
+cudaError_t go(const LaunchArgs &a, int csize, int64_t wait_ns, int starve) {
+    return a.whole ? go_as<T, THREADS, VPT, TMA, true>(a, csize, wait_ns, starve)
+                   : go_as<T, THREADS, VPT, TMA, false>(a, csize, wait_ns, starve);
 }
 
 // 2 or 4 vectors per thread: slices staged in shared memory by TMA; 8: slices

@@ -37,7 +37,7 @@ namespace mbrs {
 // ---------------------------------------------------------------------------
 // path 1: a lane group per row
 // ---------------------------------------------------------------------------
-template <typename T, int G, int VPT>
+template <typename T, int G, int VPT, bool WHOLE>
 __global__ void __launch_bounds__(256) k_warp_rows(const T *in, T *out, int64_t rows, int64_t cols,
                                                    int64_t stride, int vec_store) {
     static_assert(G >= 2 && G <= 32 && (G & (G - 1)) == 0, "lane group is a power of two");
@@ -56,11 +56,11 @@ __global__ void __launch_bounds__(256) k_warp_rows(const T *in, T *out, int64_t 
         RowView<T> rv(in + (active ? row : 0) * stride, out + (active ? row : 0) * stride, cols,
                       vec_store != 0);
         Tile<T, VPT> tile;
-        tile.load(rv, t, G, active ? rv.nvec : 0);
+        tile.template load<WHOLE>(rv, t, G, active ? rv.nvec : 0);
         const float2 s = tile.stats();
         float m = s.x, l = s.y;
         group_merge<G>(m, l);
-        if (active) tile.scale_store(rv, t, G, rv.nvec, out_factor(s.x, m, l));
+        if (active) tile.template scale_store<WHOLE>(rv, t, G, rv.nvec, out_factor(s.x, m, l));
     }
 }
 
@@ -80,7 +80,7 @@ __device__ __forceinline__ void block_merge(float &m, float &l, float2 *red) {
     group_merge<32>(m, l);
 }
 
-template <typename T, int THREADS, int VPT>
+template <typename T, int THREADS, int VPT, bool WHOLE>
 __device__ __forceinline__ void cta_rows_body(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride,
                                               int vec_store) {
     constexpr int NW = THREADS / 32;
@@ -91,29 +91,29 @@ __device__ __forceinline__ void cta_rows_body(const T *in, T *out, int64_t rows,
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
         RowView<T> rv(in + row * stride, out + row * stride, cols, vec_store != 0);
         Tile<T, VPT> tile;
-        tile.load(rv, threadIdx.x, THREADS, rv.nvec);
+        tile.template load<WHOLE>(rv, threadIdx.x, THREADS, rv.nvec);
         const float2 s = tile.stats();
         float m = s.x, l = s.y;
         block_merge<NW>(m, l, red[parity]);
-        tile.scale_store(rv, threadIdx.x, THREADS, rv.nvec, out_factor(s.x, m, l));
+        tile.template scale_store<WHOLE>(rv, threadIdx.x, THREADS, rv.nvec, out_factor(s.x, m, l));
     }
 }
 
 // Up to 5 vectors per thread: the compiler's own register choice (an explicit
 // minimum of one block per SM lets it take more: 64 instead of 40 registers
 // for 64 threads x 4 fp16 vectors).
-template <typename T, int THREADS, int VPT>
+template <typename T, int THREADS, int VPT, bool WHOLE>
 __global__ void __launch_bounds__(THREADS) k_cta_rows(const T *in, T *out, int64_t rows, int64_t cols,
                                                       int64_t stride, int vec_store) {
-    cta_rows_body<T, THREADS, VPT>(in, out, rows, cols, stride, vec_store);
+    cta_rows_body<T, THREADS, VPT, WHOLE>(in, out, rows, cols, stride, vec_store);
 }
 
 // 6 or more vectors per thread: bounded to 64 registers (1024 threads per SM),
 // so that such wide rows still have two in flight per SM.
-template <typename T, int THREADS, int VPT>
+template <typename T, int THREADS, int VPT, bool WHOLE>
 __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
     k_cta_rows_wide(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store) {
-    cta_rows_body<T, THREADS, VPT>(in, out, rows, cols, stride, vec_store);
+    cta_rows_body<T, THREADS, VPT, WHOLE>(in, out, rows, cols, stride, vec_store);
 }
 
 // ---------------------------------------------------------------------------
@@ -140,7 +140,7 @@ struct ClusterSmem {
 // TMA = true: each block pulls its slice into shared memory with bulk copies;
 // TMA = false: each block loads its slice straight into registers (no
 // staging, so occupancy is bounded by registers alone).
-template <typename T, int THREADS, int VPT, bool TMA>
+template <typename T, int THREADS, int VPT, bool TMA, bool WHOLE>
 __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS))
     k_cluster_rows(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store,
                    int64_t wait_ns, int starve) {
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
         }
     } else {
         cluster_arrive_relaxed();
-        tile.load(rv, s0 + tid, THREADS, s1);
+        tile.template load<WHOLE>(rv, s0 + tid, THREADS, s1);
     }
     const float2 s = tile.stats();
     float m = s.x, l = s.y;
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     m = w.x;
     l = w.y;
     group_merge<32>(m, l);
-    if (ok) tile.scale_store(rv, s0 + tid, THREADS, s1, out_factor(s.x, m, l));
+    if (ok) tile.template scale_store<WHOLE>(rv, s0 + tid, THREADS, s1, out_factor(s.x, m, l));
 }
 
 // ---------------------------------------------------------------------------

@@ -17,6 +17,8 @@ struct LaunchArgs {
     int vec_store;  // out shares in's 16-byte phase
     cudaStream_t stream;
     int overlap;    // launch with programmatic stream serialisation
+    int whole;      // every row is whole 16-byte vectors: in and out 16-byte
+                    // aligned, row stride and width multiples of 16 bytes
 };
 
 // Device error word bits (k_cluster.cu / k_ring.cu each hold one word):
@@ -71,6 +73,9 @@ cudaError_t launch_warp(const LaunchArgs &a, int threads, int group, int vpt, in
 
 bool cta_shape_ok(int threads, int vpt);
 cudaError_t launch_cta(const LaunchArgs &a, int threads, int vpt, int64_t grid);
+// the instantiations for a.whole (k_warp_whole.cu, k_cta_whole.cu)
+cudaError_t launch_warp_whole(const LaunchArgs &a, int threads, int group, int vpt, int64_t grid);
+cudaError_t launch_cta_whole(const LaunchArgs &a, int threads, int vpt, int64_t grid);
 
 bool cluster_shape_ok(int threads, int vpt, int elem_bytes);
 int64_t cluster_smem_bytes(int threads, int vpt);

@@ -112,6 +112,21 @@ def test_plans_cover_every_row(rows, cols, stride, dt, in_off):
     assert p["hbm_bytes"] == mult * rows * cols * es
 
 
+@pytest.mark.parametrize("in_off,out_off,cols,stride,dt,whole", [
+    (0, 0, 2048, 2048, "f16", 1),      # aligned rows of whole vectors
+    (0, 0, 1000, 1000, "f32", 1),      # 4000-byte rows: whole vectors
+    (0, 0, 1001, 1001, "f32", 0),      # the width leaves a partial last vector
+    (0, 0, 1000, 1001, "f32", 0),      # the stride moves later rows off 16 bytes
+    (4, 4, 1000, 1000, "f32", 0),      # in and out start inside a vector
+    (0, 8, 1000, 1000, "f32", 0),      # out not aligned
+    (0, 0, 8, 8, "bf16", 1),
+    (0, 0, 7, 8, "bf16", 0),
+])
+def test_plan_reports_whole_vector_rows(in_off, out_off, cols, stride, dt, whole):
+    p = B.plan((1 << 24) + in_off, (1 << 40) + out_off, 64, cols, stride, dt, num_sms=152)
+    assert p["whole_vectors"] == whole
+
+
 def test_dispatch_follows_width_rule():
     plan = lambda r, c, dt="f32": B.plan(1 << 24, 1 << 40, r, c, c, dt, num_sms=152)["path"]
     assert plan(64, 1000) == B.PATH_WARP          # cols <= 1024: a warp per row
