@@ -90,18 +90,6 @@ bool cta_shape(int64_t nv, int *threads_out, int *vpt_out) {
     return best > 0;
 }
 
-// Row bytes the block-per-row register kernel keeps in flight per SM: rows
-// resident at once (registers: 4 per 16-byte vector -- fp32 values, or
-// 16-bit data kept packed -- plus ~24 per thread) times the row's bytes.  When this reaches ~96 KB the kernel already runs at
-// copy speed (measured: fp32 4096-wide rows); below it the shared-memory ring,
-// whose prefetch does not cost registers, keeps more bytes in flight.
-constexpr int64_t kRegInFlightEnough = 96 * 1024;
-int64_t cta_bytes_in_flight(int64_t nv) {
-    int threads = 0, vpt = 0;
-    if (!cta_shape(nv, &threads, &vpt)) return 0;
-    return cta_rows_per_sm(threads, vpt) * nv * kVecBytes;
-}
-
 int elem_bytes(int dtype) { return dtype == SOFTMAX_F32 ? 4 : 2; }
 
 // Host-side argument checks, in the order the header documents.
@@ -167,17 +155,22 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
                          ((cols * es) % kVecBytes) == 0;
     int path = fpath;
     if (path == SOFTMAX_PATH_AUTO) {
-        if (cols <= 1024 && nv <= 32 * 9) {
+        if (nv <= 32 * 9 && (cols <= 1024 || p->whole)) {
+            // a warp per row while a warp's registers hold it; past 1024
+            // columns only for rows of whole vectors (4096 x 2048 fp16: warp
+            // 5.8 us, block 6.3 us; 4096 x 2047 bf16: warp 8.9 us, block 8.7 us)
             path = SOFTMAX_PATH_WARP;
         } else if (nv > 512 * 10 && es == 2 && cdiv(nv, 2048) <= 16 && rows * cdiv(nv, 2048) >= sms) {
             // 16-bit rows longer than a block's registers: a cluster holding the
             // row in registers, 2048 vectors per block (c5: 52 us, ring 57 us)
             path = SOFTMAX_PATH_CLUSTER;
-        } else if (ring_ok && cdiv(nv, 16) <= 4096 && rows * 16 * 2 >= sms &&
-                   cta_bytes_in_flight(nv) < kRegInFlightEnough) {
-            path = SOFTMAX_PATH_RING;
         } else if (nv <= 512 * 10) {
+            // a block per row while its registers hold the row: it beats the
+            // ring at every such width measured (8192 x 2816 fp16: block 14.4
+            // us, ring 17.1; 4096 x 2816 fp32: 14.0 against 19.5)
             path = SOFTMAX_PATH_CTA;
+        } else if (ring_ok && cdiv(nv, 16) <= 4096 && rows * 16 * 2 >= sms) {
+            path = SOFTMAX_PATH_RING;
         } else {
             const int64_t csize = cdiv(nv, nv <= 16 * 512 * 4 ? 512 * 4 : 1024 * 4);
             const bool fits = csize <= 16 && rows * csize <= kMaxGrid;
@@ -215,7 +208,9 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
                 if (fvpt > 0) vpt = fvpt;
             }
             if (!warp_shape_ok(g, vpt) || (int64_t)g * vpt < nv) return SOFTMAX_ERR_UNSUPPORTED;
-            int threads = fth > 0 ? fth : 128;
+            // 8 rows per block for rows of 6+ vectors per lane (4096 x 2048
+            // fp16: 5.8 us at 256 threads, 6.0 us at 128), else 4
+            int threads = fth > 0 ? fth : (g == 32 && vpt >= 6 ? 256 : 128);
             if (fth <= 0)  // spread small problems over more SMs
                 while (threads > 32 && cdiv(rows * g, threads) < sms) threads /= 2;
             if (threads < 32 || threads > 256 || threads % 32 != 0 || threads % g != 0)
