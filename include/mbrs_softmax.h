@@ -84,9 +84,12 @@ typedef enum {
                                  part, (max, sum) exchanged through distributed shared memory */
     SOFTMAX_PATH_SPLIT = 4,   /* rows split across the whole grid: pass 1 writes
                                  per-chunk (max, sum), pass 2 merges them, re-reads and writes */
-    SOFTMAX_PATH_RING = 5     /* persistent blocks or clusters (<= 16 blocks per row) looping over
+    SOFTMAX_PATH_RING = 5,    /* persistent blocks or clusters (<= 16 blocks per row) looping over
                                  rows, fed by a ring of shared-memory stages that TMA bulk copies
                                  keep full; rows of whole aligned 16-byte vectors only */
+    SOFTMAX_PATH_STREAM = 6   /* a cluster (<= 16 blocks) per row, each block streaming its slice
+                                 of any length twice: pass 1 (max, sum), exchange through
+                                 distributed shared memory, pass 2 re-read and write; no scratch */
 } softmax_path_t;
 
 /*
@@ -115,7 +118,7 @@ int softmax_last_path(void);
  * Test and tuning hook: force every following call onto `path` (0 = automatic).
  * threads / vpt / group override the launch shape where > 0 (threads per block,
  * 16-byte vectors per thread, and lanes per row / cluster size / chunks per
- * row for paths 1 / 3 and 5 / 4).  A forced shape that cannot cover the row makes
+ * row for paths 1 / 3, 5 and 6 / 4).  A forced shape that cannot cover the row makes
  * softmax_fwd return SOFTMAX_ERR_UNSUPPORTED.  Process-wide, not thread-safe.
  */
 int softmax_set_force_path(int path, int threads, int vpt, int group);
@@ -125,13 +128,13 @@ typedef struct {
     int path;              /* softmax_path_t actually chosen */
     int threads;           /* threads per block */
     int vpt;               /* 16-byte vectors per thread per tile */
-    int group;             /* lanes per row (1), cluster size (3, 5), chunks per row (4), else 1 */
+    int group;             /* lanes per row (1), cluster size (3, 5, 6), chunks per row (4), else 1 */
     int launches;          /* kernels per call: 1, or 2 for the SPLIT path */
     int vec_store;         /* 1 if out has in's 16-byte phase (vector stores) */
     int64_t grid;          /* blocks of the (first) kernel */
     int64_t smem_bytes;    /* dynamic shared memory per block */
     int64_t scratch_bytes; /* device scratch the call needs (SPLIT only) */
-    int64_t hbm_bytes;     /* algorithmic bytes: 2 * rows * cols * elem (3x for SPLIT) */
+    int64_t hbm_bytes;     /* algorithmic bytes: 2 * rows * cols * elem (3x for SPLIT, STREAM) */
     int stages;            /* shared-memory ring stages per block (RING), else 0 */
     int whole_vectors;     /* 1 if every row is whole 16-byte vectors (in and out 16-byte
                               aligned, row stride and width multiples of 16 bytes): the
@@ -213,7 +216,8 @@ int softmax_fwd_noalloc(const void *in, void *out, int64_t rows, int64_t cols, i
                         int dtype, cudaStream_t stream);
 
 /* Version of this ABI: major * 10000 + minor * 100 + patch (1.1.0 adds the RING
- * path, 1.2.0 softmax_set_launch_overlap). */
+ * path, 1.2.0 softmax_set_launch_overlap, 1.3.0 the STREAM path and
+ * softmax_plan_t.whole_vectors). */
 int softmax_abi_version(void);
 
 #ifdef __cplusplus

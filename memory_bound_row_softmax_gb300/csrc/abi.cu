@@ -27,7 +27,7 @@ using namespace mbrs;
 
 namespace {
 
-constexpr int kAbiVersion = 10200;  // 1.2.0
+constexpr int kAbiVersion = 10300;  // 1.3.0
 constexpr int kVecBytes = 16;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDefaultWaitNs = 1000000000;  // 1 s
@@ -172,9 +172,17 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
         } else if (ring_ok && cdiv(nv, 16) <= 4096 && rows * 16 * 2 >= sms) {
             path = SOFTMAX_PATH_RING;
         } else {
+            // a cluster holding the row on chip (one tile per block); else a
+            // cluster streaming it twice when rows x 16 blocks fill the GPU;
+            // else (a few very long rows) the grid-wide split
             const int64_t csize = cdiv(nv, nv <= 16 * 512 * 4 ? 512 * 4 : 1024 * 4);
             const bool fits = csize <= 16 && rows * csize <= kMaxGrid;
-            path = (fits && rows * csize >= sms) ? SOFTMAX_PATH_CLUSTER : SOFTMAX_PATH_SPLIT;
+            if (fits && rows * csize >= sms)
+                path = SOFTMAX_PATH_CLUSTER;
+            else if (rows * 16 >= sms && rows * 16 <= kMaxGrid)
+                path = SOFTMAX_PATH_STREAM;
+            else
+                path = SOFTMAX_PATH_SPLIT;
         }
     }
     p->path = path;
@@ -300,6 +308,23 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             p->grid = units * csize;  // estimate; the launch sizes it from occupancy
             break;
         }
+        case SOFTMAX_PATH_STREAM: {
+            // 512 threads x 4 vectors per tile; blocks per row: two blocks per
+            // SM in all (one per row when the rows alone give that), at most 16
+            const int threads = fth > 0 ? fth : 512;
+            const int vpt = fvpt > 0 ? fvpt : 4;
+            const int64_t csize =
+                fgrp > 0 ? fgrp : std::min<int64_t>(16, std::max<int64_t>(1, cdiv(2 * (int64_t)sms, rows)));
+            if (!stream_shape_ok(threads, vpt) || csize < 1 || csize > 16 || rows * csize > kMaxGrid)
+                return SOFTMAX_ERR_UNSUPPORTED;
+            p->threads = threads;
+            p->vpt = vpt;
+            p->group = (int)csize;
+            p->grid = rows * csize;
+            p->smem = stream_smem_bytes(threads);
+            p->hbm = 3 * rows * cols * es;
+            break;
+        }
         case SOFTMAX_PATH_SPLIT: {
             const int threads = fth > 0 ? fth : 256;
             const int vpt = fvpt > 0 ? fvpt : 4;
@@ -368,6 +393,7 @@ int run(const Plan &p, const LaunchArgs &a) {
         case SOFTMAX_PATH_CLUSTER:
             e = launch_cluster(a, p.threads, p.vpt, p.group, g_wait_ns.load(), g_starve.load());
             break;
+        case SOFTMAX_PATH_STREAM: e = launch_stream(a, p.threads, p.vpt, p.group, g_wait_ns.load()); break;
         case SOFTMAX_PATH_RING: {
             RingCfg c{p.threads, p.vpt, p.group, p.stages, (int)p.slice_vecs, p.smem};
             e = launch_ring(a, c, g_wait_ns.load(), g_starve.load(), nullptr);
@@ -476,7 +502,7 @@ const char *softmax_status_string(int status) {
 int softmax_last_path(void) { return g_last_path.load(); }
 
 int softmax_set_force_path(int path, int threads, int vpt, int group) {
-    if (path < SOFTMAX_PATH_AUTO || path > SOFTMAX_PATH_RING) return SOFTMAX_ERR_ARG;
+    if (path < SOFTMAX_PATH_AUTO || path > SOFTMAX_PATH_STREAM) return SOFTMAX_ERR_ARG;
     g_force_path.store(path);
     g_force_threads.store(threads > 0 ? threads : 0);
     g_force_vpt.store(vpt > 0 ? vpt : 0);

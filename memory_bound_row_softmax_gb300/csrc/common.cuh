@@ -389,6 +389,36 @@ __device__ __forceinline__ int whole_fit(int64_t first, int64_t end) {
     return (int)max(min(end - first, (int64_t)0x7fffffff), (int64_t)0);
 }
 
+// Store a tile's results: for vectors first + j*step < end, val(j, y) fills
+// the V floats of vector j, rounded once to T on the way out.
+template <typename T, int VPT, bool WHOLE, typename F>
+__device__ __forceinline__ void tile_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
+                                           F &&val) {
+    constexpr int V = Elem<T>::kVec;
+    if constexpr (WHOLE) {
+        uint4 *q = reinterpret_cast<uint4 *>(row.out) + first;
+        const int fit = whole_fit(first, end);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            if (j * step < fit) {
+                float y[V];
+                val(j, y);
+                q[j * step] = Elem<T>::pack(y);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t v = first + j * step;
+            if (v < end) {
+                float y[V];
+                val(j, y);
+                row.store(v, y);
+            }
+        }
+    }
+}
+
 // A thread's tile of VPT vectors.  Two forms share one interface:
 //   FloatTile   the elements widened to fp32 (fp32 data: no extra registers);
 //               stats() overwrites them with e = 2^(x log2 e - s_t).
@@ -400,7 +430,8 @@ __device__ __forceinline__ int whole_fit(int64_t first, int64_t end) {
 // load<WHOLE>(row, first, step, end);
 // stats() -> (s_t, l_t); values(j, f, y): y = e * f for vector j;
 // values_shift(j, shift, f, y): y = 2^(x log2 e - shift) * f (inputs only,
-// before stats()); scale_store<WHOLE>(row, first, step, end, f).
+// before stats()); scale_store<WHOLE>(row, first, step, end, f);
+// shift_store<WHOLE>(row, first, step, end, shift, f) (inputs only).
 template <typename T, int VPT>
 struct FloatTile {
     static constexpr int V = Elem<T>::kVec;
@@ -467,31 +498,17 @@ struct FloatTile {
 #pragma unroll
         for (int i = 0; i < V; ++i) y[i] = ex2(fmaf(x[j][i], kLog2e, -shift)) * f;
     }
+    // y = e * f (after stats())
     template <bool WHOLE = false>
     __device__ __forceinline__ void scale_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
                                                 float f) const {
-        if constexpr (WHOLE) {
-            uint4 *q = reinterpret_cast<uint4 *>(row.out) + first;
-            const int fit = whole_fit(first, end);
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                if (j * step < fit) {
-                    float y[V];
-                    values(j, f, y);
-                    q[j * step] = Elem<T>::pack(y);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int64_t v = first + j * step;
-                if (v < end) {
-                    float y[V];
-                    values(j, f, y);
-                    row.store(v, y);
-                }
-            }
-        }
+        tile_store<T, VPT, WHOLE>(row, first, step, end, [&](int j, float *y) { values(j, f, y); });
+    }
+    // y = 2^(x log2 e - shift) * f (the tile as loaded, without stats())
+    template <bool WHOLE = false>
+    __device__ __forceinline__ void shift_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
+                                                float shift, float f) const {
+        tile_store<T, VPT, WHOLE>(row, first, step, end, [&](int j, float *y) { values_shift(j, shift, f, y); });
     }
 };
 
@@ -570,31 +587,17 @@ struct PackedTile {
         for (int i = 0; i < V; ++i) y[i] = ex2(fmaf(x[i], kLog2e, -sh)) * f;
     }
     __device__ __forceinline__ void values(int j, float f, float *y) const { values_shift(j, shift, f, y); }
+    // y = e * f (after stats())
     template <bool WHOLE = false>
     __device__ __forceinline__ void scale_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
                                                 float f) const {
-        if constexpr (WHOLE) {
-            uint4 *q = reinterpret_cast<uint4 *>(row.out) + first;
-            const int fit = whole_fit(first, end);
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                if (j * step < fit) {
-                    float y[V];
-                    values(j, f, y);
-                    q[j * step] = Elem<T>::pack(y);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int64_t v = first + j * step;
-                if (v < end) {
-                    float y[V];
-                    values(j, f, y);
-                    row.store(v, y);
-                }
-            }
-        }
+        tile_store<T, VPT, WHOLE>(row, first, step, end, [&](int j, float *y) { values(j, f, y); });
+    }
+    // y = 2^(x log2 e - shift) * f (the tile as loaded, without stats())
+    template <bool WHOLE = false>
+    __device__ __forceinline__ void shift_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
+                                                float shift, float f) const {
+        tile_store<T, VPT, WHOLE>(row, first, step, end, [&](int j, float *y) { values_shift(j, shift, f, y); });
     }
 };
 

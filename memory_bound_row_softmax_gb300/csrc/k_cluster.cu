@@ -1,6 +1,8 @@
 // k_cluster.cu -- path 3 instantiations: a thread-block cluster per row, TMA
-// bulk loads into each block's shared memory and a (max, sum) exchange through
-// distributed shared memory.  Also reads and clears the device error word.
+// bulk loads into each block's shared memory (or registers only) and a
+// (max, sum) exchange through distributed shared memory; path 6, the same
+// cluster streaming slices of any length in two passes.  Also reads and
+// clears the device error word.
 #include <atomic>
 
 #include "kernels.cuh"
@@ -16,18 +18,22 @@ constexpr int cluster_smem() {
     return TMA ? ClusterSmem<THREADS, VPT>::kBytes : ClusterSmem<THREADS, 0>::kBytes;
 }
 
-template <typename T, int THREADS, int VPT, bool TMA, bool WHOLE>
-cudaError_t prepare(int device) {
-    // per-device, once: opt in to large dynamic shared memory and clusters of 16
-    static std::atomic<unsigned long long> done{0};
+// per kernel and device, once: opt in to `smem` bytes of dynamic shared
+// memory and to clusters of up to 16 blocks
+template <typename K>
+cudaError_t opt_in(K fn, int smem, std::atomic<unsigned long long> &done, int device) {
     const unsigned long long bit = 1ull << (device & (kMaxDevices - 1));
     if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    auto fn = k_cluster_rows<T, THREADS, VPT, TMA, WHOLE>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         cluster_smem<THREADS, VPT, TMA>());
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
     return e;
+}
+
+template <typename T, int THREADS, int VPT, bool TMA, bool WHOLE>
+cudaError_t prepare(int device) {
+    static std::atomic<unsigned long long> done{0};
+    return opt_in(k_cluster_rows<T, THREADS, VPT, TMA, WHOLE>, cluster_smem<THREADS, VPT, TMA>(), done, device);
 }
 
 template <typename T, int THREADS, int VPT, bool TMA, bool WHOLE>
@@ -71,7 +77,57 @@ cudaError_t by_shape(const LaunchArgs &a, int threads, int vpt, int csize, int64
         default: return cudaErrorInvalidValue;
     }
 }
+// path 6: the streaming two-pass cluster kernel
+template <typename T, int THREADS, int VPT, bool WHOLE>
+cudaError_t stream_as(const LaunchArgs &a, int csize, int64_t wait_ns) {
+    static std::atomic<unsigned long long> done{0};
+    constexpr int smem = ClusterSmem<THREADS, 0>::kBytes;
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e == cudaSuccess) e = opt_in(k_cluster_stream<T, THREADS, VPT, WHOLE>, smem, done, device);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(k_cluster_stream<T, THREADS, VPT, WHOLE>, a, a.rows * csize, THREADS, smem, csize,
+                         static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride,
+                         a.vec_store, wait_ns);
+}
+
+template <typename T, int THREADS>
+cudaError_t stream_vpt(const LaunchArgs &a, int vpt, int csize, int64_t wait_ns) {
+    switch (vpt) {
+        case 2: return a.whole ? stream_as<T, THREADS, 2, true>(a, csize, wait_ns)
+                               : stream_as<T, THREADS, 2, false>(a, csize, wait_ns);
+        case 4: return a.whole ? stream_as<T, THREADS, 4, true>(a, csize, wait_ns)
+                               : stream_as<T, THREADS, 4, false>(a, csize, wait_ns);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t stream_shape(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns) {
+    switch (threads) {
+        case 256: return stream_vpt<T, 256>(a, vpt, csize, wait_ns);
+        case 512: return stream_vpt<T, 512>(a, vpt, csize, wait_ns);
+        case 1024: return stream_vpt<T, 1024>(a, vpt, csize, wait_ns);
+        default: return cudaErrorInvalidValue;
+    }
+}
 }  // namespace
+
+bool stream_shape_ok(int threads, int vpt) {
+    return (threads == 256 || threads == 512 || threads == 1024) && (vpt == 2 || vpt == 4);
+}
+
+int64_t stream_smem_bytes(int threads) { return 16 + (threads / 32) * 8 + kMaxCluster * 8; }
+
+cudaError_t launch_stream(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns) {
+    if (csize < 1 || csize > kMaxCluster) return cudaErrorInvalidValue;
+    switch (a.dtype) {
+        case 0: return stream_shape<float>(a, threads, vpt, csize, wait_ns);
+        case 1: return stream_shape<__half>(a, threads, vpt, csize, wait_ns);
+        case 2: return stream_shape<__nv_bfloat16>(a, threads, vpt, csize, wait_ns);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 bool cluster_shape_ok(int threads, int vpt, int elem_bytes) {
     const bool t = threads == 256 || threads == 512 || threads == 1024;

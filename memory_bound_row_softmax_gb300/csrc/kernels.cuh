@@ -137,6 +137,38 @@ struct ClusterSmem {
     static constexpr int kBytes = kSlotOff + kMaxCluster * 8;
 };
 
+// Exchange a block's (s, l) state with every block of its cluster: st.async
+// into slot `rank` of each peer (itself included), completing on the peer's
+// exchange barrier `xbar` (armed for csize * 8 bytes), then a bounded wait for
+// all csize states.  The caller has announced itself with a relaxed cluster
+// arrive after initialising xbar; the cluster wait here makes sure every peer
+// has done the same before any store targets it.  No block leaves before it
+// has received every peer's state, so no store can reach a block that has
+// gone.  Returns the merged row state in (m, l) on every thread; false when a
+// wait ran out (then the block stays resident for as long as a late peer's
+// waits can last).
+template <int NW>
+__device__ __forceinline__ bool cluster_exchange(float &m, float &l, float2 *slots, uint32_t xbar, uint32_t rank,
+                                                 uint32_t csize, int64_t wait_ns) {
+    const int lane = threadIdx.x & 31;
+    cluster_wait_acquire();
+    if (threadIdx.x == 0) {
+        const uint32_t my_slot = smem_addr(slots + rank);
+        for (uint32_t q = 0; q < csize; ++q) st_async_f2(map_to_rank(my_slot, q), m, l, map_to_rank(xbar, q));
+    }
+    bool ok = true;
+    if (!mbar_wait_bounded(xbar, 0, wait_ns)) {
+        atomicOr(&g_error_word, kErrWaitTimeout);
+        ok = false;
+        mbar_wait_bounded(xbar, 0, 2 * wait_ns);
+    }
+    const float2 w = lane < (int)csize ? slots[lane] : make_float2(-INFINITY, 0.f);
+    m = w.x;
+    l = w.y;
+    group_merge<32>(m, l);
+    return ok;
+}
+
 // TMA = true: each block pulls its slice into shared memory with bulk copies;
 // TMA = false: each block loads its slice straight into registers (no
 // staging, so occupancy is bounded by registers alone).
@@ -159,7 +191,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     float2 *slots = reinterpret_cast<float2 *>(smem + L::kSlotOff);
     const uint32_t bar = smem_addr(smem + L::kBarOff);
     const uint32_t xbar = smem_addr(smem + L::kXbarOff);
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x;
 
     const uint32_t rank = cluster_rank(), csize = cluster_size();
     const int64_t row = blockIdx.x / csize;
@@ -229,29 +261,75 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     float m = s.x, l = s.y;
     block_merge<NW>(m, l, red);
 
-    // Send this block's state into slot `rank` of every block of the cluster
-    // (itself included) with st.async, completing on the receiver's exchange
-    // barrier, and wait until this block has received all csize states.  The
-    // cluster wait first makes sure every peer runs and has initialised its
-    // barrier.  No block leaves before it has received every peer's state, so
-    // no store can target a block that has gone.
-    cluster_wait_acquire();
-    if (tid == 0) {
-        const uint32_t my_slot = smem_addr(slots + rank);
-        for (uint32_t q = 0; q < csize; ++q) st_async_f2(map_to_rank(my_slot, q), m, l, map_to_rank(xbar, q));
-    }
-    if (!mbar_wait_bounded(xbar, 0, wait_ns)) {
-        atomicOr(&g_error_word, kErrWaitTimeout);
-        ok = false;
-        // a late peer (one whose own copy wait ran out) may still send: stay
-        // resident for as long as its waits can last before leaving
-        mbar_wait_bounded(xbar, 0, 2 * wait_ns);
-    }
-    const float2 w = lane < (int)csize ? slots[lane] : make_float2(-INFINITY, 0.f);
-    m = w.x;
-    l = w.y;
-    group_merge<32>(m, l);
+    if (!cluster_exchange<NW>(m, l, slots, xbar, rank, csize, wait_ns)) ok = false;
     if (ok) tile.template scale_store<WHOLE>(rv, s0 + tid, THREADS, s1, out_factor(s.x, m, l));
+}
+
+// ---------------------------------------------------------------------------
+// path 6: a cluster per row streaming its slices twice (rows of any length)
+// ---------------------------------------------------------------------------
+// Each of the csize blocks owns a slice of the row, of any length.  Pass 1
+// streams the slice tile by tile into one (s, l) state; the states are
+// exchanged inside the cluster (distributed shared memory, nothing written to
+// global memory); pass 2 streams the slice again and writes
+// y = 2^(x log2 e - S) / L.  Three element crossings, the re-read usually
+// served by L2 (a block reads its slice again right after pass 1), and no
+// scratch: the long-row fallback that allocates nothing.
+template <typename T, int THREADS, int VPT, bool WHOLE>
+__global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS))
+    k_cluster_stream(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store,
+                     int64_t wait_ns) {
+    if (!explicit_cluster()) {  // launched without clusters: touch no cluster state
+        pdl_enter();
+        if (threadIdx.x == 0) atomicOr(&g_error_word, kErrNotCluster);
+        return;
+    }
+    constexpr int V = Elem<T>::kVec;
+    constexpr int NW = THREADS / 32;
+    constexpr int64_t kTile = (int64_t)THREADS * VPT;
+    using L = ClusterSmem<THREADS, 0>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    float2 *red = reinterpret_cast<float2 *>(smem + L::kRedOff);
+    float2 *slots = reinterpret_cast<float2 *>(smem + L::kSlotOff);
+    const uint32_t xbar = smem_addr(smem + L::kXbarOff);
+    const int tid = threadIdx.x;
+
+    const uint32_t rank = cluster_rank(), csize = cluster_size();
+    const int64_t row = blockIdx.x / csize;
+    RowView<T> rv(in + row * stride, out + row * stride, cols, vec_store != 0);
+    const int64_t per = (rv.nvec + csize - 1) / csize;
+    const int64_t s0 = min((int64_t)rank * per, rv.nvec), s1 = min(s0 + per, rv.nvec);
+    if (tid == 0) prefetch_span_l2(rv.in, s0 * V - rv.head, min(s0 + kTile, s1) * V - rv.head, cols);
+    pdl_enter();
+
+    if (tid == 0) {
+        mbar_init(xbar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(xbar, csize * 8u);  // csize states will arrive
+    }
+    __syncthreads();
+    cluster_arrive_relaxed();  // this block runs and its barrier is armed
+
+    // pass 1: the slice's state
+    float m = -INFINITY, l = 0.f;
+    for (int64_t t0 = s0; t0 < s1; t0 += kTile) {
+        Tile<T, VPT> tile;
+        tile.template load<WHOLE>(rv, t0 + tid, THREADS, s1);
+        const float2 st = tile.stats();
+        const float M = fmaxf(m, st.x);
+        l = rescale(l, m, M) + rescale(st.y, st.x, M);
+        m = M;
+    }
+    block_merge<NW>(m, l, red);
+    if (!cluster_exchange<NW>(m, l, slots, xbar, rank, csize, wait_ns)) return;
+
+    // pass 2: re-read and write (m is the row's S)
+    const float inv = m == -INFINITY ? __int_as_float(0x7fc00000) : 1.f / l;
+    for (int64_t t0 = s0; t0 < s1; t0 += kTile) {
+        Tile<T, VPT> tile;
+        tile.template load<WHOLE>(rv, t0 + tid, THREADS, s1);
+        tile.template shift_store<WHOLE>(rv, t0 + tid, THREADS, s1, m, inv);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -471,7 +549,6 @@ __global__ void __launch_bounds__(THREADS)
                   int64_t chunk_vecs, const float2 *part, int vec_store) {
     prefetch_first_chunk(in, rows, cols, stride, chunks, chunk_vecs);
     pdl_enter();
-    constexpr int V = Elem<T>::kVec;
     constexpr int NW = THREADS / 32;
     constexpr int64_t kTile = (int64_t)THREADS * VPT;
     __shared__ float2 red[2][NW];
@@ -495,15 +572,7 @@ __global__ void __launch_bounds__(THREADS)
         const float inv = m == -INFINITY ? __int_as_float(0x7fc00000) : 1.f / l;
         for (int64_t t0 = c0; t0 < c1; t0 += kTile) {
             if (t0 != c0) tile.load(rv, t0 + threadIdx.x, THREADS, c1);
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int64_t v = t0 + threadIdx.x + (int64_t)j * THREADS;
-                if (v < c1) {
-                    float y[V];
-                    tile.values_shift(j, shift, inv, y);
-                    rv.store(v, y);
-                }
-            }
+            tile.shift_store(rv, t0 + threadIdx.x, THREADS, c1, shift, inv);
         }
     }
 }

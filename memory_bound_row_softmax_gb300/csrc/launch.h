@@ -80,6 +80,11 @@ cudaError_t launch_cta_whole(const LaunchArgs &a, int threads, int vpt, int64_t 
 bool cluster_shape_ok(int threads, int vpt, int elem_bytes);
 int64_t cluster_smem_bytes(int threads, int vpt);
 cudaError_t launch_cluster(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns, int starve);
+// path 6: a cluster of csize blocks per row streaming slices of any length
+// twice (pass 1 states, cluster exchange, pass 2 re-read and write)
+bool stream_shape_ok(int threads, int vpt);
+int64_t stream_smem_bytes(int threads);
+cudaError_t launch_stream(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns);
 // read this device's error word after synchronising `stream`, then clear it
 cudaError_t read_clear_error_word(cudaStream_t stream, unsigned int *word);
 

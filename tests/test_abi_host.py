@@ -45,7 +45,7 @@ def test_status_strings():
     for s in range(11):
         assert B.status_string(s) and B.status_string(s) != "unknown status"
     assert B.status_string(99) == "unknown status"
-    assert B.abi_version() == 10200
+    assert B.abi_version() == 10300
 
 
 @pytest.mark.parametrize("args,expect", [
@@ -106,9 +106,13 @@ def test_plans_cover_every_row(rows, cols, stride, dt, in_off):
     elif path == B.PATH_CLUSTER:
         assert 1 <= p["group"] <= 16 and -(-nv // p["group"]) <= p["threads"] * p["vpt"]
         assert p["grid"] == rows * p["group"] and p["smem_bytes"] <= 227 * 1024
+    elif path == B.PATH_STREAM:  # any slice length; enough blocks to fill the GPU, nothing allocated
+        assert 1 <= p["group"] <= 16 and p["grid"] == rows * p["group"] and p["scratch_bytes"] == 0
+        assert rows * p["group"] >= min(152, rows * 16) and p["launches"] == 1
     else:
         assert path == B.PATH_SPLIT and p["launches"] == 2 and p["scratch_bytes"] == rows * p["group"] * 8
-    mult = 3 if path == B.PATH_SPLIT else 2
+        assert rows * 16 < 152  # only a few long rows still take scratch
+    mult = 3 if path in (B.PATH_SPLIT, B.PATH_STREAM) else 2
     assert p["hbm_bytes"] == mult * rows * cols * es
 
 
@@ -141,7 +145,8 @@ def test_dispatch_follows_width_rule():
     assert plan(512, 65536) == B.PATH_RING               # long aligned fp32 rows: ring of clusters
     assert plan(512, 131079, "bf16") == B.PATH_CLUSTER   # long misaligned rows, enough of them
     assert plan(4, 131072, "bf16") == B.PATH_SPLIT       # too few rows to fill the GPU
-    assert plan(64, 1 << 22) == B.PATH_SPLIT             # too long for a cluster
+    assert plan(64, 1 << 22) == B.PATH_STREAM            # too long to hold on chip: stream it twice
+    assert plan(9, 1 << 22) == B.PATH_SPLIT              # ... unless 16 blocks per row cannot fill the GPU
 
 
 def test_forced_paths_and_rejections():

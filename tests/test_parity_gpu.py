@@ -48,7 +48,7 @@ WIDTHS = [1, 2, 3, 5, 7, 8, 9, 16, 31, 33, 63, 100, 255, 257, 1000, 1023, 1024, 
 def test_auto_widths(dtype, cols):
     rows = 5 if cols > 10000 else 7
     res = run_and_compare(rnd(rows, cols, dtype, seed=cols), dtype)
-    assert res["path"] in (B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_SPLIT, B.PATH_RING)
+    assert res["path"] in (B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_SPLIT, B.PATH_RING, B.PATH_STREAM)
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -70,6 +70,7 @@ FORCED = {
     B.PATH_CLUSTER: [1, 100, 2048, 9000, 16391, 65536, 131079],
     B.PATH_SPLIT: [1, 100, 4103, 65536, 262147],
     B.PATH_RING: [8, 1024, 2048, 4096, 8192, 65536, 131072],
+    B.PATH_STREAM: [1, 100, 4103, 65536, 262147],
 }
 
 
@@ -150,6 +151,26 @@ def test_split_chunk_counts(dtype, chunks):
     assert res["path"] == B.PATH_SPLIT
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("group", [1, 2, 3, 5, 8, 16])
+@pytest.mark.parametrize("threads,vpt", [(256, 2), (512, 4), (1024, 4)])
+def test_stream_cluster_sizes_and_tiles(dtype, group, threads, vpt):
+    # 70001 columns over `group` blocks: slices of one to many tiles, a partial
+    # last tile, ragged edges on misaligned rows
+    res = run_and_compare(rnd(3, 70001, dtype, seed=group * 13 + vpt), dtype, in_off=1, path=B.PATH_STREAM,
+                          threads=threads, vpt=vpt, group=group)
+    assert res["path"] == B.PATH_STREAM
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("rows,cols", [(40, 65536), (200, 24576), (12, 400000)])
+def test_stream_whole_rows(dtype, rows, cols):
+    # aligned rows of whole vectors (the edge-free instantiations), automatic
+    # cluster size
+    res = run_and_compare(rnd(rows, cols, dtype, seed=rows + cols), dtype, path=B.PATH_STREAM)
+    assert res["path"] == B.PATH_STREAM
+
+
 def test_forced_shape_that_cannot_cover_the_row_is_rejected():
     case = DeviceCase(rnd(2, 5000, "f32", 1), "f32")
     assert case.run(5000, path=B.PATH_WARP) == B.ERR_UNSUPPORTED
@@ -173,7 +194,8 @@ def test_padded_strides(dtype, cols, extra):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("path", [0, B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_SPLIT, B.PATH_RING])
+@pytest.mark.parametrize("path", [0, B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_SPLIT, B.PATH_RING,
+                                  B.PATH_STREAM])
 def test_in_place(dtype, path):
     cols = 1000 if path in (0, B.PATH_WARP) else 6007
     off = 1
@@ -217,7 +239,7 @@ def _result_bits(x, dtype, path):
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("path,cols", [(B.PATH_WARP, 33), (B.PATH_WARP, 1000), (B.PATH_CTA, 3000),
                                        (B.PATH_CLUSTER, 20000), (B.PATH_SPLIT, 20000), (B.PATH_RING, 4096),
-                                       (B.PATH_RING, 65536)])
+                                       (B.PATH_RING, 65536), (B.PATH_STREAM, 20000), (B.PATH_STREAM, 65536)])
 def test_special_values(dtype, path, cols):
     x = special_rows(dtype, cols)
     run_and_compare(x, dtype, path=path)
@@ -332,7 +354,7 @@ def _bits_tensor(x: np.ndarray, dtype: str) -> torch.Tensor:
 
 
 OVERLAP_CASES = [(B.PATH_WARP, 700), (B.PATH_CTA, 3000), (B.PATH_CLUSTER, 20011), (B.PATH_SPLIT, 20011),
-                 (B.PATH_RING, 16384), (0, 65536)]
+                 (B.PATH_RING, 16384), (B.PATH_STREAM, 20011), (0, 65536)]
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
