@@ -169,20 +169,16 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             // ring at every such width measured (8192 x 2816 fp16: block 14.4
             // us, ring 17.1; 4096 x 2816 fp32: 14.0 against 19.5)
             path = SOFTMAX_PATH_CTA;
-        } else if (ring_ok && cdiv(nv, 16) <= 4096 && rows * 16 * 2 >= sms) {
-            path = SOFTMAX_PATH_RING;
+        } else if (rows * 16 >= sms && rows * 16 <= kMaxGrid) {
+            // longer rows: a cluster streaming its slices twice, about one
+            // 1024-vector tile per block.  Measured against the TMA ring and
+            // the one-tile TMA cluster it wins at every long width tried
+            // (1525 x 32768 fp32: 58.8 us, ring 62.5, TMA cluster 64.2;
+            // 381 x 131072: 60.4, ring 74.0; 300 x 40000: 18.7, ring 25.0)
+            path = SOFTMAX_PATH_STREAM;
         } else {
-            // a cluster holding the row on chip (one tile per block); else a
-            // cluster streaming it twice when rows x 16 blocks fill the GPU;
-            // else (a few very long rows) the grid-wide split
-            const int64_t csize = cdiv(nv, nv <= 16 * 512 * 4 ? 512 * 4 : 1024 * 4);
-            const bool fits = csize <= 16 && rows * csize <= kMaxGrid;
-            if (fits && rows * csize >= sms)
-                path = SOFTMAX_PATH_CLUSTER;
-            else if (rows * 16 >= sms && rows * 16 <= kMaxGrid)
-                path = SOFTMAX_PATH_STREAM;
-            else
-                path = SOFTMAX_PATH_SPLIT;
+            // a few very long rows: spread over the whole grid
+            path = SOFTMAX_PATH_SPLIT;
         }
     }
     p->path = path;
@@ -309,12 +305,19 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             break;
         }
         case SOFTMAX_PATH_STREAM: {
-            // 512 threads x 4 vectors per tile; blocks per row: two blocks per
-            // SM in all (one per row when the rows alone give that), at most 16
-            const int threads = fth > 0 ? fth : 512;
+            // 4 vectors per thread; 256 threads per block, or more while 16
+            // blocks would need more than two tiles each; then as many blocks
+            // (<= 16) as give about one tile each.  Measured: 1525 x 32768 fp32
+            // 58.8 us on 8 x (256 x 4); 190 x 262144 64.2 us on 16 x (512 x 4)
+            // (78.6 on 256); 64 x 2^20 105.6 us on 16 x (1024 x 4) (139 on 256)
             const int vpt = fvpt > 0 ? fvpt : 4;
+            int threads = fth;
+            if (threads <= 0) {
+                threads = 256;
+                while (threads < 1024 && cdiv(nv, 16 * (int64_t)threads * vpt) > 2) threads *= 2;
+            }
             const int64_t csize =
-                fgrp > 0 ? fgrp : std::min<int64_t>(16, std::max<int64_t>(1, cdiv(2 * (int64_t)sms, rows)));
+                fgrp > 0 ? fgrp : std::min<int64_t>(16, std::max<int64_t>(1, cdiv(nv, (int64_t)threads * vpt)));
             if (!stream_shape_ok(threads, vpt) || csize < 1 || csize > 16 || rows * csize > kMaxGrid)
                 return SOFTMAX_ERR_UNSUPPORTED;
             p->threads = threads;

@@ -142,7 +142,8 @@ def test_dispatch_follows_width_rule():
     assert B.plan(1 << 24, 1 << 40, 4096, 2047, 2047, "bf16", num_sms=152)["path"] == B.PATH_CTA  # edges
     assert plan(4096, 16384) == B.PATH_CTA           # 512 x 8 keeps two 64 KB rows per SM
     assert plan(512, 131072, "bf16") == B.PATH_CLUSTER   # long 16-bit rows: a cluster, registers
-    assert plan(512, 65536) == B.PATH_RING               # long aligned fp32 rows: ring of clusters
+    assert plan(512, 65536) == B.PATH_STREAM             # long fp32 rows: a cluster streaming them twice
+    assert plan(512, 65537) == B.PATH_STREAM             # ... aligned or not
     assert plan(512, 131079, "bf16") == B.PATH_CLUSTER   # long misaligned rows, enough of them
     assert plan(4, 131072, "bf16") == B.PATH_SPLIT       # too few rows to fill the GPU
     assert plan(64, 1 << 22) == B.PATH_STREAM            # too long to hold on chip: stream it twice
