@@ -422,6 +422,11 @@ def per_shape(args, peaks, l2, dev) -> dict:
         B.set_launch_overlap(False)
         med_plain, _, _ = time_steps(launch, sets, 200, 50)
         B.set_launch_overlap(not args.no_overlap)
+        # after softmax_autotune on this shape (its cache entry is dropped again)
+        tuned = B.autotune_ptr(sets[0][0].data_ptr(), sets[0][1].data_ptr(), w.rows, w.cols, w.stride, code,
+                               torch.cuda.current_stream().cuda_stream, iters=20)
+        med_tuned, _, _ = time_steps(launch, sets, 200, 50)
+        B.autotune_clear()
         # the copy ceiling: rows*cols*elem bytes, device to device, same
         # rotation; the size is rounded down to 64 KiB because the runtime's
         # copy runs at half speed on sizes that are not (200,000,000 bytes:
@@ -437,6 +442,8 @@ def per_shape(args, peaks, l2, dev) -> dict:
         table[w.name] = {
             "path": B.PATH_NAMES.get(plan["path"]), "us_per_call": round(med * 1e3, 2),
             "us_per_call_no_overlap": round(med_plain * 1e3, 2),
+            "us_per_call_tuned": round(med_tuned * 1e3, 2),
+            "tuned_shape": [tuned["plan"][k] for k in ("path", "threads", "vpt", "group")],
             "gbs": round(alg, 1), "frac_of_measured_hbm": round(alg / peaks["hbm_gbs"], 4),
             "frac_of_nominal_8tbs": round(alg / 8000.0, 4),
             "copy_us": round(cmed * 1e3, 2), "copy_gbs": round(copy_gbs, 1),

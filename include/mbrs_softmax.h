@@ -215,9 +215,67 @@ int softmax_set_launch_overlap(int enable);
 int softmax_fwd_noalloc(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride,
                         int dtype, cudaStream_t stream);
 
+/*
+ * Shape-keyed autotune.  (Page "GPU Kernels - Implementing and optimizing
+ * Softmax", section "Autotuning": try the launch configurations on the real
+ * shape and keep the fastest.)
+ *
+ * softmax_autotune times every candidate launch shape for these arguments
+ * (softmax_tune_candidates) on the caller's buffers -- `iters` launches each
+ * after two warm-up launches, between CUDA events on `stream` -- and keeps the
+ * fastest (another shape displaces the automatic choice only when it is at
+ * least 2% faster) in a process-wide cache keyed by (device, dtype, cols, row_stride,
+ * in and out address modulo 16, floor(log2(rows))).  From then on softmax_fwd
+ * and softmax_plan use the cached shape for every call with that key (a
+ * shape forced with softmax_set_force_path still wins).  The automatic choice
+ * is always one of the candidates, so the cached shape is never slower than
+ * it was in the tuning run.
+ *   - in and out must not be the same buffer (the candidates are run many
+ *     times and must all see the same input); `out` receives the softmax.
+ *   - The call synchronises `stream` and must not be made while the stream is
+ *     being captured (SOFTMAX_ERR_ARG).  iters <= 0 means 20.
+ *   - The candidates run on the same buffers again and again, so inputs that
+ *     fit in L2 are timed warm (as they are when a producer kernel has just
+ *     written them).
+ *   - result (may be NULL) receives the winning plan, its time and the
+ *     automatic plan's time in microseconds per call, and the number of
+ *     candidates timed.
+ * Returns a softmax_status_t (SOFTMAX_ERR_CUDA if a launch or an event failed;
+ * the cache is then unchanged).
+ */
+typedef struct {
+    softmax_plan_t plan;   /* the shape kept */
+    double best_us;        /* its time per call */
+    double auto_us;        /* the automatic shape's time per call */
+    int candidates;        /* shapes timed */
+} softmax_tune_result_t;
+int softmax_autotune(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride,
+                     int dtype, cudaStream_t stream, int iters, softmax_tune_result_t *result);
+
+/* One launch shape: path (softmax_path_t) and the threads / vpt / group that
+ * softmax_set_force_path takes (0 = the planner's choice). */
+typedef struct {
+    int path, threads, vpt, group;
+} softmax_shape_t;
+
+/*
+ * The candidate shapes softmax_autotune would time for these arguments
+ * (host only, like softmax_plan with num_sms > 0; num_sms <= 0 asks the
+ * current device).  Writes at most `capacity` shapes to `shapes` (the first
+ * is always the automatic choice, {0, 0, 0, 0}) and returns how many there
+ * are, or a negated softmax_status_t on bad arguments.
+ */
+int softmax_tune_candidates(uint64_t in_addr, uint64_t out_addr, int64_t rows, int64_t cols,
+                            int64_t row_stride, int dtype, int num_sms, softmax_shape_t *shapes,
+                            int capacity);
+
+/* Number of shapes in the autotune cache, and a call that empties it. */
+int softmax_autotune_size(void);
+int softmax_autotune_clear(void);
+
 /* Version of this ABI: major * 10000 + minor * 100 + patch (1.1.0 adds the RING
  * path, 1.2.0 softmax_set_launch_overlap, 1.3.0 the STREAM path and
- * softmax_plan_t.whole_vectors). */
+ * softmax_plan_t.whole_vectors, 1.4.0 the autotune calls). */
 int softmax_abi_version(void);
 
 #ifdef __cplusplus

@@ -32,6 +32,17 @@ class Plan(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
+class TuneResult(ctypes.Structure):
+    _fields_ = [("plan", Plan), ("best_us", ctypes.c_double), ("auto_us", ctypes.c_double), ("candidates", _int)]
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("path", _int), ("threads", _int), ("vpt", _int), ("group", _int)]
+
+    def as_tuple(self) -> tuple:
+        return (self.path, self.threads, self.vpt, self.group)
+
+
 # Every function the header declares, with its ctypes signature.
 SIGNATURES = {
     "softmax_fwd": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp]),
@@ -42,6 +53,10 @@ SIGNATURES = {
     "softmax_check_device_error": (_int, [_vp]),
     "softmax_set_wait_test": (_int, [_i64, _int]),
     "softmax_set_launch_overlap": (_int, [_int]),
+    "softmax_autotune": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp, _int, ctypes.POINTER(TuneResult)]),
+    "softmax_tune_candidates": (_int, [_u64, _u64, _i64, _i64, _i64, _int, _int, ctypes.POINTER(Shape), _int]),
+    "softmax_autotune_size": (_int, []),
+    "softmax_autotune_clear": (_int, []),
     "softmax_abi_version": (_int, []),
     "softmax_fwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp]),
 }
@@ -170,6 +185,36 @@ def set_wait_test(wait_limit_ns: int = 0, starve: bool = False) -> None:
 def set_launch_overlap(enable: bool = True) -> None:
     """Programmatic dependent launch on (default) or off, process-wide."""
     lib().softmax_set_launch_overlap(1 if enable else 0)
+
+
+def autotune_ptr(in_ptr: int, out_ptr: int, rows: int, cols: int, row_stride: int, dtype: int, stream: int = 0,
+                 iters: int = 20) -> dict:
+    """Time the candidate launch shapes for this call and cache the fastest
+    (raises on a bad status).  Returns the kept plan and the timings."""
+    r = TuneResult()
+    st = lib().softmax_autotune(in_ptr, out_ptr, rows, cols, row_stride, dtype, stream, iters, ctypes.byref(r))
+    if st != OK:
+        raise SoftmaxError(st, "softmax_autotune")
+    return {"plan": r.plan.as_dict(), "best_us": r.best_us, "auto_us": r.auto_us, "candidates": r.candidates}
+
+
+def tune_candidates(in_addr: int, out_addr: int, rows: int, cols: int, row_stride: int, dtype) -> list:
+    """The (path, threads, vpt, group) shapes softmax_autotune would time."""
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else dtype
+    n = lib().softmax_tune_candidates(in_addr, out_addr, rows, cols, row_stride, code, 0, None, 0)
+    if n < 0:
+        raise SoftmaxError(-n, "softmax_tune_candidates")
+    arr = (Shape * max(n, 1))()
+    lib().softmax_tune_candidates(in_addr, out_addr, rows, cols, row_stride, code, 0, arr, n)
+    return [arr[i].as_tuple() for i in range(n)]
+
+
+def autotune_size() -> int:
+    return lib().softmax_autotune_size()
+
+
+def autotune_clear() -> None:
+    lib().softmax_autotune_clear()
 
 
 def abi_version() -> int:

@@ -19,6 +19,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "mbrs_softmax.h"
 #include "launch.h"
@@ -27,7 +28,7 @@ using namespace mbrs;
 
 namespace {
 
-constexpr int kAbiVersion = 10300;  // 1.3.0
+constexpr int kAbiVersion = 10400;  // 1.4.0
 constexpr int kVecBytes = 16;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDefaultWaitNs = 1000000000;  // 1 s
@@ -43,6 +44,16 @@ struct Plan {
     int path = 0, threads = 0, vpt = 0, group = 1, launches = 0, vec_store = 0, stages = 0, whole = 0;
     int64_t grid = 0, smem = 0, scratch = 0, hbm = 0, chunks = 1, chunk_vecs = 0, slice_vecs = 0;
 };
+
+// A launch shape asked for: path 0 = automatic; threads / vpt / group 0 =
+// the planner's own choice for that path.
+struct Shape {
+    int path = 0, threads = 0, vpt = 0, group = 0;
+};
+
+Shape forced_shape() {
+    return Shape{g_force_path.load(), g_force_threads.load(), g_force_vpt.load(), g_force_group.load()};
+}
 
 // Ring sizing: shared memory a block may fill with stages (of the ~228 KB an
 // SM has, leaving room for the per-block reserve), and the blocks per SM that
@@ -137,7 +148,7 @@ int device_sms(int *sms) {
 // byte stride is a multiple of 16 share the first row's phase; otherwise a row
 // may start up to V-1 elements into its first vector.
 int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row_stride, int dtype, int sms,
-              Plan *p) {
+              const Shape &force, Plan *p) {
     const int es = elem_bytes(dtype), V = kVecBytes / es;
     const bool uniform = ((row_stride * es) % kVecBytes) == 0;
     const int64_t head = (int64_t)((in % kVecBytes) / es);
@@ -148,8 +159,7 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
                (cols * es) % kVecBytes == 0;
     p->hbm = 2 * rows * cols * es;
 
-    const int fpath = g_force_path.load(), fth = g_force_threads.load(), fvpt = g_force_vpt.load(),
-              fgrp = g_force_group.load();
+    const int fpath = force.path, fth = force.threads, fvpt = force.vpt, fgrp = force.group;
     // the ring moves whole aligned vectors only: every row start and row end on 16 bytes
     const bool ring_ok = (in % kVecBytes) == 0 && (out % kVecBytes) == 0 && uniform &&
                          ((cols * es) % kVecBytes) == 0;
@@ -442,6 +452,123 @@ int plan_noalloc(uint64_t in, int64_t rows, int64_t cols, int64_t row_stride, in
     return SOFTMAX_OK;
 }
 
+// ---------------------------------------------------------------------------
+// shape-keyed autotune (page "GPU Kernels - Implementing and optimizing
+// Softmax", section "Autotuning": time the candidate launch configurations on
+// the real shape, keep the fastest)
+// ---------------------------------------------------------------------------
+struct TuneKey {
+    int device = 0, dtype = 0, in_phase = 0, out_phase = 0, rows_log2 = 0;
+    int64_t cols = 0, row_stride = 0;
+    bool operator==(const TuneKey &o) const {
+        return device == o.device && dtype == o.dtype && in_phase == o.in_phase && out_phase == o.out_phase &&
+               rows_log2 == o.rows_log2 && cols == o.cols && row_stride == o.row_stride;
+    }
+};
+
+int floor_log2(int64_t v) {
+    int r = 0;
+    while (v > 1) {
+        v >>= 1;
+        ++r;
+    }
+    return r;
+}
+
+TuneKey tune_key(int device, uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row_stride, int dtype) {
+    TuneKey k;
+    k.device = device;
+    k.dtype = dtype;
+    k.in_phase = (int)(in % kVecBytes);
+    k.out_phase = (int)(out % kVecBytes);
+    k.rows_log2 = floor_log2(rows);
+    k.cols = cols;
+    k.row_stride = row_stride;
+    return k;
+}
+
+std::mutex g_tune_mu;
+std::vector<std::pair<TuneKey, Shape>> g_tuned;  // guarded by g_tune_mu
+std::atomic<int> g_tuned_count{0};
+
+void store_tuned(const TuneKey &k, const Shape &s) {
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    for (auto &e : g_tuned)
+        if (e.first == k) {
+            e.second = s;
+            return;
+        }
+    g_tuned.emplace_back(k, s);
+    g_tuned_count.store((int)g_tuned.size());
+}
+
+// The shape a call asks for: a forced one, else the tuned one for its key,
+// else automatic.  No CUDA call while the cache is empty.
+Shape call_shape(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row_stride, int dtype) {
+    const Shape f = forced_shape();
+    if (f.path != SOFTMAX_PATH_AUTO || g_tuned_count.load() == 0) return f;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return f;
+    const TuneKey k = tune_key(dev, in, out, rows, cols, row_stride, dtype);
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    for (const auto &e : g_tuned)
+        if (e.first == k) return e.second;
+    return f;
+}
+
+// Candidate shapes for rows of up to nv vectors: the automatic choice first,
+// then every lane-group / block / cluster shape that can hold the row, the
+// streaming cluster at three block sizes and, for whole aligned rows, the ring.
+std::vector<Shape> tune_candidates(int64_t nv, int es, bool ring_ok) {
+    std::vector<Shape> c;
+    c.push_back(Shape{});
+    if (nv <= 32 * 9)
+        for (int g = 2; g <= 32; g *= 2) {
+            const int64_t v = cdiv(nv, g);
+            if (!warp_shape_ok(g, (int)v)) continue;
+            for (int t = 64; t <= 256; t *= 2) c.push_back(Shape{SOFTMAX_PATH_WARP, t, (int)v, g});
+        }
+    if (nv <= 512 * 10)
+        for (int t = 64; t <= 1024; t *= 2) {
+            const int v = cta_vpt_round(cdiv(nv, t));
+            if (cta_shape_ok(t, v) && (int64_t)t * v >= nv) c.push_back(Shape{SOFTMAX_PATH_CTA, t, v, 0});
+        }
+    if (nv > 512) {
+        for (int t = 256; t <= 1024; t *= 2)
+            for (int v : {2, 4, 8}) {
+                if (!cluster_shape_ok(t, v, es) || cdiv(nv, (int64_t)t * v) > 16) continue;
+                c.push_back(Shape{SOFTMAX_PATH_CLUSTER, t, v, 0});
+            }
+        for (int t = 256; t <= 1024; t *= 2) c.push_back(Shape{SOFTMAX_PATH_STREAM, t, 4, 0});
+        if (ring_ok) c.push_back(Shape{SOFTMAX_PATH_RING, 0, 0, 0});
+    }
+    return c;
+}
+
+std::vector<Shape> candidates_for(uint64_t in, uint64_t out, int64_t cols, int64_t row_stride, int dtype) {
+    const int es = elem_bytes(dtype), V = kVecBytes / es;
+    const bool uniform = ((row_stride * es) % kVecBytes) == 0;
+    const int64_t head = (int64_t)((in % kVecBytes) / es);
+    const int64_t nv = uniform ? cdiv(head + cols, V) : cdiv(cols + V - 1, V);
+    const bool ring_ok = (in % kVecBytes) == 0 && (out % kVecBytes) == 0 && uniform && ((cols * es) % kVecBytes) == 0;
+    return tune_candidates(nv, es, ring_ok);
+}
+
+void fill_public_plan(const Plan &p, softmax_plan_t *plan) {
+    plan->path = p.path;
+    plan->threads = p.threads;
+    plan->vpt = p.vpt;
+    plan->group = p.group;
+    plan->launches = p.launches;
+    plan->vec_store = p.vec_store;
+    plan->grid = p.grid;
+    plan->smem_bytes = p.smem;
+    plan->scratch_bytes = p.scratch;
+    plan->hbm_bytes = p.hbm;
+    plan->stages = p.stages;
+    plan->whole_vectors = p.whole;
+}
+
 }  // namespace
 
 extern "C" {
@@ -456,7 +583,7 @@ int softmax_fwd(const void *in, void *out, int64_t rows, int64_t cols, int64_t r
     st = device_sms(&sms);
     if (st != SOFTMAX_OK) return st;
     Plan p;
-    st = make_plan(ia, oa, rows, cols, row_stride, dtype, sms, &p);
+    st = make_plan(ia, oa, rows, cols, row_stride, dtype, sms, call_shape(ia, oa, rows, cols, row_stride, dtype), &p);
     if (st != SOFTMAX_OK) return st;
     LaunchArgs a{in, out, rows, cols, row_stride, dtype, p.vec_store, stream, g_overlap.load(), p.whole};
     st = run(p, a);
@@ -526,20 +653,10 @@ int softmax_plan(uint64_t in_addr, uint64_t out_addr, int64_t rows, int64_t cols
         if (st != SOFTMAX_OK) return st;
     }
     Plan p;
-    st = make_plan(in_addr, out_addr, rows, cols, row_stride, dtype, sms, &p);
+    st = make_plan(in_addr, out_addr, rows, cols, row_stride, dtype, sms,
+                   call_shape(in_addr, out_addr, rows, cols, row_stride, dtype), &p);
     if (st != SOFTMAX_OK) return st;
-    plan->path = p.path;
-    plan->threads = p.threads;
-    plan->vpt = p.vpt;
-    plan->group = p.group;
-    plan->launches = p.launches;
-    plan->vec_store = p.vec_store;
-    plan->grid = p.grid;
-    plan->smem_bytes = p.smem;
-    plan->scratch_bytes = p.scratch;
-    plan->hbm_bytes = p.hbm;
-    plan->stages = p.stages;
-    plan->whole_vectors = p.whole;
+    fill_public_plan(p, plan);
     if (p.path == SOFTMAX_PATH_RING && num_sms == 0) {  // the persistent grid the launch will use
         RingCfg c{p.threads, p.vpt, p.group, p.stages, (int)p.slice_vecs, p.smem};
         LaunchArgs a{nullptr, nullptr, rows, cols, row_stride, dtype, p.vec_store, nullptr, 0, p.whole};
@@ -567,6 +684,102 @@ int softmax_set_wait_test(int64_t wait_limit_ns, int starve) {
 
 int softmax_set_launch_overlap(int enable) {
     g_overlap.store(enable ? 1 : 0);
+    return SOFTMAX_OK;
+}
+
+int softmax_tune_candidates(uint64_t in_addr, uint64_t out_addr, int64_t rows, int64_t cols, int64_t row_stride,
+                            int dtype, int num_sms, softmax_shape_t *shapes, int capacity) {
+    (void)num_sms;  // the candidate set depends on the row geometry only
+    if (capacity < 0 || (capacity > 0 && !shapes)) return -SOFTMAX_ERR_ARG;
+    int64_t ext = 0;
+    const int st = check_args(in_addr, out_addr, rows, cols, row_stride, dtype, &ext);
+    if (st != SOFTMAX_OK) return -st;
+    const std::vector<Shape> c = candidates_for(in_addr, out_addr, cols, row_stride, dtype);
+    for (int i = 0; i < (int)c.size() && i < capacity; ++i)
+        shapes[i] = softmax_shape_t{c[i].path, c[i].threads, c[i].vpt, c[i].group};
+    return (int)c.size();
+}
+
+int softmax_autotune(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride, int dtype,
+                     cudaStream_t stream, int iters, softmax_tune_result_t *result) {
+    if (result) std::memset(result, 0, sizeof(*result));
+    int64_t ext = 0;
+    const uint64_t ia = (uint64_t)(uintptr_t)in, oa = (uint64_t)(uintptr_t)out;
+    int st = check_args(ia, oa, rows, cols, row_stride, dtype, &ext);
+    if (st != SOFTMAX_OK || rows == 0) return st;
+    if (ia == oa) return SOFTMAX_ERR_ARG;  // every candidate must see the same input
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return SOFTMAX_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return SOFTMAX_ERR_ARG;
+    if (iters <= 0) iters = 20;
+    int sms = 0, dev = 0;
+    st = device_sms(&sms);
+    if (st != SOFTMAX_OK) return st;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SOFTMAX_ERR_CUDA;
+
+    cudaEvent_t ev[2] = {nullptr, nullptr};
+    if (cudaEventCreate(&ev[0]) != cudaSuccess || cudaEventCreate(&ev[1]) != cudaSuccess) {
+        if (ev[0]) cudaEventDestroy(ev[0]);
+        return SOFTMAX_ERR_CUDA;
+    }
+    const std::vector<Shape> cands = candidates_for(ia, oa, cols, row_stride, dtype);
+    Plan best_plan;
+    double best_us = 0.0, auto_us = 0.0;
+    int timed = 0;
+    bool have = false, best_is_auto = false;
+    st = SOFTMAX_OK;
+    for (size_t i = 0; i < cands.size() && st == SOFTMAX_OK; ++i) {
+        Plan p;
+        if (make_plan(ia, oa, rows, cols, row_stride, dtype, sms, cands[i], &p) != SOFTMAX_OK) continue;
+        LaunchArgs a{in, out, rows, cols, row_stride, dtype, p.vec_store, stream, g_overlap.load(), p.whole};
+        if (run(p, a) != SOFTMAX_OK || run(p, a) != SOFTMAX_OK) continue;  // a shape the launchers refuse
+        if (cudaEventRecord(ev[0], stream) != cudaSuccess) {
+            st = SOFTMAX_ERR_CUDA;
+            break;
+        }
+        for (int k = 0; k < iters && st == SOFTMAX_OK; ++k) st = run(p, a);
+        float ms = 0.f;
+        if (st != SOFTMAX_OK || cudaEventRecord(ev[1], stream) != cudaSuccess ||
+            cudaEventSynchronize(ev[1]) != cudaSuccess || cudaEventElapsedTime(&ms, ev[0], ev[1]) != cudaSuccess) {
+            st = SOFTMAX_ERR_CUDA;
+            break;
+        }
+        const double us = 1000.0 * ms / iters;
+        ++timed;
+        if (i == 0) auto_us = us;
+        // another shape replaces the automatic one only when it is at least 2%
+        // faster (run-to-run noise of these timings is about 1%)
+        if (!have || us < (best_is_auto ? 0.98 * best_us : best_us)) {
+            best_is_auto = i == 0;
+            have = true;
+            best_us = us;
+            best_plan = p;
+        }
+    }
+    cudaEventDestroy(ev[0]);
+    cudaEventDestroy(ev[1]);
+    if (st != SOFTMAX_OK) return st;
+    if (!have) return SOFTMAX_ERR_UNSUPPORTED;
+    store_tuned(tune_key(dev, ia, oa, rows, cols, row_stride, dtype),
+                Shape{best_plan.path, best_plan.threads, best_plan.vpt, best_plan.group});
+    if (result) {
+        fill_public_plan(best_plan, &result->plan);
+        result->best_us = best_us;
+        result->auto_us = auto_us;
+        result->candidates = timed;
+    }
+    return SOFTMAX_OK;
+}
+
+int softmax_autotune_size(void) {
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    return (int)g_tuned.size();
+}
+
+int softmax_autotune_clear(void) {
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    g_tuned.clear();
+    g_tuned_count.store(0);
     return SOFTMAX_OK;
 }
 
