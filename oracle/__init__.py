@@ -46,6 +46,9 @@ def _load():
             i64, vp, dp = ctypes.c_int64, ctypes.c_void_p, ctypes.POINTER(ctypes.c_double)
             lib.oracle_softmax_rows.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int]
             lib.oracle_softmax_rows.restype = ctypes.c_int
+            lib.oracle_softmax_masked_rows.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int,
+                                                       ctypes.c_double, i64, i64]
+            lib.oracle_softmax_masked_rows.restype = ctypes.c_int
             lib.oracle_row_stats.argtypes = [vp, i64, i64, i64, i64, ctypes.c_int, vp]
             lib.oracle_online_stats.argtypes = [vp, i64, vp, i64, i64, ctypes.c_int, vp]
             lib.oracle_merge.argtypes = [ctypes.c_double] * 4 + [dp, dp]
@@ -101,6 +104,46 @@ def softmax(x: np.ndarray, dtype: str, cols: int | None = None, rows=None, threa
                 r = int(sel[i])
                 rc = lib.oracle_softmax_rows(x.ctypes.data, out[i:i + 1].ctypes.data, scratch.ctypes.data,
                                              r, r + 1, cols, stride, code)
+                assert rc == 0
+
+    if threads <= 1 or nrows < 2:
+        run(0, nrows)
+    else:
+        step = (nrows + threads - 1) // threads
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda lo: run(lo, min(nrows, lo + step)), range(0, nrows, step)))
+    return out
+
+
+def softmax_masked(x: np.ndarray, dtype: str, scale: float, causal_offset: int, rows_per_seq: int = 0,
+                   cols: int | None = None, rows=None, threads: int = 1) -> np.ndarray:
+    """Scaled, causally masked row softmax in double precision: row r keeps
+    columns c <= (r mod rows_per_seq) + causal_offset (rows_per_seq <= 0: r
+    itself), scaled by ``scale``; masked outputs are 0 and masked inputs are
+    never read; a row that keeps nothing is NaN.  Arguments as ``softmax``."""
+    lib = _load()
+    x = _check_storage(x, dtype)
+    stride = x.shape[1]
+    cols = stride if cols is None else cols
+    code = _DTYPE_CODE[dtype]
+    sel = np.arange(x.shape[0], dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    nrows = len(sel)
+    out = np.empty((nrows, cols), dtype=np.float64)
+    if nrows == 0:
+        return out
+
+    def run(lo: int, hi: int):
+        scratch = np.empty(cols, dtype=np.float64)
+        if rows is None:
+            rc = lib.oracle_softmax_masked_rows(x.ctypes.data, out[lo:hi].ctypes.data, scratch.ctypes.data, lo, hi,
+                                                cols, stride, code, float(scale), causal_offset, rows_per_seq)
+            assert rc == 0
+        else:
+            for i in range(lo, hi):
+                r = int(sel[i])
+                rc = lib.oracle_softmax_masked_rows(x.ctypes.data, out[i:i + 1].ctypes.data, scratch.ctypes.data,
+                                                    r, r + 1, cols, stride, code, float(scale), causal_offset,
+                                                    rows_per_seq)
                 assert rc == 0
 
     if threads <= 1 or nrows < 2:

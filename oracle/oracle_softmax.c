@@ -147,6 +147,79 @@ int oracle_softmax_rows(const void *in, double *out, double *scratch,
 }
 
 /*
+ * Scaled, causally masked softmax.  Page "Dissecting Memory Bandwidth & SRAM
+ * Tiling in Triton: From GEMM to FlashAttention-3", section "Writing the
+ * Kernel in OpenAI Triton": a score row is (Q_i K_j^T) * scale, and the causal
+ * mask keeps key j only when j <= query i, the others becoming -inf before the
+ * softmax (so their outputs are exp(-inf) = 0).
+ *
+ * Row r is query (r mod rows_per_seq) of its group of rows_per_seq rows
+ * (rows_per_seq <= 0: one group holding every row) and keeps the columns
+ * c <= query + causal_offset, i.e. n = clamp(query + causal_offset + 1, 0,
+ * cols) of them.  The kept entries are multiplied by `scale` (in double) and
+ * go through the steps of oracle_softmax_rows; the other outputs are 0, and
+ * the masked inputs are never read.  A row that keeps no column is NaN
+ * (reading R1).  scale must be finite and > 0.  Returns 0, or -1 on bad
+ * arguments.
+ */
+int oracle_softmax_masked_rows(const void *in, double *out, double *scratch,
+                               int64_t row_begin, int64_t row_end, int64_t cols,
+                               int64_t row_stride, int dtype, double scale,
+                               int64_t causal_offset, int64_t rows_per_seq)
+{
+    if (cols < 1 || row_stride < cols || row_begin > row_end || !(scale > 0.0) || isinf(scale))
+        return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_F16 && dtype != ORACLE_BF16)
+        return -1;
+    for (int64_t r = row_begin; r < row_end; ++r) {
+        double *y = out + (r - row_begin) * cols;
+        double *x = scratch;
+        const int64_t query = rows_per_seq > 0 ? r % rows_per_seq : r;
+        int64_t n = query + causal_offset + 1;
+        if (n < 0)
+            n = 0;
+        if (n > cols)
+            n = cols;
+
+        /* the masked outputs */
+        for (int64_t c = n; c < cols; ++c)
+            y[c] = 0.0;
+        if (n == 0) {                       /* nothing kept: reading R1 */
+            for (int64_t c = 0; c < cols; ++c)
+                y[c] = NAN;
+            continue;
+        }
+
+        /* widen and scale the kept entries */
+        int has_nan = 0;
+        for (int64_t c = 0; c < n; ++c) {
+            x[c] = load_elem(in, r * row_stride + c, dtype) * scale;
+            if (isnan(x[c]))
+                has_nan = 1;
+        }
+
+        double m = -INFINITY;
+        for (int64_t c = 0; c < n; ++c)
+            if (x[c] > m)
+                m = x[c];
+        if (has_nan || m == -INFINITY || m == INFINITY) {
+            for (int64_t c = 0; c < cols; ++c)
+                y[c] = NAN;
+            continue;
+        }
+
+        double l = 0.0;
+        for (int64_t c = 0; c < n; ++c) {
+            y[c] = exp(x[c] - m);
+            l += y[c];
+        }
+        for (int64_t c = 0; c < n; ++c)
+            y[c] = y[c] / l;
+    }
+    return 0;
+}
+
+/*
  * The (max, normaliser) state of one row taken directly: m = max x,
  * l = sum exp(x - m).  Out: stats[0] = m, stats[1] = l.  Same readings as above
  * (a row with no finite shift gives m = NaN-or-inf, l = NaN).

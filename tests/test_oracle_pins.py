@@ -266,3 +266,69 @@ def test_threaded_rows_equal_serial_rows():
     c = oracle.softmax(x, "f16", rows=[5, 0, 36])
     assert (a == b).all()
     assert (c == a[[5, 0, 36]]).all()
+
+
+# -- the scaled, causally masked variant ------------------------------------------------------
+
+@pytest.mark.parametrize("off,period", [(0, 0), (3, 0), (-2, 0), (0, 4), (1, 3)])
+def test_masked_constant_rows_are_one_over_kept(off, period):
+    # every kept entry of a constant row is 1/n, n = query + off + 1 (clamped); the rest 0
+    rows, cols = 9, 6
+    y = oracle.softmax_masked(np.full((rows, cols), 0.7, np.float32), "f32", 1.5, off, period)
+    for r in range(rows):
+        q = r % period if period > 0 else r
+        n = min(max(q + off + 1, 0), cols)
+        if n == 0:
+            assert np.isnan(y[r]).all()
+        else:
+            assert np.abs(y[r, :n] - 1.0 / n).max() < 1e-15 and (y[r, n:] == 0).all()
+
+
+@pytest.mark.parametrize("a,b,scale", [(0.0, 1.0, 0.125), (2.0, -3.0, 3.0), (-1.5, 4.25, 1.0 / 3.0)])
+def test_masked_pair_is_a_logistic_in_the_scaled_gap(a, b, scale):
+    # row 1 keeps two columns: p0 = 1 / (1 + e^(scale (b - a))), a closed form
+    x = f32([[a, b, 9.0], [a, b, 9.0]])
+    y = oracle.softmax_masked(x, "f32", scale, 0)
+    p0 = 1.0 / (1.0 + math.exp(scale * (float(np.float32(b)) - float(np.float32(a)))))
+    assert abs(y[1, 0] - p0) < 1e-15 and abs(y[1, 1] - (1 - p0)) < 1e-15 and y[1, 2] == 0
+    assert y[0, 0] == 1.0 and (y[0, 1:] == 0).all()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("scale,off,period", [(0.5, 0, 0), (4.0, 5, 0), (0.25, -1, 7), (1.0, 0, 16)])
+def test_masked_equals_plain_softmax_of_the_masked_scaled_matrix(dtype, scale, off, period):
+    # With a power-of-two scale, x * scale is exact in every storage type, so the
+    # masked softmax must equal the plain softmax of the matrix whose kept entries
+    # are pre-scaled and whose masked entries are -inf (a different code path).
+    rows, cols = 40, 33
+    x = W.make_random(rows, cols, dtype, seed=11, sigma=2.0)
+    vals = oracle.decode(W.bits_view(x, dtype), dtype) if dtype != "f32" else x.astype(np.float64)
+    pre = vals * scale
+    for r in range(rows):
+        q = r % period if period > 0 else r
+        pre[r, max(0, min(cols, q + off + 1)):] = -np.inf
+    xs = W.quantise(pre, dtype)
+    back = oracle.decode(W.bits_view(xs, dtype), dtype) if dtype != "f32" else xs.astype(np.float64)
+    assert np.array_equal(back, pre)  # the pre-scaled matrix is exact in storage
+    want = oracle.softmax(xs, dtype)
+    got = oracle.softmax_masked(x, dtype, scale, off, period)
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all()
+
+
+def test_masked_inputs_are_never_read():
+    rows, cols = 12, 10
+    x = W.make_random(rows, cols, "f32", seed=4)
+    poisoned = x.copy()
+    for r in range(rows):
+        poisoned[r, r + 1:] = np.nan
+    a = oracle.softmax_masked(x, "f32", 0.3, 0)
+    b = oracle.softmax_masked(poisoned, "f32", 0.3, 0)
+    assert np.array_equal(a, b) and np.isfinite(a).all()
+
+
+def test_masked_rejects_a_scale_that_is_not_positive():
+    x = np.zeros((2, 3), np.float32)
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        with pytest.raises(AssertionError):
+            oracle.softmax_masked(x, "f32", bad, 0)
