@@ -450,6 +450,22 @@ def per_shape(args, peaks, l2, dev) -> dict:
             "frac_of_copy": round(alg / copy_gbs, 4), "time_vs_copy": round(med / cmed, 3),
             "moved_gbs": round(gbs, 1),
         }
+        if w.causal_period:  # the same rows through softmax_fwd_masked: only the kept half is read
+            def launch_masked(a, b, w=w, code=code):
+                st = lib.softmax_fwd_masked(a.data_ptr(), b.data_ptr(), w.rows, w.cols, w.stride, code, 1.0, 0,
+                                            w.causal_period, torch.cuda.current_stream().cuda_stream)
+                if st != 0:
+                    raise B.SoftmaxError(st, "softmax_fwd_masked")
+
+            mmed, _, _ = time_steps(launch_masked, sets, 200, 50)
+            kept = sum(min(w.cols, (r % w.causal_period) + 1) for r in range(w.rows))
+            mbytes = (kept + w.rows * w.cols) * w.elem_bytes  # kept entries read, every entry written
+            table[w.name + "_masked"] = {
+                "path": "masked " + B.PATH_NAMES.get(B.last_path(), "?"), "us_per_call": round(mmed * 1e3, 2),
+                "algorithmic_bytes": mbytes, "gbs": round(mbytes / (mmed / 1e3) / 1e9, 1),
+                "frac_of_measured_hbm": round(mbytes / (mmed / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                "time_vs_unmasked": round(mmed / med, 3),
+            }
         del sets, csets, xd
         torch.cuda.empty_cache()
     return table

@@ -108,6 +108,33 @@ typedef enum {
 int softmax_fwd(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride,
                 int dtype, cudaStream_t stream);
 
+/*
+ * softmax_fwd_masked -- the row softmax of scaled, causally masked scores.
+ * (Page "Dissecting Memory Bandwidth & SRAM Tiling in Triton: From GEMM to
+ * FlashAttention-3", section "Writing the Kernel in OpenAI Triton": the score
+ * row is multiplied by the scale, and key j of query i is kept only when
+ * j <= i, the others becoming -inf before the softmax.)
+ * Row r is query q = r mod rows_per_seq of its group of rows (rows_per_seq
+ * == 0: q = r) and keeps the columns c <= q + causal_offset:
+ *     y[r,c] = exp(s_c - m) / sum over kept k of exp(s_k - m),
+ *     s_c = scale * x[r,c],  m = the max of the kept s,
+ * and y[r,c] = 0 for the masked columns.  Masked entries of `in` are never
+ * read (they may hold anything); every column of `out` is written.  A row
+ * that keeps no column, or has a NaN or +inf among its kept entries, comes
+ * out all NaN.
+ *   scale          finite and > 0 (else SOFTMAX_ERR_ARG)
+ *   causal_offset  any value; <= -1 - q masks all of query q's row
+ *   rows_per_seq   >= 0 (else SOFTMAX_ERR_ARG)
+ * The other arguments, the layout, aliasing and status codes are those of
+ * softmax_fwd.  Runs the warp and block shapes of paths 1 and 2, or the
+ * streaming cluster (path 6) for longer rows; allocates nothing; ignores the
+ * autotune cache (softmax_set_force_path applies, other forced paths map to
+ * path 6).
+ */
+int softmax_fwd_masked(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride,
+                       int dtype, float scale, int64_t causal_offset, int64_t rows_per_seq,
+                       cudaStream_t stream);
+
 /* A static English string for a status code (never NULL). */
 const char *softmax_status_string(int status);
 
@@ -275,7 +302,7 @@ int softmax_autotune_clear(void);
 
 /* Version of this ABI: major * 10000 + minor * 100 + patch (1.1.0 adds the RING
  * path, 1.2.0 softmax_set_launch_overlap, 1.3.0 the STREAM path and
- * softmax_plan_t.whole_vectors, 1.4.0 the autotune calls). */
+ * softmax_plan_t.whole_vectors, 1.4.0 the autotune calls and softmax_fwd_masked). */
 int softmax_abi_version(void);
 
 #ifdef __cplusplus

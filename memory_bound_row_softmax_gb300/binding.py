@@ -59,6 +59,7 @@ SIGNATURES = {
     "softmax_autotune_clear": (_int, []),
     "softmax_abi_version": (_int, []),
     "softmax_fwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp]),
+    "softmax_fwd_masked": (_int, [_vp, _vp, _i64, _i64, _i64, _int, ctypes.c_float, _i64, _i64, _vp]),
 }
 
 _lib = None
@@ -113,6 +114,13 @@ def softmax_fwd_noalloc_ptr(in_ptr: int, out_ptr: int, rows: int, cols: int, row
     cannot allocate device memory; its scratch is a fixed array in the
     library).  Status out, no exception."""
     return lib().softmax_fwd_noalloc(in_ptr, out_ptr, rows, cols, row_stride, dtype, stream)
+
+
+def softmax_fwd_masked_ptr(in_ptr: int, out_ptr: int, rows: int, cols: int, row_stride: int, dtype: int,
+                           scale: float, causal_offset: int, rows_per_seq: int = 0, stream: int = 0) -> int:
+    """Raw call of the scaled, causally masked softmax (status out)."""
+    return lib().softmax_fwd_masked(in_ptr, out_ptr, rows, cols, row_stride, dtype, scale, causal_offset,
+                                    rows_per_seq, stream)
 
 
 def softmax_fwd(x, out=None, stream=None):

@@ -15,6 +15,7 @@
 //   other rows fitting a cluster       path 3, a cluster per row
 //   otherwise                          path 4, rows split over the grid (2 passes)
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -589,6 +590,46 @@ int softmax_fwd(const void *in, void *out, int64_t rows, int64_t cols, int64_t r
     st = run(p, a);
     if (st == SOFTMAX_OK) g_last_path.store(p.path);
     return st;
+}
+
+int softmax_fwd_masked(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride, int dtype,
+                       float scale, int64_t causal_offset, int64_t rows_per_seq, cudaStream_t stream) {
+    int64_t ext = 0;
+    const uint64_t ia = (uint64_t)(uintptr_t)in, oa = (uint64_t)(uintptr_t)out;
+    int st = check_args(ia, oa, rows, cols, row_stride, dtype, &ext);
+    if (st != SOFTMAX_OK || rows == 0) return st;
+    if (!(scale > 0.f) || !std::isfinite(scale) || rows_per_seq < 0) return SOFTMAX_ERR_ARG;
+    int sms = 0;
+    st = device_sms(&sms);
+    if (st != SOFTMAX_OK) return st;
+    Shape want = forced_shape();
+    if (want.path != SOFTMAX_PATH_AUTO && want.path != SOFTMAX_PATH_WARP && want.path != SOFTMAX_PATH_CTA &&
+        want.path != SOFTMAX_PATH_STREAM)
+        want = Shape{SOFTMAX_PATH_STREAM, 0, 0, 0};  // no masked variant: the streaming cluster
+    Plan p;
+    st = make_plan(ia, oa, rows, cols, row_stride, dtype, sms, want, &p);
+    if (st != SOFTMAX_OK) return st;
+    if (p.path != SOFTMAX_PATH_WARP && p.path != SOFTMAX_PATH_CTA && p.path != SOFTMAX_PATH_STREAM) {
+        // rows too long for a block: the streaming cluster, at its own shape
+        st = make_plan(ia, oa, rows, cols, row_stride, dtype, sms, Shape{SOFTMAX_PATH_STREAM, 0, 0, 0}, &p);
+        if (st != SOFTMAX_OK) return st;
+    }
+    LaunchArgs a{in, out, rows, cols, row_stride, dtype, p.vec_store, stream, g_overlap.load(), 0};
+    // bounds that keep (r mod rows_per_seq) + off + 1 clear of int64 overflow
+    const int64_t lim = (int64_t)1 << 62;
+    a.mask.off = std::max(-lim, std::min(causal_offset, cols));
+    a.mask.period = rows_per_seq;
+    a.mask.k = (float)((double)scale * 1.4426950408889634);  // scale * log2 e, rounded once
+    cudaError_t e = cudaSuccess;
+    switch (p.path) {
+        case SOFTMAX_PATH_WARP: e = launch_warp_masked(a, p.threads, p.group, p.vpt, p.grid); break;
+        case SOFTMAX_PATH_CTA: e = launch_cta_masked(a, p.threads, p.vpt, p.grid); break;
+        default: e = launch_stream_masked(a, p.threads, p.vpt, p.group, g_wait_ns.load()); break;
+    }
+    if (e == cudaErrorInvalidValue) return SOFTMAX_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return SOFTMAX_ERR_CUDA;
+    g_last_path.store(p.path);
+    return SOFTMAX_OK;
 }
 
 int softmax_fwd_noalloc(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride, int dtype,

@@ -428,8 +428,8 @@ __device__ __forceinline__ void tile_store(const RowView<T> &row, int64_t first,
 //               formed -- the same bits, two exps per element instead of one.
 // Interface: set(j, raw) / set_empty(j) / load_one(j, row, v) /
 // load<WHOLE>(row, first, step, end);
-// stats() -> (s_t, l_t); values(j, f, y): y = e * f for vector j;
-// values_shift(j, shift, f, y): y = 2^(x log2 e - shift) * f (inputs only,
+// stats(k = log2 e) -> (s_t, l_t); values(j, f, y): y = e * f for vector j;
+// values_shift(j, shift, f, y, k): y = 2^(x k - shift) * f (inputs only,
 // before stats()); scale_store<WHOLE>(row, first, step, end, f);
 // shift_store<WHOLE>(row, first, step, end, shift, f) (inputs only).
 template <typename T, int VPT>
@@ -467,15 +467,17 @@ struct FloatTile {
             }
         }
     }
-    // Replace x by e = 2^(x log2 e - s_t) with the tile's own max m_t and
-    // s_t = fl(m_t log2 e); return the state (s_t, l_t).
-    __device__ __forceinline__ float2 stats() {
+    // Replace x by e = 2^(x k - s_t) with the tile's own max m_t and
+    // s_t = fl(m_t k); return the state (s_t, l_t).  k = log2 e, or
+    // scale * log2 e for scaled scores (scale > 0, so the max of x is the max
+    // of x * scale).
+    __device__ __forceinline__ float2 stats(float k = kLog2e) {
         float m = -INFINITY;
 #pragma unroll
         for (int j = 0; j < VPT; ++j)
 #pragma unroll
             for (int i = 0; i < V; ++i) m = fmaxf(m, x[j][i]);
-        const float s = m * kLog2e;  // -inf stays -inf, +inf stays +inf
+        const float s = m * k;  // -inf stays -inf, +inf stays +inf
         const float shift = safe_shift(s);
         float l = 0.f;
 #pragma unroll
@@ -483,7 +485,7 @@ struct FloatTile {
             float lj = 0.f;
 #pragma unroll
             for (int i = 0; i < V; ++i) {
-                x[j][i] = ex2(fmaf(x[j][i], kLog2e, -shift));
+                x[j][i] = ex2(fmaf(x[j][i], k, -shift));
                 lj += x[j][i];
             }
             l += lj;
@@ -494,9 +496,9 @@ struct FloatTile {
 #pragma unroll
         for (int i = 0; i < V; ++i) y[i] = x[j][i] * f;
     }
-    __device__ __forceinline__ void values_shift(int j, float shift, float f, float *y) const {
+    __device__ __forceinline__ void values_shift(int j, float shift, float f, float *y, float k = kLog2e) const {
 #pragma unroll
-        for (int i = 0; i < V; ++i) y[i] = ex2(fmaf(x[j][i], kLog2e, -shift)) * f;
+        for (int i = 0; i < V; ++i) y[i] = ex2(fmaf(x[j][i], k, -shift)) * f;
     }
     // y = e * f (after stats())
     template <bool WHOLE = false>
@@ -504,11 +506,12 @@ struct FloatTile {
                                                 float f) const {
         tile_store<T, VPT, WHOLE>(row, first, step, end, [&](int j, float *y) { values(j, f, y); });
     }
-    // y = 2^(x log2 e - shift) * f (the tile as loaded, without stats())
+    // y = 2^(x k - shift) * f (the tile as loaded, without stats())
     template <bool WHOLE = false>
     __device__ __forceinline__ void shift_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
-                                                float shift, float f) const {
-        tile_store<T, VPT, WHOLE>(row, first, step, end, [&](int j, float *y) { values_shift(j, shift, f, y); });
+                                                float shift, float f, float k = kLog2e) const {
+        tile_store<T, VPT, WHOLE>(row, first, step, end,
+                                  [&](int j, float *y) { values_shift(j, shift, f, y, k); });
     }
 };
 
@@ -518,6 +521,7 @@ struct PackedTile {
     static constexpr int V = Elem<T>::kVec;
     uint4 raw[VPT];
     float shift;  // the shift stats() used
+    float lg;     // and its multiplier k
 
     __device__ __forceinline__ void set(int j, const uint4 &r) { raw[j] = r; }
     __device__ __forceinline__ void load_one(int j, const RowView<T> &row, int64_t v) { raw[j] = row.load_raw(v); }
@@ -548,7 +552,7 @@ struct PackedTile {
             }
         }
     }
-    __device__ __forceinline__ float2 stats() {
+    __device__ __forceinline__ float2 stats(float k = kLog2e) {
         // the max on the packed pairs (a NaN never wins, as with fmaxf)
         uint32_t mw = (uint32_t)Elem<T>::kNegInfBits * 0x10001u;
 #pragma unroll
@@ -560,8 +564,9 @@ struct PackedTile {
         }
         const float2 mp = Elem<T>::pair(mw);
         const float m = fmaxf(mp.x, mp.y);
-        const float s = m * kLog2e;
+        const float s = m * k;
         shift = safe_shift(s);
+        lg = k;
         float l = 0.f;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
@@ -569,7 +574,7 @@ struct PackedTile {
             Elem<T>::unpack(raw[j], x);
             float lj = 0.f;
 #pragma unroll
-            for (int i = 0; i < V; ++i) lj += ex2(fmaf(x[i], kLog2e, -shift));
+            for (int i = 0; i < V; ++i) lj += ex2(fmaf(x[i], k, -shift));
             l += lj;
         }
         // The results are formed later from the packed words again: hide the
@@ -580,24 +585,25 @@ struct PackedTile {
             asm volatile("" : "+r"(raw[j].x), "+r"(raw[j].y), "+r"(raw[j].z), "+r"(raw[j].w));
         return make_float2(s, l);
     }
-    __device__ __forceinline__ void values_shift(int j, float sh, float f, float *y) const {
+    __device__ __forceinline__ void values_shift(int j, float sh, float f, float *y, float k = kLog2e) const {
         float x[V];
         Elem<T>::unpack(raw[j], x);
 #pragma unroll
-        for (int i = 0; i < V; ++i) y[i] = ex2(fmaf(x[i], kLog2e, -sh)) * f;
+        for (int i = 0; i < V; ++i) y[i] = ex2(fmaf(x[i], k, -sh)) * f;
     }
-    __device__ __forceinline__ void values(int j, float f, float *y) const { values_shift(j, shift, f, y); }
+    __device__ __forceinline__ void values(int j, float f, float *y) const { values_shift(j, shift, f, y, lg); }
     // y = e * f (after stats())
     template <bool WHOLE = false>
     __device__ __forceinline__ void scale_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
                                                 float f) const {
         tile_store<T, VPT, WHOLE>(row, first, step, end, [&](int j, float *y) { values(j, f, y); });
     }
-    // y = 2^(x log2 e - shift) * f (the tile as loaded, without stats())
+    // y = 2^(x k - shift) * f (the tile as loaded, without stats())
     template <bool WHOLE = false>
     __device__ __forceinline__ void shift_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
-                                                float shift, float f) const {
-        tile_store<T, VPT, WHOLE>(row, first, step, end, [&](int j, float *y) { values_shift(j, shift, f, y); });
+                                                float shift, float f, float k = kLog2e) const {
+        tile_store<T, VPT, WHOLE>(row, first, step, end,
+                                  [&](int j, float *y) { values_shift(j, shift, f, y, k); });
     }
 };
 

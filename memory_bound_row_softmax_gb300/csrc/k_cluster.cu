@@ -91,23 +91,56 @@ cudaError_t stream_as(const LaunchArgs &a, int csize, int64_t wait_ns) {
                          a.vec_store, wait_ns);
 }
 
-template <typename T, int THREADS>
+// masked rows (softmax_fwd_masked): never the whole-vector variant
+template <typename T, int THREADS, int VPT>
+cudaError_t stream_masked_as(const LaunchArgs &a, int csize, int64_t wait_ns) {
+    static std::atomic<unsigned long long> done{0};
+    constexpr int smem = ClusterSmem<THREADS, 0>::kBytes;
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e == cudaSuccess) e = opt_in(k_cluster_stream_masked<T, THREADS, VPT>, smem, done, device);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(k_cluster_stream_masked<T, THREADS, VPT>, a, a.rows * csize, THREADS, smem, csize,
+                         static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride,
+                         a.vec_store, wait_ns, a.mask);
+}
+
+template <typename T, int THREADS, bool MASKED>
 cudaError_t stream_vpt(const LaunchArgs &a, int vpt, int csize, int64_t wait_ns) {
-    switch (vpt) {
-        case 2: return a.whole ? stream_as<T, THREADS, 2, true>(a, csize, wait_ns)
-                               : stream_as<T, THREADS, 2, false>(a, csize, wait_ns);
-        case 4: return a.whole ? stream_as<T, THREADS, 4, true>(a, csize, wait_ns)
-                               : stream_as<T, THREADS, 4, false>(a, csize, wait_ns);
+    if constexpr (MASKED) {
+        switch (vpt) {
+            case 2: return stream_masked_as<T, THREADS, 2>(a, csize, wait_ns);
+            case 4: return stream_masked_as<T, THREADS, 4>(a, csize, wait_ns);
+            default: return cudaErrorInvalidValue;
+        }
+    } else {
+        switch (vpt) {
+            case 2: return a.whole ? stream_as<T, THREADS, 2, true>(a, csize, wait_ns)
+                                   : stream_as<T, THREADS, 2, false>(a, csize, wait_ns);
+            case 4: return a.whole ? stream_as<T, THREADS, 4, true>(a, csize, wait_ns)
+                                   : stream_as<T, THREADS, 4, false>(a, csize, wait_ns);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+}
+
+template <typename T, bool MASKED>
+cudaError_t stream_shape(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns) {
+    switch (threads) {
+        case 256: return stream_vpt<T, 256, MASKED>(a, vpt, csize, wait_ns);
+        case 512: return stream_vpt<T, 512, MASKED>(a, vpt, csize, wait_ns);
+        case 1024: return stream_vpt<T, 1024, MASKED>(a, vpt, csize, wait_ns);
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <typename T>
-cudaError_t stream_shape(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns) {
-    switch (threads) {
-        case 256: return stream_vpt<T, 256>(a, vpt, csize, wait_ns);
-        case 512: return stream_vpt<T, 512>(a, vpt, csize, wait_ns);
-        case 1024: return stream_vpt<T, 1024>(a, vpt, csize, wait_ns);
+template <bool MASKED>
+cudaError_t stream_dtype(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns) {
+    if (csize < 1 || csize > kMaxCluster) return cudaErrorInvalidValue;
+    switch (a.dtype) {
+        case 0: return stream_shape<float, MASKED>(a, threads, vpt, csize, wait_ns);
+        case 1: return stream_shape<__half, MASKED>(a, threads, vpt, csize, wait_ns);
+        case 2: return stream_shape<__nv_bfloat16, MASKED>(a, threads, vpt, csize, wait_ns);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -120,13 +153,11 @@ bool stream_shape_ok(int threads, int vpt) {
 int64_t stream_smem_bytes(int threads) { return 16 + (threads / 32) * 8 + kMaxCluster * 8; }
 
 cudaError_t launch_stream(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns) {
-    if (csize < 1 || csize > kMaxCluster) return cudaErrorInvalidValue;
-    switch (a.dtype) {
-        case 0: return stream_shape<float>(a, threads, vpt, csize, wait_ns);
-        case 1: return stream_shape<__half>(a, threads, vpt, csize, wait_ns);
-        case 2: return stream_shape<__nv_bfloat16>(a, threads, vpt, csize, wait_ns);
-        default: return cudaErrorInvalidValue;
-    }
+    return stream_dtype<false>(a, threads, vpt, csize, wait_ns);
+}
+
+cudaError_t launch_stream_masked(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns) {
+    return stream_dtype<true>(a, threads, vpt, csize, wait_ns);
 }
 
 bool cluster_shape_ok(int threads, int vpt, int elem_bytes) {

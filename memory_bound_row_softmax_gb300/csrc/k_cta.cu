@@ -10,7 +10,7 @@ bool cta_shape_ok(int threads, int vpt) {
 }
 
 cudaError_t launch_cta(const LaunchArgs &a, int threads, int vpt, int64_t grid) {
-    return a.whole ? launch_cta_whole(a, threads, vpt, grid) : cta_detail::launch<false>(a, threads, vpt, grid);
+    return a.whole ? launch_cta_whole(a, threads, vpt, grid) : cta_detail::launch<kPlainRows>(a, threads, vpt, grid);
 }
 
 }  // namespace mbrs

@@ -5,7 +5,7 @@
 namespace mbrs {
 
 cudaError_t launch_cta_whole(const LaunchArgs &a, int threads, int vpt, int64_t grid) {
-    return cta_detail::launch<true>(a, threads, vpt, grid);
+    return cta_detail::launch<kWholeRows>(a, threads, vpt, grid);
 }
 
 }  // namespace mbrs

@@ -12,7 +12,7 @@ bool warp_shape_ok(int group, int vpt) {
 cudaError_t launch_warp(const LaunchArgs &a, int threads, int group, int vpt, int64_t grid) {
     if (threads < 32 || threads > 256 || threads % 32 != 0) return cudaErrorInvalidValue;
     return a.whole ? launch_warp_whole(a, threads, group, vpt, grid)
-                   : warp_detail::launch<false>(a, threads, group, vpt, grid);
+                   : warp_detail::launch<kPlainRows>(a, threads, group, vpt, grid);
 }
 
 }  // namespace mbrs

@@ -5,7 +5,7 @@
 namespace mbrs {
 
 cudaError_t launch_warp_whole(const LaunchArgs &a, int threads, int group, int vpt, int64_t grid) {
-    return warp_detail::launch<true>(a, threads, group, vpt, grid);
+    return warp_detail::launch<kWholeRows>(a, threads, group, vpt, grid);
 }
 
 }  // namespace mbrs

@@ -577,4 +577,159 @@ __global__ void __launch_bounds__(THREADS)
     }
 }
 
+// ---------------------------------------------------------------------------
+// scaled, causally masked rows (softmax_fwd_masked)
+// ---------------------------------------------------------------------------
+// Page "Dissecting Memory Bandwidth & SRAM Tiling in Triton: From GEMM to
+// FlashAttention-3", section "Writing the Kernel in OpenAI Triton": scores
+// are x * scale and a key after its query is -inf before the softmax.  Row r
+// keeps n = mask.kept(r, cols) columns: only those are read (a row view of n
+// columns), the row is written in full (a row view of cols columns), the
+// masked outputs being 0 -- or NaN when the row itself is NaN (nothing kept,
+// or a NaN / +inf among the kept entries): the fill is f * 0 for the row's
+// output factor f, which is NaN exactly then.
+
+// The first of the vectors first, first + step, ... that is >= lo.
+__device__ __forceinline__ int64_t first_from(int64_t first, int64_t step, int64_t lo) {
+    if (first >= lo) return first;
+    return first + ((lo - first + step - 1) / step) * step;
+}
+
+// Store `value` into every element of vectors first, first + step, ... below end.
+template <typename T>
+__device__ __forceinline__ void fill_vectors(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
+                                             float value) {
+    float y[Elem<T>::kVec];
+#pragma unroll
+    for (int i = 0; i < Elem<T>::kVec; ++i) y[i] = value;
+    for (int64_t v = first; v < end; v += step) row.store(v, y);
+}
+
+template <typename T, int G, int VPT>
+__global__ void __launch_bounds__(256) k_warp_rows_masked(const T *in, T *out, int64_t rows, int64_t cols,
+                                                          int64_t stride, int vec_store, CausalMask mask) {
+    const int t = threadIdx.x & (G - 1);
+    const int64_t groups_per_block = blockDim.x / G;
+    const int64_t row_step = (int64_t)gridDim.x * groups_per_block;
+    const int64_t warp_row0 = (int64_t)blockIdx.x * groups_per_block + (threadIdx.x & ~31) / G;
+    if (t == 0 && warp_row0 + (threadIdx.x & 31) / G < rows) {
+        const int64_t r = warp_row0 + (threadIdx.x & 31) / G;
+        prefetch_span_l2(in + r * stride, 0, mask.kept(r, cols), cols);
+    }
+    pdl_enter();
+    for (int64_t base = warp_row0; base < rows; base += row_step) {
+        const int64_t row = base + (threadIdx.x & 31) / G;
+        const bool active = row < rows;
+        const int64_t r = active ? row : 0;
+        RowView<T> rl(in + r * stride, out + r * stride, active ? mask.kept(row, cols) : 0, vec_store != 0);
+        RowView<T> rs(in + r * stride, out + r * stride, cols, vec_store != 0);
+        Tile<T, VPT> tile;
+        tile.load(rl, t, G, active ? rl.nvec : 0);
+        const float2 s = tile.stats(mask.k);
+        float m = s.x, l = s.y;
+        group_merge<G>(m, l);
+        if (active) {
+            const float f = out_factor(s.x, m, l);
+            tile.scale_store(rs, t, G, rl.nvec, f);
+            fill_vectors(rs, first_from(t, G, rl.nvec), G, rs.nvec, f * 0.f);
+        }
+    }
+}
+
+template <typename T, int THREADS, int VPT>
+__device__ __forceinline__ void cta_rows_masked_body(const T *in, T *out, int64_t rows, int64_t cols,
+                                                     int64_t stride, int vec_store, const CausalMask &mask) {
+    constexpr int NW = THREADS / 32;
+    __shared__ float2 red[2][NW];
+    if (threadIdx.x == 0 && blockIdx.x < rows)
+        prefetch_span_l2(in + blockIdx.x * stride, 0, mask.kept(blockIdx.x, cols), cols);
+    pdl_enter();
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
+        RowView<T> rl(in + row * stride, out + row * stride, mask.kept(row, cols), vec_store != 0);
+        RowView<T> rs(in + row * stride, out + row * stride, cols, vec_store != 0);
+        Tile<T, VPT> tile;
+        tile.load(rl, threadIdx.x, THREADS, rl.nvec);
+        const float2 s = tile.stats(mask.k);
+        float m = s.x, l = s.y;
+        block_merge<NW>(m, l, red[parity]);
+        const float f = out_factor(s.x, m, l);
+        tile.scale_store(rs, threadIdx.x, THREADS, rl.nvec, f);
+        fill_vectors(rs, first_from(threadIdx.x, THREADS, rl.nvec), THREADS, rs.nvec, f * 0.f);
+    }
+}
+
+template <typename T, int THREADS, int VPT>
+__global__ void __launch_bounds__(THREADS) k_cta_rows_masked(const T *in, T *out, int64_t rows, int64_t cols,
+                                                             int64_t stride, int vec_store, CausalMask mask) {
+    cta_rows_masked_body<T, THREADS, VPT>(in, out, rows, cols, stride, vec_store, mask);
+}
+
+template <typename T, int THREADS, int VPT>
+__global__ void __launch_bounds__(THREADS, 1024 / THREADS)
+    k_cta_rows_masked_wide(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store,
+                           CausalMask mask) {
+    cta_rows_masked_body<T, THREADS, VPT>(in, out, rows, cols, stride, vec_store, mask);
+}
+
+// The streaming cluster of path 6 on masked rows: every block owns a slice
+// of the full row; it reads only the kept part of its slice, in both passes.
+template <typename T, int THREADS, int VPT>
+__global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS))
+    k_cluster_stream_masked(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store,
+                            int64_t wait_ns, CausalMask mask) {
+    if (!explicit_cluster()) {  // launched without clusters: touch no cluster state
+        pdl_enter();
+        if (threadIdx.x == 0) atomicOr(&g_error_word, kErrNotCluster);
+        return;
+    }
+    constexpr int V = Elem<T>::kVec;
+    constexpr int NW = THREADS / 32;
+    constexpr int64_t kTile = (int64_t)THREADS * VPT;
+    using L = ClusterSmem<THREADS, 0>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    float2 *red = reinterpret_cast<float2 *>(smem + L::kRedOff);
+    float2 *slots = reinterpret_cast<float2 *>(smem + L::kSlotOff);
+    const uint32_t xbar = smem_addr(smem + L::kXbarOff);
+    const int tid = threadIdx.x;
+
+    const uint32_t rank = cluster_rank(), csize = cluster_size();
+    const int64_t row = blockIdx.x / csize;
+    RowView<T> rl(in + row * stride, out + row * stride, mask.kept(row, cols), vec_store != 0);
+    RowView<T> rs(in + row * stride, out + row * stride, cols, vec_store != 0);
+    const int64_t per = (rs.nvec + csize - 1) / csize;
+    const int64_t s0 = min((int64_t)rank * per, rs.nvec), s1 = min(s0 + per, rs.nvec);
+    const int64_t k1 = min(s1, rl.nvec);  // this slice's kept vectors: [s0, k1)
+    if (tid == 0) prefetch_span_l2(rl.in, s0 * V - rl.head, min(s0 + kTile, k1) * V - rl.head, rl.cols);
+    pdl_enter();
+
+    if (tid == 0) {
+        mbar_init(xbar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(xbar, csize * 8u);
+    }
+    __syncthreads();
+    cluster_arrive_relaxed();
+
+    float m = -INFINITY, l = 0.f;
+    for (int64_t t0 = s0; t0 < k1; t0 += kTile) {
+        Tile<T, VPT> tile;
+        tile.load(rl, t0 + tid, THREADS, k1);
+        const float2 st = tile.stats(mask.k);
+        const float M = fmaxf(m, st.x);
+        l = rescale(l, m, M) + rescale(st.y, st.x, M);
+        m = M;
+    }
+    block_merge<NW>(m, l, red);
+    if (!cluster_exchange<NW>(m, l, slots, xbar, rank, csize, wait_ns)) return;
+
+    const float inv = m == -INFINITY ? __int_as_float(0x7fc00000) : 1.f / l;
+    for (int64_t t0 = s0; t0 < k1; t0 += kTile) {
+        Tile<T, VPT> tile;
+        tile.load(rl, t0 + tid, THREADS, k1);
+        tile.shift_store(rs, t0 + tid, THREADS, k1, m, inv, mask.k);
+    }
+    fill_vectors(rs, first_from(s0 + tid, THREADS, k1), THREADS, s1, inv * 0.f);
+}
+
 }  // namespace mbrs

@@ -9,6 +9,19 @@
 
 namespace mbrs {
 
+// softmax_fwd_masked: row r keeps columns c < kept(r) = clamp((r mod period)
+// + off + 1, 0, cols) (period 0: r itself), and its scores are x * scale,
+// entered into the exponent as k = scale * log2 e.
+struct CausalMask {
+    int64_t off = 0, period = 0;
+    float k = 1.4426950408889634f;  // log2 e: scale 1
+    __host__ __device__ int64_t kept(int64_t row, int64_t cols) const {
+        const int64_t q = period > 0 ? row % period : row;
+        const int64_t n = q + off + 1;
+        return n < 0 ? 0 : (n > cols ? cols : n);
+    }
+};
+
 struct LaunchArgs {
     const void *in;
     void *out;
@@ -19,6 +32,7 @@ struct LaunchArgs {
     int overlap;    // launch with programmatic stream serialisation
     int whole;      // every row is whole 16-byte vectors: in and out 16-byte
                     // aligned, row stride and width multiples of 16 bytes
+    CausalMask mask;  // masked launches only
 };
 
 // Device error word bits (k_cluster.cu / k_ring.cu each hold one word):
@@ -26,6 +40,9 @@ struct LaunchArgs {
 // cluster (it then returns before any cluster access).
 constexpr unsigned int kErrWaitTimeout = 1u;
 constexpr unsigned int kErrNotCluster = 2u;
+
+// Kernel variants of the warp and block paths.
+constexpr int kPlainRows = 0, kWholeRows = 1, kMaskedRows = 2;
 
 // Launch `kernel` on a.stream; csize >= 1 makes it a cluster launch with
 // clusters of csize blocks (kernels that use cluster instructions need it,
@@ -76,6 +93,11 @@ cudaError_t launch_cta(const LaunchArgs &a, int threads, int vpt, int64_t grid);
 // the instantiations for a.whole (k_warp_whole.cu, k_cta_whole.cu)
 cudaError_t launch_warp_whole(const LaunchArgs &a, int threads, int group, int vpt, int64_t grid);
 cudaError_t launch_cta_whole(const LaunchArgs &a, int threads, int vpt, int64_t grid);
+// scaled, causally masked rows with a.mask (k_masked_warp.cu, k_masked.cu):
+// the warp and block shapes of paths 1 and 2, and the streaming cluster
+cudaError_t launch_warp_masked(const LaunchArgs &a, int threads, int group, int vpt, int64_t grid);
+cudaError_t launch_cta_masked(const LaunchArgs &a, int threads, int vpt, int64_t grid);
+cudaError_t launch_stream_masked(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns);
 
 bool cluster_shape_ok(int threads, int vpt, int elem_bytes);
 int64_t cluster_smem_bytes(int threads, int vpt);

@@ -170,3 +170,14 @@ def test_forced_paths_and_rejections():
             B.set_force_path(9)
     finally:
         B.set_force_path(0)
+
+
+def test_masked_argument_checks_need_no_gpu():
+    p = 1 << 24
+    q = 1 << 40
+    for scale in (0.0, -2.0, float("inf"), float("nan")):
+        assert B.softmax_fwd_masked_ptr(p, q, 4, 8, 8, 0, scale, 0, 0) == B.ERR_ARG
+    assert B.softmax_fwd_masked_ptr(p, q, 4, 8, 8, 0, 1.0, 0, -1) == B.ERR_ARG
+    assert B.softmax_fwd_masked_ptr(p, q, 0, 8, 8, 0, 1.0, 0, 0) == B.OK      # no rows: nothing to do
+    assert B.softmax_fwd_masked_ptr(p, q, 4, 8, 7, 0, 1.0, 0, 0) == B.ERR_STRIDE
+    assert B.softmax_fwd_masked_ptr(p, p + 4, 4, 8, 8, 0, 1.0, 0, 0) == B.ERR_OVERLAP
