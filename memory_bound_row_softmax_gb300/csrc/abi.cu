@@ -614,7 +614,7 @@ int softmax_fwd_masked(const void *in, void *out, int64_t rows, int64_t cols, in
         st = make_plan(ia, oa, rows, cols, row_stride, dtype, sms, Shape{SOFTMAX_PATH_STREAM, 0, 0, 0}, &p);
         if (st != SOFTMAX_OK) return st;
     }
-    LaunchArgs a{in, out, rows, cols, row_stride, dtype, p.vec_store, stream, g_overlap.load(), 0};
+    LaunchArgs a{in, out, rows, cols, row_stride, dtype, p.vec_store, stream, g_overlap.load(), p.whole};
     // bounds that keep (r mod rows_per_seq) + off + 1 clear of int64 overflow
     const int64_t lim = (int64_t)1 << 62;
     a.mask.off = std::max(-lim, std::min(causal_offset, cols));

@@ -385,6 +385,13 @@ struct RowView {
 // host for the whole call): a thread's vectors first + j*step (j < VPT) move
 // as plain 16-byte accesses at constant offsets, with no edge test; those with
 // j*step >= whole_fit(first, end) lie past the tile's end.
+// How many of a tile's vectors first + j*step (j < vpt) lie below end.
+__device__ __forceinline__ int live_slots(int64_t first, int64_t step, int64_t end, int vpt) {
+    if (first >= end) return 0;
+    const int64_t n = (end - first + step - 1) / step;
+    return n < vpt ? (int)n : vpt;
+}
+
 __device__ __forceinline__ int whole_fit(int64_t first, int64_t end) {
     return (int)max(min(end - first, (int64_t)0x7fffffff), (int64_t)0);
 }
@@ -471,17 +478,21 @@ struct FloatTile {
     // s_t = fl(m_t k); return the state (s_t, l_t).  k = log2 e, or
     // scale * log2 e for scaled scores (scale > 0, so the max of x is the max
     // of x * scale).
-    __device__ __forceinline__ float2 stats(float k = kLog2e) {
+    // Only the first `live` vectors hold data (the others are empty: -inf);
+    // their exponentials are skipped, and values() of them is never asked for.
+    __device__ __forceinline__ float2 stats(float k = kLog2e, int live = VPT) {
         float m = -INFINITY;
 #pragma unroll
         for (int j = 0; j < VPT; ++j)
+            if (j < live)
 #pragma unroll
-            for (int i = 0; i < V; ++i) m = fmaxf(m, x[j][i]);
+                for (int i = 0; i < V; ++i) m = fmaxf(m, x[j][i]);
         const float s = m * k;  // -inf stays -inf, +inf stays +inf
         const float shift = safe_shift(s);
         float l = 0.f;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
+            if (j >= live) continue;
             float lj = 0.f;
 #pragma unroll
             for (int i = 0; i < V; ++i) {
@@ -552,11 +563,13 @@ struct PackedTile {
             }
         }
     }
-    __device__ __forceinline__ float2 stats(float k = kLog2e) {
+    // As FloatTile::stats: only the first `live` vectors hold data.
+    __device__ __forceinline__ float2 stats(float k = kLog2e, int live = VPT) {
         // the max on the packed pairs (a NaN never wins, as with fmaxf)
         uint32_t mw = (uint32_t)Elem<T>::kNegInfBits * 0x10001u;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
+            if (j >= live) continue;
             mw = Elem<T>::max2(mw, raw[j].x);
             mw = Elem<T>::max2(mw, raw[j].y);
             mw = Elem<T>::max2(mw, raw[j].z);
@@ -570,6 +583,7 @@ struct PackedTile {
         float l = 0.f;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
+            if (j >= live) continue;
             float x[V];
             Elem<T>::unpack(raw[j], x);
             float lj = 0.f;

@@ -1,7 +1,7 @@
 // cta_launch.cuh -- path 2 launch dispatch, shared by k_cta.cu (rows with
-// partial 16-byte vectors), k_cta_whole.cu (rows of whole vectors only) and
-// k_masked.cu (scaled, causally masked rows), which instantiate the three
-// variants in separate translation units.
+// partial 16-byte vectors), k_cta_whole.cu (rows of whole vectors only),
+// k_masked.cu and k_masked_whole.cu (scaled, causally masked rows), which
+// instantiate the four variants in separate translation units.
 #pragma once
 
 #include "kernels.cuh"
@@ -12,13 +12,14 @@ namespace mbrs {
 namespace cta_detail {
 template <typename T, int THREADS, int VPT, int VAR>
 cudaError_t go(const LaunchArgs &a, int64_t grid) {
-    constexpr bool whole = VAR == kWholeRows;
-    if constexpr (VAR == kMaskedRows && VPT >= 6)
-        return launch_kernel(k_cta_rows_masked_wide<T, THREADS, VPT>, a, grid, THREADS, 0, 0,
+    constexpr bool whole = VAR == kWholeRows || VAR == kMaskedWholeRows;
+    constexpr bool masked = VAR == kMaskedRows || VAR == kMaskedWholeRows;
+    if constexpr (masked && VPT >= 6)
+        return launch_kernel(k_cta_rows_masked_wide<T, THREADS, VPT, whole>, a, grid, THREADS, 0, 0,
                              static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride,
                              a.vec_store, a.mask);
-    else if constexpr (VAR == kMaskedRows)
-        return launch_kernel(k_cta_rows_masked<T, THREADS, VPT>, a, grid, THREADS, 0, 0,
+    else if constexpr (masked)
+        return launch_kernel(k_cta_rows_masked<T, THREADS, VPT, whole>, a, grid, THREADS, 0, 0,
                              static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride,
                              a.vec_store, a.mask);
     else if constexpr (VPT >= 6)

@@ -91,16 +91,16 @@ cudaError_t stream_as(const LaunchArgs &a, int csize, int64_t wait_ns) {
                          a.vec_store, wait_ns);
 }
 
-// masked rows (softmax_fwd_masked): never the whole-vector variant
-template <typename T, int THREADS, int VPT>
+// masked rows (softmax_fwd_masked)
+template <typename T, int THREADS, int VPT, bool WHOLE>
 cudaError_t stream_masked_as(const LaunchArgs &a, int csize, int64_t wait_ns) {
     static std::atomic<unsigned long long> done{0};
     constexpr int smem = ClusterSmem<THREADS, 0>::kBytes;
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
-    if (e == cudaSuccess) e = opt_in(k_cluster_stream_masked<T, THREADS, VPT>, smem, done, device);
+    if (e == cudaSuccess) e = opt_in(k_cluster_stream_masked<T, THREADS, VPT, WHOLE>, smem, done, device);
     if (e != cudaSuccess) return e;
-    return launch_kernel(k_cluster_stream_masked<T, THREADS, VPT>, a, a.rows * csize, THREADS, smem, csize,
+    return launch_kernel(k_cluster_stream_masked<T, THREADS, VPT, WHOLE>, a, a.rows * csize, THREADS, smem, csize,
                          static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride,
                          a.vec_store, wait_ns, a.mask);
 }
@@ -109,8 +109,10 @@ template <typename T, int THREADS, bool MASKED>
 cudaError_t stream_vpt(const LaunchArgs &a, int vpt, int csize, int64_t wait_ns) {
     if constexpr (MASKED) {
         switch (vpt) {
-            case 2: return stream_masked_as<T, THREADS, 2>(a, csize, wait_ns);
-            case 4: return stream_masked_as<T, THREADS, 4>(a, csize, wait_ns);
+            case 2: return a.whole ? stream_masked_as<T, THREADS, 2, true>(a, csize, wait_ns)
+                                   : stream_masked_as<T, THREADS, 2, false>(a, csize, wait_ns);
+            case 4: return a.whole ? stream_masked_as<T, THREADS, 4, true>(a, csize, wait_ns)
+                                   : stream_masked_as<T, THREADS, 4, false>(a, csize, wait_ns);
             default: return cudaErrorInvalidValue;
         }
     } else {

@@ -5,7 +5,7 @@
 namespace mbrs {
 
 cudaError_t launch_cta_masked(const LaunchArgs &a, int threads, int vpt, int64_t grid) {
-    return cta_detail::launch<kMaskedRows>(a, threads, vpt, grid);
+    return a.whole ? launch_cta_masked_whole(a, threads, vpt, grid) : cta_detail::launch<kMaskedRows>(a, threads, vpt, grid);
 }
 
 }  // namespace mbrs

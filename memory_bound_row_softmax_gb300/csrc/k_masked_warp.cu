@@ -6,7 +6,8 @@ namespace mbrs {
 
 cudaError_t launch_warp_masked(const LaunchArgs &a, int threads, int group, int vpt, int64_t grid) {
     if (threads < 32 || threads > 256 || threads % 32 != 0) return cudaErrorInvalidValue;
-    return warp_detail::launch<kMaskedRows>(a, threads, group, vpt, grid);
+    return a.whole ? launch_warp_masked_whole(a, threads, group, vpt, grid)
+                   : warp_detail::launch<kMaskedRows>(a, threads, group, vpt, grid);
 }
 
 }  // namespace mbrs

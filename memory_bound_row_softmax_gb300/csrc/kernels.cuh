@@ -586,8 +586,9 @@ __global__ void __launch_bounds__(THREADS)
 // keeps n = mask.kept(r, cols) columns: only those are read (a row view of n
 // columns), the row is written in full (a row view of cols columns), the
 // masked outputs being 0 -- or NaN when the row itself is NaN (nothing kept,
-// or a NaN / +inf among the kept entries): the fill is f * 0 for the row's
-// output factor f, which is NaN exactly then.
+// or a NaN / +inf among the kept entries), which the row's output factor f
+// shows: the zeros are stored while the loads are in flight, and a NaN row
+// stores its masked part again.
 
 // The first of the vectors first, first + step, ... that is >= lo.
 __device__ __forceinline__ int64_t first_from(int64_t first, int64_t step, int64_t lo) {
@@ -595,17 +596,44 @@ __device__ __forceinline__ int64_t first_from(int64_t first, int64_t step, int64
     return first + ((lo - first + step - 1) / step) * step;
 }
 
-// Store `value` into every element of vectors first, first + step, ... below end.
-template <typename T>
+// Store `value` into every element of vectors first, first + step, ... below
+// end (WHOLE: rows of whole vectors, plain 16-byte stores).
+template <bool WHOLE, typename T>
 __device__ __forceinline__ void fill_vectors(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
                                              float value) {
     float y[Elem<T>::kVec];
 #pragma unroll
     for (int i = 0; i < Elem<T>::kVec; ++i) y[i] = value;
-    for (int64_t v = first; v < end; v += step) row.store(v, y);
+    if constexpr (WHOLE) {
+        const uint4 w = Elem<T>::pack(y);
+        uint4 *q = reinterpret_cast<uint4 *>(row.out);
+        for (int64_t v = first; v < end; v += step) q[v] = w;
+    } else {
+        for (int64_t v = first; v < end; v += step) row.store(v, y);
+    }
 }
 
-template <typename T, int G, int VPT>
+// Load a thread's kept vectors first + j*step of a row view `rl` of the kept
+// columns.  WHOLE (the full rows are whole vectors): every kept vector but a
+// last partial one moves as a plain 16-byte load, the partial one (if any)
+// element by element.
+template <bool WHOLE, int VPT, typename Tl, typename T>
+__device__ __forceinline__ void load_kept(Tl &tile, const RowView<T> &rl, int64_t first, int64_t step) {
+    if constexpr (WHOLE) {
+        constexpr int V = Elem<T>::kVec;
+        const int64_t nw = rl.cols / V;  // whole kept vectors (rows start on 16 bytes)
+        tile.template load<true>(rl, first, step, nw);
+        if (rl.cols % V != 0) {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j)
+                if (first + j * step == nw) tile.load_one(j, rl, nw);
+        }
+    } else {
+        tile.load(rl, first, step, rl.nvec);
+    }
+}
+
+template <typename T, int G, int VPT, bool WHOLE>
 __global__ void __launch_bounds__(256) k_warp_rows_masked(const T *in, T *out, int64_t rows, int64_t cols,
                                                           int64_t stride, int vec_store, CausalMask mask) {
     const int t = threadIdx.x & (G - 1);
@@ -624,19 +652,23 @@ __global__ void __launch_bounds__(256) k_warp_rows_masked(const T *in, T *out, i
         RowView<T> rl(in + r * stride, out + r * stride, active ? mask.kept(row, cols) : 0, vec_store != 0);
         RowView<T> rs(in + r * stride, out + r * stride, cols, vec_store != 0);
         Tile<T, VPT> tile;
-        tile.load(rl, t, G, active ? rl.nvec : 0);
-        const float2 s = tile.stats(mask.k);
+        load_kept<WHOLE, VPT>(tile, rl, t, G);
+        // the masked outputs do not depend on the loads: their zeros go out
+        // while the loads are in flight
+        const int64_t fill0 = first_from(t, G, rl.nvec);
+        if (active) fill_vectors<WHOLE>(rs, fill0, G, rs.nvec, 0.f);
+        const float2 s = tile.stats(mask.k, live_slots(t, G, rl.nvec, VPT));
         float m = s.x, l = s.y;
         group_merge<G>(m, l);
         if (active) {
             const float f = out_factor(s.x, m, l);
-            tile.scale_store(rs, t, G, rl.nvec, f);
-            fill_vectors(rs, first_from(t, G, rl.nvec), G, rs.nvec, f * 0.f);
+            tile.template scale_store<WHOLE>(rs, t, G, rl.nvec, f);
+            if (isnan(f)) fill_vectors<WHOLE>(rs, fill0, G, rs.nvec, f);  // a NaN row
         }
     }
 }
 
-template <typename T, int THREADS, int VPT>
+template <typename T, int THREADS, int VPT, bool WHOLE>
 __device__ __forceinline__ void cta_rows_masked_body(const T *in, T *out, int64_t rows, int64_t cols,
                                                      int64_t stride, int vec_store, const CausalMask &mask) {
     constexpr int NW = THREADS / 32;
@@ -649,32 +681,34 @@ __device__ __forceinline__ void cta_rows_masked_body(const T *in, T *out, int64_
         RowView<T> rl(in + row * stride, out + row * stride, mask.kept(row, cols), vec_store != 0);
         RowView<T> rs(in + row * stride, out + row * stride, cols, vec_store != 0);
         Tile<T, VPT> tile;
-        tile.load(rl, threadIdx.x, THREADS, rl.nvec);
-        const float2 s = tile.stats(mask.k);
+        load_kept<WHOLE, VPT>(tile, rl, threadIdx.x, THREADS);
+        const int64_t fill0 = first_from(threadIdx.x, THREADS, rl.nvec);
+        fill_vectors<WHOLE>(rs, fill0, THREADS, rs.nvec, 0.f);  // while the loads are in flight
+        const float2 s = tile.stats(mask.k, live_slots(threadIdx.x, THREADS, rl.nvec, VPT));
         float m = s.x, l = s.y;
         block_merge<NW>(m, l, red[parity]);
         const float f = out_factor(s.x, m, l);
-        tile.scale_store(rs, threadIdx.x, THREADS, rl.nvec, f);
-        fill_vectors(rs, first_from(threadIdx.x, THREADS, rl.nvec), THREADS, rs.nvec, f * 0.f);
+        tile.template scale_store<WHOLE>(rs, threadIdx.x, THREADS, rl.nvec, f);
+        if (isnan(f)) fill_vectors<WHOLE>(rs, fill0, THREADS, rs.nvec, f);  // a NaN row
     }
 }
 
-template <typename T, int THREADS, int VPT>
+template <typename T, int THREADS, int VPT, bool WHOLE>
 __global__ void __launch_bounds__(THREADS) k_cta_rows_masked(const T *in, T *out, int64_t rows, int64_t cols,
                                                              int64_t stride, int vec_store, CausalMask mask) {
-    cta_rows_masked_body<T, THREADS, VPT>(in, out, rows, cols, stride, vec_store, mask);
+    cta_rows_masked_body<T, THREADS, VPT, WHOLE>(in, out, rows, cols, stride, vec_store, mask);
 }
 
-template <typename T, int THREADS, int VPT>
+template <typename T, int THREADS, int VPT, bool WHOLE>
 __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
     k_cta_rows_masked_wide(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store,
                            CausalMask mask) {
-    cta_rows_masked_body<T, THREADS, VPT>(in, out, rows, cols, stride, vec_store, mask);
+    cta_rows_masked_body<T, THREADS, VPT, WHOLE>(in, out, rows, cols, stride, vec_store, mask);
 }
 
 // The streaming cluster of path 6 on masked rows: every block owns a slice
 // of the full row; it reads only the kept part of its slice, in both passes.
-template <typename T, int THREADS, int VPT>
+template <typename T, int THREADS, int VPT, bool WHOLE>
 __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS))
     k_cluster_stream_masked(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store,
                             int64_t wait_ns, CausalMask mask) {
@@ -710,12 +744,14 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     }
     __syncthreads();
     cluster_arrive_relaxed();
+    const int64_t fill0 = first_from(s0 + tid, THREADS, k1);
+    fill_vectors<WHOLE>(rs, fill0, THREADS, s1, 0.f);  // the masked part of the slice
 
     float m = -INFINITY, l = 0.f;
     for (int64_t t0 = s0; t0 < k1; t0 += kTile) {
         Tile<T, VPT> tile;
         tile.load(rl, t0 + tid, THREADS, k1);
-        const float2 st = tile.stats(mask.k);
+        const float2 st = tile.stats(mask.k, live_slots(t0 + tid, THREADS, k1, VPT));
         const float M = fmaxf(m, st.x);
         l = rescale(l, m, M) + rescale(st.y, st.x, M);
         m = M;
@@ -727,9 +763,9 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     for (int64_t t0 = s0; t0 < k1; t0 += kTile) {
         Tile<T, VPT> tile;
         tile.load(rl, t0 + tid, THREADS, k1);
-        tile.shift_store(rs, t0 + tid, THREADS, k1, m, inv, mask.k);
+        tile.template shift_store<WHOLE>(rs, t0 + tid, THREADS, k1, m, inv, mask.k);
     }
-    fill_vectors(rs, first_from(s0 + tid, THREADS, k1), THREADS, s1, inv * 0.f);
+    if (isnan(inv)) fill_vectors<WHOLE>(rs, fill0, THREADS, s1, inv);  // a NaN row
 }
 
 }  // namespace mbrs

@@ -16,7 +16,11 @@ struct CausalMask {
     int64_t off = 0, period = 0;
     float k = 1.4426950408889634f;  // log2 e: scale 1
     __host__ __device__ int64_t kept(int64_t row, int64_t cols) const {
-        const int64_t q = period > 0 ? row % period : row;
+        // 32-bit remainder when both fit (a 64-bit one is a long instruction sequence)
+        const bool narrow = row <= 0x7fffffff && period <= 0x7fffffff;
+        const int64_t q = period <= 0 ? row
+                          : narrow   ? (int64_t)((uint32_t)row % (uint32_t)period)
+                                     : row % period;
         const int64_t n = q + off + 1;
         return n < 0 ? 0 : (n > cols ? cols : n);
     }
@@ -42,7 +46,7 @@ constexpr unsigned int kErrWaitTimeout = 1u;
 constexpr unsigned int kErrNotCluster = 2u;
 
 // Kernel variants of the warp and block paths.
-constexpr int kPlainRows = 0, kWholeRows = 1, kMaskedRows = 2;
+constexpr int kPlainRows = 0, kWholeRows = 1, kMaskedRows = 2, kMaskedWholeRows = 3;
 
 // Launch `kernel` on a.stream; csize >= 1 makes it a cluster launch with
 // clusters of csize blocks (kernels that use cluster instructions need it,
@@ -97,6 +101,9 @@ cudaError_t launch_cta_whole(const LaunchArgs &a, int threads, int vpt, int64_t 
 // the warp and block shapes of paths 1 and 2, and the streaming cluster
 cudaError_t launch_warp_masked(const LaunchArgs &a, int threads, int group, int vpt, int64_t grid);
 cudaError_t launch_cta_masked(const LaunchArgs &a, int threads, int vpt, int64_t grid);
+// ... their a.whole instantiations (k_masked_warp_whole.cu, k_masked_whole.cu)
+cudaError_t launch_warp_masked_whole(const LaunchArgs &a, int threads, int group, int vpt, int64_t grid);
+cudaError_t launch_cta_masked_whole(const LaunchArgs &a, int threads, int vpt, int64_t grid);
 cudaError_t launch_stream_masked(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns);
 
 bool cluster_shape_ok(int threads, int vpt, int elem_bytes);

@@ -1,7 +1,7 @@
 // warp_launch.cuh -- path 1 launch dispatch, shared by k_warp.cu (rows with
-// partial 16-byte vectors), k_warp_whole.cu (rows of whole vectors only) and
-// k_masked_warp.cu (scaled, causally masked rows), which instantiate the
-// three variants in separate translation units.
+// partial 16-byte vectors), k_warp_whole.cu (rows of whole vectors only),
+// k_masked_warp.cu and k_masked_warp_whole.cu (scaled, causally masked rows),
+// which instantiate the four variants in separate translation units.
 #pragma once
 
 #include "kernels.cuh"
@@ -12,9 +12,10 @@ namespace mbrs {
 namespace warp_detail {
 template <typename T, int G, int VPT, int VAR>
 cudaError_t go(const LaunchArgs &a, int threads, int64_t grid) {
-    if constexpr (VAR == kMaskedRows)
-        return launch_kernel(k_warp_rows_masked<T, G, VPT>, a, grid, threads, 0, 0, static_cast<const T *>(a.in),
-                             static_cast<T *>(a.out), a.rows, a.cols, a.stride, a.vec_store, a.mask);
+    if constexpr (VAR == kMaskedRows || VAR == kMaskedWholeRows)
+        return launch_kernel(k_warp_rows_masked<T, G, VPT, VAR == kMaskedWholeRows>, a, grid, threads, 0, 0,
+                             static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride,
+                             a.vec_store, a.mask);
     else
         return launch_kernel(k_warp_rows<T, G, VPT, VAR == kWholeRows>, a, grid, threads, 0, 0,
                              static_cast<const T *>(a.in), static_cast<T *>(a.out), a.rows, a.cols, a.stride,
