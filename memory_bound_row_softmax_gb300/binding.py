@@ -123,18 +123,14 @@ def softmax_fwd_masked_ptr(in_ptr: int, out_ptr: int, rows: int, cols: int, row_
                                     rows_per_seq, stream)
 
 
-def softmax_fwd(x, out=None, stream=None):
-    """Row softmax of a 2-D CUDA tensor (last dimension contiguous).
-
-    ``out`` (optional) must have x's shape, dtype, device and row stride; it
-    may be ``x`` itself.  Launches on ``stream`` (default: the current stream of
-    x's device) and returns ``out``.
-    """
+def _prepare(x, out, what: str):
+    """Check a 2-D CUDA tensor (last dimension contiguous) and its output;
+    returns (rows, cols, row_stride, dtype code, out)."""
     import torch
     if not isinstance(x, torch.Tensor) or not x.is_cuda:
-        raise TypeError("softmax_fwd needs a CUDA tensor")
+        raise TypeError(f"{what} needs a CUDA tensor")
     if x.dim() != 2:
-        raise ValueError(f"softmax_fwd needs a 2-D tensor, got {tuple(x.shape)}")
+        raise ValueError(f"{what} needs a 2-D tensor, got {tuple(x.shape)}")
     rows, cols = x.shape
     if cols > 1 and x.stride(1) != 1:
         raise ValueError("the last dimension must be contiguous (stride 1)")
@@ -148,13 +144,57 @@ def softmax_fwd(x, out=None, stream=None):
         o_stride = out.stride(0) if rows > 1 else row_stride
         if (cols > 1 and out.stride(1) != 1) or o_stride != row_stride:
             raise ValueError("out must have x's row stride")
+    return rows, cols, row_stride, code, out
+
+
+def _stream_handle(x, stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    return s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
+
+
+def softmax_fwd(x, out=None, stream=None):
+    """Row softmax of a 2-D CUDA tensor (last dimension contiguous).
+
+    ``out`` (optional) must have x's shape, dtype, device and row stride; it
+    may be ``x`` itself.  Launches on ``stream`` (default: the current stream of
+    x's device) and returns ``out``.
+    """
+    import torch
+    rows, cols, row_stride, code, out = _prepare(x, out, "softmax_fwd")
     with torch.cuda.device(x.device):
-        s = stream if stream is not None else torch.cuda.current_stream(x.device)
-        handle = s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
-        st = lib().softmax_fwd(x.data_ptr(), out.data_ptr(), rows, cols, row_stride, code, handle)
+        st = lib().softmax_fwd(x.data_ptr(), out.data_ptr(), rows, cols, row_stride, code, _stream_handle(x, stream))
     if st != OK:
         raise SoftmaxError(st)
     return out
+
+
+def softmax_fwd_masked(x, scale: float = 1.0, causal_offset: int = 0, rows_per_seq: int = 0, out=None,
+                       stream=None):
+    """Softmax of scaled, causally masked rows: row r keeps the columns
+    c <= (r mod rows_per_seq) + causal_offset (rows_per_seq 0: r itself), its
+    scores are x * scale, masked outputs are 0 and masked inputs are never
+    read.  Arguments otherwise as ``softmax_fwd``; returns ``out``."""
+    import torch
+    rows, cols, row_stride, code, out = _prepare(x, out, "softmax_fwd_masked")
+    with torch.cuda.device(x.device):
+        st = lib().softmax_fwd_masked(x.data_ptr(), out.data_ptr(), rows, cols, row_stride, code, float(scale),
+                                      int(causal_offset), int(rows_per_seq), _stream_handle(x, stream))
+    if st != OK:
+        raise SoftmaxError(st, "softmax_fwd_masked")
+    return out
+
+
+def autotune(x, out=None, stream=None, iters: int = 20) -> dict:
+    """softmax_autotune on a tensor (``out`` must be another buffer): time the
+    candidate launch shapes and cache the fastest for calls of this shape."""
+    import torch
+    rows, cols, row_stride, code, out = _prepare(x, out, "autotune")
+    if out.data_ptr() == x.data_ptr():
+        raise ValueError("autotune needs an out buffer other than x")
+    with torch.cuda.device(x.device):
+        return autotune_ptr(x.data_ptr(), out.data_ptr(), rows, cols, row_stride, code, _stream_handle(x, stream),
+                            iters)
 
 
 def plan(in_addr: int, out_addr: int, rows: int, cols: int, row_stride: int, dtype,

@@ -135,3 +135,14 @@ def test_rejects_bad_scale_and_period():
     for scale in (0.0, -1.0, float("inf"), float("nan")):
         assert B.softmax_fwd_masked_ptr(p, p, 4, 8, 8, 0, scale, 0, 0) == B.ERR_ARG
     assert B.softmax_fwd_masked_ptr(p, p, 4, 8, 8, 0, 1.0, 0, -1) == B.ERR_ARG
+
+
+@pytest.mark.parametrize("tdtype,name", [(torch.float32, "f32"), (torch.float16, "f16"), (torch.bfloat16, "bf16")])
+def test_torch_binding_matches_torch_on_a_masked_score_matrix(tdtype, name):
+    # an attention-score matrix: 2 sequences of 300 queries over 300 keys
+    g = torch.Generator(device="cpu").manual_seed(5)
+    x = (torch.randn(600, 300, generator=g) * 4).to(tdtype).cuda()
+    y = B.softmax_fwd_masked(x, scale=0.125, causal_offset=0, rows_per_seq=300)
+    q = torch.arange(600).remainder(300)[:, None]
+    s = (x.double() * 0.125).masked_fill(torch.arange(300)[None, :].cuda() > q.cuda(), float("-inf"))
+    assert (y.double() - torch.softmax(s, dim=1)).abs().max().item() <= TOL[name]
