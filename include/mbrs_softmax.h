@@ -87,9 +87,12 @@ typedef enum {
     SOFTMAX_PATH_RING = 5,    /* persistent blocks or clusters (<= 16 blocks per row) looping over
                                  rows, fed by a ring of shared-memory stages that TMA bulk copies
                                  keep full; rows of whole aligned 16-byte vectors only */
-    SOFTMAX_PATH_STREAM = 6   /* a cluster (<= 16 blocks) per row, each block streaming its slice
+    SOFTMAX_PATH_STREAM = 6,  /* a cluster (<= 16 blocks) per row, each block streaming its slice
                                  of any length twice: pass 1 (max, sum), exchange through
                                  distributed shared memory, pass 2 re-read and write; no scratch */
+    SOFTMAX_PATH_PACKED = 7   /* narrow rows of a dense matrix (row_stride == cols) staged through
+                                 shared memory many rows at a time as one contiguous span of
+                                 whole 16-byte vectors; one thread per row */
 } softmax_path_t;
 
 /*
@@ -145,7 +148,8 @@ int softmax_last_path(void);
  * Test and tuning hook: force every following call onto `path` (0 = automatic).
  * threads / vpt / group override the launch shape where > 0 (threads per block,
  * 16-byte vectors per thread, and lanes per row / cluster size / chunks per
- * row for paths 1 / 3, 5 and 6 / 4).  A forced shape that cannot cover the row makes
+ * row for paths 1 / 3, 5 and 6 / 4; for path 7 vpt is the rows each thread
+ * takes per staged span and group must be 0 or 1).  A forced shape that cannot cover the row makes
  * softmax_fwd return SOFTMAX_ERR_UNSUPPORTED.  Process-wide, not thread-safe.
  */
 int softmax_set_force_path(int path, int threads, int vpt, int group);
@@ -154,7 +158,7 @@ int softmax_set_force_path(int path, int threads, int vpt, int group);
 typedef struct {
     int path;              /* softmax_path_t actually chosen */
     int threads;           /* threads per block */
-    int vpt;               /* 16-byte vectors per thread per tile */
+    int vpt;               /* 16-byte vectors per thread per tile (7: rows per lane group per span) */
     int group;             /* lanes per row (1), cluster size (3, 5, 6), chunks per row (4), else 1 */
     int launches;          /* kernels per call: 1, or 2 for the SPLIT path */
     int vec_store;         /* 1 if out has in's 16-byte phase (vector stores) */

@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 
 SOURCES = ["abi.cu", "k_warp.cu", "k_warp_whole.cu", "k_cta.cu", "k_cta_whole.cu", "k_cluster.cu", "k_split.cu",
            "k_ring.cu", "k_noalloc.cu", "k_masked_warp.cu", "k_masked_warp_whole.cu", "k_masked.cu",
-           "k_masked_whole.cu"]
+           "k_masked_whole.cu", "k_packed.cu"]
 HEADERS = ["common.cuh", "kernels.cuh", "launch.h", "warp_launch.cuh", "cta_launch.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -166,7 +166,13 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
                          ((cols * es) % kVecBytes) == 0;
     int path = fpath;
     if (path == SOFTMAX_PATH_AUTO) {
-        if (nv <= 32 * 9 && (cols <= 1024 || p->whole)) {
+        if (row_stride == cols && (cols * es) % kVecBytes != 0 && p->vec_store && cols <= 48) {
+            // narrow dense rows off the 16-byte grid: staged through shared
+            // memory, one thread per row (fp32 1282051 x 39: 64.7 us, a warp
+            // path lane group per row 81.5; 400000 x 7: 6.7 against 15.0;
+            // 71 wide it loses, 77.8 against 58.9)
+            path = SOFTMAX_PATH_PACKED;
+        } else if (nv <= 32 * 9 && (cols <= 1024 || p->whole)) {
             // a warp per row while a warp's registers hold it; past 1024
             // columns only for rows of whole vectors (4096 x 2048 fp16: warp
             // 5.8 us, block 6.3 us; 4096 x 2047 bf16: warp 8.9 us, block 8.7 us)
@@ -315,6 +321,20 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             p->grid = units * csize;  // estimate; the launch sizes it from occupancy
             break;
         }
+        case SOFTMAX_PATH_PACKED: {
+            // one thread per row, 128 rows (times vpt, 1 unless forced: more
+            // rows per span measured slower) per staged span
+            if (row_stride != cols || !p->vec_store || (fgrp > 0 && fgrp != 1)) return SOFTMAX_ERR_UNSUPPORTED;
+            const int64_t k = fvpt > 0 ? fvpt : 1;
+            const int64_t rps = (int64_t)kPackedThreads * k;
+            if (rps > 0x7fffffff || packed_smem_bytes(rps, cols, es) > kPackedMaxSmem) return SOFTMAX_ERR_UNSUPPORTED;
+            p->threads = kPackedThreads;
+            p->vpt = (int)k;
+            p->group = 1;
+            p->grid = std::min<int64_t>(cdiv(rows, rps), kMaxGrid);
+            p->smem = packed_smem_bytes(rps, cols, es);
+            break;
+        }
         case SOFTMAX_PATH_STREAM: {
             // 4 vectors per thread; 256 threads per block, or more while 16
             // blocks would need more than two tiles each; then as many blocks
@@ -408,6 +428,7 @@ int run(const Plan &p, const LaunchArgs &a) {
             e = launch_cluster(a, p.threads, p.vpt, p.group, g_wait_ns.load(), g_starve.load());
             break;
         case SOFTMAX_PATH_STREAM: e = launch_stream(a, p.threads, p.vpt, p.group, g_wait_ns.load()); break;
+        case SOFTMAX_PATH_PACKED: e = launch_packed(a, kPackedThreads * p.vpt, p.grid); break;
         case SOFTMAX_PATH_RING: {
             RingCfg c{p.threads, p.vpt, p.group, p.stages, (int)p.slice_vecs, p.smem};
             e = launch_ring(a, c, g_wait_ns.load(), g_starve.load(), nullptr);
@@ -518,11 +539,13 @@ Shape call_shape(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t 
 }
 
 // Candidate shapes for rows of up to nv vectors: the automatic choice first,
-// then every lane-group / block / cluster shape that can hold the row, the
-// streaming cluster at three block sizes and, for whole aligned rows, the ring.
-std::vector<Shape> tune_candidates(int64_t nv, int es, bool ring_ok) {
+// the shared-memory staged path for narrow dense rows, then every lane-group /
+// block / cluster shape that can hold the row, the streaming cluster at three
+// block sizes and, for whole aligned rows, the ring.
+std::vector<Shape> tune_candidates(int64_t nv, int es, bool ring_ok, bool packed_ok) {
     std::vector<Shape> c;
     c.push_back(Shape{});
+    if (packed_ok) c.push_back(Shape{SOFTMAX_PATH_PACKED, 0, 1, 0});
     if (nv <= 32 * 9)
         for (int g = 2; g <= 32; g *= 2) {
             const int64_t v = cdiv(nv, g);
@@ -552,7 +575,9 @@ std::vector<Shape> candidates_for(uint64_t in, uint64_t out, int64_t cols, int64
     const int64_t head = (int64_t)((in % kVecBytes) / es);
     const int64_t nv = uniform ? cdiv(head + cols, V) : cdiv(cols + V - 1, V);
     const bool ring_ok = (in % kVecBytes) == 0 && (out % kVecBytes) == 0 && uniform && ((cols * es) % kVecBytes) == 0;
-    return tune_candidates(nv, es, ring_ok);
+    const bool packed_ok = row_stride == cols && (in % kVecBytes) == (out % kVecBytes) &&
+                           packed_smem_bytes(kPackedThreads, cols, es) <= kPackedMaxSmem;
+    return tune_candidates(nv, es, ring_ok, packed_ok);
 }
 
 void fill_public_plan(const Plan &p, softmax_plan_t *plan) {
@@ -673,7 +698,7 @@ const char *softmax_status_string(int status) {
 int softmax_last_path(void) { return g_last_path.load(); }
 
 int softmax_set_force_path(int path, int threads, int vpt, int group) {
-    if (path < SOFTMAX_PATH_AUTO || path > SOFTMAX_PATH_STREAM) return SOFTMAX_ERR_ARG;
+    if (path < SOFTMAX_PATH_AUTO || path > SOFTMAX_PATH_PACKED) return SOFTMAX_ERR_ARG;
     g_force_path.store(path);
     g_force_threads.store(threads > 0 ? threads : 0);
     g_force_vpt.store(vpt > 0 ? vpt : 0);

@@ -578,6 +578,89 @@ __global__ void __launch_bounds__(THREADS)
 }
 
 // ---------------------------------------------------------------------------
+// path 7: narrow dense rows staged through shared memory
+// ---------------------------------------------------------------------------
+// Rows of a dense matrix (row stride == cols) too narrow and too misaligned
+// for per-row vector access (fp32 rows 39 wide: two of every row's ten
+// vectors are partial, and a lane group per row pays its per-row costs on
+// every lane) are taken rows_per_span at a time as one contiguous span.  The
+// span moves between HBM and shared memory in whole 16-byte vectors -- only
+// its two end vectors, which it shares with the neighbouring spans, go
+// element by element -- and one thread per row works on the staged floats in
+// three sweeps: the max, then e = 2^(x log2 e - s) with its sum (e written
+// back), then e / sum.  A thread's rows start cols floats apart, so odd widths
+// read shared memory without bank conflicts.
+template <typename T>
+__global__ void __launch_bounds__(128) k_packed_rows(const T *in, T *out, int64_t rows, int64_t cols,
+                                                     int rows_per_span) {
+    constexpr int THREADS = 128, V = Elem<T>::kVec;
+    extern __shared__ __align__(16) float span[];
+    const int64_t total = rows * cols;
+    const int head0 = (int)((reinterpret_cast<uintptr_t>(in) & (kVecBytes - 1)) / sizeof(T));
+    const uint4 *vin = reinterpret_cast<const uint4 *>(in - head0);
+    uint4 *vout = reinterpret_cast<uint4 *>(out - head0);  // out has in's 16-byte phase
+    const int64_t nspans = (rows + rows_per_span - 1) / rows_per_span;
+    if (threadIdx.x == 0 && (int64_t)blockIdx.x < nspans) {
+        const int64_t r0 = (int64_t)blockIdx.x * rows_per_span;
+        prefetch_span_l2(in, r0 * cols, min(r0 + rows_per_span, rows) * cols, total);
+    }
+    pdl_enter();
+    for (int64_t sp = blockIdx.x; sp < nspans; sp += gridDim.x) {
+        const int64_t r0 = sp * rows_per_span, r1 = min(r0 + rows_per_span, rows);
+        const int64_t e0 = r0 * cols, e1 = r1 * cols;
+        const int64_t k_lo = (e0 + head0) / V, k_hi = (e1 + head0 + V - 1) / V;
+        const int64_t a0 = k_lo * V - head0;  // the element held by span[0]
+        // HBM -> shared memory, whole vectors but at the matrix's two ends
+        for (int64_t k = k_lo + threadIdx.x; k < k_hi; k += THREADS) {
+            const int64_t el = k * V - head0;
+            float x[V];
+            if (el >= 0 && el + V <= total) {
+                Elem<T>::unpack(vin[k], x);
+            } else {
+#pragma unroll
+                for (int i = 0; i < V; ++i) x[i] = (el + i >= 0 && el + i < total) ? Elem<T>::to_f(in[el + i]) : 0.f;
+            }
+            float4 *d = reinterpret_cast<float4 *>(span + (el - a0));
+#pragma unroll
+            for (int i = 0; i < V / 4; ++i) d[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+        }
+        __syncthreads();
+        // one thread per row
+        for (int64_t r = r0 + threadIdx.x; r < r1; r += THREADS) {
+            float *row = span + (r * cols - a0);
+            float m = -INFINITY;
+            for (int64_t c = 0; c < cols; ++c) m = fmaxf(m, row[c]);
+            const float s = m * kLog2e;
+            const float shift = safe_shift(s);
+            float l = 0.f;
+            for (int64_t c = 0; c < cols; ++c) {
+                const float e = ex2(fmaf(row[c], kLog2e, -shift));
+                row[c] = e;
+                l += e;
+            }
+            const float f = out_factor(s, s, l);
+            for (int64_t c = 0; c < cols; ++c) row[c] *= f;
+        }
+        __syncthreads();
+        // shared memory -> HBM: whole vectors inside the span, its two end
+        // vectors element by element (their other elements belong to the
+        // neighbouring spans)
+        for (int64_t k = k_lo + threadIdx.x; k < k_hi; k += THREADS) {
+            const int64_t el = k * V - head0;
+            const float *src = span + (el - a0);
+            if (el >= e0 && el + V <= e1) {
+                vout[k] = Elem<T>::pack(src);
+            } else {
+#pragma unroll
+                for (int i = 0; i < V; ++i)
+                    if (el + i >= e0 && el + i < e1) out[el + i] = Elem<T>::from_f(src[i]);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
 // scaled, causally masked rows (softmax_fwd_masked)
 // ---------------------------------------------------------------------------
 // Page "Dissecting Memory Bandwidth & SRAM Tiling in Triton: From GEMM to

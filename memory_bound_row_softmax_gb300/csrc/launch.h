@@ -109,6 +109,13 @@ cudaError_t launch_stream_masked(const LaunchArgs &a, int threads, int vpt, int 
 bool cluster_shape_ok(int threads, int vpt, int elem_bytes);
 int64_t cluster_smem_bytes(int threads, int vpt);
 cudaError_t launch_cluster(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns, int starve);
+// path 7: narrow dense rows (stride == cols) staged through shared memory
+// rows_per_span at a time, one thread per row, kPackedThreads per block
+constexpr int kPackedThreads = 128;
+constexpr int64_t kPackedMaxSmem = 48 * 1024;
+int64_t packed_smem_bytes(int64_t rows_per_span, int64_t cols, int elem_bytes);
+cudaError_t launch_packed(const LaunchArgs &a, int rows_per_span, int64_t grid);
+
 // path 6: a cluster of csize blocks per row streaming slices of any length
 // twice (pass 1 states, cluster exchange, pass 2 re-read and write)
 bool stream_shape_ok(int threads, int vpt);

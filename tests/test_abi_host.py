@@ -106,6 +106,9 @@ def test_plans_cover_every_row(rows, cols, stride, dt, in_off):
     elif path == B.PATH_CLUSTER:
         assert 1 <= p["group"] <= 16 and -(-nv // p["group"]) <= p["threads"] * p["vpt"]
         assert p["grid"] == rows * p["group"] and p["smem_bytes"] <= 227 * 1024
+    elif path == B.PATH_PACKED:  # dense narrow rows, one thread each, 128 rows per staged span
+        assert stride == cols and cols <= 48 and p["threads"] == 128 and p["grid"] == -(-rows // 128)
+        assert p["smem_bytes"] >= 128 * cols * 4
     elif path == B.PATH_STREAM:  # any slice length; enough blocks to fill the GPU, nothing allocated
         assert 1 <= p["group"] <= 16 and p["grid"] == rows * p["group"] and p["scratch_bytes"] == 0
         assert rows * p["group"] >= min(152, rows * 16) and p["launches"] == 1
@@ -134,6 +137,10 @@ def test_plan_reports_whole_vector_rows(in_off, out_off, cols, stride, dt, whole
 def test_dispatch_follows_width_rule():
     plan = lambda r, c, dt="f32": B.plan(1 << 24, 1 << 40, r, c, c, dt, num_sms=152)["path"]
     assert plan(64, 1000) == B.PATH_WARP          # cols <= 1024: a warp per row
+    assert plan(1000, 39) == B.PATH_PACKED        # narrow dense rows off the 16-byte grid: staged
+    assert plan(1000, 40) == B.PATH_WARP          # ... but 40 fp32 are whole vectors
+    assert plan(1000, 71) == B.PATH_WARP          # ... and 71 is too wide for a thread per row
+    assert B.plan(1 << 24, 1 << 40, 1000, 39, 41, "f32", num_sms=152)["path"] == B.PATH_WARP  # padded
     assert plan(64, 1024) == B.PATH_WARP
     assert plan(64, 1025) == B.PATH_CTA           # misaligned medium rows: a block per row
     assert plan(4096, 16391) == B.PATH_CTA

@@ -28,6 +28,9 @@ def test_candidates_start_with_the_automatic_choice():
 def test_candidates_follow_the_row_length():
     narrow = B.tune_candidates(A_IN, A_OUT, 64, 1000, 1000, "f32")
     assert _paths(narrow) == {0, B.PATH_WARP, B.PATH_CTA}
+    dense = B.tune_candidates(A_IN, A_OUT, 64, 39, 39, "f32")
+    assert B.PATH_PACKED in _paths(dense)
+    assert B.PATH_PACKED not in _paths(B.tune_candidates(A_IN, A_OUT, 64, 39, 40, "f32"))  # padded
     medium = B.tune_candidates(A_IN, A_OUT, 64, 16384, 16384, "f32")      # 4096 vectors
     assert {B.PATH_CTA, B.PATH_CLUSTER, B.PATH_STREAM, B.PATH_RING} <= _paths(medium)
     assert B.PATH_WARP not in _paths(medium)
@@ -64,7 +67,7 @@ def test_bad_arguments_and_empty_cache():
 # -- on the GPU -------------------------------------------------------------------------------
 
 CASES = [(64, 1000, "f32", 0), (300, 2048, "f16", 0), (7, 3001, "bf16", 1), (40, 40000, "f32", 0),
-         (24, 70001, "f16", 3), (20, 131072, "bf16", 0)]
+         (24, 70001, "f16", 3), (20, 131072, "bf16", 0), (3000, 39, "f32", 0), (700, 13, "bf16", 1)]
 
 
 @pytest.fixture()

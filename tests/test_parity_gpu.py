@@ -48,7 +48,8 @@ WIDTHS = [1, 2, 3, 5, 7, 8, 9, 16, 31, 33, 63, 100, 255, 257, 1000, 1023, 1024, 
 def test_auto_widths(dtype, cols):
     rows = 5 if cols > 10000 else 7
     res = run_and_compare(rnd(rows, cols, dtype, seed=cols), dtype)
-    assert res["path"] in (B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_SPLIT, B.PATH_RING, B.PATH_STREAM)
+    assert res["path"] in (B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_SPLIT, B.PATH_RING, B.PATH_STREAM,
+                           B.PATH_PACKED)
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -71,6 +72,7 @@ FORCED = {
     B.PATH_SPLIT: [1, 100, 4103, 65536, 262147],
     B.PATH_RING: [8, 1024, 2048, 4096, 8192, 65536, 131072],
     B.PATH_STREAM: [1, 100, 4103, 65536, 262147],
+    B.PATH_PACKED: [1, 7, 39, 90],
 }
 
 
@@ -171,6 +173,30 @@ def test_stream_whole_rows(dtype, rows, cols):
     assert res["path"] == B.PATH_STREAM
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("cols", [1, 3, 8, 9, 33, 39, 71, 90])
+@pytest.mark.parametrize("off", [0, 1, 3])
+@pytest.mark.parametrize("rows,k", [(1, 1), (5, 1), (700, 2), (1537, 1)])
+def test_packed_spans(dtype, cols, off, rows, k):
+    # dense rows staged through shared memory: spans that end inside a vector,
+    # a last partial span, the matrix starting `off` elements into a vector
+    if k > 1 and 128 * k * cols * 4 > 48 * 1024:
+        k = 1  # the span would not fit its 48 KB
+    res = run_and_compare(rnd(rows, cols, dtype, seed=cols * 31 + rows + off), dtype, in_off=off, out_off=off,
+                          path=B.PATH_PACKED, vpt=k)
+    assert res["path"] == B.PATH_PACKED
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_packed_refuses_what_it_cannot_stage(dtype):
+    x = rnd(40, 39, dtype, 3, stride=41)                         # padded stride
+    assert DeviceCase(x, dtype).run(39, path=B.PATH_PACKED) == B.ERR_UNSUPPORTED
+    y = rnd(40, 300, dtype, 3)                                   # a 128-row span over 48 KB
+    assert DeviceCase(y, dtype).run(300, path=B.PATH_PACKED) == B.ERR_UNSUPPORTED
+    z = rnd(40, 39, dtype, 3)                                    # out in another 16-byte phase
+    assert DeviceCase(z, dtype, in_off=1, out_off=2).run(39, path=B.PATH_PACKED) == B.ERR_UNSUPPORTED
+
+
 def test_forced_shape_that_cannot_cover_the_row_is_rejected():
     case = DeviceCase(rnd(2, 5000, "f32", 1), "f32")
     assert case.run(5000, path=B.PATH_WARP) == B.ERR_UNSUPPORTED
@@ -195,12 +221,14 @@ def test_padded_strides(dtype, cols, extra):
 
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("path", [0, B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_SPLIT, B.PATH_RING,
-                                  B.PATH_STREAM])
+                                  B.PATH_STREAM, B.PATH_PACKED])
 def test_in_place(dtype, path):
     cols = 1000 if path in (0, B.PATH_WARP) else 6007
     off = 1
     if path == B.PATH_RING:
         cols, off = 6016, 0
+    if path == B.PATH_PACKED:
+        cols = 39
     run_and_compare(rnd(300, cols, dtype, seed=path), dtype, inplace=True, in_off=off, path=path)
 
 
