@@ -256,6 +256,16 @@ def run_ours(args) -> dict | None:
         if st != 0:
             raise B.SoftmaxError(st)
 
+    if args.masked:  # the workload's causal mask through softmax_fwd_masked (for --only-kernel captures)
+        if not (args.only_kernel and w.causal_period):
+            raise SystemExit("--masked needs --only-kernel and a causal workload (c4)")
+
+        def launch(a, b):  # noqa: F811 -- the masked call replaces the plain one
+            st = lib.softmax_fwd_masked(a.data_ptr(), b.data_ptr(), w.rows, w.cols, w.stride, code, 1.0, 0,
+                                        w.causal_period, torch.cuda.current_stream().cuda_stream)
+            if st != 0:
+                raise B.SoftmaxError(st, "softmax_fwd_masked")
+
     if args.force:
         B.set_force_path(*[int(v) for v in args.force.split(",")])
     B.set_launch_overlap(not args.no_overlap)
@@ -528,6 +538,8 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="add the fp32 width sweep to the per-shape table")
     ap.add_argument("--force", default="",
                     help="path[,threads,vpt,group]: force a kernel path and launch shape (profiling, tuning)")
+    ap.add_argument("--masked", action="store_true",
+                    help="with --only-kernel on c4: run its causal mask through softmax_fwd_masked")
     ap.add_argument("--only-kernel", action="store_true",
                     help="warm-up and timed launches only (the command profiled with ncu)")
     ap.add_argument("--json-out", default="")

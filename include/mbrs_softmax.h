@@ -306,7 +306,8 @@ int softmax_autotune_clear(void);
 
 /* Version of this ABI: major * 10000 + minor * 100 + patch (1.1.0 adds the RING
  * path, 1.2.0 softmax_set_launch_overlap, 1.3.0 the STREAM path and
- * softmax_plan_t.whole_vectors, 1.4.0 the autotune calls and softmax_fwd_masked). */
+ * softmax_plan_t.whole_vectors, 1.4.0 the autotune calls and softmax_fwd_masked,
+ * 1.5.0 the PACKED path). */
 int softmax_abi_version(void);
 
 #ifdef __cplusplus

@@ -45,7 +45,7 @@ def test_status_strings():
     for s in range(11):
         assert B.status_string(s) and B.status_string(s) != "unknown status"
     assert B.status_string(99) == "unknown status"
-    assert B.abi_version() == 10400
+    assert B.abi_version() == 10500
 
 
 @pytest.mark.parametrize("args,expect", [
