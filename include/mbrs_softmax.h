@@ -138,6 +138,45 @@ int softmax_fwd_masked(const void *in, void *out, int64_t rows, int64_t cols, in
                        int dtype, float scale, int64_t causal_offset, int64_t rows_per_seq,
                        cudaStream_t stream);
 
+/*
+ * softmax_fwd_host -- the same softmax for a matrix in host memory, written
+ * back to host memory.  (The pages have no counterpart: they time device
+ * buffers only; this is the call whose end-to-end throughput includes the
+ * host <-> device copies.)
+ *   in_host, out_host  host pointers (may be equal); page-locked memory lets the
+ *                      copies run asynchronously and overlap, pageable memory
+ *                      works but the driver then stages and serialises them
+ *   workspace          device memory the caller owns (256-byte aligned),
+ *                      workspace_bytes long: three slots of at least one row
+ *                      each; softmax_host_workspace_bytes(rows, cols,
+ *                      row_stride, dtype, 0) gives the recommended size
+ *   stream             the call is ordered after the work already queued on
+ *                      stream, and work queued on stream afterwards waits for
+ *                      it; it returns without waiting (synchronise stream
+ *                      before reading out_host)
+ * The rows move in chunks through the three workspace slots on three streams
+ * of the library's own, so that the host-to-device copy of one chunk, the
+ * softmax of another and the device-to-host copy of a third are in flight at
+ * once.  Only the rows' cols elements are copied (pitched copies): padding
+ * between host rows is neither read nor written.  Calls on one device are serialised by a lock while they are queued.
+ * Other arguments, layout, aliasing and status codes as softmax_fwd
+ * (SOFTMAX_ERR_ARG for a workspace too small).  Allocates nothing on the
+ * device; the streams and events are created once per device.
+ */
+int softmax_fwd_host(const void *in_host, void *out_host, int64_t rows, int64_t cols, int64_t row_stride,
+                     int dtype, void *workspace, int64_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Workspace for softmax_fwd_host: three chunks of about chunk_bytes of row
+ * data each (<= 0: a quarter of the matrix, within 2 to 8 MiB), whole rows
+ * packed densely, never more than the matrix needs.  softmax_fwd_host makes
+ * its chunks as large as the workspace it is given allows, so the workspace
+ * size sets the pipeline's granularity.  Returns the
+ * bytes, or a negated softmax_status_t on bad arguments.
+ */
+int64_t softmax_host_workspace_bytes(int64_t rows, int64_t cols, int64_t row_stride, int dtype,
+                                     int64_t chunk_bytes);
+
 /* A static English string for a status code (never NULL). */
 const char *softmax_status_string(int status);
 
@@ -307,7 +346,7 @@ int softmax_autotune_clear(void);
 /* Version of this ABI: major * 10000 + minor * 100 + patch (1.1.0 adds the RING
  * path, 1.2.0 softmax_set_launch_overlap, 1.3.0 the STREAM path and
  * softmax_plan_t.whole_vectors, 1.4.0 the autotune calls and softmax_fwd_masked,
- * 1.5.0 the PACKED path). */
+ * 1.5.0 the PACKED path and softmax_fwd_host). */
 int softmax_abi_version(void);
 
 #ifdef __cplusplus

@@ -53,6 +53,8 @@ SIGNATURES = {
     "softmax_check_device_error": (_int, [_vp]),
     "softmax_set_wait_test": (_int, [_i64, _int]),
     "softmax_set_launch_overlap": (_int, [_int]),
+    "softmax_fwd_host": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _vp]),
+    "softmax_host_workspace_bytes": (_i64, [_i64, _i64, _i64, _int, _i64]),
     "softmax_autotune": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp, _int, ctypes.POINTER(TuneResult)]),
     "softmax_tune_candidates": (_int, [_u64, _u64, _i64, _i64, _i64, _int, _int, ctypes.POINTER(Shape), _int]),
     "softmax_autotune_size": (_int, []),
@@ -182,6 +184,45 @@ def softmax_fwd_masked(x, scale: float = 1.0, causal_offset: int = 0, rows_per_s
                                       int(causal_offset), int(rows_per_seq), _stream_handle(x, stream))
     if st != OK:
         raise SoftmaxError(st, "softmax_fwd_masked")
+    return out
+
+
+def host_workspace_bytes(rows: int, cols: int, row_stride: int, dtype, chunk_bytes: int = 0) -> int:
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else dtype
+    n = lib().softmax_host_workspace_bytes(rows, cols, row_stride, code, chunk_bytes)
+    if n < 0:
+        raise SoftmaxError(-n, "softmax_host_workspace_bytes")
+    return n
+
+
+def softmax_fwd_host(x, out=None, workspace=None, stream=None):
+    """Row softmax of a 2-D CPU tensor (pinned for overlapping copies),
+    written to ``out`` (a CPU tensor, default a new pinned one) through the
+    library's chunked copy / softmax / copy pipeline on the current CUDA
+    device.  ``workspace`` (a CUDA tensor) defaults to a new one of
+    softmax_host_workspace_bytes.  Synchronises ``stream`` before returning."""
+    import torch
+    if not isinstance(x, torch.Tensor) or x.is_cuda or x.dim() != 2:
+        raise TypeError("softmax_fwd_host needs a 2-D CPU tensor")
+    rows, cols = x.shape
+    if cols > 1 and x.stride(1) != 1:
+        raise ValueError("the last dimension must be contiguous (stride 1)")
+    row_stride = x.stride(0) if rows > 1 else max(cols, x.stride(0))
+    code = _torch_dtype_code(x)
+    if out is None:
+        out = torch.empty_strided((rows, cols), (row_stride, 1), dtype=x.dtype, pin_memory=True)
+    elif out.shape != x.shape or out.dtype != x.dtype or out.is_cuda or (rows > 1 and out.stride(0) != row_stride):
+        raise ValueError("out must be a CPU tensor with x's shape, dtype and row stride")
+    if workspace is None:
+        workspace = torch.empty(max(host_workspace_bytes(rows, cols, row_stride, code), 1), dtype=torch.uint8,
+                                device="cuda")
+    s = stream if stream is not None else torch.cuda.current_stream()
+    handle = s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
+    st = lib().softmax_fwd_host(x.data_ptr(), out.data_ptr(), rows, cols, row_stride, code, workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), handle)
+    if st != OK:
+        raise SoftmaxError(st, "softmax_fwd_host")
+    torch.cuda.current_stream().synchronize() if stream is None else s.synchronize()
     return out
 
 

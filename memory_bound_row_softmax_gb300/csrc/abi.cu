@@ -599,6 +599,48 @@ void fill_public_plan(const Plan &p, softmax_plan_t *plan) {
     plan->whole_vectors = p.whole;
 }
 
+// ---------------------------------------------------------------------------
+// host buffers (softmax_fwd_host): chunks of rows through three device slots,
+// each slot with its own stream, so that a host-to-device copy, a softmax and
+// a device-to-host copy of three chunks are in flight at once
+// ---------------------------------------------------------------------------
+constexpr int kHostSlots = 3;
+// Default chunk: a quarter of the matrix, within 2 to 8 MiB (measured, fp16
+// 4096 x 2048 through pinned memory: 1 MiB chunks 146 GB/s, 4 MiB 210,
+// 64 MiB -- no overlap -- 179; fp32 4096 x 4096: 8 MiB 254, 1 MiB 154).
+constexpr int64_t kHostChunkMin = 2 << 20, kHostChunkMax = 8 << 20;
+
+struct HostPipe {
+    std::mutex mu;  // held while a call queues its work
+    bool ready = false;
+    cudaStream_t s[kHostSlots] = {};
+    cudaEvent_t start = nullptr;
+    cudaEvent_t done[kHostSlots] = {};
+};
+HostPipe g_host_pipes[kMaxDevices];
+
+// Create the pipe's streams and events (caller holds hp.mu).
+cudaError_t host_pipe_ready(HostPipe &hp) {
+    if (hp.ready) return cudaSuccess;
+    cudaError_t e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming);
+    for (int j = 0; j < kHostSlots && e == cudaSuccess; ++j) {
+        e = cudaStreamCreateWithFlags(&hp.s[j], cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.done[j], cudaEventDisableTiming);
+    }
+    if (e == cudaSuccess) hp.ready = true;
+    return e;
+}
+
+// A slot holds n rows packed densely (row stride = cols: the host rows'
+// padding is neither copied in nor out), starting 256-byte aligned.
+int64_t host_slot_bytes(int64_t n, int64_t cols, int es) { return (n * cols * es + 255) / 256 * 256; }
+
+// Rows per chunk: about chunk_bytes of row data, at least one, at most all.
+int64_t host_chunk_rows(int64_t rows, int64_t cols, int es, int64_t chunk_bytes) {
+    const int64_t cr = std::max<int64_t>(1, chunk_bytes / (cols * es));
+    return std::min(cr, rows);
+}
+
 }  // namespace
 
 extern "C" {
@@ -659,6 +701,88 @@ int softmax_fwd_masked(const void *in, void *out, int64_t rows, int64_t cols, in
     if (e != cudaSuccess) return SOFTMAX_ERR_CUDA;
     g_last_path.store(p.path);
     return SOFTMAX_OK;
+}
+
+int64_t softmax_host_workspace_bytes(int64_t rows, int64_t cols, int64_t row_stride, int dtype,
+                                     int64_t chunk_bytes) {
+    if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_F16 && dtype != SOFTMAX_BF16) return -SOFTMAX_ERR_DTYPE;
+    if (rows < 0 || cols < 1) return -SOFTMAX_ERR_SHAPE;
+    if (row_stride < cols) return -SOFTMAX_ERR_STRIDE;
+    if (rows == 0) return 0;
+    const int es = elem_bytes(dtype);
+    if (row_stride > INT64_MAX / 4 / es) return -SOFTMAX_ERR_SHAPE;
+    const int64_t quarter = rows * cols * es / 4;
+    const int64_t def = std::min(kHostChunkMax, std::max(kHostChunkMin, quarter));
+    const int64_t cr = host_chunk_rows(rows, cols, es, chunk_bytes > 0 ? chunk_bytes : def);
+    return kHostSlots * host_slot_bytes(cr, cols, es);
+}
+
+int softmax_fwd_host(const void *in_host, void *out_host, int64_t rows, int64_t cols, int64_t row_stride,
+                     int dtype, void *workspace, int64_t workspace_bytes, cudaStream_t stream) {
+    int64_t ext = 0;
+    const uint64_t ia = (uint64_t)(uintptr_t)in_host, oa = (uint64_t)(uintptr_t)out_host;
+    int st = check_args(ia, oa, rows, cols, row_stride, dtype, &ext);
+    if (st != SOFTMAX_OK || rows == 0) return st;
+    if (!workspace) return SOFTMAX_ERR_NULL;
+    if ((uintptr_t)workspace % 256 != 0 || workspace_bytes < 0) return SOFTMAX_ERR_ARG;
+    const int es = elem_bytes(dtype);
+    // the largest chunk (up to the default) of which three fit the workspace
+    // chunks as large as the workspace's three slots allow (its size sets the
+    // pipeline's granularity: softmax_host_workspace_bytes)
+    const int64_t fit = workspace_bytes / kHostSlots / 256 * 256 / es;  // elements per slot
+    if (fit < cols) return SOFTMAX_ERR_ARG;
+    const int64_t cr = std::min(rows, fit / cols);
+    const int64_t sb = host_slot_bytes(cr, cols, es);
+    int sms = 0, dev = 0;
+    st = device_sms(&sms);
+    if (st != SOFTMAX_OK) return st;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SOFTMAX_ERR_CUDA;
+
+    HostPipe &hp = g_host_pipes[dev & (kMaxDevices - 1)];
+    std::lock_guard<std::mutex> lock(hp.mu);
+    if (host_pipe_ready(hp) != cudaSuccess) return SOFTMAX_ERR_CUDA;
+    cudaError_t e = cudaEventRecord(hp.start, stream);
+    for (int j = 0; j < kHostSlots && e == cudaSuccess; ++j) e = cudaStreamWaitEvent(hp.s[j], hp.start, 0);
+    if (e != cudaSuccess) return SOFTMAX_ERR_CUDA;
+    const size_t row_bytes = (size_t)(row_stride * es), data_bytes = (size_t)(cols * es);
+    int path = 0;
+    for (int64_t r0 = 0, i = 0; r0 < rows && st == SOFTMAX_OK; r0 += cr, ++i) {
+        const int j = (int)(i % kHostSlots);
+        const int64_t n = std::min(cr, rows - r0);
+        char *slot = static_cast<char *>(workspace) + j * sb;
+        // the rows' data only: pitched copies skip the host rows' padding
+        const char *src = static_cast<const char *>(in_host) + r0 * row_bytes;
+        const cudaError_t ce = row_bytes == data_bytes
+                                   ? cudaMemcpyAsync(slot, src, data_bytes * n, cudaMemcpyHostToDevice, hp.s[j])
+                                   : cudaMemcpy2DAsync(slot, data_bytes, src, row_bytes, data_bytes, (size_t)n,
+                                                       cudaMemcpyHostToDevice, hp.s[j]);
+        if (ce != cudaSuccess) {
+            st = SOFTMAX_ERR_CUDA;
+            break;
+        }
+        const uint64_t sa = (uint64_t)(uintptr_t)slot;
+        Plan p;
+        st = make_plan(sa, sa, n, cols, cols, dtype, sms, call_shape(sa, sa, n, cols, cols, dtype), &p);
+        if (st != SOFTMAX_OK) break;
+        LaunchArgs a{slot, slot, n, cols, cols, dtype, p.vec_store, hp.s[j], g_overlap.load(), p.whole};
+        st = run(p, a);  // in place in the slot
+        if (st != SOFTMAX_OK) break;
+        path = p.path;
+        char *dst = static_cast<char *>(out_host) + r0 * row_bytes;
+        const cudaError_t de = row_bytes == data_bytes
+                                   ? cudaMemcpyAsync(dst, slot, data_bytes * n, cudaMemcpyDeviceToHost, hp.s[j])
+                                   : cudaMemcpy2DAsync(dst, row_bytes, slot, data_bytes, data_bytes, (size_t)n,
+                                                       cudaMemcpyDeviceToHost, hp.s[j]);
+        if (de != cudaSuccess) st = SOFTMAX_ERR_CUDA;
+    }
+    // the caller's stream waits for all three slot streams, whatever happened
+    for (int j = 0; j < kHostSlots; ++j) {
+        if (cudaEventRecord(hp.done[j], hp.s[j]) != cudaSuccess ||
+            cudaStreamWaitEvent(stream, hp.done[j], 0) != cudaSuccess)
+            st = SOFTMAX_ERR_CUDA;
+    }
+    if (st == SOFTMAX_OK) g_last_path.store(path);
+    return st;
 }
 
 int softmax_fwd_noalloc(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride, int dtype,

@@ -188,3 +188,25 @@ def test_masked_argument_checks_need_no_gpu():
     assert B.softmax_fwd_masked_ptr(p, q, 0, 8, 8, 0, 1.0, 0, 0) == B.OK      # no rows: nothing to do
     assert B.softmax_fwd_masked_ptr(p, q, 4, 8, 7, 0, 1.0, 0, 0) == B.ERR_STRIDE
     assert B.softmax_fwd_masked_ptr(p, p + 4, 4, 8, 8, 0, 1.0, 0, 0) == B.ERR_OVERLAP
+
+
+def test_host_workspace_sizes():
+    # three slots of whole rows, about chunk_bytes each, never more than the matrix
+    assert B.host_workspace_bytes(0, 10, 10, "f32") == 0
+    small = B.host_workspace_bytes(5, 10, 10, "f32")
+    assert small == 3 * 256                                  # 5 rows of 40 B: one 200-byte slot, 256-aligned
+    big = B.host_workspace_bytes(4096, 2048, 2048, "f16", 1 << 20)
+    assert big == 3 * (256 * 2048 * 2)                       # 256 rows of 4 KiB per 1 MiB chunk
+    assert B.host_workspace_bytes(4096, 2048, 2048, "f16") == 3 * (1024 * 4096)  # a quarter: 4 MiB
+    assert B.host_workspace_bytes(4096, 4096, 4096, "f32") == 3 * (8 << 20)      # capped at 8 MiB
+    assert B.host_workspace_bytes(100, 100, 100, "f32") == 3 * 40192              # small: the whole matrix
+    with pytest.raises(B.SoftmaxError):
+        B.host_workspace_bytes(4, 10, 9, "f32")              # stride < cols
+
+
+def test_host_call_argument_checks_need_no_gpu():
+    h = 1 << 24
+    assert B.lib().softmax_fwd_host(h, h + (1 << 20), 4, 8, 8, 0, None, 1 << 20, None) == B.ERR_NULL
+    assert B.lib().softmax_fwd_host(h, h + 4, 4, 8, 8, 0, 1 << 30, 1 << 20, None) == B.ERR_OVERLAP
+    assert B.lib().softmax_fwd_host(h, h + (1 << 20), 4, 8, 8, 0, (1 << 30) + 4, 1 << 20, None) == B.ERR_ARG
+    assert B.lib().softmax_fwd_host(h, h + (1 << 20), 4, 8, 8, 0, 1 << 30, 16, None) == B.ERR_ARG  # too small
