@@ -49,6 +49,9 @@ def _load():
             lib.oracle_softmax_masked_rows.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int,
                                                        ctypes.c_double, i64, i64]
             lib.oracle_softmax_masked_rows.restype = ctypes.c_int
+            lib.oracle_attention_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int, ctypes.c_double,
+                                                 ctypes.c_int, i64]
+            lib.oracle_attention_fwd.restype = ctypes.c_int
             lib.oracle_row_stats.argtypes = [vp, i64, i64, i64, i64, ctypes.c_int, vp]
             lib.oracle_online_stats.argtypes = [vp, i64, vp, i64, i64, ctypes.c_int, vp]
             lib.oracle_merge.argtypes = [ctypes.c_double] * 4 + [dp, dp]
@@ -152,6 +155,25 @@ def softmax_masked(x: np.ndarray, dtype: str, scale: float, causal_offset: int, 
         step = (nrows + threads - 1) // threads
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(lambda lo: run(lo, min(nrows, lo + step)), range(0, nrows, step)))
+    return out
+
+
+def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, dtype: str, scale: float, causal: bool = False,
+                  causal_offset: int = 0) -> np.ndarray:
+    """One head of attention in double precision: O = softmax(Q K^T * scale,
+    causal mask keeping key j <= query i + causal_offset) V.  q: (n_q, d),
+    k, v: (n_k, d) storage arrays of ``dtype``; returns float64 (n_q, d)."""
+    lib = _load()
+    q, k, v = (_check_storage(a, dtype) for a in (q, k, v))
+    if k.shape != v.shape or q.shape[1] != k.shape[1]:
+        raise ValueError(f"shapes q {q.shape}, k {k.shape}, v {v.shape} do not fit")
+    n_q, d = q.shape
+    out = np.empty((n_q, d), dtype=np.float64)
+    scratch = np.empty(k.shape[0], dtype=np.float64)
+    rc = lib.oracle_attention_fwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, out.ctypes.data, scratch.ctypes.data,
+                                  n_q, k.shape[0], d, _DTYPE_CODE[dtype], float(scale), 1 if causal else 0,
+                                  causal_offset)
+    assert rc == 0
     return out
 
 

@@ -220,6 +220,83 @@ int oracle_softmax_masked_rows(const void *in, double *out, double *scratch,
 }
 
 /*
+ * Attention forward for one head.  Page "Dissecting Memory Bandwidth & SRAM
+ * Tiling in Triton: From GEMM to FlashAttention-3", sections "Memory
+ * Hierarchy: Why Standard Attention Collapses" and "Writing the Kernel in
+ * OpenAI Triton": scores S = Q K^T * scale, the causal mask (key j kept for
+ * query i only when j <= i + causal_offset), P = the row softmax of S, and
+ * O = P V.  Written out as the plain definition, one query row at a time in
+ * double precision: the scores of the kept keys, their max, the shifted
+ * exponentials and their sequential sum, then the weighted sum of the value
+ * rows.
+ *
+ * q: n_q x d, k and v: n_k x d, row-major, dense, in the storage dtype;
+ * out: n_q x d doubles.  `scratch` holds n_k doubles.  causal == 0 keeps
+ * every key.  A query that keeps no key gets NaN (reading R1).  Returns 0, or
+ * -1 on bad arguments.
+ */
+int oracle_attention_fwd(const void *q, const void *k, const void *v, double *out, double *scratch,
+                         int64_t n_q, int64_t n_k, int64_t d, int dtype, double scale, int causal,
+                         int64_t causal_offset)
+{
+    if (n_q < 0 || n_k < 1 || d < 1 || !(scale > 0.0) || isinf(scale))
+        return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_F16 && dtype != ORACLE_BF16)
+        return -1;
+    for (int64_t i = 0; i < n_q; ++i) {
+        double *o = out + i * d;
+        double *p = scratch;
+        int64_t n = n_k;
+        if (causal) {
+            n = i + causal_offset + 1;
+            if (n < 0)
+                n = 0;
+            if (n > n_k)
+                n = n_k;
+        }
+        if (n == 0) {
+            for (int64_t c = 0; c < d; ++c)
+                o[c] = NAN;
+            continue;
+        }
+        /* scores of the kept keys */
+        for (int64_t j = 0; j < n; ++j) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < d; ++c)
+                acc += load_elem(q, i * d + c, dtype) * load_elem(k, j * d + c, dtype);
+            p[j] = acc * scale;
+        }
+        /* their softmax */
+        double m = -INFINITY;
+        int has_nan = 0;
+        for (int64_t j = 0; j < n; ++j) {
+            if (isnan(p[j]))
+                has_nan = 1;
+            if (p[j] > m)
+                m = p[j];
+        }
+        if (has_nan || m == -INFINITY || m == INFINITY) {
+            for (int64_t c = 0; c < d; ++c)
+                o[c] = NAN;
+            continue;
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < n; ++j) {
+            p[j] = exp(p[j] - m);
+            l += p[j];
+        }
+        /* the weighted sum of the value rows */
+        for (int64_t c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < n; ++j)
+                acc += p[j] * load_elem(v, j * d + c, dtype);
+            o[c] = acc / l;
+        }
+    }
+    return 0;
+}
+
+/*
  * The (max, normaliser) state of one row taken directly: m = max x,
  * l = sum exp(x - m).  Out: stats[0] = m, stats[1] = l.  Same readings as above
  * (a row with no finite shift gives m = NaN-or-inf, l = NaN).

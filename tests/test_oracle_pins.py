@@ -332,3 +332,76 @@ def test_masked_rejects_a_scale_that_is_not_positive():
     for bad in (0.0, -1.0, float("inf"), float("nan")):
         with pytest.raises(AssertionError):
             oracle.softmax_masked(x, "f32", bad, 0)
+
+
+# -- one head of attention (groundwork for the fused attention forward) -------------------------
+
+def _qkv(n_q, n_k, d, dtype, seed):
+    q = W.make_random(n_q, d, dtype, seed=seed, sigma=1.0)
+    k = W.make_random(n_k, d, dtype, seed=seed + 1, sigma=1.0)
+    v = W.make_random(n_k, d, dtype, seed=seed + 2, sigma=1.0)
+    return q, k, v
+
+
+def _dec(a, dtype):
+    return a.astype(np.float64) if dtype == "f32" else oracle.decode(W.bits_view(a, dtype), dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_attention_with_zero_queries_averages_the_kept_values(dtype):
+    # Q = 0: every score is 0, the weights are uniform over the kept keys, so
+    # output row i is the mean of the first i + 1 value rows (causal) or of all
+    q, k, v = _qkv(6, 9, 8, dtype, 21)
+    q[:] = W.quantise(np.zeros((6, 8)), dtype)
+    vd = _dec(v, dtype)
+    full = oracle.attention_fwd(q, k, v, dtype, 0.25)
+    assert np.abs(full - vd.mean(axis=0)).max() < 1e-14
+    causal = oracle.attention_fwd(q, k, v, dtype, 0.25, causal=True)
+    for i in range(6):
+        assert np.abs(causal[i] - vd[:i + 1].mean(axis=0)).max() < 1e-14
+
+
+def test_attention_causal_rows_see_exactly_their_prefix():
+    # query 0 of a causal head sees key 0 only: its output is value row 0
+    # exactly; with offset -1 it sees nothing (NaN) and query 1 sees key 0;
+    # an offset past every key keeps them all (the unmasked head)
+    q, k, v = _qkv(5, 7, 4, "f32", 31)
+    o = oracle.attention_fwd(q, k, v, "f32", 1.0, causal=True)
+    assert np.array_equal(o[0], v[0].astype(np.float64))
+    o = oracle.attention_fwd(q, k, v, "f32", 1.0, causal=True, causal_offset=-1)
+    assert np.isnan(o[0]).all() and np.array_equal(o[1], v[0].astype(np.float64))
+    full = oracle.attention_fwd(q, k, v, "f32", 1.0)
+    assert np.array_equal(oracle.attention_fwd(q, k, v, "f32", 1.0, causal=True, causal_offset=10), full)
+    two = oracle.attention_fwd(q, k, v, "f32", 1.0, causal=True, causal_offset=1)
+    assert np.array_equal(two[5 - 1], oracle.attention_fwd(q[4:5], k[:6], v[:6], "f32", 1.0)[0])
+
+
+def test_attention_with_one_dominant_key_returns_its_value():
+    # a key aligned with the query and far larger than the rest: its weight
+    # is 1 up to e^-90, so the output is its value row
+    d = 16
+    q = np.zeros((1, d), np.float32)
+    q[0, 3] = 10.0
+    k = W.make_random(8, d, "f32", seed=5, sigma=0.1)
+    k[6, 3] = 10.0                                      # score 100 against about 1 for the others
+    v = W.make_random(8, d, "f32", seed=6)
+    o = oracle.attention_fwd(q, k, v, "f32", 1.0)
+    assert np.abs(o[0] - v[6]).max() < 1e-30
+
+
+def test_attention_is_linear_in_the_values_and_invariant_to_key_order():
+    q, k, v = _qkv(4, 10, 8, "f32", 41)
+    v2 = W.make_random(10, 8, "f32", seed=99)
+    a = oracle.attention_fwd(q, k, v, "f32", 0.3)
+    b = oracle.attention_fwd(q, k, v2, "f32", 0.3)
+    vs = (v.astype(np.float64) + v2.astype(np.float64)).astype(np.float32)
+    assert np.allclose(oracle.attention_fwd(q, k, vs, "f32", 0.3), a + b, atol=1e-6)
+    perm = np.random.default_rng(0).permutation(10)
+    c = oracle.attention_fwd(q, k[perm], v[perm], "f32", 0.3)
+    assert np.abs(c - a).max() < 1e-12
+
+
+def test_attention_scale_is_the_same_as_scaling_the_queries():
+    # scale 2 on the scores equals doubled queries (exact in fp32) at scale 1
+    q, k, v = _qkv(5, 6, 8, "f32", 51)
+    assert np.array_equal(oracle.attention_fwd(q, k, v, "f32", 2.0), oracle.attention_fwd(q * 2, k, v, "f32", 1.0))
