@@ -238,6 +238,27 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             int threads = fth > 0 ? fth : (g == 32 && vpt >= 6 ? 256 : 128);
             if (fth <= 0)  // spread small problems over more SMs
                 while (threads > 32 && cdiv(rows * g, threads) < sms) threads /= 2;
+            if (fth <= 0 && cdiv(rows * g, threads) >= sms) {
+                // One wave of blocks: the SM with the most blocks sets the time,
+                // so take the block size (down to half, in whole warps) that
+                // gives the fewest rows to the busiest SM (fp16 4096 x 2048:
+                // 8 rows per block put 32 rows on some SMs, 5.53 us; 7 rows,
+                // 28 at most, 5.37 us).  Several waves balance themselves.
+                const int64_t regs = 4 * vpt + 24;
+                int best_t = threads;
+                int64_t best_load = INT64_MAX;
+                for (int t = threads; t >= std::max(32, threads / 2); t -= 32) {
+                    if (t % g != 0) continue;
+                    const int64_t rpb = t / g, blocks = cdiv(rows, rpb);
+                    const int64_t per_sm = std::min<int64_t>({32, 2048 / t, 65536 / (t * regs)});
+                    const int64_t load = blocks <= per_sm * sms ? cdiv(blocks, sms) * rpb : cdiv(rows, sms);
+                    if (load < best_load) {
+                        best_load = load;
+                        best_t = t;
+                    }
+                }
+                threads = best_t;
+            }
             if (threads < 32 || threads > 256 || threads % 32 != 0 || threads % g != 0)
                 return SOFTMAX_ERR_UNSUPPORTED;
             p->threads = threads;
