@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 from memory_bound_row_softmax_gb300 import binding as B
@@ -210,3 +211,47 @@ def test_host_call_argument_checks_need_no_gpu():
     assert B.lib().softmax_fwd_host(h, h + 4, 4, 8, 8, 0, 1 << 30, 1 << 20, None) == B.ERR_OVERLAP
     assert B.lib().softmax_fwd_host(h, h + (1 << 20), 4, 8, 8, 0, (1 << 30) + 4, 1 << 20, None) == B.ERR_ARG
     assert B.lib().softmax_fwd_host(h, h + (1 << 20), 4, 8, 8, 0, 1 << 30, 16, None) == B.ERR_ARG  # too small
+
+
+def _check_plan_covers(p, rows, cols, stride, dt, in_off, out_off):
+    es = 4 if dt == "f32" else 2
+    V = 16 // es
+    uniform = (stride * es) % 16 == 0
+    head = (in_off // es) % V if uniform else V - 1
+    nv = -(-(head + cols) // V)
+    path = p["path"]
+    if path == B.PATH_WARP:
+        assert p["group"] * p["vpt"] >= nv and p["threads"] % p["group"] == 0 and 32 <= p["threads"] <= 256
+        assert p["grid"] * (p["threads"] // p["group"]) >= min(rows, p["grid"] * (p["threads"] // p["group"]))
+    elif path == B.PATH_CTA:
+        assert p["threads"] * p["vpt"] >= nv and p["grid"] == min(rows, 2 ** 31 - 1)
+    elif path == B.PATH_CLUSTER:
+        assert 1 <= p["group"] <= 16 and -(-nv // p["group"]) <= p["threads"] * p["vpt"]
+        assert p["grid"] == rows * p["group"]
+    elif path == B.PATH_STREAM:
+        assert 1 <= p["group"] <= 16 and p["grid"] == rows * p["group"] and p["scratch_bytes"] == 0
+    elif path == B.PATH_PACKED:
+        assert stride == cols and p["group"] == 1 and p["smem_bytes"] <= 48 * 1024
+        assert p["grid"] * 128 * p["vpt"] >= rows
+    elif path == B.PATH_RING:
+        assert p["whole_vectors"] and 1 <= p["group"] <= 16
+    else:
+        assert path == B.PATH_SPLIT and p["scratch_bytes"] == rows * p["group"] * 8
+
+
+def test_planner_fuzz_covers_every_row():
+    # random shapes, strides and base offsets: the automatic plan always exists
+    # and always covers the row (host only: an SM count is given)
+    rng = np.random.default_rng(7)
+    for _ in range(3000):
+        dt = ["f32", "f16", "bf16"][rng.integers(3)]
+        es = 4 if dt == "f32" else 2
+        cols = int(np.exp(rng.uniform(0, np.log(3_000_000))))
+        stride = cols + int(rng.choice([0, 0, 0, 1, 5, 8, 64]))
+        rows = int(np.exp(rng.uniform(0, np.log(2_000_000))))
+        off = int(rng.integers(0, 16 // es)) * es
+        out_off = off if rng.integers(3) else int(rng.integers(0, 16 // es)) * es
+        p = B.plan((1 << 30) + off, (1 << 46) + out_off, rows, cols, stride, dt,
+                   num_sms=int(rng.choice([1, 16, 152])))
+        _check_plan_covers(p, rows, cols, stride, dt, off, out_off)
+        assert p["vec_store"] == (off == out_off)
