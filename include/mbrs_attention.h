@@ -1,0 +1,65 @@
+/*
+ * mbrs_attention.h -- C ABI of the fused attention forward on GB300 (sm_103a).
+ *
+ * The operation (page "Dissecting Memory Bandwidth & SRAM Tiling in Triton:
+ * From GEMM to FlashAttention-3", sections "The Mathematical Remedy: Online
+ * Softmax Tiling" and "Writing the Kernel in OpenAI Triton"), for every batch
+ * b < batch, head h < heads and query i < n_ctx:
+ *
+ *     s_ij = sm_scale * sum_c Q[b,h,i,c] K[b,h,j,c]
+ *     O[b,h,i,:] = sum_j softmax_j(s_ij) V[b,h,j,:]
+ *
+ * over the keys j < n_ctx, or with causal != 0 over the keys j <= i only.  The
+ * score matrix never leaves the chip: scores are formed tile by tile in tensor
+ * memory, their softmax is taken with a running max and normaliser per query,
+ * and O is accumulated in tensor memory and divided by the normaliser once.
+ *
+ * Layout: Q, K, V and O are [batch, heads, n_ctx, head_dim] contiguous
+ * (element (b,h,i,c) at ((b * heads + h) * n_ctx + i) * head_dim + c), all of
+ * the same dtype: SOFTMAX_F16 or SOFTMAX_BF16.  head_dim must be 128 (the
+ * pages' benchmark shape); any n_ctx >= 1.
+ *
+ * Arithmetic: products of the 16-bit inputs accumulated in fp32 on the tensor
+ * cores; exp in fp32; the probabilities P rounded to the input dtype for the
+ * second product (as the pages' kernel does); O accumulated in fp32, divided
+ * by the fp32 normaliser and rounded once to the dtype (round-to-nearest-even).
+ *
+ * Ownership: the caller owns all four device buffers and the stream.  Every
+ * pointer must be 16-byte aligned.  Q, K and V may overlap one another; O may
+ * overlap none of them.  The call is asynchronous on `stream`; nothing is
+ * allocated on the device.
+ *
+ * Errors (checked on the host before any launch; nothing is launched unless
+ * the result is SOFTMAX_OK):
+ *   SOFTMAX_ERR_SHAPE       batch, heads or n_ctx < 0, head_dim < 1, or sizes
+ *                           beyond the kernel's index range (2^31 - 1 query
+ *                           tiles, n_ctx < 2^31 - 128)
+ *   SOFTMAX_ERR_UNSUPPORTED head_dim != 128, or dtype SOFTMAX_F32
+ *   SOFTMAX_ERR_DTYPE       dtype not a softmax_dtype_t
+ *   SOFTMAX_ERR_NULL        a NULL pointer while there is work to do
+ *   SOFTMAX_ERR_ALIGN       a pointer not 16-byte aligned
+ *   SOFTMAX_ERR_OVERLAP     O overlaps Q, K or V
+ *   SOFTMAX_ERR_ARG         causal not 0 or 1, sm_scale not finite and > 0
+ *   SOFTMAX_ERR_CUDA        the tensor-map encoder or the launch failed
+ * batch * heads * n_ctx == 0 returns SOFTMAX_OK without a launch.  A bounded
+ * wait inside the kernel that runs out sets the device error word that
+ * softmax_check_device_error() reports as SOFTMAX_ERR_TIMEOUT.
+ */
+#ifndef MBRS_ATTENTION_H
+#define MBRS_ATTENTION_H
+
+#include "mbrs_softmax.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+int softmax_attention_fwd(const void *q, const void *k, const void *v, void *o, int64_t batch, int64_t heads,
+                          int64_t n_ctx, int64_t head_dim, int dtype, int causal, float sm_scale,
+                          cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MBRS_ATTENTION_H */

@@ -62,6 +62,7 @@ SIGNATURES = {
     "softmax_abi_version": (_int, []),
     "softmax_fwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp]),
     "softmax_fwd_masked": (_int, [_vp, _vp, _i64, _i64, _i64, _int, ctypes.c_float, _i64, _i64, _vp]),
+    "softmax_attention_fwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, ctypes.c_float, _vp]),
 }
 
 _lib = None
@@ -184,6 +185,40 @@ def softmax_fwd_masked(x, scale: float = 1.0, causal_offset: int = 0, rows_per_s
                                       int(causal_offset), int(rows_per_seq), _stream_handle(x, stream))
     if st != OK:
         raise SoftmaxError(st, "softmax_fwd_masked")
+    return out
+
+
+def attention_fwd_ptr(q: int, k: int, v: int, o: int, batch: int, heads: int, n_ctx: int, head_dim: int,
+                      dtype: int, causal: bool, sm_scale: float, stream: int = 0) -> int:
+    """Raw call of the fused attention forward (status out)."""
+    return lib().softmax_attention_fwd(q, k, v, o, batch, heads, n_ctx, head_dim, dtype, 1 if causal else 0,
+                                       sm_scale, stream)
+
+
+def attention_fwd(q, k, v, causal: bool = True, sm_scale: float | None = None, out=None, stream=None):
+    """Fused attention forward O = softmax(Q K^T * sm_scale [causal]) V of
+    [batch, heads, n_ctx, 128] contiguous fp16 / bf16 CUDA tensors (sm_scale
+    defaults to 1 / sqrt(head_dim)); returns ``out``."""
+    import torch
+    for t in (q, k, v):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError("attention_fwd needs CUDA tensors")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError("attention_fwd needs contiguous [batch, heads, n_ctx, head_dim] tensors")
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k and v must have one shape and dtype")
+    batch, heads, n_ctx, head_dim = q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / float(head_dim) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of q's shape and dtype")
+    with torch.cuda.device(q.device):
+        st = attention_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), batch, heads, n_ctx,
+                               head_dim, _torch_dtype_code(q), causal, float(sm_scale), _stream_handle(q, stream))
+    if st != OK:
+        raise SoftmaxError(st, "attention_fwd")
     return out
 
 

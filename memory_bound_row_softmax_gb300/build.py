@@ -22,8 +22,10 @@ INCLUDE = os.path.join(ROOT, "include")
 
 SOURCES = ["abi.cu", "k_warp.cu", "k_warp_whole.cu", "k_cta.cu", "k_cta_whole.cu", "k_cluster.cu", "k_split.cu",
            "k_ring.cu", "k_noalloc.cu", "k_masked_warp.cu", "k_masked_warp_whole.cu", "k_masked.cu",
-           "k_masked_whole.cu", "k_packed.cu"]
-HEADERS = ["common.cuh", "kernels.cuh", "launch.h", "warp_launch.cuh", "cta_launch.cuh"]
+           "k_masked_whole.cu", "k_packed.cu", "k_attention.cu"]
+HEADERS = ["common.cuh", "kernels.cuh", "launch.h", "warp_launch.cuh", "cta_launch.cuh", "attention.cuh",
+           "attention_launch.h"]
+PUBLIC_HEADERS = ["mbrs_softmax.h", "mbrs_attention.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -44,14 +46,15 @@ def sources_digest() -> str:
     for f in sorted(SOURCES + HEADERS):
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
-    with open(os.path.join(INCLUDE, "mbrs_softmax.h"), "rb") as fh:
-        h.update(fh.read())
+    for f in PUBLIC_HEADERS:
+        with open(os.path.join(INCLUDE, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def _newest_input() -> float:
     files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
-    files.append(os.path.join(INCLUDE, "mbrs_softmax.h"))
+    files += [os.path.join(INCLUDE, f) for f in PUBLIC_HEADERS]
     files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 

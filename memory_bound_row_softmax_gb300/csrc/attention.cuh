@@ -1,0 +1,150 @@
+// attention.cuh -- fifth-generation tensor-core (tcgen05) building blocks for
+// the fused attention forward: tensor-memory allocation, loads and stores,
+// shared-memory matrix descriptors, the instruction descriptor, MMA issue and
+// completion tracking, and tiled TMA loads.  All of it is inline PTX for
+// sm_103a.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (the 128-byte TMA descriptor)
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace mbrs {
+namespace attn {
+
+// ---------------------------------------------------------------------------
+// Tensor memory (TMEM): 128 lanes x 512 columns of 32-bit cells per SM.  An
+// address is (lane << 16) | column.  A warp may touch only the 32 lanes of its
+// quarter: warp w of a block reaches lanes 32 (w mod 4) .. 32 (w mod 4) + 31.
+// ---------------------------------------------------------------------------
+// Whole-warp calls.  alloc writes the base address of `cols` columns (a power
+// of two >= 32) into the shared-memory word at slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(cols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+// Ordering of tcgen05 operations across a thread synchronisation (a barrier
+// or an mbarrier wait): `before` on the side that signals, `after` on the side
+// that waits.
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive columns of this thread's lane (shape 32x32b: thread i of the
+// warp reads lane base + i) into v[0..31].  Completes at tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// v[0..31] into 32 consecutive columns of this thread's lane.  Completes at
+// tmem_wait_st().
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// Shared-memory matrix descriptor (64 bits) for operands in the 128-byte
+// swizzled layout: rows of 128 bytes, the 16-byte chunks of row r stored at
+// chunk position (chunk XOR (r mod 8)), eight rows (1024 bytes) per swizzle
+// atom, atoms 1024-byte aligned -- the layout a TMA load with 128-byte
+// swizzle writes.
+//   bits  0-13  start address >> 4
+//   bits 16-29  leading-dimension byte offset >> 4
+//   bits 32-45  stride-dimension byte offset >> 4
+//   bits 46-48  0b001 (descriptor version of this architecture)
+//   bits 49-51  base offset (0: atoms are 1024-byte aligned)
+//   bit  52     leading offset mode (0: relative)
+//   bits 61-63  swizzle mode (2: 128-byte)
+// K-major operand (K contiguous within a row): the stride offset is the
+// distance between 8-row groups (1024 bytes); the leading offset is unused by
+// this swizzle and set to 16 bytes.  MN-major operand (M or N contiguous): the
+// leading offset is the distance between successive 64-element column blocks,
+// the stride offset that between 8-row groups along K.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lead_bytes, uint32_t stride_bytes) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lead_bytes >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((stride_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor (32 bits) of kind::f16 with an fp32 accumulator:
+//   bits 4-5 D type (1: f32); bits 7-9 / 10-12 A / B type (0: f16, 1: bf16);
+//   bit 15 / 16 A / B major (0: K-major, 1: MN-major); bits 17-22 N >> 3;
+//   bits 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t f16_idesc(bool bf16, bool b_mn_major, int m, int n) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] . B[smem]; issued by one thread.
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// One arrival on the mbarrier at `bar` once every MMA this thread issued so
+// far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Tiled 3-D TMA load (coordinates innermost first) into shared memory,
+// completing `bar`'s transaction count.  x * element size must be a multiple
+// of 16 bytes; out-of-range elements read as zero.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int32_t x, int32_t y, int32_t z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+        "%4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+}  // namespace attn
+}  // namespace mbrs

@@ -1,0 +1,447 @@
+// k_attention.cu -- fused attention forward on the fifth-generation tensor cores:
+//
+//     O = softmax(Q K^T * sm_scale, causal: key j <= query i) V
+//
+// for every (batch, head), with Q, K, V, O stored [batch, heads, n_ctx, 128]
+// (page "Dissecting Memory Bandwidth & SRAM Tiling in Triton: From GEMM to
+// FlashAttention-3", sections "The Mathematical Remedy: Online Softmax
+// Tiling" and "Writing the Kernel in OpenAI Triton": tiles of 128 queries,
+// running max and normaliser per query, the output accumulator rescaled when
+// the max moves, P rounded to the input type before the second product, the
+// accumulator divided by the normaliser at the end).
+//
+// One block per 128-query tile, 192 threads in three roles:
+//   warp 4, one lane  -- TMA: the Q tile once, then K and V tiles of 128 keys
+//                        into a two-stage ring (128-byte swizzled rows);
+//   warp 5, one lane  -- tcgen05.mma: S_j = Q K_j^T into one of two TMEM
+//                        buffers (the next one is computed while the softmax
+//                        works on this one), O += P_j V_j into TMEM;
+//                        warp 5 also owns the TMEM allocation;
+//   warps 0-3         -- softmax: thread t owns query row t of the tile, which
+//                        is TMEM lane t, so the row max and row sum are
+//                        thread-local: no shuffles, no shared-memory
+//                        reduction.  P_j goes to shared memory as the A
+//                        operand of the second product.  At the end the same
+//                        threads read O from TMEM, divide by the normaliser
+//                        and store their row.
+// The running max moves lazily: the shift m used for exp only changes when a
+// tile's max exceeds it by more than 2^8 (in log2 units), so O in TMEM is
+// rescaled rarely; both O and the normaliser carry the same shift, which
+// cancels in O / l, and entries of P stay below 2^8.
+//
+// Every wait is bounded: a wait that runs out sets the device error word and
+// an abort flag the other roles see, outstanding TMA loads and MMAs are
+// waited for (bounded), TMEM is released and the block returns.
+#include <atomic>
+#include <mutex>
+
+#include "attention.cuh"
+#include "attention_launch.h"
+#include "launch.h"
+
+namespace mbrs {
+namespace attn {
+
+__device__ unsigned int g_attn_error;
+
+namespace {
+
+constexpr int kBlockM = 128;  // queries per tile (= TMEM lanes)
+constexpr int kBlockN = 128;  // keys per tile
+constexpr int kHeadDim = kAttnHeadDim;
+constexpr int kThreads = 192;
+constexpr int kStages = 2;
+constexpr uint32_t kTileBytes = kBlockN * kHeadDim * 2;  // one 128 x 128 tile of 16-bit elements
+constexpr uint32_t kHalfBytes = kTileBytes / 2;          // its 64-column half: 128 rows of 128 bytes
+// shared memory, from a 1024-byte aligned base
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffKV = kTileBytes;  // stage s: K at kOffKV + 2 s kTileBytes, V right after it
+constexpr uint32_t kOffP = kOffKV + kStages * 2 * kTileBytes;
+constexpr uint32_t kOffBar = kOffP + kTileBytes;
+enum : int {
+    kBarQ = 0,
+    kBarK = 1,        // + stage
+    kBarV = 3,        // + stage
+    kBarKVEmpty = 5,  // + stage
+    kBarS = 7,        // + S buffer
+    kBarP = 9,
+    kBarO = 10,
+    kBarDrain = 11,
+    kNumBars = 12
+};
+constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
+constexpr size_t kSmemBytes = kOffAbort + 4 + 1024;  // + slack for aligning the base
+// tensor memory columns: S buffers at 0 and 128, O at 256
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 256;
+constexpr float kShiftSlack = 8.f;  // log2 units
+
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
+static_assert(kBlockM == 128 && kBlockN == 128 && kHeadDim == 128, "tile shapes the descriptors assume");
+
+template <typename T> __device__ __forceinline__ uint32_t pack2(float a, float b);
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);  // a at the lower address
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void flag_timeout(volatile uint32_t *abort_flag) {
+    *abort_flag = 1u;
+    atomicOr(&g_attn_error, kErrWaitTimeout);
+}
+
+// Wait for phase `parity` of the mbarrier at bar; false once the block is
+// aborting or after limit_ns (which starts the abort).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                           uint32_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint32_t t0 = global_timer_lo();
+    for (uint32_t it = 0; it < (1u << 30); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_lo() - t0 > limit_ns) break;
+    }
+    flag_timeout(abort_flag);
+    return false;
+}
+// The same without the abort check: waits for work already in flight (TMA
+// loads, MMAs) before the block lets go of its memory.
+__device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                            uint32_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return;
+    const uint32_t t0 = global_timer_lo();
+    for (uint32_t it = 0; it < (1u << 30); ++it) {
+        if (mbar_try_wait(bar, parity)) return;
+        if (global_timer_lo() - t0 > limit_ns) break;
+    }
+    flag_timeout(abort_flag);
+}
+
+}  // namespace
+
+// Block t of the grid takes head bh = t / m_tiles and, within the head, the
+// query tiles from the last (the most keys under a causal mask) to the first,
+// so that the blocks resident at one time share a few heads' K and V in L2.
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attention_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, T *__restrict__ o, int n_ctx, int m_tiles,
+                    float kscale, int causal, uint32_t wait_ns) {
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    volatile uint32_t *const abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + kOffAbort);
+    const auto bar = [base](int i) { return base + kOffBar + 8u * (uint32_t)i; };
+
+    const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
+    const int bh = (int)(blockIdx.x / (unsigned)m_tiles);
+    const int mt = m_tiles - 1 - (int)(blockIdx.x % (unsigned)m_tiles);
+    const int m0 = mt * kBlockM;
+    const int kv_tiles = causal ? mt + 1 : (n_ctx + kBlockN - 1) / kBlockN;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), i == kBarP ? kBlockM : 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+    }
+    if (warp == 5) {
+        tmem_alloc(base + kOffTmemSlot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + kOffTmemSlot);
+
+    if (warp == 4) {
+        // ---- TMA producer ------------------------------------------------
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(kBarQ), kTileBytes);
+            tma_load_3d(base + kOffQ, &tq, 0, m0, bh, bar(kBarQ));
+            tma_load_3d(base + kOffQ + kHalfBytes, &tq, 64, m0, bh, bar(kBarQ));
+            int j = 0;
+            for (; j < kv_tiles; ++j) {
+                const int s = j & 1;
+                // stage s last held tile j - 2; its PV product must be done
+                if (j >= 2 && !wait_phase(bar(kBarKVEmpty + s), ((j >> 1) + 1) & 1, abort_flag, wait_ns)) break;
+                const uint32_t kdst = base + kOffKV + (uint32_t)s * 2u * kTileBytes;
+                const uint32_t vdst = kdst + kTileBytes;
+                const int y = j * kBlockN;
+                mbar_arrive_expect_tx(bar(kBarK + s), kTileBytes);
+                tma_load_3d(kdst, &tk, 0, y, bh, bar(kBarK + s));
+                tma_load_3d(kdst + kHalfBytes, &tk, 64, y, bh, bar(kBarK + s));
+                mbar_arrive_expect_tx(bar(kBarV + s), kTileBytes);
+                tma_load_3d(vdst, &tv, 0, y, bh, bar(kBarV + s));
+                tma_load_3d(vdst + kHalfBytes, &tv, 64, y, bh, bar(kBarV + s));
+            }
+            // every load issued lands before the block may exit
+            drain_phase(bar(kBarQ), 0, abort_flag, wait_ns);
+            for (int jj = (j >= 2 ? j - 2 : 0); jj < j; ++jj) {
+                drain_phase(bar(kBarK + (jj & 1)), (jj >> 1) & 1, abort_flag, wait_ns);
+                drain_phase(bar(kBarV + (jj & 1)), (jj >> 1) & 1, abort_flag, wait_ns);
+            }
+        }
+    } else if (warp == 5) {
+        // ---- MMA issuer ----------------------------------------------------
+        if (lane == 0) {
+            constexpr uint32_t id_s = f16_idesc(kBf16, false, kBlockM, kBlockN);   // S = Q K^T
+            constexpr uint32_t id_o = f16_idesc(kBf16, true, kBlockM, kHeadDim);   // O += P V
+            // S_j = Q K_j^T: K = head dim, 8 steps of 16; both operands K-major
+            const auto issue_s = [&](int j) -> bool {
+                const int s = j & 1;
+                if (!wait_phase(bar(kBarK + s), (j >> 1) & 1, abort_flag, wait_ns)) return false;
+                tc_fence_after();
+                const uint32_t kb = base + kOffKV + (uint32_t)s * 2u * kTileBytes;
+                const uint32_t d = tmem + kColS + (uint32_t)s * kBlockN;
+#pragma unroll
+                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kHalfBytes + (uint32_t)(kk & 3) * 32u;
+                    mma_ss(d, sw128_desc(base + kOffQ + off, 16, 1024), sw128_desc(kb + off, 16, 1024), id_s,
+                           kk > 0);
+                }
+                mma_commit(bar(kBarS + s));
+                return true;
+            };
+            bool ok = wait_phase(bar(kBarQ), 0, abort_flag, wait_ns);
+            if (ok) ok = issue_s(0);
+            for (int j = 0; ok && j < kv_tiles; ++j) {
+                if (j + 1 < kv_tiles && !(ok = issue_s(j + 1))) break;
+                const int s = j & 1;
+                if (!(ok = wait_phase(bar(kBarV + s), (j >> 1) & 1, abort_flag, wait_ns))) break;
+                if (!(ok = wait_phase(bar(kBarP), j & 1, abort_flag, wait_ns))) break;
+                tc_fence_after();
+                // O += P_j V_j: K = keys, 8 steps of 16; P K-major, V MN-major
+                // (head dim contiguous; its two 64-column halves kHalfBytes apart)
+                const uint32_t vb = base + kOffKV + (uint32_t)s * 2u * kTileBytes + kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                    const uint32_t aoff = (uint32_t)(kk >> 2) * kHalfBytes + (uint32_t)(kk & 3) * 32u;
+                    mma_ss(tmem + kColO, sw128_desc(base + kOffP + aoff, 16, 1024),
+                           sw128_desc(vb + (uint32_t)kk * 16u * 128u, kHalfBytes, 1024), id_o, (j > 0 || kk > 0));
+                }
+                mma_commit(bar(kBarKVEmpty + s));
+                mma_commit(bar(kBarO));
+            }
+            // every MMA issued completes before TMEM is released
+            mma_commit(bar(kBarDrain));
+            drain_phase(bar(kBarDrain), 0, abort_flag, wait_ns);
+        }
+    } else {
+        // ---- softmax: thread r owns query row r of the tile ---------------
+        const int r = (int)threadIdx.x;
+        const int q = m0 + r;
+        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+        const int q_lim = causal ? min(q + 1, n_ctx) : n_ctx;  // keys [0, q_lim) are kept
+        const uint32_t prow = base + kOffP + (uint32_t)r * 128u;
+        float m_run = -INFINITY;  // the shift, in log2 units
+        float l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < kv_tiles; ++j) {
+            const int b = j & 1;
+            ok = __all_sync(0xffffffffu, wait_phase(bar(kBarS + b), (j >> 1) & 1, abort_flag, wait_ns));
+            if (!ok) break;
+            tc_fence_after();
+            float s[kBlockN];
+#pragma unroll
+            for (int c = 0; c < kBlockN / 32; ++c) tmem_ld32(lane_addr + kColS + (uint32_t)b * kBlockN + c * 32, s + c * 32);
+            tmem_wait_ld();
+            const int lim = q_lim - j * kBlockN;  // kept columns of this tile: [0, lim)
+            if (lim < kBlockN) {
+#pragma unroll
+                for (int c = 0; c < kBlockN; ++c)
+                    if (c >= lim) s[c] = -INFINITY;
+            }
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+            for (int c = 8; c < kBlockN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+            const float m_tile =
+                fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                kscale;
+            float alpha = 1.f;
+            bool moved = false;
+            if (m_tile > m_run + kShiftSlack) {
+                alpha = ex2(m_run - m_tile);  // 0 on the first tile
+                l_run *= alpha;
+                m_run = m_tile;
+                moved = j > 0;
+            }
+            // p = 2^(s kscale - m_run), rounded to T in pairs
+            uint32_t pk[kBlockN / 2];
+            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < kBlockN / 2; ++c) {
+                const float p0 = ex2(fmaf(s[2 * c], kscale, -m_run));
+                const float p1 = ex2(fmaf(s[2 * c + 1], kscale, -m_run));
+                sum[c & 3] += p0 + p1;
+                pk[c] = pack2<T>(p0, p1);
+            }
+            l_run += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+            // PV_{j-1} must be done with the P buffer and with O
+            if (j > 0) {
+                ok = __all_sync(0xffffffffu, wait_phase(bar(kBarO), (j - 1) & 1, abort_flag, wait_ns));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, moved)) {
+                // the whole warp takes part (the TMEM accesses are warp-wide);
+                // rows whose shift did not move scale by 1
+#pragma unroll
+                for (int c = 0; c < kHeadDim / 32; ++c) {
+                    float ov[32];
+                    tmem_ld32(lane_addr + kColO + c * 32, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+                    tmem_st32(lane_addr + kColO + c * 32, ov);
+                }
+                tmem_wait_st();
+            }
+            // row r of P: 16 chunks of 8 keys; chunk c of a 64-key half sits
+            // at position c ^ (r mod 8) of the row's 128 bytes
+#pragma unroll
+            for (int ch = 0; ch < kBlockN / 8; ++ch) {
+                const uint32_t addr = prow + (uint32_t)(ch >> 3) * kHalfBytes + (uint32_t)(((ch & 7) ^ (r & 7)) * 16);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * ch]),
+                             "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
+                             : "memory");
+            }
+            fence_proxy_async_smem();  // visible to the tensor core's reads
+            tc_fence_before();
+            mbar_arrive(bar(kBarP));
+        }
+        if (ok) ok = __all_sync(0xffffffffu, wait_phase(bar(kBarO), (kv_tiles - 1) & 1, abort_flag, wait_ns));
+        if (ok) {
+            tc_fence_after();
+            const float inv = 1.f / l_run;
+            T *orow = o + ((int64_t)bh * n_ctx + q) * kHeadDim;
+#pragma unroll
+            for (int c = 0; c < kHeadDim / 32; ++c) {
+                float ov[32];
+                tmem_ld32(lane_addr + kColO + c * 32, ov);
+                tmem_wait_ld();
+                if (q < n_ctx) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w;
+                        w.x = pack2<T>(ov[8 * v + 0] * inv, ov[8 * v + 1] * inv);
+                        w.y = pack2<T>(ov[8 * v + 2] * inv, ov[8 * v + 3] * inv);
+                        w.z = pack2<T>(ov[8 * v + 4] * inv, ov[8 * v + 5] * inv);
+                        w.w = pack2<T>(ov[8 * v + 6] * inv, ov[8 * v + 7] * inv);
+                        *reinterpret_cast<uint4 *>(orow + c * 32 + v * 8) = w;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime (the
+// library does not link the driver library itself).
+EncodeTiled encoder() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    });
+    return fn;
+}
+
+// [batch * heads, n_ctx, 128] viewed as a 3-D tensor (head dim innermost);
+// boxes of 64 x 128 x 1 elements (128-byte rows) with 128-byte swizzle.
+bool make_map(CUtensorMap *map, const void *ptr, int dtype, int64_t n_ctx, int64_t bh) {
+    const EncodeTiled enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)n_ctx, (cuuint64_t)bh};
+    const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)n_ctx * kHeadDim * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kBlockN, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, dtype == kAttnBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+               const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+
+template <typename T>
+cudaError_t go(const AttnArgs &a, int64_t wait_ns) {
+    static std::atomic<unsigned long long> opted{0};
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (device & (kMaxDevices - 1));
+    if (!(opted.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(k_attention_fwd<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        opted.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const int64_t bh = a.batch * a.heads;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, a.q, a.dtype, a.n_ctx, bh) || !make_map(&mk, a.k, a.dtype, a.n_ctx, bh) ||
+        !make_map(&mv, a.v, a.dtype, a.n_ctx, bh))
+        return cudaErrorInvalidValue;
+    const int64_t m_tiles = (a.n_ctx + kBlockM - 1) / kBlockM;
+    const float kscale = a.sm_scale * kLog2e;
+    const uint32_t limit = (uint32_t)std::min<int64_t>(std::max<int64_t>(wait_ns, 1), 0x7fffffff);
+    k_attention_fwd<T><<<(unsigned)(bh * m_tiles), kThreads, kSmemBytes, a.stream>>>(
+        mq, mk, mv, static_cast<T *>(a.o), (int)a.n_ctx, (int)m_tiles, kscale, a.causal, limit);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnArgs &a, int64_t wait_ns) {
+    return a.dtype == kAttnBf16 ? go<__nv_bfloat16>(a, wait_ns) : go<__half>(a, wait_ns);
+}
+
+int64_t attention_grid(int64_t batch, int64_t heads, int64_t n_ctx) {
+    return batch * heads * ((n_ctx + kBlockM - 1) / kBlockM);
+}
+
+size_t attention_smem_bytes() { return kSmemBytes; }
+
+cudaError_t read_clear_attn_error_word(unsigned int *word) {
+    cudaError_t e = cudaMemcpyFromSymbol(word, g_attn_error, sizeof(unsigned int), 0, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_attn_error, &zero, sizeof(unsigned int), 0, cudaMemcpyHostToDevice);
+}
+
+}  // namespace attn
+}  // namespace mbrs

@@ -278,3 +278,62 @@ def sweep_workload(cols: int, total_elems: int = 50_000_000) -> Workload:
     return Workload(f"sweep_f32_w{cols}", total_elems // cols, cols, "f32", 5 * 100003 + cols,
                     "uniform", lo=-100.0, hi=100.0,
                     note="fp32 width sweep, ~200 MB per tensor, U(-100,100)")
+
+
+# ---------------------------------------------------------------------------
+# attention inputs: Q, K, V of shape [batch, heads, n_ctx, head_dim]
+# ---------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class AttentionWorkload:
+    """The attention forward the pages benchmark (page "Dissecting Memory
+    Bandwidth & SRAM Tiling in Triton", section "Benchmark Results": batch 4,
+    32 heads, head dim 128, fp16, causal, context 1,024 .. 32,768).  Q, K and V
+    are N(0, 1) quantised to ``dtype``, each from its own sub-stream."""
+    name: str
+    batch: int
+    heads: int
+    n_ctx: int
+    head_dim: int
+    dtype: str
+    seed: int
+    causal: bool = True
+
+    @property
+    def elems(self) -> int:
+        return self.batch * self.heads * self.n_ctx * self.head_dim
+
+    def flops(self) -> float:
+        """Matmul FLOPs of the two products: 4 B H N^2 D, halved under a
+        causal mask (the usual count for a causal attention forward)."""
+        f = 4.0 * self.batch * self.heads * self.n_ctx * self.n_ctx * self.head_dim
+        return f / 2 if self.causal else f
+
+
+ATTENTION_CONFIGS: dict[str, AttentionWorkload] = {
+    "a4k": AttentionWorkload("attn_f16_b4_h32_n4096_d128_causal", 4, 32, 4096, 128, "f16", 6),
+    "a16k": AttentionWorkload("attn_f16_b4_h32_n16384_d128_causal", 4, 32, 16384, 128, "f16", 7),
+}
+
+QKV_STREAMS = {"q": 0, "k": 1, "v": 2}
+
+
+def qkv_heads(seed: int, which: str, bh0: int, bh1: int, n_ctx: int, head_dim: int, dtype: str) -> np.ndarray:
+    """Heads bh0 .. bh1-1 (flattened batch * heads index) of one of Q, K, V as
+    a storage array of shape (bh1 - bh0, n_ctx, head_dim): element (bh, i, c)
+    is normal deviate number (bh * n_ctx + i) * head_dim + c of its stream."""
+    per_head = n_ctx * head_dim
+    idx = np.arange(bh0 * per_head, bh1 * per_head, dtype=np.uint64)
+    x = normal(seed, QKV_STREAMS[which], idx)
+    return quantise(x, dtype).reshape(bh1 - bh0, n_ctx, head_dim)
+
+
+def make_qkv(w: AttentionWorkload, chunk_heads: int = 8) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Q, K, V of a workload as storage arrays [batch, heads, n_ctx, head_dim]."""
+    bh = w.batch * w.heads
+    out = []
+    for which in ("q", "k", "v"):
+        parts = [qkv_heads(w.seed, which, h0, min(bh, h0 + chunk_heads), w.n_ctx, w.head_dim, w.dtype)
+                 for h0 in range(0, bh, chunk_heads)]
+        out.append(np.concatenate(parts).reshape(w.batch, w.heads, w.n_ctx, w.head_dim))
+    return out[0], out[1], out[2]

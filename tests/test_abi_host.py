@@ -255,3 +255,42 @@ def test_planner_fuzz_covers_every_row():
                    num_sms=int(rng.choice([1, 16, 152])))
         _check_plan_covers(p, rows, cols, stride, dt, off, out_off)
         assert p["vec_store"] == (off == out_off)
+
+
+# softmax_attention_fwd: every argument error is reported before any CUDA call
+_A = 1 << 32  # well-separated fake device addresses, 16-byte aligned
+_MB = 1 << 24
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((_A, _A + _MB, _A + 2 * _MB, _A + 3 * _MB, -1, 1, 128, 128, 1, 1, 0.1), B.ERR_SHAPE),
+    ((_A, _A + _MB, _A + 2 * _MB, _A + 3 * _MB, 1, 1, 128, 0, 1, 1, 0.1), B.ERR_SHAPE),
+    ((_A, _A + _MB, _A + 2 * _MB, _A + 3 * _MB, 1, 1, 128, 64, 1, 1, 0.1), B.ERR_UNSUPPORTED),
+    ((_A, _A + _MB, _A + 2 * _MB, _A + 3 * _MB, 1, 1, 128, 128, 0, 1, 0.1), B.ERR_UNSUPPORTED),
+    ((_A, _A + _MB, _A + 2 * _MB, _A + 3 * _MB, 1, 1, 128, 128, 7, 1, 0.1), B.ERR_DTYPE),
+    ((_A, _A + _MB, _A + 2 * _MB, _A + 3 * _MB, 1, 1, 128, 128, 1, 2, 0.1), B.ERR_ARG),
+    ((_A, _A + _MB, _A + 2 * _MB, _A + 3 * _MB, 1, 1, 128, 128, 1, 1, 0.0), B.ERR_ARG),
+    ((_A, _A + _MB, _A + 2 * _MB, _A + 3 * _MB, 1, 1, 128, 128, 1, 1, float("inf")), B.ERR_ARG),
+    ((_A, _A + _MB, _A + 2 * _MB, _A + 3 * _MB, 1, 1, 128, 128, 1, 1, float("nan")), B.ERR_ARG),
+    ((0, 0, 0, 0, 0, 1, 128, 128, 1, 1, 0.1), B.OK),          # no work: nothing launched
+    ((0, 0, 0, 0, 3, 2, 0, 128, 2, 0, 0.1), B.OK),
+    ((0, _A + _MB, _A + 2 * _MB, _A + 3 * _MB, 1, 1, 128, 128, 1, 1, 0.1), B.ERR_NULL),
+    ((_A, _A + _MB, _A + 2 * _MB, 0, 1, 1, 128, 128, 1, 1, 0.1), B.ERR_NULL),
+    ((_A + 8, _A + _MB, _A + 2 * _MB, _A + 3 * _MB, 1, 1, 128, 128, 1, 1, 0.1), B.ERR_ALIGN),
+    ((_A, _A + _MB, _A + 2 * _MB, _A + 3 * _MB + 2, 1, 1, 128, 128, 1, 1, 0.1), B.ERR_ALIGN),
+    ((_A, _A + _MB, _A + 2 * _MB, _A + _MB + 16, 1, 1, 128, 128, 1, 1, 0.1), B.ERR_OVERLAP),
+    ((_A, _A + _MB, _A + 2 * _MB, _A + 2 * _MB - 16, 1, 1, 128, 128, 1, 1, 0.1), B.ERR_OVERLAP),
+    ((_A, _A + _MB, _A + 2 * _MB, _A, 1, 1, 128, 128, 2, 0, 0.1), B.ERR_OVERLAP),
+    ((_A, _A, _A, _A + 3 * _MB, 1, 1, 128, 128, 1, 1, 0.1), None),   # q, k, v may share memory
+    ((_A, _A + _MB, _A + 2 * _MB, _A + 3 * _MB, 1, 1, 1 << 31, 128, 1, 1, 0.1), B.ERR_SHAPE),
+    ((_A, _A + _MB, _A + 2 * _MB, _A + 3 * _MB, 1 << 20, 1 << 10, 1024, 128, 1, 1, 0.1), B.ERR_SHAPE),
+])
+def test_attention_argument_checks(args, expect):
+    if expect is None:
+        # valid arguments would launch: only check that none of the argument
+        # errors is raised (without a device the launch itself fails)
+        st = B.lib().softmax_attention_fwd(*args, None)
+        assert st not in (B.ERR_SHAPE, B.ERR_NULL, B.ERR_ALIGN, B.ERR_OVERLAP, B.ERR_ARG, B.ERR_DTYPE,
+                          B.ERR_UNSUPPORTED)
+        return
+    assert B.lib().softmax_attention_fwd(*args, None) == expect

@@ -1,0 +1,218 @@
+"""Fused attention forward (softmax_attention_fwd) against the oracle's
+one-head attention in double precision, on the same quantised inputs.
+
+Tolerance, per output element o (derived from the kernel's arithmetic): with
+u the unit roundoff of the 16-bit type (2^-11 fp16, 2^-8 bf16),
+  * P is rounded to the type before the second product while the normaliser
+    sums the unrounded fp32 values: |sum_j p_j e_j v_j| / l <= u max|v|;
+  * O is rounded once: u |o|;
+  * fp32 work: the scores' fp32 sums over 128 products perturb each exponent
+    by at most 128 * 2^-24 * scale * sum_c |q_c k_c| (counted twice: numerator
+    and normaliser), the PV sums over n kept keys add n * 2^-24 max|v|, and
+    ex2.approx adds 2^-22 relative.
+so |o_gpu - o| <= (u + 2 * score_err + n 2^-24 + 2^-21) max|v| + u |o|.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from memory_bound_row_softmax_gb300 import binding as B
+from memory_bound_row_softmax_gb300 import build as build_mod
+from memory_bound_row_softmax_gb300 import workloads as W
+
+from gpu_harness import decode
+
+pytestmark = pytest.mark.gpu
+
+U = {"f16": 2.0 ** -11, "bf16": 2.0 ** -8}
+TORCH = {"f16": torch.float16, "bf16": torch.bfloat16}
+CODE = {"f16": 1, "bf16": 2}
+D = 128
+GUARD_ELEMS = 256  # guard elements on each side of O (512 bytes)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build_mod.build()
+    yield
+    assert B.check_device_error() == B.OK
+
+
+def to_dev(a: np.ndarray, dtype: str) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(TORCH[dtype])
+
+
+def from_dev(t: torch.Tensor, dtype: str) -> np.ndarray:
+    return decode(t.view(torch.int16).cpu().numpy().view(np.uint16), dtype)
+
+
+def run(q, k, v, dtype, causal, scale=None, guard=True):
+    """softmax_attention_fwd on storage arrays [b, h, n, d]; returns O (float64)
+    and checks that the guard regions around O were not written."""
+    b, h, n, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq, dk, dv = to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype)
+    total = b * h * n * d
+    buf = torch.full((total + 2 * GUARD_ELEMS,), 0x7D0B, dtype=torch.int16, device="cuda")
+    out_ptr = buf.data_ptr() + GUARD_ELEMS * 2
+    st = B.attention_fwd_ptr(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), out_ptr, b, h, n, d, CODE[dtype], causal,
+                             scale, torch.cuda.current_stream().cuda_stream)
+    assert st == B.OK, B.status_string(st)
+    torch.cuda.synchronize()
+    assert B.check_device_error() == B.OK
+    raw = buf.cpu().numpy()
+    if guard:
+        assert (raw[:GUARD_ELEMS] == 0x7D0B).all() and (raw[GUARD_ELEMS + total:] == 0x7D0B).all()
+    return decode(raw[GUARD_ELEMS:GUARD_ELEMS + total].view(np.uint16), dtype).reshape(b, h, n, d)
+
+
+def row_tolerance(q, k, v, dtype, scale, causal, rows=None):
+    """Per-row bound of the module docstring for one head: q, k, v decoded to
+    float64 (n, d); returns an (n_rows, 1) array."""
+    n = k.shape[0]
+    rows = np.arange(q.shape[0]) if rows is None else np.asarray(rows)
+    qa, ka = np.abs(q[rows]), np.abs(k)
+    score_err = 128 * 2.0 ** -24 * scale * (qa @ ka.T)           # (rows, n)
+    keep = np.arange(n)[None, :] <= rows[:, None] if causal else np.ones((len(rows), n), bool)
+    n_kept = keep.sum(axis=1)
+    se = np.where(keep, score_err, 0).max(axis=1)
+    vmax = np.array([np.abs(v[:c]).max() if causal else np.abs(v).max() for c in n_kept])
+    return ((U[dtype] + 2 * se + n_kept * 2.0 ** -24 + 2.0 ** -21) * vmax)[:, None]
+
+
+def check_head(o_gpu, q, k, v, dtype, scale, causal, rows=None):
+    """One head against the oracle (all rows, or the listed query rows)."""
+    qd, kd, vd = (decode(a, dtype) for a in (q, k, v))
+    if rows is None:
+        ref = oracle.attention_fwd(q, k, v, dtype, scale, causal=causal)
+        got = o_gpu
+    else:
+        ref = np.concatenate([oracle.attention_fwd(q[i:i + 1], k, v, dtype, scale, causal=causal, causal_offset=i)
+                              for i in rows])
+        got = o_gpu[rows]
+    tol = row_tolerance(qd, kd, vd, dtype, scale, causal, rows) + U[dtype] * np.abs(ref)
+    err = np.abs(got - ref)
+    assert np.isfinite(got).all()
+    bad = np.argwhere(err > tol)
+    assert bad.size == 0, f"{len(bad)} elements off; first {bad[0]}: got {got[tuple(bad[0])]}, " \
+                          f"ref {ref[tuple(bad[0])]}, tol {tol[bad[0][0], 0]}"
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("b,h,n", [(1, 1, 128), (1, 1, 1), (1, 2, 200), (2, 1, 384), (1, 1, 1000), (1, 1, 129)])
+def test_parity_small(dtype, causal, b, h, n):
+    w = W.AttentionWorkload("t", b, h, n, D, dtype, seed=100 + n, causal=causal)
+    q, k, v = W.make_qkv(w)
+    scale = 1.0 / math.sqrt(D)
+    o = run(q, k, v, dtype, causal, scale)
+    for bi in range(b):
+        for hi in range(h):
+            check_head(o[bi, hi], q[bi, hi], k[bi, hi], v[bi, hi], dtype, scale, causal)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("scale", [0.02, 0.5])
+def test_parity_scales(dtype, scale):
+    # a small scale flattens the weights over all keys; a large one makes them
+    # peaked (exercises the moving shift and the O rescale)
+    w = W.AttentionWorkload("t", 1, 2, 640, D, dtype, seed=7, causal=True)
+    q, k, v = W.make_qkv(w)
+    o = run(q, k, v, dtype, True, scale)
+    for hi in range(2):
+        check_head(o[0, hi], q[0, hi], k[0, hi], v[0, hi], dtype, scale, True)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_rising_scores_rescale(dtype):
+    # keys whose scores rise along the sequence: the running max moves by more
+    # than the 2^8 slack from one key tile to the next, so O is rescaled often
+    n = 768
+    w = W.AttentionWorkload("t", 1, 1, n, D, dtype, seed=9, causal=True)
+    q, k, v = W.make_qkv(w)
+    qd = np.ones((1, 1, n, D))
+    kd = np.repeat(np.linspace(-1.0, 1.0, n)[:, None], D, axis=1)[None, None]
+    q, k = W.quantise(qd, dtype), W.quantise(kd, dtype)
+    o = run(q, k, v, dtype, True, 0.5)
+    check_head(o[0, 0], q[0, 0], k[0, 0], v[0, 0], dtype, 0.5, True)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_ones_value_gives_ones(dtype, causal):
+    # V = 1 everywhere: every output is sum_j p~_j / sum_j p_j = 1 within u
+    w = W.AttentionWorkload("t", 1, 3, 333, D, dtype, seed=11, causal=causal)
+    q, k, _ = W.make_qkv(w)
+    v = W.quantise(np.ones(q.shape), dtype)
+    o = run(q, k, v, dtype, causal)
+    assert np.abs(o - 1.0).max() <= U[dtype] + 2.0 ** -20
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_causal_first_query_is_first_value(dtype):
+    # under the causal mask query 0 sees key 0 only: its weight is exactly 1
+    w = W.AttentionWorkload("t", 2, 2, 300, D, dtype, seed=13, causal=True)
+    q, k, v = W.make_qkv(w)
+    o = run(q, k, v, dtype, True)
+    assert (o[:, :, 0, :] == decode(v[:, :, 0, :], dtype)).all()
+
+
+def test_equal_keys_average_the_values():
+    # all keys equal: every kept key has the same weight, so query i gets the
+    # mean of V[0..i] (causal) -- a closed form independent of the oracle
+    n, dtype = 300, "f16"
+    w = W.AttentionWorkload("t", 1, 1, n, D, dtype, seed=17, causal=True)
+    q, _, v = W.make_qkv(w)
+    k = W.quantise(np.full((1, 1, n, D), 0.25), dtype)
+    o = run(q, k, v, dtype, True)
+    vd = decode(v[0, 0], dtype)
+    mean = np.cumsum(vd, axis=0) / np.arange(1, n + 1)[:, None]
+    assert np.abs(o[0, 0] - mean).max() <= U[dtype] * (np.abs(vd).max() + np.abs(mean).max()) + 1e-5
+
+
+@pytest.mark.parametrize("key", ["a4k"])
+def test_bench_size_sampled_rows(key):
+    # the benchmarked configuration, inputs from a seeded device generator;
+    # sampled query rows (tile edges, first and last) of sampled heads are
+    # checked against the oracle one by one
+    w = W.ATTENTION_CONFIGS[key]
+    g = torch.Generator(device="cuda").manual_seed(w.seed)
+    shape = (w.batch, w.heads, w.n_ctx, w.head_dim)
+    q, k, v = (torch.randn(shape, generator=g, device="cuda").to(TORCH[w.dtype]) for _ in range(3))
+    o = B.attention_fwd(q, k, v, causal=w.causal)
+    torch.cuda.synchronize()
+    assert B.check_device_error() == B.OK
+    scale = 1.0 / math.sqrt(w.head_dim)
+    rng = np.random.default_rng(5)
+    rows = sorted({0, 1, 127, 128, 129, 1000, 2047, 2048, w.n_ctx - 129, w.n_ctx - 1,
+                   *rng.integers(0, w.n_ctx, 6).tolist()})
+    for bi, hi in [(0, 0), (w.batch - 1, w.heads - 1), (1, 17), (2, 5)]:
+        bits = [t[bi, hi].view(torch.int16).cpu().numpy().view(np.uint16) for t in (q, k, v)]
+        got = from_dev(o[bi, hi], w.dtype)
+        check_head(got, bits[0], bits[1], bits[2], w.dtype, scale, w.causal, rows=rows)
+
+
+def test_repeatable():
+    # the same inputs twice give the same bits (no dependence on timing)
+    w = W.AttentionWorkload("t", 2, 2, 500, D, "bf16", seed=19, causal=True)
+    q, k, v = W.make_qkv(w)
+    a = run(q, k, v, "bf16", True)
+    b = run(q, k, v, "bf16", True)
+    assert (a == b).all()
+
+
+def test_bad_arguments_launch_nothing():
+    q = torch.zeros(1, 1, 128, D, dtype=torch.float16, device="cuda")
+    o = torch.zeros_like(q)
+    p = q.data_ptr()
+    s = torch.cuda.current_stream().cuda_stream
+    assert B.attention_fwd_ptr(p, p, p, p, 1, 1, 128, D, 1, True, 0.1, s) == B.ERR_OVERLAP
+    assert B.attention_fwd_ptr(p, p, p, o.data_ptr() + 2, 1, 1, 128, D, 1, True, 0.1, s) == B.ERR_ALIGN
+    assert B.attention_fwd_ptr(p, p, p, o.data_ptr(), 1, 1, 128, 64, 1, True, 0.1, s) == B.ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert (o == 0).all()
