@@ -33,6 +33,7 @@ if ROOT not in sys.path:
 
 METRIC = "achieved HBM GB/s and % of GB300 roofline (2×bytes/peak) per shape; µs/call"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED = 1900.0, 1700.0
 
 
 # ---------------------------------------------------------------------------
@@ -76,9 +77,11 @@ def measured_peaks() -> dict:
     try:
         with open(path) as f:
             p = json.load(f)
-        return {"hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p["bf16_tflops_sustained"]), "source": "measured"}
     except (OSError, KeyError, ValueError):
-        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": FALLBACK_BF16_TFLOPS_SUSTAINED, "source": "fallback"}
 
 
 class ClockSampler:
@@ -235,6 +238,17 @@ def run_ours(args) -> dict | None:
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     peaks = measured_peaks()
 
+    if args.attention:  # the attention forward alone (ncu captures, quick looks)
+        if rank != 0:
+            return None
+        if args.only_kernel:
+            w = W.ATTENTION_CONFIGS[args.attention]
+            ms, _ = attention_time(w, dev, args.steps, args.warmup)
+            print(json.dumps({"workload": w.name, "steps": args.steps, "ms_mean": ms,
+                              "tflops": w.flops() / (ms / 1e3) / 1e12}))
+            return None
+        return {"attention": attention_block(peaks, dev, keys=(args.attention,))}
+
     if args.workload.startswith("w"):  # a width of the fp32 sweep, seeded on the device
         w = W.sweep_workload(int(args.workload[1:]))
         x = None
@@ -336,6 +350,8 @@ def run_ours(args) -> dict | None:
         result["cpu_baseline"] = cpu_baseline(x, w)
     if rank == 0 and world == 1 and not args.no_per_shape:
         result["per_shape"] = per_shape(args, peaks, l2, dev)
+    if rank == 0 and world == 1 and not args.no_attention:
+        result["attention"] = attention_block(peaks, dev)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -491,6 +507,100 @@ def per_shape(args, peaks, l2, dev) -> dict:
 
 
 # ---------------------------------------------------------------------------
+# the fused attention forward (softmax_attention_fwd)
+# ---------------------------------------------------------------------------
+
+def attention_inputs(w, dev):
+    """Q, K, V ~ N(0, 1) from a seeded device generator, rounded to the dtype."""
+    import torch
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    shape = (w.batch, w.heads, w.n_ctx, w.head_dim)
+    tdt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+    return tuple(torch.randn(shape, generator=g, device=dev).to(tdt) for _ in range(3))
+
+
+def attention_time(w, dev, steps: int, warmup: int) -> tuple[float, int]:
+    """Mean ms per softmax_attention_fwd call over `steps` eager launches
+    bracketed by CUDA events on the launching stream (Q, K and V together are
+    larger than L2 for the benchmarked sizes)."""
+    import torch
+
+    from memory_bound_row_softmax_gb300 import binding as B
+    q, k, v = attention_inputs(w, dev)
+    o = torch.empty_like(q)
+    lib = B.lib()
+    code = B.DTYPE_CODES[w.dtype]
+    scale = 1.0 / w.head_dim ** 0.5
+
+    def launch():
+        st = lib.softmax_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), w.batch, w.heads,
+                                       w.n_ctx, w.head_dim, code, 1 if w.causal else 0, scale,
+                                       torch.cuda.current_stream().cuda_stream)
+        if st != 0:
+            raise B.SoftmaxError(st, "softmax_attention_fwd")
+
+    for _ in range(warmup):
+        launch()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        launch()
+    t1.record()
+    torch.cuda.synchronize()
+    if B.check_device_error() != B.OK:
+        raise RuntimeError("attention kernel reported a device error")
+    nbytes = 4 * q.numel() * q.element_size()
+    del q, k, v, o
+    torch.cuda.empty_cache()
+    return t0.elapsed_time(t1) / steps, nbytes
+
+
+def attention_cpu_baseline(w, rows: int = 48) -> dict:
+    """The oracle's one-head attention (double precision, one thread) on the
+    last `rows` queries of one head of the workload (the rows with the most
+    keys under the causal mask), in matmul FLOPs per second."""
+    import oracle
+    from memory_bound_row_softmax_gb300 import workloads as W
+    q = W.qkv_heads(w.seed, "q", 0, 1, w.n_ctx, w.head_dim, w.dtype)[0]
+    k = W.qkv_heads(w.seed, "k", 0, 1, w.n_ctx, w.head_dim, w.dtype)[0]
+    v = W.qkv_heads(w.seed, "v", 0, 1, w.n_ctx, w.head_dim, w.dtype)[0]
+    r0 = w.n_ctx - rows
+    t0 = time.perf_counter()
+    oracle.attention_fwd(q[r0:], k, v, w.dtype, 1.0 / w.head_dim ** 0.5, causal=w.causal, causal_offset=r0)
+    el = time.perf_counter() - t0
+    keys = sum(min(w.n_ctx, r + 1) if w.causal else w.n_ctx for r in range(r0, w.n_ctx))
+    flops = 4.0 * keys * w.head_dim
+    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"queries {r0}..{w.n_ctx - 1} of head 0 of {w.name} ({keys} query-key pairs, "
+                      f"{el:.2f} s, double-precision C, one thread)"}
+
+
+def attention_block(peaks, dev, keys=("a4k", "a16k")) -> dict:
+    """Per workload: ms per call, TFLOP/s (4 B H N^2 D, halved when causal) and
+    the tensor roofline (the measured bf16 dense GEMM rate; fp16 runs at the
+    same nominal rate)."""
+    from memory_bound_row_softmax_gb300 import workloads as W
+    out = {"call": "softmax_attention_fwd", "workloads": {}}
+    for key in keys:
+        w = W.ATTENTION_CONFIGS[key]
+        ms, nbytes = attention_time(w, dev, steps=20 if w.n_ctx <= 4096 else 5, warmup=3)
+        tf = w.flops() / (ms / 1e3) / 1e12
+        out["workloads"][w.name] = {
+            "batch": w.batch, "heads": w.heads, "n_ctx": w.n_ctx, "head_dim": w.head_dim, "dtype": w.dtype,
+            "causal": w.causal, "ms_per_call": round(ms, 4), "tflops": round(tf, 1),
+            "flops_per_call": w.flops(), "hbm_bytes_min": nbytes,
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops_sustained"],
+                         "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops_sustained"], 4),
+                         "peak_kind": "sustained (back-to-back launches)",
+                         "frac_of_burst": round(tf / peaks["bf16_tflops"], 4), "peak_source": peaks["source"]},
+        }
+    out["cpu_baseline"] = attention_cpu_baseline(W.ATTENTION_CONFIGS[keys[0]])
+    return out
+
+
+# ---------------------------------------------------------------------------
 # reference arm: the CPU oracle, as it stands
 # ---------------------------------------------------------------------------
 
@@ -551,6 +661,9 @@ def main(argv=None):
                     help="with --only-kernel on c4: run its causal mask through softmax_fwd_masked")
     ap.add_argument("--only-kernel", action="store_true",
                     help="warm-up and timed launches only (the command profiled with ncu)")
+    ap.add_argument("--no-attention", action="store_true", help="leave out the attention forward block")
+    ap.add_argument("--attention", default="",
+                    help="a4k | a16k | a4k_small: time only the fused attention forward on that workload")
     ap.add_argument("--json-out", default="")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch in plain stream order (no programmatic dependent launch)")

@@ -313,6 +313,8 @@ class AttentionWorkload:
 ATTENTION_CONFIGS: dict[str, AttentionWorkload] = {
     "a4k": AttentionWorkload("attn_f16_b4_h32_n4096_d128_causal", 4, 32, 4096, 128, "f16", 6),
     "a16k": AttentionWorkload("attn_f16_b4_h32_n16384_d128_causal", 4, 32, 16384, 128, "f16", 7),
+    # a small case of the same kernel for detailed profiler captures
+    "a4k_small": AttentionWorkload("attn_f16_b1_h8_n4096_d128_causal", 1, 8, 4096, 128, "f16", 8),
 }
 
 QKV_STREAMS = {"q": 0, "k": 1, "v": 2}
