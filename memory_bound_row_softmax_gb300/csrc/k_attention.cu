@@ -10,20 +10,28 @@
 // the max moves, P rounded to the input type before the second product, the
 // accumulator divided by the normaliser at the end).
 //
-// One block per 128-query tile, 192 threads in three roles:
-//   warp 4, one lane  -- TMA: the Q tile once, then K and V tiles of 128 keys
-//                        into a two-stage ring (128-byte swizzled rows);
-//   warp 5, one lane  -- tcgen05.mma: S_j = Q K_j^T into one of two TMEM
-//                        buffers (the next one is computed while the softmax
-//                        works on this one), O += P_j V_j into TMEM;
-//                        warp 5 also owns the TMEM allocation;
-//   warps 0-3         -- softmax: thread t owns query row t of the tile, which
-//                        is TMEM lane t, so the row max and row sum are
-//                        thread-local: no shuffles, no shared-memory
-//                        reduction.  P_j goes to shared memory as the A
-//                        operand of the second product.  At the end the same
-//                        threads read O from TMEM, divide by the normaliser
-//                        and store their row.
+// One block per 256 queries of one head: two query tiles A and B of 128, 320
+// threads in four roles:
+//   warp 8, one lane  -- TMA: both Q tiles once, then K_0, V_0, K_1, V_1, ...
+//                        (tiles of 128 keys, 128-byte swizzled rows) into a
+//                        ring of kSlots shared-memory slots;
+//   warp 9, one lane  -- tcgen05.mma: S_t = Q_t K_j^T into tensor memory (TMEM)
+//                        and O_t += P_t V_j, with P_t read from TMEM where the
+//                        softmax wrote it over S_t; warp 9 owns the TMEM
+//                        allocation;
+//   warps 0-3 / 4-7   -- softmax of tile A / B: thread r of the group owns
+//                        query row r of its tile, which is TMEM lane r, so the
+//                        row max and row sum are thread-local (no shuffles, no
+//                        shared-memory reduction).  At the end the same threads
+//                        read O from TMEM, divide by the normaliser and store
+//                        their row.
+// The two softmax groups take turns with the tensor core: while group A turns
+// S_A into P_A, the tensor core computes P_B V and the next S_B, and the
+// other way round.  Per key tile the MMA thread issues, in this order,
+// O_A += P_A V_j, S_A = Q_A K_{j+1}^T, O_B += P_B V_j, S_B = Q_B K_{j+1}^T:
+// MMAs from one thread run in order, so S_t of the next tile overwrites P_t
+// only after the product that reads it, and by the time S_t of a tile is
+// complete the previous O_t update is too (the softmax may rescale O_t then).
 // The running max moves lazily: the shift m used for exp only changes when a
 // tile's max exceeds it by more than 2^8 (in log2 units), so O in TMEM is
 // rescaled rarely; both O and the normaliser carry the same shift, which
@@ -49,37 +57,41 @@ namespace {
 constexpr int kBlockM = 128;  // queries per tile (= TMEM lanes)
 constexpr int kBlockN = 128;  // keys per tile
 constexpr int kHeadDim = kAttnHeadDim;
-constexpr int kThreads = 192;
-constexpr int kStages = 2;
+constexpr int kTiles = 2;     // query tiles per block, one softmax warpgroup each
+constexpr int kRowsPerBlock = kTiles * kBlockM;
+constexpr int kThreads = 320;  // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kSlots = 5;  // K / V ring: load n (K_{n/2} or V_{n/2}) goes to slot n mod kSlots
 constexpr uint32_t kTileBytes = kBlockN * kHeadDim * 2;  // one 128 x 128 tile of 16-bit elements
 constexpr uint32_t kHalfBytes = kTileBytes / 2;          // its 64-column half: 128 rows of 128 bytes
 // shared memory, from a 1024-byte aligned base
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKV = kTileBytes;  // stage s: K at kOffKV + 2 s kTileBytes, V right after it
-constexpr uint32_t kOffP = kOffKV + kStages * 2 * kTileBytes;
-constexpr uint32_t kOffBar = kOffP + kTileBytes;
+constexpr uint32_t kOffQ = 0;                        // Q tile t at kOffQ + t kTileBytes
+constexpr uint32_t kOffRing = kTiles * kTileBytes;   // slot i at kOffRing + i kTileBytes
+constexpr uint32_t kOffBar = kOffRing + kSlots * kTileBytes;
 enum : int {
     kBarQ = 0,
-    kBarK = 1,        // + stage
-    kBarV = 3,        // + stage
-    kBarKVEmpty = 5,  // + stage
-    kBarS = 7,        // + S buffer
-    kBarP = 9,
-    kBarO = 10,
-    kBarDrain = 11,
-    kNumBars = 12
+    kBarFull = 1,                 // + slot: the load landed
+    kBarEmpty = 1 + kSlots,       // + slot: its last MMA completed
+    kBarS = 1 + 2 * kSlots,       // + tile: S_t is in TMEM
+    kBarP = kBarS + kTiles,       // + tile: P_t is in TMEM (128 arrivals)
+    kBarO = kBarP + kTiles,       // + tile: O_t is final
+    kBarDrain = kBarO + kTiles,
+    kNumBars = kBarDrain + 1
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
 constexpr size_t kSmemBytes = kOffAbort + 4 + 1024;  // + slack for aligning the base
-// tensor memory columns: S buffers at 0 and 128, O at 256
+// tensor memory: tile t has S_t (P_t over its first 64 columns) at 128 t and
+// O_t at 256 + 128 t
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 256;
 constexpr float kShiftSlack = 8.f;  // log2 units
+
+__host__ __device__ constexpr uint32_t col_s(int t) { return 128u * (uint32_t)t; }
+__host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * (uint32_t)t; }
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
 static_assert(kBlockM == 128 && kBlockN == 128 && kHeadDim == 128, "tile shapes the descriptors assume");
+static_assert(col_o(kTiles - 1) + kHeadDim <= kTmemCols, "tensor memory columns");
 
 template <typename T> __device__ __forceinline__ uint32_t pack2(float a, float b);
 template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
@@ -125,13 +137,15 @@ __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, volat
 
 }  // namespace
 
-// Block t of the grid takes head bh = t / m_tiles and, within the head, the
-// query tiles from the last (the most keys under a causal mask) to the first,
-// so that the blocks resident at one time share a few heads' K and V in L2.
+
+// Block b of the grid takes head bh = b / m_blocks and, within the head, the
+// 256-query blocks from the last (the most keys under a causal mask) to the
+// first, so that the blocks resident at one time share a few heads' K and V
+// in L2.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, T *__restrict__ o, int n_ctx, int m_tiles,
+                    const __grid_constant__ CUtensorMap tv, T *__restrict__ o, int n_ctx, int m_blocks,
                     float kscale, int causal, uint32_t wait_ns) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
@@ -142,22 +156,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const auto bar = [base](int i) { return base + kOffBar + 8u * (uint32_t)i; };
 
     const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
-    const int bh = (int)(blockIdx.x / (unsigned)m_tiles);
-    const int mt = m_tiles - 1 - (int)(blockIdx.x % (unsigned)m_tiles);
-    const int m0 = mt * kBlockM;
-    const int kv_tiles = causal ? mt + 1 : (n_ctx + kBlockN - 1) / kBlockN;
+    const int bh = (int)(blockIdx.x / (unsigned)m_blocks);
+    const int mb = m_blocks - 1 - (int)(blockIdx.x % (unsigned)m_blocks);
+    const int m0 = mb * kRowsPerBlock;
+    // key tiles of tile A (queries m0 ..) and B (m0 + 128 ..): under the causal
+    // mask up to each one's diagonal tile, never past the last key
+    const int n_all = (n_ctx + kBlockN - 1) / kBlockN;
+    const int n_a = causal ? min(2 * mb + 1, n_all) : n_all;
+    const int n_b = causal ? min(2 * mb + 2, n_all) : n_all;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), i == kBarP ? kBlockM : 1);
+        for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), (i == kBarP || i == kBarP + 1) ? kBlockM : 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == kWarpTma && lane == 0) {
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
     }
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tmem_alloc(base + kOffTmemSlot, kTmemCols);
         tmem_relinquish();
     }
@@ -166,97 +184,122 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + kOffTmemSlot);
 
-    if (warp == 4) {
+    if (warp == kWarpTma) {
         // ---- TMA producer ------------------------------------------------
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar(kBarQ), kTileBytes);
-            tma_load_3d(base + kOffQ, &tq, 0, m0, bh, bar(kBarQ));
-            tma_load_3d(base + kOffQ + kHalfBytes, &tq, 64, m0, bh, bar(kBarQ));
-            int j = 0;
-            for (; j < kv_tiles; ++j) {
-                const int s = j & 1;
-                // stage s last held tile j - 2; its PV product must be done
-                if (j >= 2 && !wait_phase(bar(kBarKVEmpty + s), ((j >> 1) + 1) & 1, abort_flag, wait_ns)) break;
-                const uint32_t kdst = base + kOffKV + (uint32_t)s * 2u * kTileBytes;
-                const uint32_t vdst = kdst + kTileBytes;
-                const int y = j * kBlockN;
-                mbar_arrive_expect_tx(bar(kBarK + s), kTileBytes);
-                tma_load_3d(kdst, &tk, 0, y, bh, bar(kBarK + s));
-                tma_load_3d(kdst + kHalfBytes, &tk, 64, y, bh, bar(kBarK + s));
-                mbar_arrive_expect_tx(bar(kBarV + s), kTileBytes);
-                tma_load_3d(vdst, &tv, 0, y, bh, bar(kBarV + s));
-                tma_load_3d(vdst + kHalfBytes, &tv, 64, y, bh, bar(kBarV + s));
+            mbar_arrive_expect_tx(bar(kBarQ), kTiles * kTileBytes);
+            for (int t = 0; t < kTiles; ++t) {
+                const uint32_t dst = base + kOffQ + (uint32_t)t * kTileBytes;
+                tma_load_3d(dst, &tq, 0, m0 + t * kBlockM, bh, bar(kBarQ));
+                tma_load_3d(dst + kHalfBytes, &tq, 64, m0 + t * kBlockM, bh, bar(kBarQ));
+            }
+            const int loads = 2 * n_b;
+            int n = 0;
+            for (; n < loads; ++n) {
+                const int slot = n % kSlots;
+                // the slot last held load n - kSlots; its MMAs must be done
+                if (n >= kSlots && !wait_phase(bar(kBarEmpty + slot), ((n / kSlots) - 1) & 1, abort_flag, wait_ns))
+                    break;
+                const uint32_t dst = base + kOffRing + (uint32_t)slot * kTileBytes;
+                const CUtensorMap *map = (n & 1) ? &tv : &tk;
+                const int y = (n >> 1) * kBlockN;
+                mbar_arrive_expect_tx(bar(kBarFull + slot), kTileBytes);
+                tma_load_3d(dst, map, 0, y, bh, bar(kBarFull + slot));
+                tma_load_3d(dst + kHalfBytes, map, 64, y, bh, bar(kBarFull + slot));
             }
             // every load issued lands before the block may exit
             drain_phase(bar(kBarQ), 0, abort_flag, wait_ns);
-            for (int jj = (j >= 2 ? j - 2 : 0); jj < j; ++jj) {
-                drain_phase(bar(kBarK + (jj & 1)), (jj >> 1) & 1, abort_flag, wait_ns);
-                drain_phase(bar(kBarV + (jj & 1)), (jj >> 1) & 1, abort_flag, wait_ns);
-            }
+            for (int nn = (n > kSlots ? n - kSlots : 0); nn < n; ++nn)
+                drain_phase(bar(kBarFull + nn % kSlots), (nn / kSlots) & 1, abort_flag, wait_ns);
         }
-    } else if (warp == 5) {
+    } else if (warp == kWarpMma) {
         // ---- MMA issuer ----------------------------------------------------
         if (lane == 0) {
-            constexpr uint32_t id_s = f16_idesc(kBf16, false, kBlockM, kBlockN);   // S = Q K^T
-            constexpr uint32_t id_o = f16_idesc(kBf16, true, kBlockM, kHeadDim);   // O += P V
-            // S_j = Q K_j^T: K = head dim, 8 steps of 16; both operands K-major
-            const auto issue_s = [&](int j) -> bool {
-                const int s = j & 1;
-                if (!wait_phase(bar(kBarK + s), (j >> 1) & 1, abort_flag, wait_ns)) return false;
-                tc_fence_after();
-                const uint32_t kb = base + kOffKV + (uint32_t)s * 2u * kTileBytes;
-                const uint32_t d = tmem + kColS + (uint32_t)s * kBlockN;
+            constexpr uint32_t id_s = f16_idesc(kBf16, false, kBlockM, kBlockN);  // S = Q K^T
+            constexpr uint32_t id_o = f16_idesc(kBf16, true, kBlockM, kHeadDim);  // O += P V
+            const auto landed = [&](int n) {
+                return wait_phase(bar(kBarFull + n % kSlots), (n / kSlots) & 1, abort_flag, wait_ns);
+            };
+            // S_t = Q_t K_j^T: K = head dim, 8 steps of 16; both operands
+            // K-major in shared memory
+            const auto issue_s = [&](int t, int j) {
+                const uint32_t kb = base + kOffRing + (uint32_t)((2 * j) % kSlots) * kTileBytes;
+                const uint32_t qb = base + kOffQ + (uint32_t)t * kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 2) * kHalfBytes + (uint32_t)(kk & 3) * 32u;
-                    mma_ss(d, sw128_desc(base + kOffQ + off, 16, 1024), sw128_desc(kb + off, 16, 1024), id_s,
+                    mma_ss(tmem + col_s(t), sw128_desc(qb + off, 16, 1024), sw128_desc(kb + off, 16, 1024), id_s,
                            kk > 0);
                 }
-                mma_commit(bar(kBarS + s));
-                return true;
+                mma_commit(bar(kBarS + t));
             };
-            bool ok = wait_phase(bar(kBarQ), 0, abort_flag, wait_ns);
-            if (ok) ok = issue_s(0);
-            for (int j = 0; ok && j < kv_tiles; ++j) {
-                if (j + 1 < kv_tiles && !(ok = issue_s(j + 1))) break;
-                const int s = j & 1;
-                if (!(ok = wait_phase(bar(kBarV + s), (j >> 1) & 1, abort_flag, wait_ns))) break;
-                if (!(ok = wait_phase(bar(kBarP), j & 1, abort_flag, wait_ns))) break;
-                tc_fence_after();
-                // O += P_j V_j: K = keys, 8 steps of 16; P K-major, V MN-major
-                // (head dim contiguous; its two 64-column halves kHalfBytes apart)
-                const uint32_t vb = base + kOffKV + (uint32_t)s * 2u * kTileBytes + kTileBytes;
+            // O_t += P_t V_j: K = keys, 8 steps of 16; P_t in TMEM (16 keys =
+            // 8 columns per step), V_j MN-major in shared memory (head dim
+            // contiguous, its two 64-column halves kHalfBytes apart)
+            const auto issue_pv = [&](int t, int j) {
+                const uint32_t vb = base + kOffRing + (uint32_t)((2 * j + 1) % kSlots) * kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    const uint32_t aoff = (uint32_t)(kk >> 2) * kHalfBytes + (uint32_t)(kk & 3) * 32u;
-                    mma_ss(tmem + kColO, sw128_desc(base + kOffP + aoff, 16, 1024),
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    mma_ts(tmem + col_o(t), tmem + col_s(t) + (uint32_t)kk * 8u,
                            sw128_desc(vb + (uint32_t)kk * 16u * 128u, kHalfBytes, 1024), id_o, (j > 0 || kk > 0));
+            };
+            bool ok = wait_phase(bar(kBarQ), 0, abort_flag, wait_ns) && landed(0);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                issue_s(1, 0);
+                mma_commit(bar(kBarEmpty + 0));  // K_0 done
+            }
+            for (int j = 0; ok && j < n_b; ++j) {
+                if (!(ok = landed(2 * j + 1))) break;  // V_j
+                const bool more_a = j + 1 < n_a, more_b = j + 1 < n_b;
+                if (j < n_a) {
+                    if (!(ok = wait_phase(bar(kBarP + 0), j & 1, abort_flag, wait_ns))) break;
+                    tc_fence_after();
+                    issue_pv(0, j);
+                    if (more_a) {
+                        if (!(ok = landed(2 * j + 2))) break;  // K_{j+1}
+                        tc_fence_after();
+                        issue_s(0, j + 1);
+                    } else {
+                        mma_commit(bar(kBarO + 0));
+                    }
                 }
-                mma_commit(bar(kBarKVEmpty + s));
-                mma_commit(bar(kBarO));
+                if (!(ok = wait_phase(bar(kBarP + 1), j & 1, abort_flag, wait_ns))) break;
+                tc_fence_after();
+                issue_pv(1, j);
+                mma_commit(bar(kBarEmpty + (2 * j + 1) % kSlots));  // V_j done
+                if (more_b) {
+                    if (!more_a && !(ok = landed(2 * j + 2))) break;  // K_{j+1}, unless waited above
+                    tc_fence_after();
+                    issue_s(1, j + 1);
+                    mma_commit(bar(kBarEmpty + (2 * j + 2) % kSlots));  // K_{j+1} done
+                } else {
+                    mma_commit(bar(kBarO + 1));
+                }
             }
             // every MMA issued completes before TMEM is released
             mma_commit(bar(kBarDrain));
             drain_phase(bar(kBarDrain), 0, abort_flag, wait_ns);
         }
     } else {
-        // ---- softmax: thread r owns query row r of the tile ---------------
-        const int r = (int)threadIdx.x;
-        const int q = m0 + r;
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+        // ---- softmax: thread r of group t owns query row r of tile t -------
+        const int t = warp >> 2;
+        const int r = (int)(threadIdx.x & 127);
+        const int q = m0 + t * kBlockM + r;
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const int n_t = t ? n_b : n_a;
         const int q_lim = causal ? min(q + 1, n_ctx) : n_ctx;  // keys [0, q_lim) are kept
-        const uint32_t prow = base + kOffP + (uint32_t)r * 128u;
         float m_run = -INFINITY;  // the shift, in log2 units
         float l_run = 0.f;
         bool ok = true;
-        for (int j = 0; j < kv_tiles; ++j) {
-            const int b = j & 1;
-            ok = __all_sync(0xffffffffu, wait_phase(bar(kBarS + b), (j >> 1) & 1, abort_flag, wait_ns));
+        for (int j = 0; j < n_t; ++j) {
+            ok = __all_sync(0xffffffffu, wait_phase(bar(kBarS + t), j & 1, abort_flag, wait_ns));
             if (!ok) break;
             tc_fence_after();
             float s[kBlockN];
 #pragma unroll
-            for (int c = 0; c < kBlockN / 32; ++c) tmem_ld32(lane_addr + kColS + (uint32_t)b * kBlockN + c * 32, s + c * 32);
+            for (int c = 0; c < kBlockN / 32; ++c) tmem_ld32(lane_addr + col_s(t) + c * 32, s + c * 32);
             tmem_wait_ld();
             const int lim = q_lim - j * kBlockN;  // kept columns of this tile: [0, lim)
             if (lim < kBlockN) {
@@ -280,51 +323,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_run = m_tile;
                 moved = j > 0;
             }
-            // p = 2^(s kscale - m_run), rounded to T in pairs
-            uint32_t pk[kBlockN / 2];
+            // p = 2^(s kscale - m_run), rounded to T in pairs and written over
+            // S_t's first 64 columns, in quarters of 32 keys (this thread's S
+            // values are all in registers already)
             float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < kBlockN / 2; ++c) {
-                const float p0 = ex2(fmaf(s[2 * c], kscale, -m_run));
-                const float p1 = ex2(fmaf(s[2 * c + 1], kscale, -m_run));
-                sum[c & 3] += p0 + p1;
-                pk[c] = pack2<T>(p0, p1);
+            for (int h = 0; h < 4; ++h) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float p0 = ex2(fmaf(s[32 * h + 2 * c], kscale, -m_run));
+                    const float p1 = ex2(fmaf(s[32 * h + 2 * c + 1], kscale, -m_run));
+                    sum[c & 3] += p0 + p1;
+                    pk[c] = pack2<T>(p0, p1);
+                }
+                tmem_st16(lane_addr + col_s(t) + 16 * h, pk);
             }
             l_run += (sum[0] + sum[1]) + (sum[2] + sum[3]);
-            // PV_{j-1} must be done with the P buffer and with O
-            if (j > 0) {
-                ok = __all_sync(0xffffffffu, wait_phase(bar(kBarO), (j - 1) & 1, abort_flag, wait_ns));
-                if (!ok) break;
-                tc_fence_after();
-            }
             if (__any_sync(0xffffffffu, moved)) {
-                // the whole warp takes part (the TMEM accesses are warp-wide);
-                // rows whose shift did not move scale by 1
+                // O_t += P_t V_{j-1} has completed (S_t of this tile was issued
+                // after it).  The whole warp takes part (TMEM accesses are
+                // warp-wide); rows whose shift did not move scale by 1.
 #pragma unroll
                 for (int c = 0; c < kHeadDim / 32; ++c) {
                     float ov[32];
-                    tmem_ld32(lane_addr + kColO + c * 32, ov);
+                    tmem_ld32(lane_addr + col_o(t) + c * 32, ov);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-                    tmem_st32(lane_addr + kColO + c * 32, ov);
+                    tmem_st32(lane_addr + col_o(t) + c * 32, ov);
                 }
-                tmem_wait_st();
             }
-            // row r of P: 16 chunks of 8 keys; chunk c of a 64-key half sits
-            // at position c ^ (r mod 8) of the row's 128 bytes
-#pragma unroll
-            for (int ch = 0; ch < kBlockN / 8; ++ch) {
-                const uint32_t addr = prow + (uint32_t)(ch >> 3) * kHalfBytes + (uint32_t)(((ch & 7) ^ (r & 7)) * 16);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * ch]),
-                             "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
-                             : "memory");
-            }
-            fence_proxy_async_smem();  // visible to the tensor core's reads
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(kBarP));
+            mbar_arrive(bar(kBarP + t));
         }
-        if (ok) ok = __all_sync(0xffffffffu, wait_phase(bar(kBarO), (kv_tiles - 1) & 1, abort_flag, wait_ns));
+        if (ok) ok = __all_sync(0xffffffffu, wait_phase(bar(kBarO + t), 0, abort_flag, wait_ns));
         if (ok) {
             tc_fence_after();
             const float inv = 1.f / l_run;
@@ -332,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < kHeadDim / 32; ++c) {
                 float ov[32];
-                tmem_ld32(lane_addr + kColO + c * 32, ov);
+                tmem_ld32(lane_addr + col_o(t) + c * 32, ov);
                 tmem_wait_ld();
                 if (q < n_ctx) {
 #pragma unroll
@@ -351,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -416,11 +450,11 @@ cudaError_t go(const AttnArgs &a, int64_t wait_ns) {
     if (!make_map(&mq, a.q, a.dtype, a.n_ctx, bh) || !make_map(&mk, a.k, a.dtype, a.n_ctx, bh) ||
         !make_map(&mv, a.v, a.dtype, a.n_ctx, bh))
         return cudaErrorInvalidValue;
-    const int64_t m_tiles = (a.n_ctx + kBlockM - 1) / kBlockM;
+    const int64_t m_blocks = (a.n_ctx + kRowsPerBlock - 1) / kRowsPerBlock;
     const float kscale = a.sm_scale * kLog2e;
     const uint32_t limit = (uint32_t)std::min<int64_t>(std::max<int64_t>(wait_ns, 1), 0x7fffffff);
-    k_attention_fwd<T><<<(unsigned)(bh * m_tiles), kThreads, kSmemBytes, a.stream>>>(
-        mq, mk, mv, static_cast<T *>(a.o), (int)a.n_ctx, (int)m_tiles, kscale, a.causal, limit);
+    k_attention_fwd<T><<<(unsigned)(bh * m_blocks), kThreads, kSmemBytes, a.stream>>>(
+        mq, mk, mv, static_cast<T *>(a.o), (int)a.n_ctx, (int)m_blocks, kscale, a.causal, limit);
     return cudaGetLastError();
 }
 
@@ -431,7 +465,7 @@ cudaError_t launch_attention(const AttnArgs &a, int64_t wait_ns) {
 }
 
 int64_t attention_grid(int64_t batch, int64_t heads, int64_t n_ctx) {
-    return batch * heads * ((n_ctx + kBlockM - 1) / kBlockM);
+    return batch * heads * ((n_ctx + kRowsPerBlock - 1) / kRowsPerBlock);
 }
 
 size_t attention_smem_bytes() { return kSmemBytes; }
