@@ -530,9 +530,7 @@ template <typename T, int VPT>
 struct PackedTile {
     static_assert(sizeof(T) == 2, "packed tiles hold 16-bit data");
     static constexpr int V = Elem<T>::kVec;
-    uint4 raw[VPT];
-    float shift;  // the shift stats() used
-    float lg;     // and its multiplier k
+    uint4 raw[VPT];  // the inputs; after stats(), their exponentials as fp16 pairs
 
     __device__ __forceinline__ void set(int j, const uint4 &r) { raw[j] = r; }
     __device__ __forceinline__ void load_one(int j, const RowView<T> &row, int64_t v) { raw[j] = row.load_raw(v); }
@@ -563,7 +561,13 @@ struct PackedTile {
             }
         }
     }
-    // As FloatTile::stats: only the first `live` vectors hold data.
+    // As FloatTile::stats: only the first `live` vectors hold data.  The
+    // exponentials e = 2^(x k - shift), in [0, 1], then replace the inputs in
+    // the tile, rounded to fp16 pairs (relative error 2^-11 whatever T is):
+    // a result is e * f, one multiply, instead of a second exponential.  With
+    // the output rounded once more, |error| <= 2^-11 y + half an ulp of y,
+    // inside the 16-bit tolerances (fp16 1e-3, bf16 4e-3).  After stats() the
+    // tile holds exponentials, not inputs: shift_store() needs a fresh load.
     __device__ __forceinline__ float2 stats(float k = kLog2e, int live = VPT) {
         // the max on the packed pairs (a NaN never wins, as with fmaxf)
         uint32_t mw = (uint32_t)Elem<T>::kNegInfBits * 0x10001u;
@@ -578,25 +582,25 @@ struct PackedTile {
         const float2 mp = Elem<T>::pair(mw);
         const float m = fmaxf(mp.x, mp.y);
         const float s = m * k;
-        shift = safe_shift(s);
-        lg = k;
+        const float shift = safe_shift(s);
         float l = 0.f;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
-            if (j >= live) continue;
+            if (j >= live) {
+                raw[j] = make_uint4(0u, 0u, 0u, 0u);
+                continue;
+            }
             float x[V];
             Elem<T>::unpack(raw[j], x);
             float lj = 0.f;
 #pragma unroll
-            for (int i = 0; i < V; ++i) lj += ex2(fmaf(x[i], k, -shift));
+            for (int i = 0; i < V; ++i) {
+                x[i] = ex2(fmaf(x[i], k, -shift));
+                lj += x[i];
+            }
             l += lj;
+            raw[j] = Elem<__half>::pack(x);
         }
-        // The results are formed later from the packed words again: hide the
-        // words' values from the compiler so that it recomputes the
-        // exponentials there instead of keeping 8 fp32 values per vector live.
-#pragma unroll
-        for (int j = 0; j < VPT; ++j)
-            asm volatile("" : "+r"(raw[j].x), "+r"(raw[j].y), "+r"(raw[j].z), "+r"(raw[j].w));
         return make_float2(s, l);
     }
     __device__ __forceinline__ void values_shift(int j, float sh, float f, float *y, float k = kLog2e) const {
@@ -605,7 +609,12 @@ struct PackedTile {
 #pragma unroll
         for (int i = 0; i < V; ++i) y[i] = ex2(fmaf(x[i], k, -sh)) * f;
     }
-    __device__ __forceinline__ void values(int j, float f, float *y) const { values_shift(j, shift, f, y, lg); }
+    // y = e * f from the exponentials stats() left in the tile
+    __device__ __forceinline__ void values(int j, float f, float *y) const {
+        Elem<__half>::unpack(raw[j], y);
+#pragma unroll
+        for (int i = 0; i < V; ++i) y[i] *= f;
+    }
     // y = e * f (after stats())
     template <bool WHOLE = false>
     __device__ __forceinline__ void scale_store(const RowView<T> &row, int64_t first, int64_t step, int64_t end,
