@@ -321,6 +321,7 @@ struct RowView {
     const T *in;   // row start (input)
     T *out;        // row start (output)
     int head;      // elements before the row start in its first vector
+    int tail;      // elements of the row in its last vector (V when that vector is whole)
     int64_t cols;
     int64_t nvec;
     bool vec_store;  // out has the same 16-byte phase as in
@@ -329,7 +330,16 @@ struct RowView {
         : in(in_row), out(out_row), cols(cols_), vec_store(vec_store_) {
         head = (int)((reinterpret_cast<uintptr_t>(in_row) & (kVecBytes - 1)) / sizeof(T));
         nvec = (head + cols + V - 1) / V;
+        tail = (int)(head + cols - (nvec - 1) * V);
     }
+    // The row's vectors as aligned 16-byte words: vector v is vec_in()[v].
+    // Loading a whole aligned vector that holds at least one element of the
+    // row cannot fault, also for the row's partial end vectors (an aligned
+    // 16-byte block never straddles a page); their elements outside the row
+    // must then be masked.  vec_out() is only meaningful with vec_store.
+    __device__ __forceinline__ const uint4 *vec_in() const { return reinterpret_cast<const uint4 *>(in - head); }
+    __device__ __forceinline__ uint4 *vec_out() const { return reinterpret_cast<uint4 *>(out - head); }
+
     __device__ __forceinline__ bool full(int64_t v) const {
         const int64_t p = v * V;
         return p >= head && p + V <= head + cols;
@@ -396,6 +406,18 @@ __device__ __forceinline__ int whole_fit(int64_t first, int64_t end) {
     return (int)max(min(end - first, (int64_t)0x7fffffff), (int64_t)0);
 }
 
+// The 16-bit elements i of a packed vector with lo <= i < hi, the others
+// replaced by the bit pattern ninf.
+__device__ __forceinline__ uint4 keep_range16(const uint4 &r, int lo, int hi, uint32_t ninf) {
+    uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const bool a = 2 * k >= lo && 2 * k < hi, b = 2 * k + 1 >= lo && 2 * k + 1 < hi;
+        w[k] = (a ? (w[k] & 0xffffu) : ninf) | (b ? (w[k] & 0xffff0000u) : (ninf << 16));
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // Store a tile's results: for vectors first + j*step < end, val(j, y) fills
 // the V floats of vector j, rounded once to T on the way out.
 template <typename T, int VPT, bool WHOLE, typename F>
@@ -411,6 +433,25 @@ __device__ __forceinline__ void tile_store(const RowView<T> &row, int64_t first,
                 float y[V];
                 val(j, y);
                 q[j * step] = Elem<T>::pack(y);
+            }
+        }
+    } else if constexpr (sizeof(T) == 2) {
+        // interior vectors at constant offsets from the row's aligned base;
+        // the row's two partial end vectors element by element
+        uint4 *q = row.vec_out() + first;
+        const int fit = whole_fit(first, end);
+        const bool head_edge = first == 0 && row.head != 0;
+        const int64_t last = row.tail < V ? row.nvec - 1 - first : -1;  // slot offset of a partial last vector
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            if (j * step < fit) {
+                float y[V];
+                val(j, y);
+                const bool edge = (j == 0 && head_edge) || (int64_t)j * step == last;
+                if (row.vec_store && !edge)
+                    q[j * step] = Elem<T>::pack(y);
+                else
+                    row.store(first + j * step, y);
             }
         }
     } else {
@@ -430,9 +471,8 @@ __device__ __forceinline__ void tile_store(const RowView<T> &row, int64_t first,
 //   FloatTile   the elements widened to fp32 (fp32 data: no extra registers);
 //               stats() overwrites them with e = 2^(x log2 e - s_t).
 //   PackedTile  the raw 16-bit storage (half the registers of FloatTile for
-//               fp16/bf16); stats() only accumulates, and the exponentials are
-//               computed again, with the same shift, when the results are
-//               formed -- the same bits, two exps per element instead of one.
+//               fp16/bf16); stats() overwrites it with the exponentials
+//               rounded to fp16 pairs.
 // Interface: set(j, raw) / set_empty(j) / load_one(j, row, v) /
 // load<WHOLE>(row, first, step, end);
 // stats(k = log2 e) -> (s_t, l_t); values(j, f, y): y = e * f for vector j;
@@ -551,13 +591,25 @@ struct PackedTile {
                     set_empty(j);
             }
         } else {
+            // every vector as an aligned 16-byte load at a constant offset
+            // (RowView::vec_in), then the elements of the row's partial end
+            // vectors that lie outside the row set to -inf
+            const uint4 *p = row.vec_in() + first;
+            const int fit = whole_fit(first, end);
+            const uint32_t ninf = Elem<T>::kNegInfBits;
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
-                const int64_t v = first + j * step;
-                if (v < end)
-                    raw[j] = row.load_raw(v);
+                if (j * step < fit)
+                    raw[j] = p[j * step];
                 else
                     set_empty(j);
+            }
+            if (first == 0 && row.head != 0 && fit > 0) raw[0] = keep_range16(raw[0], row.head, V, ninf);
+            if (row.tail < V) {
+                const int64_t last = row.nvec - 1 - first;
+#pragma unroll
+                for (int j = 0; j < VPT; ++j)
+                    if ((int64_t)j * step == last && j * step < fit) raw[j] = keep_range16(raw[j], 0, row.tail, ninf);
             }
         }
     }
