@@ -19,7 +19,10 @@
  *     result goes to out + r * row_stride + c (strides in ELEMENTS, one stride
  *     for both buffers, row_stride >= cols);
  *   - in and out hold the same dtype: IEEE binary32, binary16 or bfloat16;
- *   - columns cols .. row_stride-1 of each row are neither read nor written;
+ *   - columns cols .. row_stride-1 of each row are never written and never
+ *     affect the result (they may hold anything; the aligned 16-byte vectors
+ *     that hold a row's first and last element are loaded whole and the
+ *     elements outside the row discarded);
  *   - arithmetic is fp32 (one exp per element); the result is rounded once
  *     to the output dtype, round-to-nearest-even.
  *
@@ -121,8 +124,10 @@ int softmax_fwd(const void *in, void *out, int64_t rows, int64_t cols, int64_t r
  * == 0: q = r) and keeps the columns c <= q + causal_offset:
  *     y[r,c] = exp(s_c - m) / sum over kept k of exp(s_k - m),
  *     s_c = scale * x[r,c],  m = the max of the kept s,
- * and y[r,c] = 0 for the masked columns.  Masked entries of `in` are never
- * read (they may hold anything); every column of `out` is written.  A row
+ * and y[r,c] = 0 for the masked columns.  Masked entries of `in` never
+ * affect the result (they may hold anything; only the 16-byte vector holding
+ * a row's last kept entry is loaded past it, and discarded); every column of
+ * `out` is written.  A row
  * that keeps no column, or has a NaN or +inf among its kept entries, comes
  * out all NaN.
  *   scale          finite and > 0 (else SOFTMAX_ERR_ARG)
