@@ -20,9 +20,9 @@
  *     for both buffers, row_stride >= cols);
  *   - in and out hold the same dtype: IEEE binary32, binary16 or bfloat16;
  *   - columns cols .. row_stride-1 of each row are never written and never
- *     affect the result (they may hold anything; the aligned 16-byte vectors
- *     that hold a row's first and last element are loaded whole and the
- *     elements outside the row discarded);
+ *     affect the result (they may hold anything; for 16-bit types the
+ *     aligned 16-byte vectors that hold a row's first and last element are
+ *     loaded whole and the elements outside the row discarded);
  *   - arithmetic is fp32 (one exp per element); the result is rounded once
  *     to the output dtype, round-to-nearest-even.
  *
