@@ -25,6 +25,10 @@ struct AttnArgs {
 };
 
 cudaError_t launch_attention(const AttnArgs &a, int64_t wait_ns);
+// heads per block-order group: as many as keep the group's K and V within
+// kAttnGroupBytes (a share of the 126 MB L2), at least 1, at most all
+constexpr int64_t kAttnGroupBytes = 48ll << 20;
+int attention_head_group(int64_t heads_total, int64_t n_ctx);
 int64_t attention_grid(int64_t batch, int64_t heads, int64_t n_ctx);
 size_t attention_smem_bytes();
 // the attention kernel's device error word (kErrWaitTimeout when a bounded

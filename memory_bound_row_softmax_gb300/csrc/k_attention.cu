@@ -138,15 +138,18 @@ __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, volat
 }  // namespace
 
 
-// Block b of the grid takes head bh = b / m_blocks and, within the head, the
-// 256-query blocks from the last (the most keys under a causal mask) to the
-// first, so that the blocks resident at one time share a few heads' K and V
-// in L2.
+// Block order: the heads go in groups of `group` heads (sized by the host so
+// that a group's K and V fit in L2 with room to spare); within a group the
+// 256-query blocks come heaviest first -- every head's last block (the most
+// keys under a causal mask), then every head's second-to-last, and so on --
+// so that the blocks resident at one time share the group's K and V in L2
+// and the light blocks of one group fill the SMs while the next group's heavy
+// ones start (longest-first list scheduling within the group).
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, T *__restrict__ o, int n_ctx, int m_blocks,
-                    float kscale, int causal, uint32_t wait_ns) {
+                    int heads_total, int group, float kscale, int causal, uint32_t wait_ns) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -156,8 +159,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const auto bar = [base](int i) { return base + kOffBar + 8u * (uint32_t)i; };
 
     const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
-    const int bh = (int)(blockIdx.x / (unsigned)m_blocks);
-    const int mb = m_blocks - 1 - (int)(blockIdx.x % (unsigned)m_blocks);
+    const int per_group = group * m_blocks;
+    const int grp = (int)(blockIdx.x / (unsigned)per_group);
+    const int within = (int)blockIdx.x - grp * per_group;
+    const int g0 = grp * group;
+    const int heads_here = min(group, heads_total - g0);
+    const int bh = g0 + within % heads_here;
+    const int mb = m_blocks - 1 - within / heads_here;
     const int m0 = mb * kRowsPerBlock;
     // key tiles of tile A (queries m0 ..) and B (m0 + 128 ..): under the causal
     // mask up to each one's diagonal tile, never past the last key
@@ -451,10 +459,12 @@ cudaError_t go(const AttnArgs &a, int64_t wait_ns) {
         !make_map(&mv, a.v, a.dtype, a.n_ctx, bh))
         return cudaErrorInvalidValue;
     const int64_t m_blocks = (a.n_ctx + kRowsPerBlock - 1) / kRowsPerBlock;
+    const int group = attention_head_group(bh, a.n_ctx);
     const float kscale = a.sm_scale * kLog2e;
     const uint32_t limit = (uint32_t)std::min<int64_t>(std::max<int64_t>(wait_ns, 1), 0x7fffffff);
     k_attention_fwd<T><<<(unsigned)(bh * m_blocks), kThreads, kSmemBytes, a.stream>>>(
-        mq, mk, mv, static_cast<T *>(a.o), (int)a.n_ctx, (int)m_blocks, kscale, a.causal, limit);
+        mq, mk, mv, static_cast<T *>(a.o), (int)a.n_ctx, (int)m_blocks, (int)bh, group, kscale, a.causal,
+        limit);
     return cudaGetLastError();
 }
 
@@ -462,6 +472,12 @@ cudaError_t go(const AttnArgs &a, int64_t wait_ns) {
 
 cudaError_t launch_attention(const AttnArgs &a, int64_t wait_ns) {
     return a.dtype == kAttnBf16 ? go<__nv_bfloat16>(a, wait_ns) : go<__half>(a, wait_ns);
+}
+
+int attention_head_group(int64_t heads_total, int64_t n_ctx) {
+    const int64_t kv_bytes = n_ctx * kHeadDim * 2 * 2;  // one head's K and V
+    const int64_t g = kAttnGroupBytes / std::max<int64_t>(kv_bytes, 1);
+    return (int)std::max<int64_t>(1, std::min<int64_t>(g, heads_total));
 }
 
 int64_t attention_grid(int64_t batch, int64_t heads, int64_t n_ctx) {
