@@ -175,12 +175,10 @@ def test_equal_keys_average_the_values():
     assert np.abs(o[0, 0] - mean).max() <= U[dtype] * (np.abs(vd).max() + np.abs(mean).max()) + 1e-5
 
 
-@pytest.mark.parametrize("key", ["a4k"])
-def test_bench_size_sampled_rows(key):
-    # the benchmarked configuration, inputs from a seeded device generator;
-    # sampled query rows (tile edges, first and last) of sampled heads are
-    # checked against the oracle one by one
-    w = W.ATTENTION_CONFIGS[key]
+def sampled_check(w, heads):
+    """Inputs from a seeded device generator; sampled query rows (tile edges,
+    first and last, a few random ones) of the listed (batch, head) pairs are
+    checked against the oracle one by one."""
     g = torch.Generator(device="cuda").manual_seed(w.seed)
     shape = (w.batch, w.heads, w.n_ctx, w.head_dim)
     q, k, v = (torch.randn(shape, generator=g, device="cuda").to(TORCH[w.dtype]) for _ in range(3))
@@ -189,12 +187,28 @@ def test_bench_size_sampled_rows(key):
     assert B.check_device_error() == B.OK
     scale = 1.0 / math.sqrt(w.head_dim)
     rng = np.random.default_rng(5)
-    rows = sorted({0, 1, 127, 128, 129, 1000, 2047, 2048, w.n_ctx - 129, w.n_ctx - 1,
+    rows = sorted({0, 1, 127, 128, 129, 255, 256, 1000, 2047, 2048, w.n_ctx - 129, w.n_ctx - 1,
                    *rng.integers(0, w.n_ctx, 6).tolist()})
-    for bi, hi in [(0, 0), (w.batch - 1, w.heads - 1), (1, 17), (2, 5)]:
+    for bi, hi in heads:
         bits = [t[bi, hi].view(torch.int16).cpu().numpy().view(np.uint16) for t in (q, k, v)]
         got = from_dev(o[bi, hi], w.dtype)
         check_head(got, bits[0], bits[1], bits[2], w.dtype, scale, w.causal, rows=rows)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_bench_size_sampled_rows(dtype):
+    # the benchmarked configuration (B4 H32 N4096, causal), fp16 and bf16
+    from dataclasses import replace
+    w = replace(W.ATTENTION_CONFIGS["a4k"], dtype=dtype)
+    sampled_check(w, [(0, 0), (w.batch - 1, w.heads - 1), (1, 17), (2, 5)])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_long_context_partial_head_group(causal):
+    # N = 16384: the block order takes heads in groups of 6, so 7 heads make a
+    # full group and a group of one; every head is checked on sampled rows
+    w = W.AttentionWorkload("long", 1, 7, 16384, D, "f16", seed=23, causal=causal)
+    sampled_check(w, [(0, h) for h in range(7)])
 
 
 def test_repeatable():
