@@ -1030,7 +1030,10 @@ int softmax_attention_fwd(const void *q, const void *k, const void *v, void *o, 
         return SOFTMAX_ERR_SHAPE;
     const auto overlaps = [bytes](uint64_t a, uint64_t b) { return a < b + bytes && b < a + bytes; };
     if (overlaps(oa, qa) || overlaps(oa, ka) || overlaps(oa, va)) return SOFTMAX_ERR_OVERLAP;
-    attn::AttnArgs a{q, k, v, o, batch, heads, n_ctx, dtype, causal, sm_scale, stream};
+    int sms = 0;
+    const int st = device_sms(&sms);
+    if (st != SOFTMAX_OK) return st;
+    attn::AttnArgs a{q, k, v, o, batch, heads, n_ctx, dtype, causal, sm_scale, stream, sms};
     const cudaError_t e = attn::launch_attention(a, g_wait_ns.load());
     return e == cudaSuccess ? SOFTMAX_OK : SOFTMAX_ERR_CUDA;
 }

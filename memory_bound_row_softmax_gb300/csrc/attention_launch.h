@@ -22,6 +22,7 @@ struct AttnArgs {
     int causal;
     float sm_scale;
     cudaStream_t stream;
+    int sms;  // the device's SM count: the persistent grid's size
 };
 
 cudaError_t launch_attention(const AttnArgs &a, int64_t wait_ns);
@@ -29,7 +30,8 @@ cudaError_t launch_attention(const AttnArgs &a, int64_t wait_ns);
 // kAttnGroupBytes (a share of the 126 MB L2), at least 1, at most all
 constexpr int64_t kAttnGroupBytes = 48ll << 20;
 int attention_head_group(int64_t heads_total, int64_t n_ctx);
-int64_t attention_grid(int64_t batch, int64_t heads, int64_t n_ctx);
+// 256-query work items of a call (the persistent grid walks them)
+int64_t attention_items(int64_t batch, int64_t heads, int64_t n_ctx);
 size_t attention_smem_bytes();
 // the attention kernel's device error word (kErrWaitTimeout when a bounded
 // wait ran out); read after the stream has been synchronised, then cleared

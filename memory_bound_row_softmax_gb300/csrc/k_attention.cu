@@ -76,11 +76,14 @@ enum : int {
     kBarP = kBarS + kTiles,       // + tile: P_t is in TMEM (128 arrivals)
     kBarO = kBarP + kTiles,       // + tile: O_t is final
     kBarDrain = kBarO + kTiles,
-    kNumBars = kBarDrain + 1
+    kBarItem = kBarDrain + 1,    // the next ring entry of items is published
+    kBarQEmpty = kBarItem + 1,   // the item's S products are done with Q
+    kNumBars = kBarQEmpty + 1
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
-constexpr size_t kSmemBytes = kOffAbort + 4 + 1024;  // + slack for aligning the base
+constexpr uint32_t kOffItems = kOffAbort + 4;      // two-entry ring of item indices
+constexpr size_t kSmemBytes = kOffItems + 8 + 1024;  // + slack for aligning the base
 // tensor memory: tile t has S_t (P_t over its first 64 columns) at 128 t and
 // O_t at 256 + 128 t
 constexpr uint32_t kTmemCols = 512;
@@ -138,40 +141,63 @@ __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, volat
 }  // namespace
 
 
-// Block order: the heads go in groups of `group` heads (sized by the host so
-// that a group's K and V fit in L2 with room to spare); within a group the
-// 256-query blocks come heaviest first -- every head's last block (the most
-// keys under a causal mask), then every head's second-to-last, and so on --
-// so that the blocks resident at one time share the group's K and V in L2
-// and the light blocks of one group fill the SMs while the next group's heavy
-// ones start (longest-first list scheduling within the group).
+// Work items are 256-query blocks of one head.  Item i (in the order the
+// blocks are handed out) maps to (head, block) so that heads go in groups of
+// `group` heads (sized by the host so that a group's K and V fit in L2 with
+// room to spare) and, within a group, the heaviest blocks come first: every
+// head's last block (the most keys under a causal mask), then every head's
+// second-to-last, and so on.  Resident blocks then share the group's K and V
+// in L2, and handing items out in this order to whichever block is free is
+// longest-first list scheduling within the group.
+struct Item {
+    int bh, mb;
+};
+__device__ __forceinline__ Item decode_item(int i, int m_blocks, int heads_total, int group) {
+    const int per_group = group * m_blocks;
+    const int grp = i / per_group;
+    const int within = i - grp * per_group;
+    const int g0 = grp * group;
+    const int heads_here = min(group, heads_total - g0);
+    return Item{g0 + within % heads_here, m_blocks - 1 - within / heads_here};
+}
+
+// Per-launch work counters (next item, finished blocks).  A launch takes slot
+// `work_slot` (the host cycles through kWorkSlots); the last block to finish
+// resets the slot for its next user.
+constexpr int kWorkSlots = 64;
+__device__ unsigned int g_work[kWorkSlots][2];
+
+// One block per SM, persistent: the TMA lane fetches items from the slot's
+// counter and publishes each to the block through a two-entry ring in shared
+// memory; every role walks the same items.  Barrier phases run on across
+// items: the K/V ring by load count, S and P by tile count, Q and O by item
+// count.  The next item's Q is loaded as soon as the current item's last S
+// product has completed (kBarQEmpty), so its loads and first S products
+// overlap the current item's last PV product and its epilogue.  The first PV
+// product of an item overwrites O_t only after the softmax group has read
+// the previous item's O_t: the group reads it before it writes the new item's
+// first P_t, which that product waits for.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, T *__restrict__ o, int n_ctx, int m_blocks,
-                    int heads_total, int group, float kscale, int causal, uint32_t wait_ns) {
+                    int heads_total, int group, int work_slot, float kscale, int causal, uint32_t wait_ns) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *const gbase = smem_raw + (base - raw);
     volatile uint32_t *const abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + kOffAbort);
+    volatile int *const item_ring = reinterpret_cast<volatile int *>(gbase + kOffItems);
     const auto bar = [base](int i) { return base + kOffBar + 8u * (uint32_t)i; };
 
     const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
-    const int per_group = group * m_blocks;
-    const int grp = (int)(blockIdx.x / (unsigned)per_group);
-    const int within = (int)blockIdx.x - grp * per_group;
-    const int g0 = grp * group;
-    const int heads_here = min(group, heads_total - g0);
-    const int bh = g0 + within % heads_here;
-    const int mb = m_blocks - 1 - within / heads_here;
-    const int m0 = mb * kRowsPerBlock;
-    // key tiles of tile A (queries m0 ..) and B (m0 + 128 ..): under the causal
-    // mask up to each one's diagonal tile, never past the last key
+    const int total = heads_total * m_blocks;
     const int n_all = (n_ctx + kBlockN - 1) / kBlockN;
-    const int n_a = causal ? min(2 * mb + 1, n_all) : n_all;
-    const int n_b = causal ? min(2 * mb + 2, n_all) : n_all;
+    // key tiles of tile A (queries m0 ..) and B (m0 + 128 ..) of block mb: under
+    // the causal mask up to each one's diagonal tile, never past the last key
+    const auto tiles_a = [=](int mb) { return causal ? min(2 * mb + 1, n_all) : n_all; };
+    const auto tiles_b = [=](int mb) { return causal ? min(2 * mb + 2, n_all) : n_all; };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), (i == kBarP || i == kBarP + 1) ? kBlockM : 1);
@@ -193,45 +219,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + kOffTmemSlot);
 
     if (warp == kWarpTma) {
-        // ---- TMA producer ------------------------------------------------
+        // ---- item fetch and TMA producer ----------------------------------
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar(kBarQ), kTiles * kTileBytes);
-            for (int t = 0; t < kTiles; ++t) {
-                const uint32_t dst = base + kOffQ + (uint32_t)t * kTileBytes;
-                tma_load_3d(dst, &tq, 0, m0 + t * kBlockM, bh, bar(kBarQ));
-                tma_load_3d(dst + kHalfBytes, &tq, 64, m0 + t * kBlockM, bh, bar(kBarQ));
+            int n = 0;  // loads issued so far (all items)
+            int k = 0;  // items published so far
+            bool ok = true;
+            for (;; ++k) {
+                // the previous item's S products must be done with Q before
+                // the next item (or the end mark) is published: by then every
+                // role has read the previous entry, so the ring never runs two
+                // entries ahead of a reader
+                if (k > 0 && ok) ok = wait_phase(bar(kBarQEmpty), (k - 1) & 1, abort_flag, wait_ns);
+                const int item = ok ? (int)atomicAdd(&g_work[work_slot][0], 1u) : total;
+                item_ring[k & 1] = item < total ? item : -1;
+                mbar_arrive(bar(kBarItem));  // release: the entry is visible to whoever waits
+                if (item >= total) break;
+                const Item it = decode_item(item, m_blocks, heads_total, group);
+                const int m0 = it.mb * kRowsPerBlock;
+                mbar_arrive_expect_tx(bar(kBarQ), kTiles * kTileBytes);
+                for (int t = 0; t < kTiles; ++t) {
+                    const uint32_t dst = base + kOffQ + (uint32_t)t * kTileBytes;
+                    tma_load_3d(dst, &tq, 0, m0 + t * kBlockM, it.bh, bar(kBarQ));
+                    tma_load_3d(dst + kHalfBytes, &tq, 64, m0 + t * kBlockM, it.bh, bar(kBarQ));
+                }
+                const int loads = 2 * tiles_b(it.mb);
+                for (int i = 0; i < loads; ++i, ++n) {
+                    const int slot = n % kSlots;
+                    // the slot last held load n - kSlots; its MMAs must be done
+                    if (n >= kSlots &&
+                        !(ok = wait_phase(bar(kBarEmpty + slot), ((n / kSlots) - 1) & 1, abort_flag, wait_ns)))
+                        break;
+                    const uint32_t dst = base + kOffRing + (uint32_t)slot * kTileBytes;
+                    const CUtensorMap *map = (i & 1) ? &tv : &tk;
+                    const int y = (i >> 1) * kBlockN;
+                    mbar_arrive_expect_tx(bar(kBarFull + slot), kTileBytes);
+                    tma_load_3d(dst, map, 0, y, it.bh, bar(kBarFull + slot));
+                    tma_load_3d(dst + kHalfBytes, map, 64, y, it.bh, bar(kBarFull + slot));
+                }
             }
-            const int loads = 2 * n_b;
-            int n = 0;
-            for (; n < loads; ++n) {
-                const int slot = n % kSlots;
-                // the slot last held load n - kSlots; its MMAs must be done
-                if (n >= kSlots && !wait_phase(bar(kBarEmpty + slot), ((n / kSlots) - 1) & 1, abort_flag, wait_ns))
-                    break;
-                const uint32_t dst = base + kOffRing + (uint32_t)slot * kTileBytes;
-                const CUtensorMap *map = (n & 1) ? &tv : &tk;
-                const int y = (n >> 1) * kBlockN;
-                mbar_arrive_expect_tx(bar(kBarFull + slot), kTileBytes);
-                tma_load_3d(dst, map, 0, y, bh, bar(kBarFull + slot));
-                tma_load_3d(dst + kHalfBytes, map, 64, y, bh, bar(kBarFull + slot));
-            }
-            // every load issued lands before the block may exit
-            drain_phase(bar(kBarQ), 0, abort_flag, wait_ns);
+            // every load issued lands before the block may exit: the last Q
+            // and the last kSlots ring loads (earlier ones were consumed)
+            if (k > 0) drain_phase(bar(kBarQ), (k - 1) & 1, abort_flag, wait_ns);
             for (int nn = (n > kSlots ? n - kSlots : 0); nn < n; ++nn)
                 drain_phase(bar(kBarFull + nn % kSlots), (nn / kSlots) & 1, abort_flag, wait_ns);
+            // this block takes no more items: the last one to get here resets
+            // the launch's counters
+            __threadfence();
+            if (atomicAdd(&g_work[work_slot][1], 1u) == gridDim.x - 1) {
+                g_work[work_slot][0] = 0u;
+                g_work[work_slot][1] = 0u;
+                __threadfence();
+            }
         }
     } else if (warp == kWarpMma) {
         // ---- MMA issuer ----------------------------------------------------
         if (lane == 0) {
             constexpr uint32_t id_s = f16_idesc(kBf16, false, kBlockM, kBlockN);  // S = Q K^T
             constexpr uint32_t id_o = f16_idesc(kBf16, true, kBlockM, kHeadDim);  // O += P V
+            int nb = 0;               // first load of the current item
+            int p_cnt[kTiles] = {0, 0};  // P tiles consumed so far, per query tile
             const auto landed = [&](int n) {
                 return wait_phase(bar(kBarFull + n % kSlots), (n / kSlots) & 1, abort_flag, wait_ns);
             };
-            // S_t = Q_t K_j^T: K = head dim, 8 steps of 16; both operands
-            // K-major in shared memory
+            // S_t = Q_t K_j^T (K_j = load nb + 2j): K = head dim, 8 steps of 16;
+            // both operands K-major in shared memory
             const auto issue_s = [&](int t, int j) {
-                const uint32_t kb = base + kOffRing + (uint32_t)((2 * j) % kSlots) * kTileBytes;
+                const uint32_t kb = base + kOffRing + (uint32_t)((nb + 2 * j) % kSlots) * kTileBytes;
                 const uint32_t qb = base + kOffQ + (uint32_t)t * kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk) {
@@ -241,50 +294,70 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(bar(kBarS + t));
             };
-            // O_t += P_t V_j: K = keys, 8 steps of 16; P_t in TMEM (16 keys =
-            // 8 columns per step), V_j MN-major in shared memory (head dim
-            // contiguous, its two 64-column halves kHalfBytes apart)
+            // O_t += P_t V_j (V_j = load nb + 2j + 1): K = keys, 8 steps of 16;
+            // P_t in TMEM (16 keys = 8 columns per step), V_j MN-major in
+            // shared memory (head dim contiguous, its two 64-column halves
+            // kHalfBytes apart)
             const auto issue_pv = [&](int t, int j) {
-                const uint32_t vb = base + kOffRing + (uint32_t)((2 * j + 1) % kSlots) * kTileBytes;
+                const uint32_t vb = base + kOffRing + (uint32_t)((nb + 2 * j + 1) % kSlots) * kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk)
                     mma_ts(tmem + col_o(t), tmem + col_s(t) + (uint32_t)kk * 8u,
                            sw128_desc(vb + (uint32_t)kk * 16u * 128u, kHalfBytes, 1024), id_o, (j > 0 || kk > 0));
             };
-            bool ok = wait_phase(bar(kBarQ), 0, abort_flag, wait_ns) && landed(0);
-            if (ok) {
+            const auto wait_p = [&](int t) {
+                const bool r = wait_phase(bar(kBarP + t), p_cnt[t] & 1, abort_flag, wait_ns);
+                ++p_cnt[t];
+                return r;
+            };
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                if (!(ok = wait_phase(bar(kBarItem), k & 1, abort_flag, wait_ns))) break;
+                const int item = item_ring[k & 1];
+                if (item < 0) break;
+                const int mb = decode_item(item, m_blocks, heads_total, group).mb;
+                const int n_a = tiles_a(mb), n_b = tiles_b(mb);
+                if (!(ok = wait_phase(bar(kBarQ), k & 1, abort_flag, wait_ns) && landed(nb))) break;
                 tc_fence_after();
+                // S_t of the new item overwrites P_t of the previous one only
+                // after the PV product that reads it (issued earlier, in order)
                 issue_s(0, 0);
                 issue_s(1, 0);
-                mma_commit(bar(kBarEmpty + 0));  // K_0 done
-            }
-            for (int j = 0; ok && j < n_b; ++j) {
-                if (!(ok = landed(2 * j + 1))) break;  // V_j
-                const bool more_a = j + 1 < n_a, more_b = j + 1 < n_b;
-                if (j < n_a) {
-                    if (!(ok = wait_phase(bar(kBarP + 0), j & 1, abort_flag, wait_ns))) break;
-                    tc_fence_after();
-                    issue_pv(0, j);
-                    if (more_a) {
-                        if (!(ok = landed(2 * j + 2))) break;  // K_{j+1}
+                mma_commit(bar(kBarEmpty + nb % kSlots));  // K_0 done
+                for (int j = 0; j < n_b; ++j) {
+                    if (!(ok = landed(nb + 2 * j + 1))) break;  // V_j
+                    const bool more_a = j + 1 < n_a, more_b = j + 1 < n_b;
+                    if (j < n_a) {
+                        if (!(ok = wait_p(0))) break;
                         tc_fence_after();
-                        issue_s(0, j + 1);
-                    } else {
-                        mma_commit(bar(kBarO + 0));
+                        issue_pv(0, j);
+                        if (more_a) {
+                            if (!(ok = landed(nb + 2 * j + 2))) break;  // K_{j+1}
+                            tc_fence_after();
+                            issue_s(0, j + 1);
+                        } else {
+                            mma_commit(bar(kBarO + 0));
+                        }
                     }
-                }
-                if (!(ok = wait_phase(bar(kBarP + 1), j & 1, abort_flag, wait_ns))) break;
-                tc_fence_after();
-                issue_pv(1, j);
-                mma_commit(bar(kBarEmpty + (2 * j + 1) % kSlots));  // V_j done
-                if (more_b) {
-                    if (!more_a && !(ok = landed(2 * j + 2))) break;  // K_{j+1}, unless waited above
+                    if (!(ok = wait_p(1))) break;
                     tc_fence_after();
-                    issue_s(1, j + 1);
-                    mma_commit(bar(kBarEmpty + (2 * j + 2) % kSlots));  // K_{j+1} done
-                } else {
-                    mma_commit(bar(kBarO + 1));
+                    issue_pv(1, j);
+                    mma_commit(bar(kBarEmpty + (nb + 2 * j + 1) % kSlots));  // V_j done
+                    if (more_b) {
+                        if (!more_a && !(ok = landed(nb + 2 * j + 2))) break;  // K_{j+1}, unless waited above
+                        tc_fence_after();
+                        issue_s(1, j + 1);
+                        mma_commit(bar(kBarEmpty + (nb + 2 * j + 2) % kSlots));  // K_{j+1} done
+                    } else {
+                        mma_commit(bar(kBarO + 1));
+                    }
+                    // Q is free once the item's last S product is done; it is
+                    // signalled no earlier than after both groups' first P of
+                    // the item, so that both have read the item's ring entry
+                    // before the producer can publish the entry after next
+                    if (j + 2 == n_b || (n_b == 1 && j == 0)) mma_commit(bar(kBarQEmpty));
                 }
+                nb += 2 * n_b;
             }
             // every MMA issued completes before TMEM is released
             mma_commit(bar(kBarDrain));
@@ -294,83 +367,92 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- softmax: thread r of group t owns query row r of tile t -------
         const int t = warp >> 2;
         const int r = (int)(threadIdx.x & 127);
-        const int q = m0 + t * kBlockM + r;
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        const int n_t = t ? n_b : n_a;
-        const int q_lim = causal ? min(q + 1, n_ctx) : n_ctx;  // keys [0, q_lim) are kept
-        float m_run = -INFINITY;  // the shift, in log2 units
-        float l_run = 0.f;
+        int s_cnt = 0;  // S tiles consumed so far
         bool ok = true;
-        for (int j = 0; j < n_t; ++j) {
-            ok = __all_sync(0xffffffffu, wait_phase(bar(kBarS + t), j & 1, abort_flag, wait_ns));
+        for (int k = 0; ok; ++k) {
+            ok = __all_sync(0xffffffffu, wait_phase(bar(kBarItem), k & 1, abort_flag, wait_ns));
+            if (!ok) break;
+            const int item = item_ring[k & 1];
+            if (item < 0) break;
+            const Item it = decode_item(item, m_blocks, heads_total, group);
+            const int q = it.mb * kRowsPerBlock + t * kBlockM + r;
+            const int n_t = t ? tiles_b(it.mb) : tiles_a(it.mb);
+            const int q_lim = causal ? min(q + 1, n_ctx) : n_ctx;  // keys [0, q_lim) are kept
+            float m_run = -INFINITY;  // the shift, in log2 units
+            float l_run = 0.f;
+            for (int j = 0; j < n_t; ++j) {
+                ok = __all_sync(0xffffffffu, wait_phase(bar(kBarS + t), s_cnt & 1, abort_flag, wait_ns));
+                ++s_cnt;
+                if (!ok) break;
+                tc_fence_after();
+                float s[kBlockN];
+#pragma unroll
+                for (int c = 0; c < kBlockN / 32; ++c)
+                    tmem_ld32(lane_addr + col_s(t) + c * 32, s + c * 32);
+                tmem_wait_ld();
+                const int lim = q_lim - j * kBlockN;  // kept columns of this tile: [0, lim)
+                if (lim < kBlockN) {
+#pragma unroll
+                    for (int c = 0; c < kBlockN; ++c)
+                        if (c >= lim) s[c] = -INFINITY;
+                }
+                float mx[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) mx[i] = s[i];
+#pragma unroll
+                for (int c = 4; c < kBlockN; ++c) mx[c & 3] = fmaxf(mx[c & 3], s[c]);
+                const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * kscale;
+                float alpha = 1.f;
+                bool moved = false;
+                if (m_tile > m_run + kShiftSlack) {
+                    alpha = ex2(m_run - m_tile);  // 0 on the first tile
+                    l_run *= alpha;
+                    m_run = m_tile;
+                    moved = j > 0;
+                }
+                // p = 2^(s kscale - m_run), rounded to T in pairs and written
+                // over S_t's first 64 columns, in quarters of 32 keys (this
+                // thread's S values are all in registers already)
+                float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float p0 = ex2(fmaf(s[32 * h + 2 * c], kscale, -m_run));
+                        const float p1 = ex2(fmaf(s[32 * h + 2 * c + 1], kscale, -m_run));
+                        sum[c & 3] += p0 + p1;
+                        pk[c] = pack2<T>(p0, p1);
+                    }
+                    tmem_st16(lane_addr + col_s(t) + 16 * h, pk);
+                }
+                l_run += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+                if (__any_sync(0xffffffffu, moved)) {
+                    // O_t += P_t V_{j-1} has completed (S_t of this tile was
+                    // issued after it).  The whole warp takes part (TMEM
+                    // accesses are warp-wide); rows whose shift did not move
+                    // scale by 1.
+#pragma unroll
+                    for (int c = 0; c < kHeadDim / 32; ++c) {
+                        float ov[32];
+                        tmem_ld32(lane_addr + col_o(t) + c * 32, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+                        tmem_st32(lane_addr + col_o(t) + c * 32, ov);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(kBarP + t));
+            }
+            if (!ok) break;
+            ok = __all_sync(0xffffffffu, wait_phase(bar(kBarO + t), k & 1, abort_flag, wait_ns));
             if (!ok) break;
             tc_fence_after();
-            float s[kBlockN];
-#pragma unroll
-            for (int c = 0; c < kBlockN / 32; ++c) tmem_ld32(lane_addr + col_s(t) + c * 32, s + c * 32);
-            tmem_wait_ld();
-            const int lim = q_lim - j * kBlockN;  // kept columns of this tile: [0, lim)
-            if (lim < kBlockN) {
-#pragma unroll
-                for (int c = 0; c < kBlockN; ++c)
-                    if (c >= lim) s[c] = -INFINITY;
-            }
-            float mx[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx[i] = s[i];
-#pragma unroll
-            for (int c = 8; c < kBlockN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-            const float m_tile =
-                fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
-                kscale;
-            float alpha = 1.f;
-            bool moved = false;
-            if (m_tile > m_run + kShiftSlack) {
-                alpha = ex2(m_run - m_tile);  // 0 on the first tile
-                l_run *= alpha;
-                m_run = m_tile;
-                moved = j > 0;
-            }
-            // p = 2^(s kscale - m_run), rounded to T in pairs and written over
-            // S_t's first 64 columns, in quarters of 32 keys (this thread's S
-            // values are all in registers already)
-            float sum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float p0 = ex2(fmaf(s[32 * h + 2 * c], kscale, -m_run));
-                    const float p1 = ex2(fmaf(s[32 * h + 2 * c + 1], kscale, -m_run));
-                    sum[c & 3] += p0 + p1;
-                    pk[c] = pack2<T>(p0, p1);
-                }
-                tmem_st16(lane_addr + col_s(t) + 16 * h, pk);
-            }
-            l_run += (sum[0] + sum[1]) + (sum[2] + sum[3]);
-            if (__any_sync(0xffffffffu, moved)) {
-                // O_t += P_t V_{j-1} has completed (S_t of this tile was issued
-                // after it).  The whole warp takes part (TMEM accesses are
-                // warp-wide); rows whose shift did not move scale by 1.
-#pragma unroll
-                for (int c = 0; c < kHeadDim / 32; ++c) {
-                    float ov[32];
-                    tmem_ld32(lane_addr + col_o(t) + c * 32, ov);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-                    tmem_st32(lane_addr + col_o(t) + c * 32, ov);
-                }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(kBarP + t));
-        }
-        if (ok) ok = __all_sync(0xffffffffu, wait_phase(bar(kBarO + t), 0, abort_flag, wait_ns));
-        if (ok) {
-            tc_fence_after();
             const float inv = 1.f / l_run;
-            T *orow = o + ((int64_t)bh * n_ctx + q) * kHeadDim;
+            T *orow = o + ((int64_t)it.bh * n_ctx + q) * kHeadDim;
 #pragma unroll
             for (int c = 0; c < kHeadDim / 32; ++c) {
                 float ov[32];
@@ -388,6 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            // this group's reads of O_t are done before it writes the next
+            // item's first P_t (tcgen05.wait::ld above, fence before the
+            // arrival that the next item's first PV product waits for)
         }
     }
 
@@ -462,8 +547,13 @@ cudaError_t go(const AttnArgs &a, int64_t wait_ns) {
     const int group = attention_head_group(bh, a.n_ctx);
     const float kscale = a.sm_scale * kLog2e;
     const uint32_t limit = (uint32_t)std::min<int64_t>(std::max<int64_t>(wait_ns, 1), 0x7fffffff);
-    k_attention_fwd<T><<<(unsigned)(bh * m_blocks), kThreads, kSmemBytes, a.stream>>>(
-        mq, mk, mv, static_cast<T *>(a.o), (int)a.n_ctx, (int)m_blocks, (int)bh, group, kscale, a.causal,
+    // one persistent block per SM (at most one per item); each launch takes
+    // the next slot of work counters
+    static std::atomic<unsigned> launches{0};
+    const int slot = (int)(launches.fetch_add(1, std::memory_order_relaxed) % kWorkSlots);
+    const int64_t grid = std::min<int64_t>(std::max(a.sms, 1), bh * m_blocks);
+    k_attention_fwd<T><<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(
+        mq, mk, mv, static_cast<T *>(a.o), (int)a.n_ctx, (int)m_blocks, (int)bh, group, slot, kscale, a.causal,
         limit);
     return cudaGetLastError();
 }
@@ -480,7 +570,7 @@ int attention_head_group(int64_t heads_total, int64_t n_ctx) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(g, heads_total));
 }
 
-int64_t attention_grid(int64_t batch, int64_t heads, int64_t n_ctx) {
+int64_t attention_items(int64_t batch, int64_t heads, int64_t n_ctx) {
     return batch * heads * ((n_ctx + kRowsPerBlock - 1) / kRowsPerBlock);
 }
 
