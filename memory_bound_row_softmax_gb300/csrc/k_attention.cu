@@ -10,11 +10,12 @@
 // the max moves, P rounded to the input type before the second product, the
 // accumulator divided by the normaliser at the end).
 //
-// One block per 256 queries of one head: two query tiles A and B of 128, 320
-// threads in four roles:
-//   warp 8, one lane  -- TMA: both Q tiles once, then K_0, V_0, K_1, V_1, ...
-//                        (tiles of 128 keys, 128-byte swizzled rows) into a
-//                        ring of kSlots shared-memory slots;
+// A persistent grid, one block per SM, works through items of 256 queries of
+// one head: two query tiles A and B of 128.  320 threads in four roles:
+//   warp 8, one lane  -- fetches the next item and publishes it to the block;
+//                        TMA: the item's two Q tiles, then K_0, V_0, K_1,
+//                        V_1, ... (tiles of 128 keys, 128-byte swizzled rows)
+//                        into a ring of kSlots shared-memory slots;
 //   warp 9, one lane  -- tcgen05.mma: S_t = Q_t K_j^T into tensor memory (TMEM)
 //                        and O_t += P_t V_j, with P_t read from TMEM where the
 //                        softmax wrote it over S_t; warp 9 owns the TMEM
