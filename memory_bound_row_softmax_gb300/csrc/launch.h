@@ -143,6 +143,11 @@ constexpr int64_t kNoAllocMaxStates = 65536;
 constexpr int kNoAllocThreads = 256, kNoAllocVpt = 4;
 cudaError_t launch_split_noalloc(const LaunchArgs &a, int64_t chunks, int64_t chunk_vecs, int64_t grid);
 
+// host state of the softmax ABI that the attention ABI (attention_abi.cu)
+// shares: the device's SM count (cached) and the bounded-wait limit
+int host_device_sms(int *sms);
+int64_t host_wait_ns();
+
 bool split_shape_ok(int threads, int vpt);
 cudaError_t launch_split(const LaunchArgs &a, int threads, int vpt, int64_t chunks, int64_t chunk_vecs,
                          int64_t grid, void *scratch);
