@@ -58,6 +58,16 @@ int softmax_attention_fwd(const void *q, const void *k, const void *v, void *o, 
                           int64_t n_ctx, int64_t head_dim, int dtype, int causal, float sm_scale,
                           cudaStream_t stream);
 
+/*
+ * Test hook for the attention forward's bounded waits.  starve != 0 makes the
+ * next launches leave every block's first Q barrier unarmed, so that wait can
+ * only run out: the kernel records SOFTMAX_ERR_TIMEOUT (read it with
+ * softmax_check_device_error), skips its stores and returns normally.  The
+ * wait limit is the one softmax_set_wait_test sets (default 1 s).
+ * Process-wide, not thread-safe; returns SOFTMAX_OK.
+ */
+int softmax_attention_set_wait_test(int starve);
+
 #ifdef __cplusplus
 }
 #endif

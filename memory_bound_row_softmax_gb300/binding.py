@@ -63,6 +63,7 @@ SIGNATURES = {
     "softmax_fwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp]),
     "softmax_fwd_masked": (_int, [_vp, _vp, _i64, _i64, _i64, _int, ctypes.c_float, _i64, _i64, _vp]),
     "softmax_attention_fwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, ctypes.c_float, _vp]),
+    "softmax_attention_set_wait_test": (_int, [_int]),
 }
 
 _lib = None
@@ -304,6 +305,12 @@ def check_device_error(stream=None) -> int:
 
 def set_wait_test(wait_limit_ns: int = 0, starve: bool = False) -> None:
     lib().softmax_set_wait_test(wait_limit_ns, 1 if starve else 0)
+
+
+def set_attention_wait_test(starve: bool = False) -> None:
+    """Attention forward test hook: leave the first Q barrier of every block
+    unarmed so that its bounded wait runs out (see set_wait_test for the limit)."""
+    lib().softmax_attention_set_wait_test(1 if starve else 0)
 
 
 def set_launch_overlap(enable: bool = True) -> None:

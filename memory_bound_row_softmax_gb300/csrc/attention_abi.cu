@@ -1,6 +1,7 @@
 // attention_abi.cu -- the C ABI of the fused attention forward declared in
 // include/mbrs_attention.h: argument checks, then the persistent launch
 // (k_attention.cu).
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -10,7 +11,16 @@
 
 using namespace mbrs;
 
+namespace {
+std::atomic<int> g_attn_starve{0};
+}
+
 extern "C" {
+
+int softmax_attention_set_wait_test(int starve) {
+    g_attn_starve.store(starve ? 1 : 0);
+    return SOFTMAX_OK;
+}
 
 int softmax_attention_fwd(const void *q, const void *k, const void *v, void *o, int64_t batch, int64_t heads,
                           int64_t n_ctx, int64_t head_dim, int dtype, int causal, float sm_scale,
@@ -42,7 +52,7 @@ int softmax_attention_fwd(const void *q, const void *k, const void *v, void *o, 
     const int st = mbrs::host_device_sms(&sms);
     if (st != SOFTMAX_OK) return st;
     attn::AttnArgs a{q, k, v, o, batch, heads, n_ctx, dtype, causal, sm_scale, stream, sms};
-    const cudaError_t e = attn::launch_attention(a, mbrs::host_wait_ns());
+    const cudaError_t e = attn::launch_attention(a, mbrs::host_wait_ns(), g_attn_starve.load());
     return e == cudaSuccess ? SOFTMAX_OK : SOFTMAX_ERR_CUDA;
 }
 

@@ -25,7 +25,9 @@ struct AttnArgs {
     int sms;  // the device's SM count: the persistent grid's size
 };
 
-cudaError_t launch_attention(const AttnArgs &a, int64_t wait_ns);
+// starve != 0 (a test hook): every block leaves its first item's Q barrier
+// unarmed, so that wait runs out and the whole launch takes its abort path
+cudaError_t launch_attention(const AttnArgs &a, int64_t wait_ns, int starve);
 // heads per block-order group: as many as keep the group's K and V within
 // kAttnGroupBytes (a share of the 126 MB L2), at least 1, at most all
 constexpr int64_t kAttnGroupBytes = 48ll << 20;

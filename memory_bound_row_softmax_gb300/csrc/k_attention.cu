@@ -182,7 +182,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, T *__restrict__ o, int n_ctx, int m_blocks,
-                    int heads_total, int group, int work_slot, float kscale, int causal, uint32_t wait_ns) {
+                    int heads_total, int group, int work_slot, float kscale, int causal, uint32_t wait_ns,
+                    int starve) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -237,11 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (item >= total) break;
                 const Item it = decode_item(item, m_blocks, heads_total, group);
                 const int m0 = it.mb * kRowsPerBlock;
-                mbar_arrive_expect_tx(bar(kBarQ), kTiles * kTileBytes);
-                for (int t = 0; t < kTiles; ++t) {
-                    const uint32_t dst = base + kOffQ + (uint32_t)t * kTileBytes;
-                    tma_load_3d(dst, &tq, 0, m0 + t * kBlockM, it.bh, bar(kBarQ));
-                    tma_load_3d(dst + kHalfBytes, &tq, 64, m0 + t * kBlockM, it.bh, bar(kBarQ));
+                if (!(starve && k == 0)) {  // the test hook leaves the first Q barrier unarmed
+                    mbar_arrive_expect_tx(bar(kBarQ), kTiles * kTileBytes);
+                    for (int t = 0; t < kTiles; ++t) {
+                        const uint32_t dst = base + kOffQ + (uint32_t)t * kTileBytes;
+                        tma_load_3d(dst, &tq, 0, m0 + t * kBlockM, it.bh, bar(kBarQ));
+                        tma_load_3d(dst + kHalfBytes, &tq, 64, m0 + t * kBlockM, it.bh, bar(kBarQ));
+                    }
                 }
                 const int loads = 2 * tiles_b(it.mb);
                 for (int i = 0; i < loads; ++i, ++n) {
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // every load issued lands before the block may exit: the last Q
             // and the last kSlots ring loads (earlier ones were consumed)
-            if (k > 0) drain_phase(bar(kBarQ), (k - 1) & 1, abort_flag, wait_ns);
+            if (k > 0 && !(starve && k == 1)) drain_phase(bar(kBarQ), (k - 1) & 1, abort_flag, wait_ns);
             for (int nn = (n > kSlots ? n - kSlots : 0); nn < n; ++nn)
                 drain_phase(bar(kBarFull + nn % kSlots), (nn / kSlots) & 1, abort_flag, wait_ns);
             // this block takes no more items: the last one to get here resets
@@ -528,7 +531,7 @@ bool make_map(CUtensorMap *map, const void *ptr, int dtype, int64_t n_ctx, int64
 constexpr int kMaxDevices = 64;
 
 template <typename T>
-cudaError_t go(const AttnArgs &a, int64_t wait_ns) {
+cudaError_t go(const AttnArgs &a, int64_t wait_ns, int starve) {
     static std::atomic<unsigned long long> opted{0};
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
@@ -555,14 +558,14 @@ cudaError_t go(const AttnArgs &a, int64_t wait_ns) {
     const int64_t grid = std::min<int64_t>(std::max(a.sms, 1), bh * m_blocks);
     k_attention_fwd<T><<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(
         mq, mk, mv, static_cast<T *>(a.o), (int)a.n_ctx, (int)m_blocks, (int)bh, group, slot, kscale, a.causal,
-        limit);
+        limit, starve ? 1 : 0);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attention(const AttnArgs &a, int64_t wait_ns) {
-    return a.dtype == kAttnBf16 ? go<__nv_bfloat16>(a, wait_ns) : go<__half>(a, wait_ns);
+cudaError_t launch_attention(const AttnArgs &a, int64_t wait_ns, int starve) {
+    return a.dtype == kAttnBf16 ? go<__nv_bfloat16>(a, wait_ns, starve) : go<__half>(a, wait_ns, starve);
 }
 
 int attention_head_group(int64_t heads_total, int64_t n_ctx) {

@@ -230,3 +230,34 @@ def test_bad_arguments_launch_nothing():
     assert B.attention_fwd_ptr(p, p, p, o.data_ptr(), 1, 1, 128, 64, 1, True, 0.1, s) == B.ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert (o == 0).all()
+
+
+def test_wait_timeout_is_reported_and_recoverable():
+    # every block's first Q barrier left unarmed: its bounded wait (1 ms here)
+    # runs out, the launch takes its abort path (drains its loads and MMAs,
+    # frees tensor memory, resets its work counter) and reports a timeout;
+    # the next 65 launches -- more than the 64 work-counter slots, so the
+    # aborted launch's slot is used again -- are exact
+    w = W.AttentionWorkload("t", 2, 3, 700, D, "f16", seed=29, causal=True)
+    q, k, v = W.make_qkv(w)
+    dq, dk, dv = to_dev(q, "f16"), to_dev(k, "f16"), to_dev(v, "f16")
+    out = torch.empty_like(dq)
+    s = torch.cuda.current_stream().cuda_stream
+    args = (dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), out.data_ptr(), 2, 3, 700, D, CODE["f16"], True,
+            1.0 / math.sqrt(D), s)
+    B.set_wait_test(1_000_000)
+    B.set_attention_wait_test(True)
+    try:
+        assert B.attention_fwd_ptr(*args) == B.OK
+        assert B.check_device_error() == B.ERR_TIMEOUT
+    finally:
+        B.set_attention_wait_test(False)
+        B.set_wait_test(0)
+    for _ in range(65):
+        assert B.attention_fwd_ptr(*args) == B.OK
+    assert B.check_device_error() == B.OK
+    got = from_dev(out, "f16")
+    scale = 1.0 / math.sqrt(D)
+    for bi in range(2):
+        for hi in range(3):
+            check_head(got[bi, hi], q[bi, hi], k[bi, hi], v[bi, hi], "f16", scale, True)
