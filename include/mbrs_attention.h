@@ -27,7 +27,10 @@
  * Ownership: the caller owns all four device buffers and the stream.  Every
  * pointer must be 16-byte aligned.  Q, K and V may overlap one another; O may
  * overlap none of them.  The call is asynchronous on `stream`; nothing is
- * allocated on the device.
+ * allocated on the device.  The kernel is a persistent grid that hands out
+ * its work through one of 64 device-side counter slots, taken in turn by
+ * successive calls: at most 64 calls may be in flight at the same time on one
+ * device (over all streams).
  *
  * Errors (checked on the host before any launch; nothing is launched unless
  * the result is SOFTMAX_OK):
