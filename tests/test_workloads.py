@@ -82,3 +82,29 @@ def test_sweep_widths():
     w = W.sweep_workload(4103)
     assert w.rows == 50_000_000 // 4103
     assert math.isclose(w.rows * w.cols * 4, 200e6, rel_tol=1e-3)
+
+
+def test_attention_workloads_are_the_pages_shapes():
+    # batch 4, 32 heads, head dim 128, fp16, causal (the pages' attention table)
+    for key in ("a4k", "a16k"):
+        w = W.ATTENTION_CONFIGS[key]
+        assert (w.batch, w.heads, w.head_dim, w.dtype, w.causal) == (4, 32, 128, "f16", True)
+    assert W.ATTENTION_CONFIGS["a4k"].n_ctx == 4096 and W.ATTENTION_CONFIGS["a16k"].n_ctx == 16384
+    w = W.ATTENTION_CONFIGS["a4k"]
+    assert w.flops() == 4.0 * 4 * 32 * 4096 * 4096 * 128 / 2
+
+
+def test_qkv_heads_are_slices_of_the_whole():
+    # any head range regenerates exactly the same bits as the whole tensor
+    w = W.AttentionWorkload("t", 2, 3, 70, 128, "bf16", seed=3, causal=False)
+    q, k, v = W.make_qkv(w, chunk_heads=4)
+    assert q.shape == (2, 3, 70, 128) and q.dtype == np.uint16
+    flat = {"q": q.reshape(6, 70, 128), "k": k.reshape(6, 70, 128), "v": v.reshape(6, 70, 128)}
+    for which in ("q", "k", "v"):
+        part = W.qkv_heads(w.seed, which, 2, 5, 70, 128, "bf16")
+        assert (part == flat[which][2:5]).all()
+    # Q, K and V come from different streams
+    assert not (q == k).all() and not (k == v).all()
+    vals = q.astype(np.uint32) << 16
+    x = vals.view(np.float32)
+    assert abs(float(x.mean())) < 0.05 and 0.9 < float(x.std()) < 1.1
