@@ -61,6 +61,27 @@ int softmax_attention_fwd(const void *q, const void *k, const void *v, void *o, 
                           int64_t n_ctx, int64_t head_dim, int dtype, int causal, float sm_scale,
                           cudaStream_t stream);
 
+/* The launch softmax_attention_fwd makes for a shape (host only). */
+typedef struct {
+    int64_t items;        /* work items: 256-query blocks of one head (batch * heads * ceil(n_ctx / 256)) */
+    int64_t grid;         /* persistent blocks launched: min(SMs, items) */
+    int head_group;       /* heads per group of the item order (their K and V fit 48 MiB of L2) */
+    int threads;          /* threads per block */
+    int64_t smem_bytes;   /* dynamic shared memory per block */
+    int tmem_columns;     /* tensor-memory columns per block */
+    double flops;         /* matmul FLOPs of the call: 4 * batch * heads * n_ctx^2 * head_dim, halved when causal */
+} softmax_attention_plan_t;
+
+/*
+ * Fill *plan with the launch softmax_attention_fwd would make for these
+ * arguments on a device with num_sms SMs (num_sms <= 0: the current device's
+ * count, which needs the CUDA runtime).  Returns the status the call would
+ * return for the shape, dtype, causal and head_dim arguments (pointers are not
+ * checked); SOFTMAX_ERR_ARG when plan is NULL.
+ */
+int softmax_attention_plan(int64_t batch, int64_t heads, int64_t n_ctx, int64_t head_dim, int dtype, int causal,
+                           int num_sms, softmax_attention_plan_t *plan);
+
 /*
  * Test hook for the attention forward's bounded waits.  starve != 0 makes the
  * next launches leave every block's first Q barrier unarmed, so that wait can

@@ -8,7 +8,7 @@ import importlib
 
 _BINDING_NAMES = ("softmax_fwd", "softmax_fwd_ptr", "softmax_fwd_masked", "softmax_fwd_masked_ptr",
                   "softmax_fwd_noalloc_ptr", "softmax_fwd_host", "host_workspace_bytes", "attention_fwd",
-                  "attention_fwd_ptr", "autotune", "autotune_ptr", "tune_candidates", "autotune_size",
+                  "attention_fwd_ptr", "attention_plan", "set_attention_wait_test", "autotune", "autotune_ptr", "tune_candidates", "autotune_size",
                   "autotune_clear", "plan", "set_force_path", "set_launch_overlap", "last_path",
                   "check_device_error", "set_wait_test", "abi_version", "status_string", "SoftmaxError")
 

@@ -36,6 +36,14 @@ class TuneResult(ctypes.Structure):
     _fields_ = [("plan", Plan), ("best_us", ctypes.c_double), ("auto_us", ctypes.c_double), ("candidates", _int)]
 
 
+class AttentionPlan(ctypes.Structure):
+    _fields_ = [("items", _i64), ("grid", _i64), ("head_group", _int), ("threads", _int), ("smem_bytes", _i64),
+                ("tmem_columns", _int), ("flops", ctypes.c_double)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
 class Shape(ctypes.Structure):
     _fields_ = [("path", _int), ("threads", _int), ("vpt", _int), ("group", _int)]
 
@@ -64,6 +72,7 @@ SIGNATURES = {
     "softmax_fwd_masked": (_int, [_vp, _vp, _i64, _i64, _i64, _int, ctypes.c_float, _i64, _i64, _vp]),
     "softmax_attention_fwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, ctypes.c_float, _vp]),
     "softmax_attention_set_wait_test": (_int, [_int]),
+    "softmax_attention_plan": (_int, [_i64, _i64, _i64, _i64, _int, _int, _int, ctypes.POINTER(AttentionPlan)]),
 }
 
 _lib = None
@@ -305,6 +314,19 @@ def check_device_error(stream=None) -> int:
 
 def set_wait_test(wait_limit_ns: int = 0, starve: bool = False) -> None:
     lib().softmax_set_wait_test(wait_limit_ns, 1 if starve else 0)
+
+
+def attention_plan(batch: int, heads: int, n_ctx: int, head_dim: int = 128, dtype="f16", causal: bool = True,
+                   num_sms: int = 0) -> dict:
+    """The launch softmax_attention_fwd makes for a shape (host only when
+    num_sms > 0); raises SoftmaxError for arguments the call would refuse."""
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else dtype
+    p = AttentionPlan()
+    st = lib().softmax_attention_plan(batch, heads, n_ctx, head_dim, code, 1 if causal else 0, num_sms,
+                                      ctypes.byref(p))
+    if st != OK:
+        raise SoftmaxError(st, "softmax_attention_plan")
+    return p.as_dict()
 
 
 def set_attention_wait_test(starve: bool = False) -> None:

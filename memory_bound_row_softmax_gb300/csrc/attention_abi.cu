@@ -1,6 +1,7 @@
 // attention_abi.cu -- the C ABI of the fused attention forward declared in
 // include/mbrs_attention.h: argument checks, then the persistent launch
 // (k_attention.cu).
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -22,14 +23,14 @@ int softmax_attention_set_wait_test(int starve) {
     return SOFTMAX_OK;
 }
 
-int softmax_attention_fwd(const void *q, const void *k, const void *v, void *o, int64_t batch, int64_t heads,
-                          int64_t n_ctx, int64_t head_dim, int dtype, int causal, float sm_scale,
-                          cudaStream_t stream) {
+namespace {
+
+// The checks of everything but the pointers, shared by the call and its plan.
+int check_shape(int64_t batch, int64_t heads, int64_t n_ctx, int64_t head_dim, int dtype, int causal) {
     if (batch < 0 || heads < 0 || n_ctx < 0 || head_dim < 1) return SOFTMAX_ERR_SHAPE;
     if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_F16 && dtype != SOFTMAX_BF16) return SOFTMAX_ERR_DTYPE;
     if (dtype == SOFTMAX_F32 || head_dim != attn::kAttnHeadDim) return SOFTMAX_ERR_UNSUPPORTED;
     if (causal != 0 && causal != 1) return SOFTMAX_ERR_ARG;
-    if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return SOFTMAX_ERR_ARG;
     if (batch == 0 || heads == 0 || n_ctx == 0) return SOFTMAX_OK;
     // index ranges of the kernel: n_ctx and the query-tile count fit int32
     constexpr int64_t kInt = 0x7fffffff;
@@ -39,7 +40,43 @@ int softmax_attention_fwd(const void *q, const void *k, const void *v, void *o, 
     if (bh > kInt / m_tiles) return SOFTMAX_ERR_SHAPE;
     const int64_t row_bytes = head_dim * 2;
     if (bh > INT64_MAX / n_ctx || bh * n_ctx > INT64_MAX / row_bytes) return SOFTMAX_ERR_SHAPE;
-    const uint64_t bytes = (uint64_t)(bh * n_ctx * row_bytes);
+    return SOFTMAX_OK;
+}
+
+}  // namespace
+
+int softmax_attention_plan(int64_t batch, int64_t heads, int64_t n_ctx, int64_t head_dim, int dtype, int causal,
+                           int num_sms, softmax_attention_plan_t *plan) {
+    if (!plan) return SOFTMAX_ERR_ARG;
+    *plan = softmax_attention_plan_t{};
+    const int st = check_shape(batch, heads, n_ctx, head_dim, dtype, causal);
+    if (st != SOFTMAX_OK) return st;
+    plan->threads = attn::attention_threads();
+    plan->smem_bytes = (int64_t)attn::attention_smem_bytes();
+    plan->tmem_columns = attn::attention_tmem_columns();
+    if (batch == 0 || heads == 0 || n_ctx == 0) return SOFTMAX_OK;
+    int sms = num_sms;
+    if (sms <= 0) {
+        const int e = mbrs::host_device_sms(&sms);
+        if (e != SOFTMAX_OK) return e;
+    }
+    plan->items = attn::attention_items(batch, heads, n_ctx);
+    plan->grid = std::min<int64_t>(sms, plan->items);
+    plan->head_group = attn::attention_head_group(batch * heads, n_ctx);
+    const double f = 4.0 * (double)batch * (double)heads * (double)n_ctx * (double)n_ctx * (double)head_dim;
+    plan->flops = causal ? f / 2 : f;
+    return SOFTMAX_OK;
+}
+
+int softmax_attention_fwd(const void *q, const void *k, const void *v, void *o, int64_t batch, int64_t heads,
+                          int64_t n_ctx, int64_t head_dim, int dtype, int causal, float sm_scale,
+                          cudaStream_t stream) {
+    int st = check_shape(batch, heads, n_ctx, head_dim, dtype, causal);
+    if (st != SOFTMAX_OK) return st;
+    if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return SOFTMAX_ERR_ARG;
+    if (batch == 0 || heads == 0 || n_ctx == 0) return SOFTMAX_OK;
+    const int64_t bh = batch * heads;
+    const uint64_t bytes = (uint64_t)(bh * n_ctx * head_dim * 2);
     if (!q || !k || !v || !o) return SOFTMAX_ERR_NULL;
     const uint64_t qa = (uint64_t)(uintptr_t)q, ka = (uint64_t)(uintptr_t)k, va = (uint64_t)(uintptr_t)v,
                    oa = (uint64_t)(uintptr_t)o;
@@ -49,7 +86,7 @@ int softmax_attention_fwd(const void *q, const void *k, const void *v, void *o, 
     const auto overlaps = [bytes](uint64_t a, uint64_t b) { return a < b + bytes && b < a + bytes; };
     if (overlaps(oa, qa) || overlaps(oa, ka) || overlaps(oa, va)) return SOFTMAX_ERR_OVERLAP;
     int sms = 0;
-    const int st = mbrs::host_device_sms(&sms);
+    st = mbrs::host_device_sms(&sms);
     if (st != SOFTMAX_OK) return st;
     attn::AttnArgs a{q, k, v, o, batch, heads, n_ctx, dtype, causal, sm_scale, stream, sms};
     const cudaError_t e = attn::launch_attention(a, mbrs::host_wait_ns(), g_attn_starve.load());

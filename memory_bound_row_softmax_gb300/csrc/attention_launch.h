@@ -35,6 +35,8 @@ int attention_head_group(int64_t heads_total, int64_t n_ctx);
 // 256-query work items of a call (the persistent grid walks them)
 int64_t attention_items(int64_t batch, int64_t heads, int64_t n_ctx);
 size_t attention_smem_bytes();
+int attention_threads();
+int attention_tmem_columns();
 // the attention kernel's device error word (kErrWaitTimeout when a bounded
 // wait ran out); read after the stream has been synchronised, then cleared
 cudaError_t read_clear_attn_error_word(unsigned int *word);

@@ -579,6 +579,8 @@ int64_t attention_items(int64_t batch, int64_t heads, int64_t n_ctx) {
 }
 
 size_t attention_smem_bytes() { return kSmemBytes; }
+int attention_threads() { return kThreads; }
+int attention_tmem_columns() { return (int)kTmemCols; }
 
 cudaError_t read_clear_attn_error_word(unsigned int *word) {
     cudaError_t e = cudaMemcpyFromSymbol(word, g_attn_error, sizeof(unsigned int), 0, cudaMemcpyDeviceToHost);

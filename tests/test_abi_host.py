@@ -294,3 +294,25 @@ def test_attention_argument_checks(args, expect):
                           B.ERR_UNSUPPORTED)
         return
     assert B.lib().softmax_attention_fwd(*args, None) == expect
+
+
+def test_attention_plan_on_the_host():
+    # the pages' shape on 152 SMs: 4 x 32 heads x 16 items each, one block per SM,
+    # head groups whose K and V (2 MiB per head at N = 4096) fit 48 MiB
+    p = B.attention_plan(4, 32, 4096, num_sms=152)
+    assert p["items"] == 4 * 32 * 16 and p["grid"] == 152 and p["head_group"] == 24
+    assert p["threads"] == 320 and p["tmem_columns"] == 512 and p["smem_bytes"] <= 227 * 1024
+    assert p["flops"] == 4.0 * 4 * 32 * 4096 ** 2 * 128 / 2
+    assert B.attention_plan(4, 32, 16384, num_sms=152)["head_group"] == 6
+    assert B.attention_plan(4, 32, 16384, causal=False, num_sms=152)["flops"] == 4.0 * 4 * 32 * 16384 ** 2 * 128
+    # fewer items than SMs: one block per item; tiny contexts: every head in one group
+    small = B.attention_plan(1, 3, 100, num_sms=152)
+    assert small["items"] == 3 and small["grid"] == 3 and small["head_group"] == 3
+    assert B.attention_plan(0, 3, 100, num_sms=152)["items"] == 0
+    for args, status in [((1, 1, 128, 64), B.ERR_UNSUPPORTED), ((1, -1, 128, 128), B.ERR_SHAPE),
+                         ((1, 1, 1 << 31, 128), B.ERR_SHAPE)]:
+        with pytest.raises(B.SoftmaxError) as e:
+            B.attention_plan(*args, num_sms=152)
+        assert e.value.status == status
+    with pytest.raises(B.SoftmaxError):
+        B.attention_plan(1, 1, 128, dtype="f32", num_sms=152)
