@@ -15,6 +15,13 @@ are larger than 2.5x the L2, so every step's input comes from HBM.
 ranks / max-over-ranks time of the K steps); the roofline block uses the
 mean per-launch device time.  Under torchrun every rank runs its own copy of
 the workload (weak scaling, rows are independent: no data-path collective).
+
+The same line carries an `attention` object: the fused attention forward
+(softmax_attention_fwd) on the pages' attention shapes (batch 4, 32 heads,
+head dim 128, fp16, causal, N = 4096 and 16384) in TFLOP/s against the
+measured dense tensor rate, with the oracle's one-head attention as its CPU
+baseline.  `--attention KEY` prints only that object (with `--only-kernel`:
+the command the attention profiler capture runs).
 """
 from __future__ import annotations
 
