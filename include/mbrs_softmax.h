@@ -33,7 +33,10 @@
  * never pre-initialised (page "I Wrote My First GPU Kernel", section "The
  * Honest Part": empty_like instead of zeros_like).  in == out (exact
  * aliasing) is allowed; any other overlap of the two byte ranges is rejected.
- * Calls are asynchronous on `stream`; nothing is synchronised.
+ * The library allocates no device memory per call: every path keeps its
+ * partial (max, sum) states on chip (registers, shared memory, or the
+ * distributed shared memory of a thread-block cluster).  Calls are
+ * asynchronous on `stream`; nothing is synchronised.
  *
  * Errors: arguments are checked on the host before any launch and a status
  * code is returned (no launch happens unless the status is SOFTMAX_OK).
@@ -78,18 +81,20 @@ typedef enum {
     SOFTMAX_ERR_SCRATCH_LIMIT = 11 /* softmax_fwd_noalloc: rows exceed its fixed scratch array */
 } softmax_status_t;
 
-/* Kernel paths the dispatcher chooses between. */
+/* Kernel paths the dispatcher chooses between.  (5 is unused: it named a
+ * TMA-fed ring of shared-memory stages, measured slower than paths 2 and 6 at
+ * every width and removed; forcing it returns SOFTMAX_ERR_ARG.) */
 typedef enum {
     SOFTMAX_PATH_AUTO = 0,    /* width-based choice (default) */
-    SOFTMAX_PATH_WARP = 1,    /* a warp (or 2..16 lanes) per row, cols <= 1024 */
+    SOFTMAX_PATH_WARP = 1,    /* a warp (or 2..16 lanes) per row */
     SOFTMAX_PATH_CTA = 2,     /* a thread block per row, row held in registers (any alignment) */
-    SOFTMAX_PATH_CLUSTER = 3, /* a thread-block cluster per row: TMA bulk loads of the aligned
-                                 part, (max, sum) exchanged through distributed shared memory */
-    SOFTMAX_PATH_SPLIT = 4,   /* rows split across the whole grid: pass 1 writes
-                                 per-chunk (max, sum), pass 2 merges them, re-reads and writes */
-    SOFTMAX_PATH_RING = 5,    /* persistent blocks or clusters (<= 16 blocks per row) looping over
-                                 rows, fed by a ring of shared-memory stages that TMA bulk copies
-                                 keep full; rows of whole aligned 16-byte vectors only */
+    SOFTMAX_PATH_CLUSTER = 3, /* 16-bit rows: a thread-block cluster per row, each block holding
+                                 its slice in registers, (max, sum) exchanged through distributed
+                                 shared memory */
+    SOFTMAX_PATH_SPLIT = 4,   /* softmax_fwd_noalloc only: rows split across the whole grid, pass 1
+                                 writes per-chunk (max, sum) into the library's fixed array, pass 2
+                                 merges them, re-reads and writes.  softmax_fwd never takes it
+                                 (forcing it returns SOFTMAX_ERR_ARG) */
     SOFTMAX_PATH_STREAM = 6,  /* a cluster (<= 16 blocks) per row, each block streaming its slice
                                  of any length twice: pass 1 (max, sum), exchange through
                                  distributed shared memory, pass 2 re-read and write; no scratch */
@@ -106,10 +111,9 @@ typedef enum {
  *   row_stride  distance between row starts in elements (>= cols), both buffers
  *   dtype       a softmax_dtype_t
  *   stream      the CUDA stream to launch on (0 = legacy default stream)
- * The SPLIT path (very long rows, or few long rows) needs rows * chunks * 8
- * bytes of scratch; softmax_fwd takes it stream-ordered from a pool the
- * library keeps per device and returns it on the same stream.
- * Returns a softmax_status_t.
+ * Rows too long for the registers of a block or cluster (path 6) are read
+ * twice, the second read usually served by L2: 3 element crossings instead of
+ * 2, and still no scratch.  Allocates nothing.  Returns a softmax_status_t.
  */
 int softmax_fwd(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride,
                 int dtype, cudaStream_t stream);
@@ -191,10 +195,12 @@ int softmax_last_path(void);
 /*
  * Test and tuning hook: force every following call onto `path` (0 = automatic).
  * threads / vpt / group override the launch shape where > 0 (threads per block,
- * 16-byte vectors per thread, and lanes per row / cluster size / chunks per
- * row for paths 1 / 3, 5 and 6 / 4; for path 7 vpt is the rows each thread
- * takes per staged span and group must be 0 or 1).  A forced shape that cannot cover the row makes
- * softmax_fwd return SOFTMAX_ERR_UNSUPPORTED.  Process-wide, not thread-safe.
+ * 16-byte vectors per thread, and lanes per row / cluster size for paths 1 /
+ * 3 and 6; for path 7 vpt is the rows each thread takes per staged span and
+ * group must be 0 or 1).  A forced shape that cannot cover the row makes
+ * softmax_fwd return SOFTMAX_ERR_UNSUPPORTED.  Paths 4 and 5, and values
+ * outside 0..7, return SOFTMAX_ERR_ARG and leave the setting unchanged.
+ * Process-wide, not thread-safe.
  */
 int softmax_set_force_path(int path, int threads, int vpt, int group);
 
@@ -203,14 +209,14 @@ typedef struct {
     int path;              /* softmax_path_t actually chosen */
     int threads;           /* threads per block */
     int vpt;               /* 16-byte vectors per thread per tile (7: rows per lane group per span) */
-    int group;             /* lanes per row (1), cluster size (3, 5, 6), chunks per row (4), else 1 */
-    int launches;          /* kernels per call: 1, or 2 for the SPLIT path */
+    int group;             /* lanes per row (1), cluster size (3, 6), else 1 */
+    int launches;          /* kernels per call (1) */
     int vec_store;         /* 1 if out has in's 16-byte phase (vector stores) */
-    int64_t grid;          /* blocks of the (first) kernel */
+    int64_t grid;          /* blocks of the kernel */
     int64_t smem_bytes;    /* dynamic shared memory per block */
-    int64_t scratch_bytes; /* device scratch the call needs (SPLIT only) */
-    int64_t hbm_bytes;     /* algorithmic bytes: 2 * rows * cols * elem (3x for SPLIT, STREAM) */
-    int stages;            /* shared-memory ring stages per block (RING), else 0 */
+    int64_t scratch_bytes; /* device scratch the call needs: 0 on every path */
+    int64_t hbm_bytes;     /* bytes moved: 2 * rows * cols * elem (3x for STREAM, whose
+                              second read is usually served by L2) */
     int whole_vectors;     /* 1 if every row is whole 16-byte vectors (in and out 16-byte
                               aligned, row stride and width multiples of 16 bytes): the
                               kernels then run their variants without edge tests */
@@ -236,12 +242,13 @@ int softmax_plan(uint64_t in_addr, uint64_t out_addr, int64_t rows, int64_t cols
 int softmax_check_device_error(cudaStream_t stream);
 
 /*
- * Test hooks for the bounded waits of the CLUSTER and RING paths.  wait_limit_ns
- * bounds each wait on a TMA completion barrier (default 1 s; <= 0 restores it;
- * values above 1 s are capped at 1 s, since the waits time 32-bit intervals).
- * starve != 0 makes the next launches skip arming that barrier, so the wait
- * can only run out: the kernel records SOFTMAX_ERR_TIMEOUT, skips its stores
- * and returns normally.  Process-wide, not thread-safe.
+ * Test hooks for the bounded waits of the cluster paths (CLUSTER, STREAM and
+ * the masked STREAM).  wait_limit_ns bounds each wait for the cluster's
+ * (max, sum) exchange (default 1 s; <= 0 restores it; values above 1 s are
+ * capped at 1 s, since the waits time 32-bit intervals).  starve != 0 makes
+ * the next launches send no state, so every exchange wait can only run out:
+ * the kernel records SOFTMAX_ERR_TIMEOUT, skips its stores and returns
+ * normally.  Process-wide, not thread-safe.
  */
 int softmax_set_wait_test(int64_t wait_limit_ns, int starve);
 
@@ -259,27 +266,32 @@ int softmax_set_wait_test(int64_t wait_limit_ns, int starve);
 int softmax_set_launch_overlap(int enable);
 
 /*
- * softmax_fwd_noalloc -- the same softmax for callers that cannot allocate
- * device memory.  (The pages have no counterpart: this entry point answers a
- * deployment constraint, not a step of the method.)
+ * softmax_fwd_noalloc -- the grid-wide split path for callers that cannot
+ * allocate device memory.  (The pages have no counterpart: this entry point
+ * answers a deployment constraint, not a step of the method.)
  *
- * softmax_fwd's split path takes a little scratch per call from a stream-
- * ordered memory pool.  Some callers cannot allow that: code running under an
+ * The split path cuts every row into chunks spread over all SMs, which suits
+ * a few very long rows (one fp32 row of 4 M elements: about 3x faster than
+ * softmax_fwd's streaming cluster, which can give a row at most 16 SMs).  Its
+ * two passes meet in a global array of per-chunk (s, l) states: scratch
+ * memory.  Some callers cannot obtain scratch: code running under an
  * allocator that a host framework owns exclusively, real-time loops where an
  * allocation's latency or failure is not acceptable, or processes that must
- * not grow their device footprint after start-up.  This entry point always
- * runs the split path (two passes, 3 element crossings) with its per-chunk
+ * not grow their device footprint after start-up.  This entry point keeps the
  * states in a fixed array of SOFTMAX_NOALLOC_MAX_STATES (s, l) pairs
  * (512 KiB) compiled into the library; every GPU that loads the library holds
  * that array until the process exits.  It calls no cudaMalloc, cudaFree or
- * other allocating routine.
+ * other allocating routine.  It always takes the split path (two passes, 3
+ * element crossings).
  *   - Arguments, layout and status codes are those of softmax_fwd.  rows may
  *     be at most SOFTMAX_NOALLOC_MAX_STATES; larger calls return
  *     SOFTMAX_ERR_SCRATCH_LIMIT before any launch (each row needs at least one
  *     state; chunks per row are reduced to fit).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  The cached address belongs
+ *     to the device's primary context: after cudaDeviceReset on that device,
+ *     do not call this entry point there again in the same process.
  *   - Every call on a device shares the array and leaves its states there.
  *     Nothing in it needs to start at zero: the second pass reads only states
  *     the first pass of the same call wrote.  Calls whose kernels overlap on
@@ -351,7 +363,9 @@ int softmax_autotune_clear(void);
 /* Version of this ABI: major * 10000 + minor * 100 + patch (1.1.0 adds the RING
  * path, 1.2.0 softmax_set_launch_overlap, 1.3.0 the STREAM path and
  * softmax_plan_t.whole_vectors, 1.4.0 the autotune calls and softmax_fwd_masked,
- * 1.5.0 the PACKED path and softmax_fwd_host). */
+ * 1.5.0 the PACKED path and softmax_fwd_host; 2.0.0 removes the RING path and
+ * softmax_plan_t.stages, and softmax_fwd no longer takes the SPLIT path or any
+ * scratch). */
 int softmax_abi_version(void);
 
 #ifdef __cplusplus

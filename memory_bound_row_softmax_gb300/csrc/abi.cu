@@ -7,13 +7,13 @@
 // Softmax", sections "CUDA optimized for block per row" and "CUDA scaling
 // threads": wide rows need more threads per row so that enough loads are in
 // flight):
-//   cols <= 1024                       path 1, 2..32 lanes per row
-//   rows of whole aligned 16-B vectors path 5, persistent blocks / clusters fed
-//                                      by a TMA ring (cluster size grows with
-//                                      the row), if they can fill the GPU
-//   other rows fitting a block         path 2, a block per row in registers
-//   other rows fitting a cluster       path 3, a cluster per row
-//   otherwise                          path 4, rows split over the grid (2 passes)
+//   narrow dense rows off the 16-byte grid  path 7, staged through shared memory
+//   rows a warp's registers hold            path 1, 2..32 lanes per row
+//   16-bit rows a cluster's registers hold  path 3, a cluster per row
+//   other rows a block's registers hold     path 2, a block per row
+//   longer rows                             path 6, a cluster per row streaming
+//                                           its slices twice
+// Every path keeps its partial states on chip: no call allocates memory.
 #include <algorithm>
 #include <cmath>
 #include <atomic>
@@ -30,7 +30,7 @@ using namespace mbrs;
 
 namespace {
 
-constexpr int kAbiVersion = 10500;  // 1.5.0
+constexpr int kAbiVersion = 20000;  // 2.0.0
 constexpr int kVecBytes = 16;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDefaultWaitNs = 1000000000;  // 1 s
@@ -43,8 +43,8 @@ std::atomic<int> g_starve{0};
 std::atomic<int> g_overlap{1};
 
 struct Plan {
-    int path = 0, threads = 0, vpt = 0, group = 1, launches = 0, vec_store = 0, stages = 0, whole = 0;
-    int64_t grid = 0, smem = 0, scratch = 0, hbm = 0, chunks = 1, chunk_vecs = 0, slice_vecs = 0;
+    int path = 0, threads = 0, vpt = 0, group = 1, launches = 0, vec_store = 0, whole = 0;
+    int64_t grid = 0, smem = 0, hbm = 0;
 };
 
 // A launch shape asked for: path 0 = automatic; threads / vpt / group 0 =
@@ -56,12 +56,6 @@ struct Shape {
 Shape forced_shape() {
     return Shape{g_force_path.load(), g_force_threads.load(), g_force_vpt.load(), g_force_group.load()};
 }
-
-// Ring sizing: shared memory a block may fill with stages (of the ~228 KB an
-// SM has, leaving room for the per-block reserve), and the blocks per SM that
-// the ring aims for.
-constexpr int64_t kRingSmemPerSm = 220 * 1024;
-constexpr int kRingMaxStages = 32;
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int next_pow2(int64_t v) {
@@ -166,9 +160,6 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
     p->hbm = 2 * rows * cols * es;
 
     const int fpath = force.path, fth = force.threads, fvpt = force.vpt, fgrp = force.group;
-    // the ring moves whole aligned vectors only: every row start and row end on 16 bytes
-    const bool ring_ok = (in % kVecBytes) == 0 && (out % kVecBytes) == 0 && uniform &&
-                         ((cols * es) % kVecBytes) == 0;
     int path = fpath;
     if (path == SOFTMAX_PATH_AUTO) {
         if (row_stride == cols && (cols * es) % kVecBytes != 0 && p->vec_store && cols <= 48) {
@@ -191,16 +182,17 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             // ring at every such width measured (8192 x 2816 fp16: block 14.4
             // us, ring 17.1; 4096 x 2816 fp32: 14.0 against 19.5)
             path = SOFTMAX_PATH_CTA;
-        } else if (rows * 16 >= sms && rows * 16 <= kMaxGrid) {
-            // longer rows: a cluster streaming its slices twice, about one
-            // 1024-vector tile per block.  Measured against the TMA ring and
-            // the one-tile TMA cluster it wins at every long width tried
-            // (1525 x 32768 fp32: 58.8 us, ring 62.5, TMA cluster 64.2;
-            // 381 x 131072: 60.4, ring 74.0; 300 x 40000: 18.7, ring 25.0)
-            path = SOFTMAX_PATH_STREAM;
         } else {
-            // a few very long rows: spread over the whole grid
-            path = SOFTMAX_PATH_SPLIT;
+            // longer rows: a cluster streaming its slices twice, about one
+            // 1024-vector tile per block.  Measured against a TMA-fed ring and
+            // a TMA-staged cluster it won at every long width tried
+            // (1525 x 32768 fp32: 58.8 us, ring 62.5, TMA cluster 64.2;
+            // 381 x 131072: 60.4, ring 74.0; 300 x 40000: 18.7, ring 25.0).
+            // Also for a few very long rows (rows * 16 < SMs), which no
+            // cluster can spread over the whole GPU: a grid-wide split would
+            // need its states in global scratch (bf16 9 x 262144: 4.7 us
+            // here, 6.1 split; fp32 3 x 10^6: 12.3 against 10.1)
+            path = SOFTMAX_PATH_STREAM;
         }
     }
     p->path = path;
@@ -286,13 +278,12 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             break;
         }
         case SOFTMAX_PATH_CLUSTER: {
-            // 16-bit rows: slices of 256 threads x 8 vectors held in registers;
-            // fp32 rows (which would spill there): TMA-staged slices of 512 or
-            // 1024 threads x 4 vectors
-            const bool regs = es == 2 && fth <= 0 && fvpt <= 0 && cdiv(nv, 2048) <= 16;
-            int threads = fth > 0 ? fth : (regs ? 256 : (nv <= 16 * 512 * 4 ? 512 : 1024));
-            int vpt = fvpt > 0 ? fvpt : (regs ? 8 : 4);
-            int64_t csize = fgrp > 0 ? fgrp : cdiv(nv, (int64_t)threads * vpt);
+            // 16-bit rows: slices of 256 (or 512) threads x 8 vectors held in
+            // registers, as many blocks as the row needs (fp32 rows would
+            // spill there)
+            const int threads = fth > 0 ? fth : (cdiv(nv, 256 * 8) <= 16 ? 256 : 512);
+            const int vpt = fvpt > 0 ? fvpt : 8;
+            const int64_t csize = fgrp > 0 ? fgrp : cdiv(nv, (int64_t)threads * vpt);
             if (!cluster_shape_ok(threads, vpt, es) || csize < 1 || csize > 16) return SOFTMAX_ERR_UNSUPPORTED;
             if (cdiv(nv, csize) > (int64_t)threads * vpt) return SOFTMAX_ERR_UNSUPPORTED;
             if (rows * csize > kMaxGrid) return SOFTMAX_ERR_UNSUPPORTED;
@@ -300,51 +291,7 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             p->vpt = vpt;
             p->group = (int)csize;
             p->grid = rows * csize;
-            p->smem = cluster_smem_bytes(threads, vpt);
-            break;
-        }
-        case SOFTMAX_PATH_RING: {
-            if (!ring_ok) return SOFTMAX_ERR_UNSUPPORTED;
-            // cluster size: slices of at most 1024 x 4 vectors for fp32 and 512 x 4
-            // for 16-bit data (whose 1024-thread ring would spill at 64 registers),
-            // more blocks while the rows alone cannot occupy every SM
-            const int64_t max_slice = (es == 4 || cdiv(nv, 2048) > 16) ? 4096 : 2048;
-            int64_t csize = fgrp > 0 ? fgrp : std::max<int64_t>(1, cdiv(nv, max_slice));
-            if (fgrp <= 0)
-                while (csize < 16 && rows * csize < sms && cdiv(nv, csize * 2) >= 256) csize *= 2;
-            if (csize < 1 || csize > 16) return SOFTMAX_ERR_UNSUPPORTED;
-            const int64_t slice = cdiv(nv, csize);
-            // 4 vectors per thread (fewer only for slices under 256 vectors)
-            int vpt = fvpt > 0 ? fvpt : (int)std::min<int64_t>(4, cdiv(slice, 64));
-            if (vpt == 3) vpt = 4;
-            int threads = fth > 0 ? fth : std::max(64, next_pow2(cdiv(slice, vpt)));
-            if (csize > 1 && fth <= 0 && threads < 256) {  // cluster rings start at 256 threads
-                threads = 256;
-                vpt = (int)std::max<int64_t>(2, cdiv(slice, 256));
-                if (vpt == 3) vpt = 4;
-            }
-            if (!ring_shape_ok(threads, vpt, (int)csize) || (int64_t)threads * vpt < slice)
-                return SOFTMAX_ERR_UNSUPPORTED;
-            const int64_t stage_bytes = slice * kVecBytes;
-            // blocks per SM the ring aims for: 1024 threads' worth (<= 64 registers each)
-            int per_sm = std::max(1, std::min(8, 1024 / threads));
-            int64_t stages = 0;
-            for (; per_sm >= 1; --per_sm) {
-                stages = (kRingSmemPerSm / per_sm - 1024) / stage_bytes;
-                if (stages >= 2) break;
-            }
-            if (stages < 2) return SOFTMAX_ERR_UNSUPPORTED;
-            stages = std::min<int64_t>(stages, kRingMaxStages);
-            // no more stages than a block has rows to prefetch
-            const int64_t units = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)sms * per_sm / csize));
-            stages = std::max<int64_t>(2, std::min<int64_t>(stages, cdiv(rows, units)));
-            p->threads = threads;
-            p->vpt = vpt;
-            p->group = (int)csize;
-            p->stages = (int)stages;
-            p->slice_vecs = slice;
-            p->smem = ring_smem_bytes((int)stages, (int)slice, threads);
-            p->grid = units * csize;  // estimate; the launch sizes it from occupancy
+            p->smem = cluster_smem_bytes(threads);
             break;
         }
         case SOFTMAX_PATH_PACKED: {
@@ -366,12 +313,20 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             // blocks would need more than two tiles each; then as many blocks
             // (<= 16) as give about one tile each.  Measured: 1525 x 32768 fp32
             // 58.8 us on 8 x (256 x 4); 190 x 262144 64.2 us on 16 x (512 x 4)
-            // (78.6 on 256); 64 x 2^20 105.6 us on 16 x (1024 x 4) (139 on 256)
+            // (78.6 on 256); 64 x 2^20 105.6 us on 16 x (1024 x 4) (139 on 256).
+            // With too few rows to give every SM a block (rows * 16 < SMs) a
+            // block's bytes in flight bound the time, so the blocks grow to one
+            // tile per block, up to 1024 threads (bf16 9 x 262144: 4.7 us on
+            // 512 threads, 5.5 on 256; fp32 3 x 10^6: 12.3 on 1024, 14.5 on 512)
             const int vpt = fvpt > 0 ? fvpt : 4;
             int threads = fth;
             if (threads <= 0) {
                 threads = 256;
-                while (threads < 1024 && cdiv(nv, 16 * (int64_t)threads * vpt) > 2) threads *= 2;
+                if (rows * 16 < sms) {
+                    while (threads < 1024 && cdiv(nv, 16 * (int64_t)vpt) > threads) threads *= 2;
+                } else {
+                    while (threads < 1024 && cdiv(nv, 16 * (int64_t)threads * vpt) > 2) threads *= 2;
+                }
             }
             const int64_t csize =
                 fgrp > 0 ? fgrp : std::min<int64_t>(16, std::max<int64_t>(1, cdiv(nv, (int64_t)threads * vpt)));
@@ -385,64 +340,10 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             p->hbm = 3 * rows * cols * es;
             break;
         }
-        case SOFTMAX_PATH_SPLIT: {
-            const int threads = fth > 0 ? fth : 256;
-            const int vpt = fvpt > 0 ? fvpt : 4;
-            if (!split_shape_ok(threads, vpt)) return SOFTMAX_ERR_UNSUPPORTED;
-            const int64_t tile = (int64_t)threads * vpt;
-            const int64_t per_sm = 2048 / threads;
-            int64_t k;
-            if (fgrp > 0) {
-                k = std::min<int64_t>(fgrp, nv);
-            } else {
-                const int64_t target = (int64_t)sms * per_sm * 2;
-                k = std::max<int64_t>(1, std::min(cdiv(target, rows), cdiv(nv, tile)));
-            }
-            const int64_t chunk_vecs = cdiv(cdiv(nv, k), tile) * tile;
-            k = cdiv(nv, chunk_vecs);
-            if (rows > INT64_MAX / k / 8) return SOFTMAX_ERR_UNSUPPORTED;
-            p->threads = threads;
-            p->vpt = vpt;
-            p->group = (int)std::min<int64_t>(k, 0x7fffffff);
-            p->chunks = k;
-            p->chunk_vecs = chunk_vecs;
-            p->grid = std::min<int64_t>(rows * k, (int64_t)sms * per_sm * 4);
-            p->scratch = rows * k * 8;
-            p->launches = 2;
-            p->hbm = 3 * rows * cols * es;
-            break;
-        }
         default:
             return SOFTMAX_ERR_UNSUPPORTED;
     }
     return SOFTMAX_OK;
-}
-
-// Stream-ordered scratch for the split path: one pool per device that keeps
-// its memory (release threshold = max), so steady-state calls do not reach
-// the driver's allocator.
-cudaError_t scratch_pool(int dev, cudaMemPool_t *pool) {
-    static std::mutex mu;
-    static cudaMemPool_t pools[kMaxDevices] = {};
-    std::lock_guard<std::mutex> lock(mu);
-    cudaMemPool_t &slot = pools[dev & (kMaxDevices - 1)];
-    if (!slot) {
-        cudaMemPoolProps props;
-        std::memset(&props, 0, sizeof(props));
-        props.allocType = cudaMemAllocationTypePinned;
-        props.location.type = cudaMemLocationTypeDevice;
-        props.location.id = dev;
-        cudaError_t e = cudaMemPoolCreate(&slot, &props);
-        if (e != cudaSuccess) {
-            slot = nullptr;
-            return e;
-        }
-        uint64_t keep = UINT64_MAX;
-        e = cudaMemPoolSetAttribute(slot, cudaMemPoolAttrReleaseThreshold, &keep);
-        if (e != cudaSuccess) return e;
-    }
-    *pool = slot;
-    return cudaSuccess;
 }
 
 int run(const Plan &p, const LaunchArgs &a) {
@@ -453,35 +354,19 @@ int run(const Plan &p, const LaunchArgs &a) {
         case SOFTMAX_PATH_CLUSTER:
             e = launch_cluster(a, p.threads, p.vpt, p.group, g_wait_ns.load(), g_starve.load());
             break;
-        case SOFTMAX_PATH_STREAM: e = launch_stream(a, p.threads, p.vpt, p.group, g_wait_ns.load()); break;
+        case SOFTMAX_PATH_STREAM:
+            e = launch_stream(a, p.threads, p.vpt, p.group, g_wait_ns.load(), g_starve.load());
+            break;
         case SOFTMAX_PATH_PACKED: e = launch_packed(a, kPackedThreads * p.vpt, p.grid); break;
-        case SOFTMAX_PATH_RING: {
-            RingCfg c{p.threads, p.vpt, p.group, p.stages, (int)p.slice_vecs, p.smem};
-            e = launch_ring(a, c, g_wait_ns.load(), g_starve.load(), nullptr);
-            break;
-        }
-        case SOFTMAX_PATH_SPLIT: {
-            int dev = 0;
-            cudaMemPool_t pool;
-            void *scratch = nullptr;
-            e = cudaGetDevice(&dev);
-            if (e == cudaSuccess) e = scratch_pool(dev, &pool);
-            if (e == cudaSuccess) e = cudaMallocFromPoolAsync(&scratch, (size_t)p.scratch, pool, a.stream);
-            if (e == cudaSuccess) {
-                e = launch_split(a, p.threads, p.vpt, p.chunks, p.chunk_vecs, p.grid, scratch);
-                cudaError_t f = cudaFreeAsync(scratch, a.stream);
-                if (e == cudaSuccess) e = f;
-            }
-            break;
-        }
         default: return SOFTMAX_ERR_UNSUPPORTED;
     }
     if (e == cudaErrorInvalidValue) return SOFTMAX_ERR_UNSUPPORTED;
     return e == cudaSuccess ? SOFTMAX_OK : SOFTMAX_ERR_CUDA;
 }
 
-// Split-path shape for softmax_fwd_noalloc: as the split path's own choice,
-// with chunks per row capped so that rows * chunks fits the fixed array.
+// Split-path shape for softmax_fwd_noalloc: enough chunks to give every SM two
+// blocks' worth of 256-thread blocks twice over, no chunk smaller than one
+// tile, and chunks per row capped so that rows * chunks fits the fixed array.
 int plan_noalloc(uint64_t in, int64_t rows, int64_t cols, int64_t row_stride, int dtype, int sms, int64_t *chunks,
                  int64_t *chunk_vecs, int64_t *grid) {
     if (rows > kNoAllocMaxStates) return SOFTMAX_ERR_SCRATCH_LIMIT;
@@ -566,9 +451,9 @@ Shape call_shape(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t 
 
 // Candidate shapes for rows of up to nv vectors: the automatic choice first,
 // the shared-memory staged path for narrow dense rows, then every lane-group /
-// block / cluster shape that can hold the row, the streaming cluster at three
-// block sizes and, for whole aligned rows, the ring.
-std::vector<Shape> tune_candidates(int64_t nv, int es, bool ring_ok, bool packed_ok) {
+// block / cluster shape that can hold the row and the streaming cluster at
+// three block sizes.
+std::vector<Shape> tune_candidates(int64_t nv, int es, bool packed_ok) {
     std::vector<Shape> c;
     c.push_back(Shape{});
     if (packed_ok) c.push_back(Shape{SOFTMAX_PATH_PACKED, 0, 1, 0});
@@ -584,13 +469,10 @@ std::vector<Shape> tune_candidates(int64_t nv, int es, bool ring_ok, bool packed
             if (cta_shape_ok(t, v) && (int64_t)t * v >= nv) c.push_back(Shape{SOFTMAX_PATH_CTA, t, v, 0});
         }
     if (nv > 512) {
-        for (int t = 256; t <= 1024; t *= 2)
-            for (int v : {2, 4, 8}) {
-                if (!cluster_shape_ok(t, v, es) || cdiv(nv, (int64_t)t * v) > 16) continue;
-                c.push_back(Shape{SOFTMAX_PATH_CLUSTER, t, v, 0});
-            }
+        for (int t = 256; t <= 512; t *= 2)
+            if (cluster_shape_ok(t, 8, es) && cdiv(nv, (int64_t)t * 8) <= 16)
+                c.push_back(Shape{SOFTMAX_PATH_CLUSTER, t, 8, 0});
         for (int t = 256; t <= 1024; t *= 2) c.push_back(Shape{SOFTMAX_PATH_STREAM, t, 4, 0});
-        if (ring_ok) c.push_back(Shape{SOFTMAX_PATH_RING, 0, 0, 0});
     }
     return c;
 }
@@ -600,10 +482,9 @@ std::vector<Shape> candidates_for(uint64_t in, uint64_t out, int64_t cols, int64
     const bool uniform = ((row_stride * es) % kVecBytes) == 0;
     const int64_t head = (int64_t)((in % kVecBytes) / es);
     const int64_t nv = uniform ? cdiv(head + cols, V) : cdiv(cols + V - 1, V);
-    const bool ring_ok = (in % kVecBytes) == 0 && (out % kVecBytes) == 0 && uniform && ((cols * es) % kVecBytes) == 0;
     const bool packed_ok = row_stride == cols && (in % kVecBytes) == (out % kVecBytes) &&
                            packed_smem_bytes(kPackedThreads, cols, es) <= kPackedMaxSmem;
-    return tune_candidates(nv, es, ring_ok, packed_ok);
+    return tune_candidates(nv, es, packed_ok);
 }
 
 void fill_public_plan(const Plan &p, softmax_plan_t *plan) {
@@ -615,9 +496,8 @@ void fill_public_plan(const Plan &p, softmax_plan_t *plan) {
     plan->vec_store = p.vec_store;
     plan->grid = p.grid;
     plan->smem_bytes = p.smem;
-    plan->scratch_bytes = p.scratch;
+    plan->scratch_bytes = 0;  // no path takes scratch
     plan->hbm_bytes = p.hbm;
-    plan->stages = p.stages;
     plan->whole_vectors = p.whole;
 }
 
@@ -717,7 +597,7 @@ int softmax_fwd_masked(const void *in, void *out, int64_t rows, int64_t cols, in
     switch (p.path) {
         case SOFTMAX_PATH_WARP: e = launch_warp_masked(a, p.threads, p.group, p.vpt, p.grid); break;
         case SOFTMAX_PATH_CTA: e = launch_cta_masked(a, p.threads, p.vpt, p.grid); break;
-        default: e = launch_stream_masked(a, p.threads, p.vpt, p.group, g_wait_ns.load()); break;
+        default: e = launch_stream_masked(a, p.threads, p.vpt, p.group, g_wait_ns.load(), g_starve.load()); break;
     }
     if (e == cudaErrorInvalidValue) return SOFTMAX_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return SOFTMAX_ERR_CUDA;
@@ -848,7 +728,8 @@ const char *softmax_status_string(int status) {
 int softmax_last_path(void) { return g_last_path.load(); }
 
 int softmax_set_force_path(int path, int threads, int vpt, int group) {
-    if (path < SOFTMAX_PATH_AUTO || path > SOFTMAX_PATH_PACKED) return SOFTMAX_ERR_ARG;
+    if (path < SOFTMAX_PATH_AUTO || path > SOFTMAX_PATH_PACKED || path == SOFTMAX_PATH_SPLIT || path == 5)
+        return SOFTMAX_ERR_ARG;
     g_force_path.store(path);
     g_force_threads.store(threads > 0 ? threads : 0);
     g_force_vpt.store(vpt > 0 ? vpt : 0);
@@ -873,24 +754,16 @@ int softmax_plan(uint64_t in_addr, uint64_t out_addr, int64_t rows, int64_t cols
                    call_shape(in_addr, out_addr, rows, cols, row_stride, dtype), &p);
     if (st != SOFTMAX_OK) return st;
     fill_public_plan(p, plan);
-    if (p.path == SOFTMAX_PATH_RING && num_sms == 0) {  // the persistent grid the launch will use
-        RingCfg c{p.threads, p.vpt, p.group, p.stages, (int)p.slice_vecs, p.smem};
-        LaunchArgs a{nullptr, nullptr, rows, cols, row_stride, dtype, p.vec_store, nullptr, 0, p.whole};
-        int64_t grid = 0;
-        if (launch_ring(a, c, 0, 0, &grid) != cudaSuccess) return SOFTMAX_ERR_CUDA;
-        plan->grid = grid;
-    }
     return SOFTMAX_OK;
 }
 
 int softmax_check_device_error(cudaStream_t stream) {
-    unsigned int word = 0, ring_word = 0;
+    unsigned int word = 0;
     if (read_clear_error_word(stream, &word) != cudaSuccess) return SOFTMAX_ERR_CUDA;
-    if (read_clear_ring_error_word(&ring_word) != cudaSuccess) return SOFTMAX_ERR_CUDA;
     unsigned int attn_word = 0;
     if (attn::read_clear_attn_error_word(&attn_word) != cudaSuccess) return SOFTMAX_ERR_CUDA;
-    if ((word | ring_word) & kErrNotCluster) return SOFTMAX_ERR_CUDA;
-    return (word | ring_word | attn_word) ? SOFTMAX_ERR_TIMEOUT : SOFTMAX_OK;
+    if (word & kErrNotCluster) return SOFTMAX_ERR_CUDA;
+    return (word | attn_word) ? SOFTMAX_ERR_TIMEOUT : SOFTMAX_OK;
 }
 
 int softmax_set_wait_test(int64_t wait_limit_ns, int starve) {

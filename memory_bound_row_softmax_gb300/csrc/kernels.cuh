@@ -1,28 +1,29 @@
-// kernels.cuh -- the four row-softmax kernels (templates; instantiated per path
+// kernels.cuh -- the row-softmax kernels (templates; instantiated per path
 // in k_*.cu).
 //
 //   path 1  k_warp_rows     G lanes (2..32) own a row, VPT vectors per lane;
 //                           shuffle-only reduction, no shared memory.
 //   path 2  k_cta_rows      a block owns a row held in registers; warp
 //                           shuffles, then one shared-memory exchange.
-//   path 3  k_cluster_rows  a cluster of blocks owns a row; each block pulls
-//                           its slice with a TMA bulk copy, and the blocks
-//                           exchange their (max, sum) through distributed
-//                           shared memory -- still one read, one write.
-//   path 5  k_ring_rows     persistent blocks (or clusters of up to 16 blocks,
-//                           each owning a slice of the row) loop over their
-//                           rows; one thread keeps a ring of shared-memory
-//                           stages filled with 1-D TMA bulk copies, so the
-//                           loads of the next rows are in flight while the
-//                           current row is reduced and stored.  Rows must be
-//                           made of whole aligned 16-byte vectors.
-//   path 4  k_split_stats / k_split_apply
+//   path 3  k_cluster_rows  a cluster of blocks owns a row, each block holding
+//                           its slice in registers; the blocks exchange their
+//                           (max, sum) through distributed shared memory --
+//                           still one read, one write.
+//   path 6  k_cluster_stream
+//                           a cluster of blocks owns a row of any length and
+//                           streams its slices twice (states exchanged in
+//                           distributed shared memory between the passes).
+//   path 7  k_packed_rows   narrow dense rows staged through shared memory,
+//                           one thread per row.
+//   k_split_stats / k_split_apply
 //                           rows cut into chunks spread over the whole grid;
 //                           pass 1 streams each chunk into a (max, sum) state
-//                           in scratch, pass 2 merges a row's states, re-reads
-//                           its chunk and writes it (the two-pass form that a
-//                           reduction spanning many blocks needs: page
-//                           "Kernel Fusion", section "What fusion cannot fix").
+//                           in a global array, pass 2 merges a row's states,
+//                           re-reads its chunk and writes it (the two-pass
+//                           form that a reduction spanning many blocks needs:
+//                           page "Kernel Fusion", section "What fusion cannot
+//                           fix").  Only softmax_fwd_noalloc runs them, with
+//                           the states in a fixed array inside the library.
 //
 // All paths keep the per-thread (s_t, l_t) scheme of common.cuh: one exp per
 // element, one merge round per row.  Variables named m / M below hold the
@@ -120,19 +121,18 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
 // path 3: a cluster per row
 // ---------------------------------------------------------------------------
 constexpr int kMaxCluster = 16;
-constexpr uint32_t kBulkPiece = 16384;  // bytes per cp.async.bulk
 
 // The device error word that bounded waits set when they run out.  Each
-// translation unit has its own copy; the cluster path's unit (the only one
+// translation unit has its own copy; the cluster paths' unit (the only one
 // with waits) owns the reader.
 static __device__ unsigned int g_error_word = 0;
 
-template <int THREADS, int VPT>
+// Shared memory of the cluster kernels: the state exchange barrier, the
+// block-merge scratch and one exchange slot per cluster block.
+template <int THREADS>
 struct ClusterSmem {
-    static constexpr int kStageBytes = THREADS * VPT * kVecBytes;
-    static constexpr int kBarOff = kStageBytes;      // TMA completion barrier
-    static constexpr int kXbarOff = kBarOff + 8;     // state exchange barrier
-    static constexpr int kRedOff = kBarOff + 16;
+    static constexpr int kXbarOff = 0;  // state exchange barrier
+    static constexpr int kRedOff = 16;
     static constexpr int kSlotOff = kRedOff + (THREADS / 32) * 8;
     static constexpr int kBytes = kSlotOff + kMaxCluster * 8;
 };
@@ -146,13 +146,14 @@ struct ClusterSmem {
 // has received every peer's state, so no store can reach a block that has
 // gone.  Returns the merged row state in (m, l) on every thread; false when a
 // wait ran out (then the block stays resident for as long as a late peer's
-// waits can last).
+// waits can last).  starve != 0 (a test hook) sends nothing, so every wait of
+// the cluster runs out and no store is in flight when the blocks leave.
 template <int NW>
 __device__ __forceinline__ bool cluster_exchange(float &m, float &l, float2 *slots, uint32_t xbar, uint32_t rank,
-                                                 uint32_t csize, int64_t wait_ns) {
+                                                 uint32_t csize, int64_t wait_ns, int starve) {
     const int lane = threadIdx.x & 31;
     cluster_wait_acquire();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && !starve) {
         const uint32_t my_slot = smem_addr(slots + rank);
         for (uint32_t q = 0; q < csize; ++q) st_async_f2(map_to_rank(my_slot, q), m, l, map_to_rank(xbar, q));
     }
@@ -169,10 +170,10 @@ __device__ __forceinline__ bool cluster_exchange(float &m, float &l, float2 *slo
     return ok;
 }
 
-// TMA = true: each block pulls its slice into shared memory with bulk copies;
-// TMA = false: each block loads its slice straight into registers (no
-// staging, so occupancy is bounded by registers alone).
-template <typename T, int THREADS, int VPT, bool TMA, bool WHOLE>
+// Each block loads its slice straight into registers (no staging, so
+// occupancy is bounded by registers alone), reduces it, exchanges its state
+// with the cluster and stores its slice.
+template <typename T, int THREADS, int VPT, bool WHOLE>
 __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS))
     k_cluster_rows(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store,
                    int64_t wait_ns, int starve) {
@@ -183,13 +184,10 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     }
     constexpr int V = Elem<T>::kVec;
     constexpr int NW = THREADS / 32;
-    // the layout the launch allocated: no staging area without TMA
-    using L = ClusterSmem<THREADS, TMA ? VPT : 0>;
+    using L = ClusterSmem<THREADS>;
     extern __shared__ __align__(128) unsigned char smem[];
-    const uint4 *stage = reinterpret_cast<const uint4 *>(smem);
     float2 *red = reinterpret_cast<float2 *>(smem + L::kRedOff);
     float2 *slots = reinterpret_cast<float2 *>(smem + L::kSlotOff);
-    const uint32_t bar = smem_addr(smem + L::kBarOff);
     const uint32_t xbar = smem_addr(smem + L::kXbarOff);
     const int tid = threadIdx.x;
 
@@ -197,72 +195,26 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     const int64_t row = blockIdx.x / csize;
     RowView<T> rv(in + row * stride, out + row * stride, cols, vec_store != 0);
 
-    // this block's slice of the row's vectors, and the part of it made of whole
-    // vectors (the only part a bulk copy may move: 16-byte aligned, inside the row)
+    // this block's slice of the row's vectors
     const int64_t per = (rv.nvec + csize - 1) / csize;
     const int64_t s0 = min((int64_t)rank * per, rv.nvec), s1 = min(s0 + per, rv.nvec);
-    const int64_t first_full = rv.head > 0 ? 1 : 0;
-    const int64_t full_end = ((rv.head + cols) % V) != 0 ? rv.nvec - 1 : rv.nvec;
-    const int64_t f0 = max(s0, first_full), f1 = min(s1, full_end);
-    const uint32_t bytes = f1 > f0 ? (uint32_t)((f1 - f0) * kVecBytes) : 0u;
     if (tid == 0) prefetch_span_l2(in + row * stride, s0 * V - rv.head, s1 * V - rv.head, cols);
     pdl_enter();
 
-    bool ok = true;
-    Tile<T, VPT> tile;
     if (tid == 0) {
-        mbar_init(bar, 1);
         mbar_init(xbar, 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(xbar, csize * 8u);  // csize states will arrive
     }
     __syncthreads();
-    if constexpr (TMA) {
-        if (tid == 0 && !starve) {
-            if (bytes > 0) {
-                mbar_arrive_expect_tx(bar, bytes);
-                const char *src = reinterpret_cast<const char *>(rv.in + (f0 * V - rv.head));
-                const uint32_t dst = smem_addr(stage + (f0 - s0));
-                for (uint32_t off = 0; off < bytes; off += kBulkPiece)
-                    bulk_g2s(dst + off, src + off, min(kBulkPiece, bytes - off), bar);
-            } else {
-                mbar_arrive(bar);
-            }
-        }
-        // announce that this block runs: peers may write into its shared memory
-        // once they have waited on this arrival
-        __syncwarp();
-        cluster_arrive_relaxed();
-
-        ok = mbar_wait_bounded(bar, 0, wait_ns);
-        if (!ok) {
-            atomicOr(&g_error_word, kErrWaitTimeout);
-            // a copy may still be landing in this block's shared memory: give it
-            // one more bounded wait before the memory is reused or released
-            if (!starve) mbar_wait_bounded(bar, 0, wait_ns);
-        }
-#pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int64_t v = s0 + j * THREADS + tid;
-            if (v < s1) {
-                if (v >= f0 && v < f1)
-                    tile.set(j, stage[v - s0]);
-                else
-                    tile.load_one(j, rv, v);  // a partial vector at the row's edge
-            } else {
-                tile.set_empty(j);
-            }
-        }
-    } else {
-        cluster_arrive_relaxed();
-        tile.template load<WHOLE>(rv, s0 + tid, THREADS, s1);
-    }
+    cluster_arrive_relaxed();  // this block runs and its barrier is armed
+    Tile<T, VPT> tile;
+    tile.template load<WHOLE>(rv, s0 + tid, THREADS, s1);
     const float2 s = tile.stats();
     float m = s.x, l = s.y;
     block_merge<NW>(m, l, red);
-
-    if (!cluster_exchange<NW>(m, l, slots, xbar, rank, csize, wait_ns)) ok = false;
-    if (ok) tile.template scale_store<WHOLE>(rv, s0 + tid, THREADS, s1, out_factor(s.x, m, l));
+    if (cluster_exchange<NW>(m, l, slots, xbar, rank, csize, wait_ns, starve))
+        tile.template scale_store<WHOLE>(rv, s0 + tid, THREADS, s1, out_factor(s.x, m, l));
 }
 
 // ---------------------------------------------------------------------------
@@ -278,7 +230,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
 template <typename T, int THREADS, int VPT, bool WHOLE>
 __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS))
     k_cluster_stream(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store,
-                     int64_t wait_ns) {
+                     int64_t wait_ns, int starve) {
     if (!explicit_cluster()) {  // launched without clusters: touch no cluster state
         pdl_enter();
         if (threadIdx.x == 0) atomicOr(&g_error_word, kErrNotCluster);
@@ -287,7 +239,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     constexpr int V = Elem<T>::kVec;
     constexpr int NW = THREADS / 32;
     constexpr int64_t kTile = (int64_t)THREADS * VPT;
-    using L = ClusterSmem<THREADS, 0>;
+    using L = ClusterSmem<THREADS>;
     extern __shared__ __align__(128) unsigned char smem[];
     float2 *red = reinterpret_cast<float2 *>(smem + L::kRedOff);
     float2 *slots = reinterpret_cast<float2 *>(smem + L::kSlotOff);
@@ -299,7 +251,14 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     RowView<T> rv(in + row * stride, out + row * stride, cols, vec_store != 0);
     const int64_t per = (rv.nvec + csize - 1) / csize;
     const int64_t s0 = min((int64_t)rank * per, rv.nvec), s1 = min(s0 + per, rv.nvec);
-    if (tid == 0) prefetch_span_l2(rv.in, s0 * V - rv.head, min(s0 + kTile, s1) * V - rv.head, cols);
+    // the first kAhead + 1 tiles of the slice start moving into L2 before the
+    // launch-overlap wait; pass 1 then keeps kAhead tiles ahead of its loads
+    // (hints: a prefetch cannot change what a later load returns).  A block
+    // holds one tile in registers at a time, so without them its bytes in
+    // flight, not HBM, bound a slice of many tiles.
+    constexpr int64_t kAhead = 2;
+    if (tid == 0)
+        prefetch_span_l2(rv.in, s0 * V - rv.head, min(s0 + (kAhead + 1) * kTile, s1) * V - rv.head, cols);
     pdl_enter();
 
     if (tid == 0) {
@@ -313,6 +272,8 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     // pass 1: the slice's state
     float m = -INFINITY, l = 0.f;
     for (int64_t t0 = s0; t0 < s1; t0 += kTile) {
+        const int64_t p0 = t0 + (kAhead + 1) * kTile;
+        if (tid == 0 && p0 < s1) prefetch_span_l2(rv.in, p0 * V - rv.head, min(p0 + kTile, s1) * V - rv.head, cols);
         Tile<T, VPT> tile;
         tile.template load<WHOLE>(rv, t0 + tid, THREADS, s1);
         const float2 st = tile.stats();
@@ -321,7 +282,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
         m = M;
     }
     block_merge<NW>(m, l, red);
-    if (!cluster_exchange<NW>(m, l, slots, xbar, rank, csize, wait_ns)) return;
+    if (!cluster_exchange<NW>(m, l, slots, xbar, rank, csize, wait_ns, starve)) return;
 
     // pass 2: re-read and write (m is the row's S)
     const float inv = m == -INFINITY ? __int_as_float(0x7fc00000) : 1.f / l;
@@ -329,175 +290,6 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
         Tile<T, VPT> tile;
         tile.template load<WHOLE>(rv, t0 + tid, THREADS, s1);
         tile.template shift_store<WHOLE>(rv, t0 + tid, THREADS, s1, m, inv);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// path 5: persistent TMA ring (a block or a cluster per row, many rows each)
-// ---------------------------------------------------------------------------
-// Shared memory: `stages` slots of slice_vecs 16-byte vectors, one mbarrier
-// per slot, two exchange mbarriers, the block-merge scratch (2 x NW states)
-// and the cluster exchange slots (2 x 16 states); the last three are
-// double-buffered by row parity.
-struct RingLayout {
-    int64_t stage_bytes, bar_off, xbar_off, red_off, slot_off, bytes;
-    __host__ __device__ RingLayout(int stages, int slice_vecs, int threads) {
-        stage_bytes = (int64_t)slice_vecs * kVecBytes;
-        bar_off = stage_bytes * stages;
-        xbar_off = bar_off + 8 * stages;
-        red_off = xbar_off + 16;
-        red_off = (red_off + 15) & ~int64_t(15);
-        slot_off = red_off + 2 * (threads / 32) * 8;
-        bytes = slot_off + 2 * kMaxCluster * 8;
-    }
-};
-
-// CLUSTER = false: one block per row (no exchange code, fewer registers);
-// CLUSTER = true: launched with clusters of csize blocks, each owning a slice,
-// bounded to 64 registers so two 512-thread blocks fit on an SM.
-template <typename T, int THREADS, int VPT, bool CLUSTER>
-__global__ void __launch_bounds__(THREADS, CLUSTER ? (THREADS >= 1024 ? 1 : 1024 / THREADS)
-                                                   : (THREADS >= 512 ? 1 : 512 / THREADS))
-    k_ring_rows(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int stages, int slice_vecs,
-                int64_t wait_ns, int starve) {
-    if constexpr (CLUSTER) {
-        if (!explicit_cluster()) {  // launched without clusters: touch no cluster state
-            pdl_enter();
-            if (threadIdx.x == 0) atomicOr(&g_error_word, kErrNotCluster);
-            return;
-        }
-    }
-    constexpr int V = Elem<T>::kVec;
-    constexpr int NW = THREADS / 32;
-    extern __shared__ __align__(128) unsigned char smem[];
-    const RingLayout L(stages, slice_vecs, THREADS);
-    const uint32_t stage_base = smem_addr(smem);
-    const uint32_t bar_base = smem_addr(smem + L.bar_off);
-    float2 *red = reinterpret_cast<float2 *>(smem + L.red_off);
-    float2 *slots = reinterpret_cast<float2 *>(smem + L.slot_off);
-    const int tid = threadIdx.x, lane = tid & 31;
-
-    const uint32_t rank = CLUSTER ? cluster_rank() : 0u, csize = CLUSTER ? cluster_size() : 1u;
-    const int64_t cid = blockIdx.x / csize, ncl = gridDim.x / csize;
-    // every row is nvec whole vectors; this block owns vectors [s0, s1) of each
-    const int64_t nvec = cols / V;
-    const int64_t per = (nvec + csize - 1) / csize;
-    const int64_t s0 = min((int64_t)rank * per, nvec), s1 = min(s0 + per, nvec);
-    const int nmine = (int)(s1 - s0);
-    const uint32_t bytes = (uint32_t)nmine * kVecBytes;
-    // rows cid, cid + ncl, ... (the same count for every block of a cluster)
-    const int64_t nrows = rows > cid ? (rows - cid + ncl - 1) / ncl : 0;
-
-    const uint32_t xbar_base = smem_addr(smem + L.xbar_off);
-    if (tid == 0) {
-        for (int st = 0; st < stages; ++st) mbar_init(bar_base + 8 * st, 1);
-        mbar_init(xbar_base, 1);
-        mbar_init(xbar_base + 8, 1);
-        fence_mbar_init();
-        for (int64_t i = 0; i < min((int64_t)stages, nrows); ++i)
-            prefetch_span_l2(in + (cid + i * ncl) * stride, s0 * V, s1 * V, cols);
-    }
-    pdl_enter();
-    __syncthreads();
-
-    // producer (thread 0): load this block's slice of local row i into slot i % stages
-    auto issue = [&](int64_t i) {
-        const int st = (int)(i % stages);
-        const uint32_t bar = bar_base + 8 * st;
-        if (starve) return;  // test hook: the slot is never armed
-        if (bytes == 0) {
-            mbar_arrive(bar);
-            return;
-        }
-        mbar_arrive_expect_tx(bar, bytes);
-        const char *src = reinterpret_cast<const char *>(in + (cid + i * ncl) * stride + s0 * V);
-        const uint32_t dst = stage_base + (uint32_t)(st * L.stage_bytes);
-        for (uint32_t off = 0; off < bytes; off += kBulkPiece)
-            bulk_g2s(dst + off, src + off, min(kBulkPiece, bytes - off), bar);
-    };
-    if (tid == 0)
-        for (int64_t i = 0; i < min((int64_t)stages, nrows); ++i) issue(i);
-    if (CLUSTER) {  // every block's exchange barriers are initialised before any peer sends
-        __syncwarp();
-        cluster_arrive_release();
-        cluster_wait_acquire();
-    }
-
-    bool timed_out = false;
-    for (int64_t i = 0; i < nrows; ++i) {
-        const int st = (int)(i % stages);
-        const bool ok = mbar_wait_bounded(bar_base + 8 * st, (uint32_t)((i / stages) & 1), wait_ns);
-        if (!ok) {
-            atomicOr(&g_error_word, kErrWaitTimeout);
-            timed_out = true;
-        }
-        const uint4 *slot = reinterpret_cast<const uint4 *>(smem + st * L.stage_bytes);
-        Tile<T, VPT> tile;
-#pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int v = tid + j * THREADS;
-            if (v < nmine)
-                tile.set(j, slot[v]);
-            else
-                tile.set_empty(j);
-        }
-        const float2 s = tile.stats();
-        float m = s.x, l = s.y;
-        block_merge<NW>(m, l, red + (i & 1) * NW);  // its barrier also frees slot st
-        if (tid == 0 && i + stages < nrows) {
-            fence_proxy_async_smem();
-            issue(i + stages);
-        }
-        bool xok = true;
-        if (CLUSTER) {
-            // Exchange without a cluster barrier: every block sends its state into
-            // slot `rank` of every peer (itself included) with st.async, which
-            // completes on the receiver's exchange barrier for this row's parity;
-            // each block then waits for its own barrier to have seen csize states.
-            // Slots and barriers alternate by row parity: a peer can only send
-            // row i+2's state after it received ours for row i+1, which we send
-            // after reading row i's slots.
-            float2 *sl = slots + (i & 1) * kMaxCluster;
-            const uint32_t xbar = xbar_base + 8 * (uint32_t)(i & 1);
-            if (tid == 0) {
-                mbar_arrive_expect_tx(xbar, csize * 8u);
-                const uint32_t mine = smem_addr(sl + rank);
-                for (uint32_t q = 0; q < csize; ++q) st_async_f2(map_to_rank(mine, q), m, l, map_to_rank(xbar, q));
-            }
-            xok = mbar_wait_bounded(xbar, (uint32_t)((i >> 1) & 1), wait_ns);
-            if (!xok) {
-                atomicOr(&g_error_word, kErrWaitTimeout);
-                timed_out = true;
-            }
-            const float2 w = lane < (int)csize ? sl[lane] : make_float2(-INFINITY, 0.f);
-            m = w.x;
-            l = w.y;
-            group_merge<32>(m, l);
-        }
-        if (ok && xok) {
-            const float f = out_factor(s.x, m, l);
-            T *orow = out + (cid + i * ncl) * stride + s0 * V;
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int v = tid + j * THREADS;
-                if (v < nmine) {
-                    float y[V];
-                    tile.values(j, f, y);
-                    *reinterpret_cast<uint4 *>(orow + (int64_t)v * V) = Elem<T>::pack(y);
-                }
-            }
-        }
-    }
-    // after a wait that ran out, copies may still be landing: wait for them
-    // (bounded) before the block's shared memory is released
-    if (timed_out && !starve && tid == 0) {
-        for (int64_t i = max((int64_t)0, nrows - stages); i < nrows; ++i)
-            mbar_wait_bounded(bar_base + 8 * (int)(i % stages), (uint32_t)((i / stages) & 1), wait_ns);
-    }
-    if (CLUSTER) {  // no block leaves while a peer may still address its shared memory
-        __syncwarp();
-        cluster_arrive_release();
-        cluster_wait_acquire();
     }
 }
 
@@ -794,7 +586,7 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
 template <typename T, int THREADS, int VPT, bool WHOLE>
 __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS))
     k_cluster_stream_masked(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int vec_store,
-                            int64_t wait_ns, CausalMask mask) {
+                            int64_t wait_ns, int starve, CausalMask mask) {
     if (!explicit_cluster()) {  // launched without clusters: touch no cluster state
         pdl_enter();
         if (threadIdx.x == 0) atomicOr(&g_error_word, kErrNotCluster);
@@ -803,7 +595,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
     constexpr int V = Elem<T>::kVec;
     constexpr int NW = THREADS / 32;
     constexpr int64_t kTile = (int64_t)THREADS * VPT;
-    using L = ClusterSmem<THREADS, 0>;
+    using L = ClusterSmem<THREADS>;
     extern __shared__ __align__(128) unsigned char smem[];
     float2 *red = reinterpret_cast<float2 *>(smem + L::kRedOff);
     float2 *slots = reinterpret_cast<float2 *>(smem + L::kSlotOff);
@@ -840,7 +632,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 1024 ? 1 : 1024 / THREADS
         m = M;
     }
     block_merge<NW>(m, l, red);
-    if (!cluster_exchange<NW>(m, l, slots, xbar, rank, csize, wait_ns)) return;
+    if (!cluster_exchange<NW>(m, l, slots, xbar, rank, csize, wait_ns, starve)) return;
 
     const float inv = m == -INFINITY ? __int_as_float(0x7fc00000) : 1.f / l;
     for (int64_t t0 = s0; t0 < k1; t0 += kTile) {

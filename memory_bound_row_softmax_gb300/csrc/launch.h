@@ -39,9 +39,9 @@ struct LaunchArgs {
     CausalMask mask;  // masked launches only
 };
 
-// Device error word bits (k_cluster.cu / k_ring.cu each hold one word):
-// a bounded wait ran out; a cluster kernel found itself launched without a
-// cluster (it then returns before any cluster access).
+// Device error word bits (k_cluster.cu holds the word): a bounded wait ran
+// out; a cluster kernel found itself launched without a cluster (it then
+// returns before any cluster access).
 constexpr unsigned int kErrWaitTimeout = 1u;
 constexpr unsigned int kErrNotCluster = 2u;
 
@@ -104,10 +104,14 @@ cudaError_t launch_cta_masked(const LaunchArgs &a, int threads, int vpt, int64_t
 // ... their a.whole instantiations (k_masked_warp_whole.cu, k_masked_whole.cu)
 cudaError_t launch_warp_masked_whole(const LaunchArgs &a, int threads, int group, int vpt, int64_t grid);
 cudaError_t launch_cta_masked_whole(const LaunchArgs &a, int threads, int vpt, int64_t grid);
-cudaError_t launch_stream_masked(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns);
+cudaError_t launch_stream_masked(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns,
+                                 int starve);
 
+// path 3: 16-bit rows, slices of threads x 8 vectors held in registers
+// (threads 256 or 512).  starve != 0 (a test hook of every cluster kernel)
+// makes the state exchange send nothing, so its bounded waits run out.
 bool cluster_shape_ok(int threads, int vpt, int elem_bytes);
-int64_t cluster_smem_bytes(int threads, int vpt);
+int64_t cluster_smem_bytes(int threads);
 cudaError_t launch_cluster(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns, int starve);
 // path 7: narrow dense rows (stride == cols) staged through shared memory
 // rows_per_span at a time, one thread per row, kPackedThreads per block
@@ -120,21 +124,9 @@ cudaError_t launch_packed(const LaunchArgs &a, int rows_per_span, int64_t grid);
 // twice (pass 1 states, cluster exchange, pass 2 re-read and write)
 bool stream_shape_ok(int threads, int vpt);
 int64_t stream_smem_bytes(int threads);
-cudaError_t launch_stream(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns);
+cudaError_t launch_stream(const LaunchArgs &a, int threads, int vpt, int csize, int64_t wait_ns, int starve);
 // read this device's error word after synchronising `stream`, then clear it
 cudaError_t read_clear_error_word(cudaStream_t stream, unsigned int *word);
-
-// path 5: persistent TMA ring.  grid (out) is the persistent grid actually
-// used; with a.in == nullptr nothing is launched (grid query only).
-struct RingCfg {
-    int threads, vpt, csize, stages, slice_vecs;
-    int64_t smem;
-};
-bool ring_shape_ok(int threads, int vpt, int csize);
-int64_t ring_smem_bytes(int stages, int slice_vecs, int threads);
-cudaError_t launch_ring(const LaunchArgs &a, const RingCfg &c, int64_t wait_ns, int starve, int64_t *grid);
-// read this translation unit's device error word (after a stream sync), then clear it
-cudaError_t read_clear_ring_error_word(unsigned int *word);
 
 // softmax_fwd_noalloc: the split path with its per-chunk states in a fixed
 // device array of kNoAllocMaxStates float2 (k_noalloc.cu); rows * chunks must
@@ -147,9 +139,5 @@ cudaError_t launch_split_noalloc(const LaunchArgs &a, int64_t chunks, int64_t ch
 // shares: the device's SM count (cached) and the bounded-wait limit
 int host_device_sms(int *sms);
 int64_t host_wait_ns();
-
-bool split_shape_ok(int threads, int vpt);
-cudaError_t launch_split(const LaunchArgs &a, int threads, int vpt, int64_t chunks, int64_t chunk_vecs,
-                         int64_t grid, void *scratch);
 
 }  // namespace mbrs

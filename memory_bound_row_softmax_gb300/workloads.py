@@ -272,6 +272,23 @@ CONFIGS: dict[str, Workload] = {
 
 SWEEP_WIDTHS = tuple(sorted([2**k for k in range(5, 15)] + [2**k + 7 for k in range(5, 15)]))
 
+# Shapes beside the pages' workloads that the benchmark also times: 16-bit
+# rows just past a power of two whose byte stride is off the 16-byte grid
+# (every row has its own alignment), and a few very long rows -- too few for
+# a cluster of blocks per row to fill the GPU (decode-time vocabulary rows).
+EXTRA_SHAPES: dict[str, Workload] = {
+    "r1": Workload("ragged_f16_8192x2055", 8192, 2055, "f16", 41, "normal", sigma=3.0,
+                   note="fp16 rows 4110 bytes apart: a different 16-byte phase per row"),
+    "r2": Workload("ragged_bf16_16384x2049", 16384, 2049, "bf16", 42, "normal", sigma=3.0,
+                   note="bf16 rows 4098 bytes apart: a different 16-byte phase per row"),
+    "l1": Workload("few_f32_3x1000000", 3, 1_000_000, "f32", 43, "normal", sigma=3.0,
+                   note="three fp32 rows of 10^6"),
+    "l2": Workload("few_bf16_9x262144", 9, 262144, "bf16", 44, "normal", sigma=3.0,
+                   note="nine bf16 vocabulary rows of 2^18"),
+    "l3": Workload("few_f32_1x4000000", 1, 4_000_000, "f32", 45, "normal", sigma=3.0,
+                   note="one fp32 row of 4 * 10^6"),
+}
+
 
 def sweep_workload(cols: int, total_elems: int = 50_000_000) -> Workload:
     """fp32 width-sweep matrix: about 200 MB per tensor, x ~ U(-100, 100)."""

@@ -46,7 +46,7 @@ def test_status_strings():
     for s in range(11):
         assert B.status_string(s) and B.status_string(s) != "unknown status"
     assert B.status_string(99) == "unknown status"
-    assert B.abi_version() == 10500
+    assert B.abi_version() == 20000
 
 
 @pytest.mark.parametrize("args,expect", [
@@ -98,25 +98,19 @@ def test_plans_cover_every_row(rows, cols, stride, dt, in_off):
         assert p["grid"] * p["threads"] // p["group"] >= min(rows, p["grid"] * p["threads"] // p["group"])
     elif path == B.PATH_CTA:
         assert p["threads"] * p["vpt"] >= nv and p["grid"] == rows
-    elif path == B.PATH_RING:
-        assert (stride * es) % 16 == 0 and (cols * es) % 16 == 0 and in_off == 0
-        slice_ = -(-nv // p["group"])
-        assert 1 <= p["group"] <= 16 and p["threads"] * p["vpt"] >= slice_
-        assert p["stages"] >= 2 and p["smem_bytes"] >= p["stages"] * slice_ * 16
-        assert p["smem_bytes"] <= 227 * 1024 and p["grid"] % p["group"] == 0
     elif path == B.PATH_CLUSTER:
+        assert es == 2 and p["vpt"] == 8 and p["threads"] in (256, 512)
         assert 1 <= p["group"] <= 16 and -(-nv // p["group"]) <= p["threads"] * p["vpt"]
         assert p["grid"] == rows * p["group"] and p["smem_bytes"] <= 227 * 1024
     elif path == B.PATH_PACKED:  # dense narrow rows, one thread each, 128 rows per staged span
         assert stride == cols and cols <= 48 and p["threads"] == 128 and p["grid"] == -(-rows // 128)
         assert p["smem_bytes"] >= 128 * cols * 4
-    elif path == B.PATH_STREAM:  # any slice length; enough blocks to fill the GPU, nothing allocated
-        assert 1 <= p["group"] <= 16 and p["grid"] == rows * p["group"] and p["scratch_bytes"] == 0
-        assert rows * p["group"] >= min(152, rows * 16) and p["launches"] == 1
-    else:
-        assert path == B.PATH_SPLIT and p["launches"] == 2 and p["scratch_bytes"] == rows * p["group"] * 8
-        assert rows * 16 < 152  # only a few long rows still take scratch
-    mult = 3 if path in (B.PATH_SPLIT, B.PATH_STREAM) else 2
+    else:  # any slice length; enough blocks to fill the GPU (or 16 per row)
+        assert path == B.PATH_STREAM
+        assert 1 <= p["group"] <= 16 and p["grid"] == rows * p["group"]
+        assert rows * p["group"] >= min(152, rows * 16)
+    assert p["scratch_bytes"] == 0 and p["launches"] == 1  # one kernel, nothing allocated
+    mult = 3 if path == B.PATH_STREAM else 2
     assert p["hbm_bytes"] == mult * rows * cols * es
 
 
@@ -153,27 +147,52 @@ def test_dispatch_follows_width_rule():
     assert plan(512, 65536) == B.PATH_STREAM             # long fp32 rows: a cluster streaming them twice
     assert plan(512, 65537) == B.PATH_STREAM             # ... aligned or not
     assert plan(512, 131079, "bf16") == B.PATH_CLUSTER   # long misaligned rows, enough of them
-    assert plan(4, 131072, "bf16") == B.PATH_SPLIT       # too few rows to fill the GPU
+    assert plan(4, 131072, "bf16") == B.PATH_STREAM      # too few rows to fill the GPU: 16 blocks each
     assert plan(64, 1 << 22) == B.PATH_STREAM            # too long to hold on chip: stream it twice
-    assert plan(9, 1 << 22) == B.PATH_SPLIT              # ... unless 16 blocks per row cannot fill the GPU
+    assert plan(9, 1 << 22) == B.PATH_STREAM             # ... also when 16 blocks per row cannot fill the GPU
+
+
+def test_few_long_rows_take_one_tile_per_block():
+    # rows * 16 < SMs: the stream blocks grow (up to 1024 threads) until each
+    # holds about one 4-vector tile of its slice
+    p = B.plan(1 << 24, 1 << 40, 9, 262144, 262144, "bf16", num_sms=152)
+    assert (p["path"], p["group"], p["threads"]) == (B.PATH_STREAM, 16, 512)
+    p = B.plan(1 << 24, 1 << 40, 3, 1_000_000, 1_000_000, "f32", num_sms=152)
+    assert (p["path"], p["group"], p["threads"]) == (B.PATH_STREAM, 16, 1024)
+    p = B.plan(1 << 24, 1 << 40, 1, 40000, 40000, "f32", num_sms=152)
+    assert (p["path"], p["group"], p["threads"]) == (B.PATH_STREAM, 10, 256)
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+def test_no_automatic_plan_takes_scratch(dt):
+    # softmax_fwd allocates nothing: every automatic plan, over rows from 1 to
+    # 2^21 and widths from 1 to 2^24, has scratch_bytes == 0 and one kernel
+    for rows in (1, 2, 3, 5, 9, 10, 64, 1000, 1 << 21):
+        for cols in (1, 39, 1000, 2055, 20000, 40961, 131072, 1_000_000, 1 << 24):
+            if rows * cols > 1 << 34:
+                continue
+            for off in (0, 4):
+                p = B.plan((1 << 24) + off, (1 << 46) + off, rows, cols, cols, dt, num_sms=152)
+                assert p["scratch_bytes"] == 0 and p["launches"] == 1 and p["path"] != B.PATH_SPLIT
 
 
 def test_forced_paths_and_rejections():
     try:
-        B.set_force_path(B.PATH_SPLIT)
-        assert B.plan(1 << 24, 1 << 40, 64, 1000, 1000, "f32", num_sms=152)["path"] == B.PATH_SPLIT
+        for retired in (B.PATH_SPLIT, 5):  # the split path is softmax_fwd_noalloc's; 5 is unused
+            with pytest.raises(B.SoftmaxError) as e:
+                B.set_force_path(retired)
+            assert e.value.status == B.ERR_ARG
         B.set_force_path(B.PATH_WARP)
         with pytest.raises(B.SoftmaxError) as e:
             B.plan(1 << 24, 1 << 40, 64, 5000, 5000, "f32", num_sms=152)
         assert e.value.status == B.ERR_UNSUPPORTED
-        B.set_force_path(B.PATH_CLUSTER, 256, 2, 2)
+        B.set_force_path(B.PATH_CLUSTER)
+        with pytest.raises(B.SoftmaxError):   # fp32 rows would spill in a register-held cluster
+            B.plan(1 << 24, 1 << 40, 64, 50000, 50000, "f32", num_sms=152)
+        assert B.plan(1 << 24, 1 << 40, 64, 50000, 50000, "bf16", num_sms=152)["path"] == B.PATH_CLUSTER
+        B.set_force_path(B.PATH_CLUSTER, 256, 2, 2)   # only 8 vectors per thread exist
         with pytest.raises(B.SoftmaxError):
-            B.plan(1 << 24, 1 << 40, 64, 5000, 5000, "f32", num_sms=152)
-        B.set_force_path(B.PATH_RING)
-        with pytest.raises(B.SoftmaxError):   # misaligned rows cannot ride the ring
-            B.plan(1 << 24, 1 << 40, 64, 5001, 5001, "f32", num_sms=152)
-        with pytest.raises(B.SoftmaxError):   # nor can an out with another 16-byte phase
-            B.plan(1 << 24, (1 << 40) + 4, 64, 5000, 5000, "f32", num_sms=152)
+            B.plan(1 << 24, 1 << 40, 64, 5000, 5000, "bf16", num_sms=152)
         with pytest.raises(B.SoftmaxError):
             B.set_force_path(9)
     finally:
@@ -228,15 +247,13 @@ def _check_plan_covers(p, rows, cols, stride, dt, in_off, out_off):
     elif path == B.PATH_CLUSTER:
         assert 1 <= p["group"] <= 16 and -(-nv // p["group"]) <= p["threads"] * p["vpt"]
         assert p["grid"] == rows * p["group"]
-    elif path == B.PATH_STREAM:
-        assert 1 <= p["group"] <= 16 and p["grid"] == rows * p["group"] and p["scratch_bytes"] == 0
     elif path == B.PATH_PACKED:
         assert stride == cols and p["group"] == 1 and p["smem_bytes"] <= 48 * 1024
         assert p["grid"] * 128 * p["vpt"] >= rows
-    elif path == B.PATH_RING:
-        assert p["whole_vectors"] and 1 <= p["group"] <= 16
     else:
-        assert path == B.PATH_SPLIT and p["scratch_bytes"] == rows * p["group"] * 8
+        assert path == B.PATH_STREAM
+        assert 1 <= p["group"] <= 16 and p["grid"] == rows * p["group"]
+    assert p["scratch_bytes"] == 0
 
 
 def test_planner_fuzz_covers_every_row():

@@ -32,12 +32,12 @@ def test_candidates_follow_the_row_length():
     assert B.PATH_PACKED in _paths(dense)
     assert B.PATH_PACKED not in _paths(B.tune_candidates(A_IN, A_OUT, 64, 39, 40, "f32"))  # padded
     medium = B.tune_candidates(A_IN, A_OUT, 64, 16384, 16384, "f32")      # 4096 vectors
-    assert {B.PATH_CTA, B.PATH_CLUSTER, B.PATH_STREAM, B.PATH_RING} <= _paths(medium)
+    assert {B.PATH_CTA, B.PATH_STREAM} <= _paths(medium)
     assert B.PATH_WARP not in _paths(medium)
+    assert B.PATH_CLUSTER not in _paths(medium)                          # fp32 slices would spill
+    assert B.PATH_CLUSTER in _paths(B.tune_candidates(A_IN, A_OUT, 64, 16384, 16384, "f16"))
     long_ = B.tune_candidates(A_IN, A_OUT, 64, 1 << 20, 1 << 20, "f32")
-    assert _paths(long_) == {0, B.PATH_STREAM, B.PATH_RING}              # nothing else holds the row
-    ragged = B.tune_candidates(A_IN + 4, A_OUT + 4, 64, 16391, 16391, "f32")
-    assert B.PATH_RING not in _paths(ragged)                             # the ring takes whole rows only
+    assert _paths(long_) == {0, B.PATH_STREAM}                           # nothing else holds the row
     bf16 = B.tune_candidates(A_IN, A_OUT, 512, 131072, 131072, "bf16")
     assert (B.PATH_CLUSTER, 256, 8, 0) in bf16                           # register-held slices
 

@@ -13,8 +13,7 @@ from gpu_harness import DeviceCase, compare
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [0, 0, 0, B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_SPLIT, B.PATH_RING, B.PATH_STREAM,
-         B.PATH_PACKED]
+PATHS = [0, 0, 0, B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_STREAM, B.PATH_STREAM, B.PATH_PACKED]
 
 
 def draw_cases(n: int, seed: int = 20261202):
@@ -50,8 +49,8 @@ def test_fuzz(case):
     dc = DeviceCase(x, dtype, in_off=off, out_off=off, inplace=inplace)
     st = dc.run(cols, path=path)
     if path and st == B.ERR_UNSUPPORTED:
-        # a forced path that cannot take this shape (the ring: only whole
-        # aligned rows; packed: dense narrow rows; warp / block: short rows)
+        # a forced path that cannot take this shape (cluster: 16-bit rows
+        # only; packed: dense narrow rows; warp / block: short rows)
         pytest.skip(f"path {path} refuses this shape")
     assert st == B.OK, B.status_string(st)
     assert B.check_device_error() == B.OK

@@ -80,7 +80,7 @@ def test_offsets(dtype, off):
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("path,cols", [(B.PATH_WARP, 300), (B.PATH_WARP, 1000), (B.PATH_CTA, 1000),
                                        (B.PATH_CTA, 9000), (B.PATH_STREAM, 1000), (B.PATH_STREAM, 40000),
-                                       (B.PATH_RING, 5000), (B.PATH_SPLIT, 5000), (B.PATH_CLUSTER, 5000)])
+                                       (B.PATH_CLUSTER, 5000)])
 def test_forced_paths(dtype, path, cols):
     x = W.make_random(64, cols, dtype, seed=path * 10 + cols, sigma=2.0)
     got = run_masked(x, dtype, 0.7, cols // 2 - 32, 0, path=path)
