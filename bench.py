@@ -1,20 +1,27 @@
 """Benchmark of the fused row softmax on GB300.
 
 One step = one softmax_fwd call (the whole hot path: load, row max, exp and
-sum, normalise and store, dispatch) over the fp16 4096 x 2048 workload the
-pages quote (x ~ N(0, 9), seed 1).  Prints ONE JSON line on rank 0.
+sum, normalise and store, dispatch) over the largest workload of the pages
+that fits one GPU: bf16 vocabulary logits, 512 x 131072 (Gumbel + Zipf(1.1)
+offsets, seed 4; 268 MB moved per call).  Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload c1..c5] [--no-per-shape] [--sweep]
+                  [--workload c1..c5|wN] [--no-per-shape] [--no-sweep]
 
 Timing: W warm-up steps, then exactly K steps bracketed by a barrier and a
-device synchronisation; every launch is bracketed by CUDA events on the
-launching stream.  Each step reads a different buffer set; the sets together
-are larger than 2.5x the L2, so every step's input comes from HBM.
-`value` is whole-job throughput (algorithmic bytes 2*rows*cols*elem of all
-ranks / max-over-ranks time of the K steps); the roofline block uses the
-mean per-launch device time.  Under torchrun every rank runs its own copy of
-the workload (weak scaling, rows are independent: no data-path collective).
+device synchronisation.  The K launches are captured once into a CUDA graph;
+the graph is replayed once untimed (its first replay uploads it) and then
+once between CUDA events on the launching stream.  Each step reads a
+different buffer set; the sets together are larger than 2.5x the L2, so every
+step's input comes from HBM.  `value` is whole-job throughput (algorithmic
+bytes 2*rows*cols*elem of all ranks / max-over-ranks time of the K steps);
+the roofline block uses the same mean per-launch device time.  Under
+torchrun every rank runs its own copy of the workload (weak scaling, rows
+are independent: no data-path collective).
+
+`per_shape` times every workload of the pages (and, unless --no-sweep, the
+fp32 width sweep and the extra shapes of EXTRA_SHAPES) with the same graph
+method: 200 launches after 50 warm-up.
 
 The same line carries an `attention` object: the fused attention forward
 (softmax_attention_fwd) on the pages' attention shapes (batch 4, 32 heads,
@@ -166,8 +173,9 @@ def time_steps(launch, sets, steps: int, warmup: int, world: int = 1, graph: boo
 
     With graph=True the timed launches are captured once into a CUDA graph and
     replayed, so the host's per-call cost (Python, ctypes, launch) cannot leave
-    the GPU idle between steps; events bracket the replay on the launching
-    stream.  Returns (mean ms per launch, total ms, per-launch ms or None)."""
+    the GPU idle between steps.  The graph's first replay (which uploads it)
+    runs untimed; events then bracket one replay on the launching stream.
+    Returns (mean ms per launch, total ms, per-launch ms or None)."""
     import torch
     for i in range(warmup):
         launch(*sets[i % len(sets)])
@@ -178,6 +186,8 @@ def time_steps(launch, sets, steps: int, warmup: int, world: int = 1, graph: boo
         with torch.cuda.graph(g):
             for i in range(steps):
                 launch(*sets[i % len(sets)])
+        torch.cuda.synchronize()
+        g.replay()  # upload: not part of the timed region
         torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
@@ -221,6 +231,31 @@ def traffic_record(workload: str):
     return rec
 
 
+L2_POLICY = "inputs larger than L2: each step reads another of a set of rotating buffers totalling > 2.5 x L2"
+
+
+def workload_config(w, world: int) -> dict:
+    """The `config` object of both arms' JSON lines (the same dict for the
+    same workload and world size)."""
+    return {"workload": w.name, "rows": w.rows, "cols": w.cols, "row_stride": w.stride,
+            "storage_dtype": w.dtype, "parallelism": f"replicas x{world} (rows independent)", "l2": L2_POLICY}
+
+
+def device_seeded(w, dev):
+    """Input bits of w drawn on the device (timing-only workloads: the sweep
+    and the extra shapes): U(lo, hi) or N(0, sigma^2) from torch's seeded
+    device generator, rounded to the storage dtype."""
+    import torch
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    if w.kind == "uniform":
+        x = torch.rand((w.rows, w.stride), generator=g, device=dev) * (w.hi - w.lo) + w.lo
+    else:
+        x = torch.randn((w.rows, w.stride), generator=g, device=dev) * w.sigma
+    if w.dtype == "f32":
+        return x.view(torch.int32)
+    return x.to(torch.float16 if w.dtype == "f16" else torch.bfloat16).view(torch.int16)
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -259,8 +294,11 @@ def run_ours(args) -> dict | None:
     if args.workload.startswith("w"):  # a width of the fp32 sweep, seeded on the device
         w = W.sweep_workload(int(args.workload[1:]))
         x = None
-        g = torch.Generator(device=dev).manual_seed(w.seed)
-        x_dev = (torch.rand((w.rows, w.stride), generator=g, device=dev) * 200 - 100).view(torch.int32)
+        x_dev = device_seeded(w, dev)
+    elif args.workload in W.EXTRA_SHAPES:
+        w = W.EXTRA_SHAPES[args.workload]
+        x = None
+        x_dev = device_seeded(w, dev)
     else:
         w = W.CONFIGS[args.workload]
         x = W.make_input(w)
@@ -330,17 +368,15 @@ def run_ours(args) -> dict | None:
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {
-            "workload": w.name, "rows": w.rows, "cols": w.cols, "row_stride": w.stride,
-            "storage_dtype": w.dtype, "arithmetic": "f32 (one exp per element)",
-            "per_rank_rows": w.rows, "parallelism": f"replicas x{world} (rows independent)",
-            "l2": f"inputs larger than L2: {len(sets)} rotating buffer sets, "
-                  f"{len(sets) * set_bytes / 1e6:.0f} MB > 2.5 x L2 ({l2 / 1e6:.0f} MB)",
-            "timing": "K launches captured in one CUDA graph, replayed between CUDA events",
-            "launch_overlap": not args.no_overlap,
-            "path": B.PATH_NAMES.get(plan["path"]), "threads": plan["threads"], "vpt": plan["vpt"],
-            "group": plan["group"],
+        "config": workload_config(w, world),
+        "timing": {
+            "method": "K launches captured in one CUDA graph; one untimed replay (graph upload), then one "
+                      "replay between CUDA events on the launching stream",
+            "buffer_sets": len(sets), "buffer_bytes": len(sets) * set_bytes, "l2_bytes": l2,
+            "launch_overlap": not args.no_overlap, "arithmetic": "f32 (one exp per element)",
         },
+        "plan": {"path": B.PATH_NAMES.get(plan["path"]), "threads": plan["threads"], "vpt": plan["vpt"],
+                 "group": plan["group"], "grid": plan["grid"]},
         "us_per_call": round(mean_launch_ms * 1e3, 3),
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -352,7 +388,7 @@ def run_ours(args) -> dict | None:
         "gpu_launches": args.steps * plan["launches"],
     }
     if rank == 0 and x is not None:
-        result["e2e"] = e2e_measure(launch, x, w, dev, min(args.steps, 2000))
+        result["e2e"] = e2e_measure(x, w, dev, min(args.steps, 2000))
     if rank == 0 and world == 1 and not args.no_cpu_baseline and x is not None:
         result["cpu_baseline"] = cpu_baseline(x, w)
     if rank == 0 and world == 1 and not args.no_per_shape:
@@ -365,11 +401,13 @@ def run_ours(args) -> dict | None:
     return result if rank == 0 else None
 
 
-def e2e_measure(launch, x, w, dev, steps: int) -> dict:
+def e2e_measure(x, w, dev, steps: int) -> dict:
     """Same metric through the C ABI with host buffers: softmax_fwd_host on a
     page-locked input and output every step (its host-to-device copies, the
     softmax and the device-to-host copies, chunked and overlapped by the
-    library), all inside the timed region."""
+    library), all inside the timed region.  Beside it, the link ceiling: the
+    same bytes copied host-to-device and device-to-host at once (two streams,
+    one copy each way per step, no kernel), timed the same way."""
     import numpy as np
     import torch
 
@@ -388,46 +426,90 @@ def e2e_measure(launch, x, w, dev, steps: int) -> dict:
         if st != 0:
             raise B.SoftmaxError(st, "softmax_fwd_host")
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(steps):
-        step()
-    t1.record()
-    torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(n):
+            fn()
+        t1.record()
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / n
+
+    ms = timed(step, steps)
+    # the link ceiling: H2D of the input and D2H of an output-sized buffer,
+    # concurrently on two streams, both ordered after the current stream
+    d_a, d_b = torch.empty_like(h_in, device=dev), torch.empty_like(h_in, device=dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    cur = torch.cuda.current_stream(dev)
+
+    def duplex():
+        s_in.wait_stream(cur)
+        s_out.wait_stream(cur)
+        with torch.cuda.stream(s_in):
+            d_a.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            h_out.copy_(d_b, non_blocking=True)
+        cur.wait_stream(s_in)
+        cur.wait_stream(s_out)
+
+    dms = timed(duplex, steps)
     nbytes = h_in.numel() * h_in.element_size()
-    return {"value": round(w.algorithmic_bytes * steps / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+    value = w.algorithmic_bytes / (ms / 1e3) / 1e9
+    ceiling = w.algorithmic_bytes / (dms / 1e3) / 1e9
+    del d_a, d_b, ws
+    return {"value": round(value, 2), "unit": "GB/s",
             "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "steps": steps,
-            "ms_per_step": round(ms / steps, 4), "call": "softmax_fwd_host"}
+            "ms_per_step": round(ms, 4), "call": "softmax_fwd_host",
+            "link_ceiling": {"value": round(ceiling, 2), "unit": "GB/s", "ms_per_step": round(dms, 4),
+                             "what": "the same bytes copied host-to-device and device-to-host at once "
+                                     "(pinned memory, two streams, no kernel)"},
+            "frac_of_link": round(value / ceiling, 4)}
 
 
-def cpu_baseline(x, w, min_seconds: float = 3.0) -> dict:
-    """The CPU oracle (untuned) over the whole workload on all host cores."""
+def cpu_baseline(x, w, seconds: float = 4.0) -> dict:
+    """The CPU oracle (untuned) on the workload: once on one thread over a
+    bounded sample of its rows, once row-partitioned over every host core the
+    process can use (whole passes over all rows, at least `seconds`)."""
     import oracle
     cores = os.cpu_count() or 1
+    # one thread: rows [0, n) with n sized to about `seconds`
+    n = max(1, min(w.rows, 8))
+    t0 = time.perf_counter()
+    oracle.softmax(x[:n], w.dtype, cols=w.cols, threads=1)
+    per_row = (time.perf_counter() - t0) / n
+    n1 = int(max(1, min(w.rows, seconds / max(per_row, 1e-9))))
+    t0 = time.perf_counter()
+    oracle.softmax(x[:n1], w.dtype, cols=w.cols, threads=1)
+    el1 = time.perf_counter() - t0
+    one = {"value": round(2 * n1 * w.cols * w.elem_bytes / el1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+           "sample": f"rows 0..{n1 - 1} of {w.name} ({n1} of {w.rows} rows, {el1:.1f} s)"}
     t0 = time.perf_counter()
     reps = 0
     while True:
         oracle.softmax(x, w.dtype, cols=w.cols, threads=cores)
         reps += 1
         el = time.perf_counter() - t0
-        if el >= min_seconds:
+        if el >= seconds:
             break
     return {"value": round(w.algorithmic_bytes * reps / el / 1e9, 3), "unit": "GB/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{reps} full pass(es) over all {w.rows} rows of {w.name} ({el:.1f} s wall, "
-                      f"double-precision C, rows split over {cores} threads)"}
+                      f"double-precision C, rows split over {cores} threads = os.cpu_count() of this "
+                      f"process, which may be a container's share of the host)",
+            "single_thread": one}
 
 
 def per_shape(args, peaks, l2, dev) -> dict:
-    """Every workload of the pages: mean us/call over 200 timed launches after
-    50 warm-up (the harness of the pages; replayed from a CUDA graph), GB/s,
+    """Every workload of the pages (and, unless --no-sweep, the fp32 width
+    sweep and the extra shapes): mean us/call over 200 timed launches after 50
+    warm-up (the harness of the pages; replayed from a CUDA graph), GB/s,
     fraction of the measured HBM peak and of a device-to-device copy of the
-    same bytes timed the same way."""
+    same bytes timed the same way.  The few-long-row shapes also time
+    softmax_fwd_noalloc (the grid-wide split path)."""
     import numpy as np
     import torch
 
@@ -435,19 +517,16 @@ def per_shape(args, peaks, l2, dev) -> dict:
     from memory_bound_row_softmax_gb300 import workloads as W
 
     lib = B.lib()
-    handle = torch.cuda.current_stream(dev).cuda_stream
     todo = [W.CONFIGS[k] for k in ("c1", "c2", "c3", "c4", "c5")]
-    if args.sweep:
-        todo += [W.sweep_workload(c) for c in W.SWEEP_WIDTHS]
+    if not args.no_sweep:
+        todo += list(W.EXTRA_SHAPES.values()) + [W.sweep_workload(c) for c in W.SWEEP_WIDTHS]
     table = {}
     for w in todo:
-        if w.kind == "uniform":  # sweep matrices: seeded on the device (timing only)
-            g = torch.Generator(device=dev).manual_seed(w.seed)
-            xd = (torch.rand((w.rows, w.stride), generator=g, device=dev, dtype=torch.float32) * 200 - 100)
-            xd = xd.view(torch.int32)
-        else:
+        if w.name.startswith("c"):
             x = W.make_input(w)
             xd = torch.from_numpy(x.view(np.int32 if w.dtype == "f32" else np.int16)).to(dev)
+        else:  # timing-only matrices: seeded on the device
+            xd = device_seeded(w, dev)
         code = B.DTYPE_CODES[w.dtype]
 
         def launch(a, b, w=w, code=code):
@@ -481,8 +560,10 @@ def per_shape(args, peaks, l2, dev) -> dict:
         gbs = plan["hbm_bytes"] / (med / 1e3) / 1e9
         alg = w.algorithmic_bytes / (med / 1e3) / 1e9
         copy_gbs = 2 * nbytes / (cmed / 1e3) / 1e9
-        table[w.name] = {
-            "path": B.PATH_NAMES.get(plan["path"]), "us_per_call": round(med * 1e3, 2),
+        row = {
+            "path": B.PATH_NAMES.get(plan["path"]),
+            "shape": [plan["threads"], plan["vpt"], plan["group"]],
+            "us_per_call": round(med * 1e3, 2),
             "us_per_call_no_overlap": round(med_plain * 1e3, 2),
             "us_per_call_tuned": round(med_tuned * 1e3, 2),
             "tuned_shape": [tuned["plan"][k] for k in ("path", "threads", "vpt", "group")],
@@ -492,6 +573,16 @@ def per_shape(args, peaks, l2, dev) -> dict:
             "frac_of_copy": round(alg / copy_gbs, 4), "time_vs_copy": round(med / cmed, 3),
             "moved_gbs": round(gbs, 1),
         }
+        if w.rows * 16 < 152:  # a few very long rows: the grid-wide split through softmax_fwd_noalloc
+            def launch_noalloc(a, b, w=w, code=code):
+                st = lib.softmax_fwd_noalloc(a.data_ptr(), b.data_ptr(), w.rows, w.cols, w.stride, code,
+                                             torch.cuda.current_stream().cuda_stream)
+                if st != 0:
+                    raise B.SoftmaxError(st, "softmax_fwd_noalloc")
+
+            nmed, _, _ = time_steps(launch_noalloc, sets, 200, 50)
+            row["us_per_call_noalloc_split"] = round(nmed * 1e3, 2)
+        table[w.name] = row
         if w.causal_period:  # the same rows through softmax_fwd_masked: only the kept half is read
             def launch_masked(a, b, w=w, code=code):
                 st = lib.softmax_fwd_masked(a.data_ptr(), b.data_ptr(), w.rows, w.cols, w.stride, code, 1.0, 0,
@@ -618,7 +709,10 @@ def run_reference(args) -> dict | None:
     import oracle
     from memory_bound_row_softmax_gb300 import workloads as W
     oracle.build()
-    w = W.CONFIGS[args.workload]
+    if args.workload.startswith("w"):
+        w = W.sweep_workload(int(args.workload[1:]))
+    else:
+        w = W.EXTRA_SHAPES[args.workload] if args.workload in W.EXTRA_SHAPES else W.CONFIGS[args.workload]
     x = W.make_input(w)
     cores = os.cpu_count() or 1
     t0 = time.perf_counter()
@@ -642,8 +736,7 @@ def run_reference(args) -> dict | None:
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "row_stride": w.stride,
-                   "storage_dtype": w.dtype, "rows_per_step": rows_per_step},
+        "config": workload_config(w, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -657,11 +750,13 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="c2",
-                    help="c1..c5 (the pages' workloads) or wN (fp32 width-sweep matrix of width N)")
+    ap.add_argument("--workload", default="c5",
+                    help="c1..c5 (the pages' workloads), r1, r2, l1..l3 (the extra shapes) or wN (fp32 "
+                         "width-sweep matrix of width N)")
     ap.add_argument("--no-per-shape", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sweep", action="store_true", help="add the fp32 width sweep to the per-shape table")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="leave the fp32 width sweep and the extra shapes out of the per-shape table")
     ap.add_argument("--force", default="",
                     help="path[,threads,vpt,group]: force a kernel path and launch shape (profiling, tuning)")
     ap.add_argument("--masked", action="store_true",
