@@ -28,9 +28,14 @@
  * pointer must be 16-byte aligned.  Q, K and V may overlap one another; O may
  * overlap none of them.  The call is asynchronous on `stream`; nothing is
  * allocated on the device.  The kernel is a persistent grid that hands out
- * its work through one of 64 device-side counter slots, taken in turn by
- * successive calls: at most 64 calls may be in flight at the same time on one
- * device (over all streams).
+ * its work through a pair of device-side counters.  softmax_attention_fwd
+ * takes them from one of 64 slots inside the library, in turn by successive
+ * calls: at most 64 of its calls may be in flight at the same time on one
+ * device (over all streams), and it cannot be captured into a CUDA graph (a
+ * captured launch would keep its slot on every replay while later calls
+ * cycle through it): called on a stream that is being captured it returns
+ * SOFTMAX_ERR_ARG without launching.  softmax_attention_fwd_counter takes
+ * the caller's counters instead, and may be captured.
  *
  * Errors (checked on the host before any launch; nothing is launched unless
  * the result is SOFTMAX_OK):
@@ -42,8 +47,10 @@
  *   SOFTMAX_ERR_NULL        a NULL pointer while there is work to do
  *   SOFTMAX_ERR_ALIGN       a pointer not 16-byte aligned
  *   SOFTMAX_ERR_OVERLAP     O overlaps Q, K or V
- *   SOFTMAX_ERR_ARG         causal not 0 or 1, sm_scale not finite and > 0
- *   SOFTMAX_ERR_CUDA        the tensor-map encoder or the launch failed
+ *   SOFTMAX_ERR_ARG         causal not 0 or 1, sm_scale not finite and > 0, or
+ *                           (softmax_attention_fwd) the stream is being captured
+ *   SOFTMAX_ERR_CUDA        the tensor-map encoder, the capture query or the
+ *                           launch failed
  * batch * heads * n_ctx == 0 returns SOFTMAX_OK without a launch.  A bounded
  * wait inside the kernel that runs out sets the device error word that
  * softmax_check_device_error() reports as SOFTMAX_ERR_TIMEOUT.
@@ -60,6 +67,24 @@ extern "C" {
 int softmax_attention_fwd(const void *q, const void *k, const void *v, void *o, int64_t batch, int64_t heads,
                           int64_t n_ctx, int64_t head_dim, int dtype, int causal, float sm_scale,
                           cudaStream_t stream);
+
+/*
+ * softmax_attention_fwd_counter -- the same forward with the persistent
+ * grid's two work counters in memory the caller owns, for launches captured
+ * into CUDA graphs (and for callers that want more than 64 calls in flight).
+ *   work_counter  device pointer to two unsigned ints, 8-byte aligned, that
+ *                 overlap none of Q, K, V and O; both zero before the first
+ *                 call that uses them.  Every call leaves them zero again when
+ *                 its kernel ends, so they need no reset between calls.
+ * Calls that share one work_counter must not run at the same time (order them
+ * on one stream, or in one graph); calls with different counters may.  Other
+ * arguments, layout and status codes as softmax_attention_fwd (also
+ * SOFTMAX_ERR_NULL / SOFTMAX_ERR_ALIGN / SOFTMAX_ERR_OVERLAP for the counter);
+ * it may be called while the stream is being captured.
+ */
+int softmax_attention_fwd_counter(const void *q, const void *k, const void *v, void *o, int64_t batch,
+                                  int64_t heads, int64_t n_ctx, int64_t head_dim, int dtype, int causal,
+                                  float sm_scale, unsigned int *work_counter, cudaStream_t stream);
 
 /* The launch softmax_attention_fwd makes for a shape (host only). */
 typedef struct {

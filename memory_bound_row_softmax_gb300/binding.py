@@ -72,6 +72,8 @@ SIGNATURES = {
     "softmax_fwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp]),
     "softmax_fwd_masked": (_int, [_vp, _vp, _i64, _i64, _i64, _int, ctypes.c_float, _i64, _i64, _vp]),
     "softmax_attention_fwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, ctypes.c_float, _vp]),
+    "softmax_attention_fwd_counter": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, ctypes.c_float,
+                                             _vp, _vp]),
     "softmax_attention_set_wait_test": (_int, [_int]),
     "softmax_attention_plan": (_int, [_i64, _i64, _i64, _i64, _int, _int, _int, ctypes.POINTER(AttentionPlan)]),
 }
@@ -204,6 +206,14 @@ def attention_fwd_ptr(q: int, k: int, v: int, o: int, batch: int, heads: int, n_
     """Raw call of the fused attention forward (status out)."""
     return lib().softmax_attention_fwd(q, k, v, o, batch, heads, n_ctx, head_dim, dtype, 1 if causal else 0,
                                        sm_scale, stream)
+
+
+def attention_fwd_counter_ptr(q: int, k: int, v: int, o: int, batch: int, heads: int, n_ctx: int, head_dim: int,
+                              dtype: int, causal: bool, sm_scale: float, counter: int, stream: int = 0) -> int:
+    """Raw call of the fused attention forward with the caller's two work
+    counters at device address ``counter`` (status out)."""
+    return lib().softmax_attention_fwd_counter(q, k, v, o, batch, heads, n_ctx, head_dim, dtype,
+                                               1 if causal else 0, sm_scale, counter, stream)
 
 
 def attention_fwd(q, k, v, causal: bool = True, sm_scale: float | None = None, out=None, stream=None):

@@ -68,9 +68,11 @@ int softmax_attention_plan(int64_t batch, int64_t heads, int64_t n_ctx, int64_t 
     return SOFTMAX_OK;
 }
 
-int softmax_attention_fwd(const void *q, const void *k, const void *v, void *o, int64_t batch, int64_t heads,
-                          int64_t n_ctx, int64_t head_dim, int dtype, int causal, float sm_scale,
-                          cudaStream_t stream) {
+namespace {
+
+int attention_call(const void *q, const void *k, const void *v, void *o, int64_t batch, int64_t heads,
+                   int64_t n_ctx, int64_t head_dim, int dtype, int causal, float sm_scale, unsigned int *counter,
+                   cudaStream_t stream) {
     int st = check_shape(batch, heads, n_ctx, head_dim, dtype, causal);
     if (st != SOFTMAX_OK) return st;
     if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return SOFTMAX_ERR_ARG;
@@ -85,12 +87,44 @@ int softmax_attention_fwd(const void *q, const void *k, const void *v, void *o, 
         return SOFTMAX_ERR_SHAPE;
     const auto overlaps = [bytes](uint64_t a, uint64_t b) { return a < b + bytes && b < a + bytes; };
     if (overlaps(oa, qa) || overlaps(oa, ka) || overlaps(oa, va)) return SOFTMAX_ERR_OVERLAP;
+    if (counter) {  // the counter's 8 bytes are written: they may overlap no tensor
+        const uint64_t ca = (uint64_t)(uintptr_t)counter;
+        const auto hits = [bytes, ca](uint64_t a) { return ca < a + bytes && a < ca + 8; };
+        if (hits(qa) || hits(ka) || hits(va) || hits(oa)) return SOFTMAX_ERR_OVERLAP;
+    } else {
+        // a captured launch would keep the library slot it took at capture on
+        // every replay, sharing it with whatever later call takes that slot:
+        // captures must bring their own counter (softmax_attention_fwd_counter)
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return SOFTMAX_ERR_CUDA;
+        if (cap != cudaStreamCaptureStatusNone) return SOFTMAX_ERR_ARG;
+    }
     int sms = 0;
     st = mbrs::host_device_sms(&sms);
     if (st != SOFTMAX_OK) return st;
-    attn::AttnArgs a{q, k, v, o, batch, heads, n_ctx, dtype, causal, sm_scale, stream, sms};
+    attn::AttnArgs a{q, k, v, o, batch, heads, n_ctx, dtype, causal, sm_scale, stream, sms, counter};
     const cudaError_t e = attn::launch_attention(a, mbrs::host_wait_ns(), g_attn_starve.load());
     return e == cudaSuccess ? SOFTMAX_OK : SOFTMAX_ERR_CUDA;
+}
+
+}  // namespace
+
+int softmax_attention_fwd(const void *q, const void *k, const void *v, void *o, int64_t batch, int64_t heads,
+                          int64_t n_ctx, int64_t head_dim, int dtype, int causal, float sm_scale,
+                          cudaStream_t stream) {
+    return attention_call(q, k, v, o, batch, heads, n_ctx, head_dim, dtype, causal, sm_scale, nullptr, stream);
+}
+
+int softmax_attention_fwd_counter(const void *q, const void *k, const void *v, void *o, int64_t batch,
+                                  int64_t heads, int64_t n_ctx, int64_t head_dim, int dtype, int causal,
+                                  float sm_scale, unsigned int *work_counter, cudaStream_t stream) {
+    const int st = check_shape(batch, heads, n_ctx, head_dim, dtype, causal);
+    if (st != SOFTMAX_OK) return st;
+    if (batch == 0 || heads == 0 || n_ctx == 0) return SOFTMAX_OK;
+    if (!work_counter) return SOFTMAX_ERR_NULL;
+    if ((uintptr_t)work_counter % 8 != 0) return SOFTMAX_ERR_ALIGN;
+    return attention_call(q, k, v, o, batch, heads, n_ctx, head_dim, dtype, causal, sm_scale, work_counter,
+                          stream);
 }
 
 }  // extern "C"

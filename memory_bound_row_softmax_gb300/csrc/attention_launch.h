@@ -23,6 +23,7 @@ struct AttnArgs {
     float sm_scale;
     cudaStream_t stream;
     int sms;  // the device's SM count: the persistent grid's size
+    unsigned int *counter;  // the caller's two work-counter words, or nullptr: a library slot
 };
 
 // starve != 0 (a test hook): every block leaves its first item's Q barrier

@@ -162,9 +162,10 @@ __device__ __forceinline__ Item decode_item(int i, int m_blocks, int heads_total
     return Item{g0 + within % heads_here, m_blocks - 1 - within / heads_here};
 }
 
-// Per-launch work counters (next item, finished blocks).  A launch takes slot
-// `work_slot` (the host cycles through kWorkSlots); the last block to finish
-// resets the slot for its next user.
+// Per-launch work counters (next item, finished blocks).  A launch uses the
+// caller's two words when it is given them (work_ext), else slot `work_slot`
+// of this array (the host cycles through kWorkSlots); the last block to
+// finish resets the counters to zero for their next user.
 constexpr int kWorkSlots = 64;
 __device__ unsigned int g_work[kWorkSlots][2];
 
@@ -182,8 +183,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, T *__restrict__ o, int n_ctx, int m_blocks,
-                    int heads_total, int group, int work_slot, float kscale, int causal, uint32_t wait_ns,
-                    int starve) {
+                    int heads_total, int group, unsigned int *work_ext, int work_slot, float kscale, int causal,
+                    uint32_t wait_ns, int starve) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpTma) {
         // ---- item fetch and TMA producer ----------------------------------
         if (lane == 0) {
+            unsigned int *const work = work_ext ? work_ext : g_work[work_slot];
             int n = 0;  // loads issued so far (all items)
             int k = 0;  // items published so far
             bool ok = true;
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // role has read the previous entry, so the ring never runs two
                 // entries ahead of a reader
                 if (k > 0 && ok) ok = wait_phase(bar(kBarQEmpty), (k - 1) & 1, abort_flag, wait_ns);
-                const int item = ok ? (int)atomicAdd(&g_work[work_slot][0], 1u) : total;
+                const int item = ok ? (int)atomicAdd(&work[0], 1u) : total;
                 item_ring[k & 1] = item < total ? item : -1;
                 mbar_arrive(bar(kBarItem));  // release: the entry is visible to whoever waits
                 if (item >= total) break;
@@ -269,9 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // this block takes no more items: the last one to get here resets
             // the launch's counters
             __threadfence();
-            if (atomicAdd(&g_work[work_slot][1], 1u) == gridDim.x - 1) {
-                g_work[work_slot][0] = 0u;
-                g_work[work_slot][1] = 0u;
+            if (atomicAdd(&work[1], 1u) == gridDim.x - 1) {
+                work[0] = 0u;
+                work[1] = 0u;
                 __threadfence();
             }
         }
@@ -551,14 +553,15 @@ cudaError_t go(const AttnArgs &a, int64_t wait_ns, int starve) {
     const int group = attention_head_group(bh, a.n_ctx);
     const float kscale = a.sm_scale * kLog2e;
     const uint32_t limit = (uint32_t)std::min<int64_t>(std::max<int64_t>(wait_ns, 1), 0x7fffffff);
-    // one persistent block per SM (at most one per item); each launch takes
-    // the next slot of work counters
+    // one persistent block per SM (at most one per item); a launch without
+    // the caller's counters takes the next slot of the library's
     static std::atomic<unsigned> launches{0};
-    const int slot = (int)(launches.fetch_add(1, std::memory_order_relaxed) % kWorkSlots);
+    const int slot =
+        a.counter ? 0 : (int)(launches.fetch_add(1, std::memory_order_relaxed) % kWorkSlots);
     const int64_t grid = std::min<int64_t>(std::max(a.sms, 1), bh * m_blocks);
     k_attention_fwd<T><<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(
-        mq, mk, mv, static_cast<T *>(a.o), (int)a.n_ctx, (int)m_blocks, (int)bh, group, slot, kscale, a.causal,
-        limit, starve ? 1 : 0);
+        mq, mk, mv, static_cast<T *>(a.o), (int)a.n_ctx, (int)m_blocks, (int)bh, group, a.counter, slot, kscale,
+        a.causal, limit, starve ? 1 : 0);
     return cudaGetLastError();
 }
 

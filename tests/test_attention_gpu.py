@@ -267,3 +267,92 @@ def test_wait_timeout_is_reported_and_recoverable():
     for bi in range(2):
         for hi in range(3):
             check_head(got[bi, hi], q[bi, hi], k[bi, hi], v[bi, hi], "f16", scale, True)
+
+
+def test_plain_call_refuses_capture():
+    # a captured plain call would keep its library counter slot on every
+    # replay: it returns SOFTMAX_ERR_ARG without launching, and the capture
+    # ends with nothing in it
+    w = W.AttentionWorkload("t", 1, 2, 256, D, "f16", seed=31, causal=True)
+    q, k, v = W.make_qkv(w)
+    dq, dk, dv = to_dev(q, "f16"), to_dev(k, "f16"), to_dev(v, "f16")
+    out = torch.zeros_like(dq)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        st = B.attention_fwd_ptr(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), out.data_ptr(), 1, 2, 256, D,
+                                 CODE["f16"], True, 0.1, s.cuda_stream)
+        out.add_(0)  # one captured kernel, so that the graph is not empty
+    assert st == B.ERR_ARG
+    g.replay()
+    torch.cuda.synchronize()
+    assert (out == 0).all()
+
+
+def test_graph_replays_beside_direct_calls():
+    # stream A replays a graph of counter-variant calls (the caller's own
+    # counters) while stream B makes plain calls (the library's slots) at the
+    # same time; every output equals the one a lone plain call gives, bit for
+    # bit (each item's arithmetic does not depend on which block takes it)
+    w1 = W.AttentionWorkload("t", 1, 4, 1000, D, "f16", seed=33, causal=True)
+    w2 = W.AttentionWorkload("t", 2, 2, 700, D, "f16", seed=34, causal=False)
+    scale = 1.0 / math.sqrt(D)
+    ins = []
+    for w in (w1, w2):
+        q, k, v = W.make_qkv(w)
+        ins.append((w, to_dev(q, "f16"), to_dev(k, "f16"), to_dev(v, "f16")))
+
+    def call(w, dq, dk, dv, o, stream, counter=None):
+        a = (dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o.data_ptr(), w.batch, w.heads, w.n_ctx, D, CODE["f16"],
+             w.causal, scale)
+        if counter is None:
+            return B.attention_fwd_ptr(*a, stream)
+        return B.attention_fwd_counter_ptr(*a, counter, stream)
+
+    refs = []
+    for w, dq, dk, dv in ins:
+        o = torch.empty_like(dq)
+        assert call(w, dq, dk, dv, o, torch.cuda.current_stream().cuda_stream) == B.OK
+        refs.append(o)
+    torch.cuda.synchronize()
+
+    counter = torch.zeros(2, dtype=torch.int32, device="cuda")
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    w, dq, dk, dv = ins[0]
+    outs_a = [torch.empty_like(dq) for _ in range(3)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=sa):
+        for o in outs_a:  # three calls in a row on one counter
+            assert call(w, dq, dk, dv, o, sa.cuda_stream, counter.data_ptr()) == B.OK
+    wb, qb, kb, vb = ins[1]
+    outs_b = [torch.empty_like(qb) for _ in range(4)]
+    for rep in range(3):
+        for o in outs_a:
+            o.zero_()
+        for o in outs_b:
+            o.zero_()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(sa):
+            g.replay()
+        for o in outs_b:
+            assert call(wb, qb, kb, vb, o, sb.cuda_stream) == B.OK
+        torch.cuda.synchronize()
+        assert B.check_device_error() == B.OK
+        for o in outs_a:
+            assert torch.equal(o, refs[0]), f"graph replay {rep}"
+        for o in outs_b:
+            assert torch.equal(o, refs[1]), f"direct call beside replay {rep}"
+    assert (counter == 0).all()  # left zero by every call
+
+
+def test_counter_argument_checks():
+    p = torch.zeros(4096, dtype=torch.int16, device="cuda")
+    o = torch.zeros(1 * 1 * 128 * D, dtype=torch.int16, device="cuda")
+    c = torch.zeros(4, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    a = (p.data_ptr(), p.data_ptr(), p.data_ptr(), o.data_ptr(), 1, 1, 128, D, 1, True, 0.1)
+    assert B.attention_fwd_counter_ptr(*a, 0, s) == B.ERR_NULL
+    assert B.attention_fwd_counter_ptr(*a, c.data_ptr() + 4, s) == B.ERR_ALIGN
+    assert B.attention_fwd_counter_ptr(*a, o.data_ptr() + 64, s) == B.ERR_OVERLAP
+    torch.cuda.synchronize()
+    assert (o == 0).all() and (c == 0).all()
