@@ -325,6 +325,16 @@ def run_ours(args) -> dict | None:
             if st != 0:
                 raise B.SoftmaxError(st, "softmax_fwd_masked")
 
+    if args.noalloc:  # the same rows through softmax_fwd_noalloc (for --only-kernel captures)
+        if not args.only_kernel:
+            raise SystemExit("--noalloc needs --only-kernel")
+
+        def launch(a, b):  # noqa: F811 -- the allocation-free split replaces the plain call
+            st = lib.softmax_fwd_noalloc(a.data_ptr(), b.data_ptr(), w.rows, w.cols, w.stride, code,
+                                         torch.cuda.current_stream().cuda_stream)
+            if st != 0:
+                raise B.SoftmaxError(st, "softmax_fwd_noalloc")
+
     if args.force:
         B.set_force_path(*[int(v) for v in args.force.split(",")])
     B.set_launch_overlap(not args.no_overlap)
@@ -761,6 +771,8 @@ def main(argv=None):
                     help="path[,threads,vpt,group]: force a kernel path and launch shape (profiling, tuning)")
     ap.add_argument("--masked", action="store_true",
                     help="with --only-kernel on c4: run its causal mask through softmax_fwd_masked")
+    ap.add_argument("--noalloc", action="store_true",
+                    help="with --only-kernel: run the workload through softmax_fwd_noalloc (the split path)")
     ap.add_argument("--only-kernel", action="store_true",
                     help="warm-up and timed launches only (the command profiled with ncu)")
     ap.add_argument("--no-attention", action="store_true", help="leave out the attention forward block")
