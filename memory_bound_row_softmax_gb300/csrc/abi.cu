@@ -168,10 +168,14 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             // path lane group per row 81.5; 400000 x 7: 6.7 against 15.0;
             // 71 wide it loses, 77.8 against 58.9)
             path = SOFTMAX_PATH_PACKED;
-        } else if (nv <= 32 * 9 && (cols <= 1024 || p->whole)) {
+        } else if (nv <= 32 * 9 && (cols <= 1024 || p->whole || es == 2)) {
             // a warp per row while a warp's registers hold it; past 1024
-            // columns only for rows of whole vectors (4096 x 2048 fp16: warp
-            // 5.8 us, block 6.3 us; 4096 x 2047 bf16: warp 8.9 us, block 8.7 us)
+            // columns for rows of whole vectors and for 16-bit rows, whose
+            // partial end vectors take a few aligned partial stores (4096 x
+            // 2048 fp16: warp 5.8 us, block 6.3 us; 8192 x 2055 fp16: warp
+            // 11.6 us, block 13.4; 16384 x 2049 bf16: 21.4 against 24.5).
+            // Ragged fp32 rows stay on the block path (their edges go element
+            // by element)
             path = SOFTMAX_PATH_WARP;
         } else if (nv > 512 * 10 && es == 2 && cdiv(nv, 2048) <= 16 && rows * cdiv(nv, 2048) >= sms) {
             // 16-bit rows longer than a block's registers: a cluster holding the
@@ -543,6 +547,36 @@ int64_t host_chunk_rows(int64_t rows, int64_t cols, int es, int64_t chunk_bytes)
     return std::min(cr, rows);
 }
 
+// Whether the current device can load and store the host range at `p`
+// directly, at the same address: page-locked memory mapped into the unified
+// address space (cudaHostAlloc, cudaHostRegister), device or managed memory,
+// or pageable memory on a device that reaches it through the host's page
+// tables (a coherent CPU-GPU link such as NVLink-C2C).  Nothing is launched
+// when the answer is no.
+int device_reaches(const void *p, bool *ok) {
+    *ok = false;
+    cudaPointerAttributes a;
+    std::memset(&a, 0, sizeof(a));
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // unregistered memory on older runtimes: not sticky
+        return SOFTMAX_ERR_CUDA;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+        *ok = true;
+    } else if (a.type == cudaMemoryTypeHost) {
+        *ok = a.devicePointer == p;
+    } else {  // pageable host memory
+        int dev = 0, pageable = 0, host_tables = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&host_tables, cudaDevAttrPageableMemoryAccessUsesHostPageTables, dev) !=
+                cudaSuccess)
+            return SOFTMAX_ERR_CUDA;
+        *ok = pageable != 0 && host_tables != 0;
+    }
+    return SOFTMAX_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -625,6 +659,21 @@ int softmax_fwd_host(const void *in_host, void *out_host, int64_t rows, int64_t 
     const uint64_t ia = (uint64_t)(uintptr_t)in_host, oa = (uint64_t)(uintptr_t)out_host;
     int st = check_args(ia, oa, rows, cols, row_stride, dtype, &ext);
     if (st != SOFTMAX_OK || rows == 0) return st;
+    if (!workspace && workspace_bytes == 0) {
+        // zero-copy: the kernels read and write the host buffers in place,
+        // the bytes crossing the CPU-GPU link inside them
+        // (the first and the last byte of each range: one allocation may end
+        // before the range does)
+        const char *ends[4] = {static_cast<const char *>(in_host), static_cast<const char *>(in_host) + ext - 1,
+                               static_cast<const char *>(out_host), static_cast<const char *>(out_host) + ext - 1};
+        for (const char *e : ends) {
+            bool ok = false;
+            st = device_reaches(e, &ok);
+            if (st != SOFTMAX_OK) return st;
+            if (!ok) return SOFTMAX_ERR_ARG;
+        }
+        return softmax_fwd(in_host, out_host, rows, cols, row_stride, dtype, stream);
+    }
     if (!workspace) return SOFTMAX_ERR_NULL;
     if ((uintptr_t)workspace % 256 != 0 || workspace_bytes < 0) return SOFTMAX_ERR_ARG;
     const int es = elem_bytes(dtype);

@@ -406,16 +406,49 @@ __device__ __forceinline__ int whole_fit(int64_t first, int64_t end) {
     return (int)max(min(end - first, (int64_t)0x7fffffff), (int64_t)0);
 }
 
-// The 16-bit elements i of a packed vector with lo <= i < hi, the others
-// replaced by the bit pattern ninf.
+// Bit mask of the 16-bit elements a <= i < b (0 <= a, b <= 4) of a 64-bit word.
+__device__ __forceinline__ uint64_t elems64(int a, int b) {
+    const uint64_t below_b = b >= 4 ? ~0ull : (1ull << (16 * b)) - 1ull;
+    const uint64_t from_a = a >= 4 ? 0ull : ~0ull << (16 * a);
+    return below_b & from_a;
+}
+
+// The 16-bit elements i of a packed vector with lo <= i < hi (0 <= lo, hi <=
+// 8), the others replaced by the bit pattern ninf: one bit select per word
+// under a mask built with shifts.
 __device__ __forceinline__ uint4 keep_range16(const uint4 &r, int lo, int hi, uint32_t ninf) {
-    uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const bool a = 2 * k >= lo && 2 * k < hi, b = 2 * k + 1 >= lo && 2 * k + 1 < hi;
-        w[k] = (a ? (w[k] & 0xffffu) : ninf) | (b ? (w[k] & 0xffff0000u) : (ninf << 16));
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
+    const uint64_t m0 = elems64(min(lo, 4), min(hi, 4));
+    const uint64_t m1 = elems64(max(lo - 4, 0), max(hi - 4, 0));
+    const uint32_t n = ninf * 0x10001u;
+    const uint32_t k0 = (uint32_t)m0, k1 = (uint32_t)(m0 >> 32), k2 = (uint32_t)m1, k3 = (uint32_t)(m1 >> 32);
+    return make_uint4((r.x & k0) | (n & ~k0), (r.y & k1) | (n & ~k1), (r.z & k2) | (n & ~k2),
+                      (r.w & k3) | (n & ~k3));
+}
+
+// Store the 16-bit elements lo <= i < hi (0 <= lo < hi <= 8) of the packed
+// vector w into the aligned 16-byte word at dst, as naturally aligned pieces
+// of 2, 4 and 8 bytes: first up to the word's 8-byte boundary, then down from
+// it.  The word's other elements belong to a neighbouring row and are not
+// touched.
+__device__ __forceinline__ void store_range16(uint4 *dst, const uint4 &w, int lo, int hi) {
+    const uint64_t h0 = (uint64_t)w.x | ((uint64_t)w.y << 32), h1 = (uint64_t)w.z | ((uint64_t)w.w << 32);
+    char *const b = reinterpret_cast<char *>(dst);
+    const auto half = [&](int k) { return k < 4 ? h0 : h1; };
+    const auto st2 = [&](int k) {
+        *reinterpret_cast<uint16_t *>(b + 2 * k) = (uint16_t)(half(k) >> (16 * (k & 3)));
+    };
+    const auto st4 = [&](int k) {
+        *reinterpret_cast<uint32_t *>(b + 2 * k) = (uint32_t)(half(k) >> (16 * (k & 3)));
+    };
+    const auto st8 = [&](int k) { *reinterpret_cast<uint64_t *>(b + 2 * k) = half(k); };
+    int i = lo;
+    if ((i & 1) && i < hi) st2(i++);
+    if ((i & 2) && i + 2 <= hi) { st4(i); i += 2; }
+    if ((i & 4) && i + 4 <= hi) { st8(i); i += 4; }
+    if (i + 4 <= hi) { st8(i); i += 4; }
+    if (i + 4 <= hi) { st8(i); i += 4; }
+    if (i + 2 <= hi) { st4(i); i += 2; }
+    if (i < hi) st2(i);
 }
 
 // Store a tile's results: for vectors first + j*step < end, val(j, y) fills
@@ -437,21 +470,42 @@ __device__ __forceinline__ void tile_store(const RowView<T> &row, int64_t first,
         }
     } else if constexpr (sizeof(T) == 2) {
         // interior vectors at constant offsets from the row's aligned base;
-        // the row's two partial end vectors element by element
+        // the row's two partial end vectors as naturally aligned pieces
+        // (store_range16), or element by element when out has another phase
         uint4 *q = row.vec_out() + first;
         const int fit = whole_fit(first, end);
-        const bool head_edge = first == 0 && row.head != 0;
-        const int64_t last = row.tail < V ? row.nvec - 1 - first : -1;  // slot offset of a partial last vector
+        // slot offsets (from `first`) of the row's partial first / last vector, -1 if none
+        const int64_t head_slot = (first == 0 && row.head != 0) ? 0 : -1;
+        const int64_t tail_slot = row.tail < V ? row.nvec - 1 - first : -1;
+        if (!row.vec_store) {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                if (j * step < fit) {
+                    float y[V];
+                    val(j, y);
+                    row.store(first + (int64_t)j * step, y);
+                }
+            }
+            return;
+        }
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
-            if (j * step < fit) {
+            const int64_t o = (int64_t)j * step;
+            if (o < fit && o != head_slot && o != tail_slot) {
                 float y[V];
                 val(j, y);
-                const bool edge = (j == 0 && head_edge) || (int64_t)j * step == last;
-                if (row.vec_store && !edge)
-                    q[j * step] = Elem<T>::pack(y);
-                else
-                    row.store(first + j * step, y);
+                q[o] = Elem<T>::pack(y);
+            }
+        }
+        // the partial end vectors last (at most two slots of one thread each)
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t o = (int64_t)j * step;
+            if (o < fit && (o == head_slot || o == tail_slot)) {
+                float y[V];
+                val(j, y);
+                store_range16(q + o, Elem<T>::pack(y), o == head_slot ? row.head : 0,
+                              o == tail_slot ? row.tail : V);
             }
         }
     } else {

@@ -489,12 +489,16 @@ __device__ __forceinline__ void fill_vectors(const RowView<T> &row, int64_t firs
 }
 
 // Load a thread's kept vectors first + j*step of a row view `rl` of the kept
-// columns.  WHOLE (the full rows are whole vectors): every kept vector but a
-// last partial one moves as a plain 16-byte load, the partial one (if any)
+// columns.  16-bit rows: every kept vector as an aligned 16-byte load, the
+// elements of a partial last one past the kept part masked to -inf (the
+// packed tile's own load).  fp32 rows of whole vectors (WHOLE): every kept
+// vector but a last partial one as a plain 16-byte load, the partial one
 // element by element.
 template <bool WHOLE, int VPT, typename Tl, typename T>
 __device__ __forceinline__ void load_kept(Tl &tile, const RowView<T> &rl, int64_t first, int64_t step) {
-    if constexpr (WHOLE) {
+    if constexpr (sizeof(T) == 2) {
+        tile.load(rl, first, step, rl.nvec);
+    } else if constexpr (WHOLE) {
         constexpr int V = Elem<T>::kVec;
         const int64_t nw = rl.cols / V;  // whole kept vectors (rows start on 16 bytes)
         tile.template load<true>(rl, first, step, nw);

@@ -94,7 +94,7 @@ def test_plans_cover_every_row(rows, cols, stride, dt, in_off):
     path = p["path"]
     assert p["vec_store"] == 1
     if path == B.PATH_WARP:
-        assert (cols <= 1024 or p["whole_vectors"]) and p["group"] * p["vpt"] >= nv
+        assert (cols <= 1024 or p["whole_vectors"] or es == 2) and p["group"] * p["vpt"] >= nv
         assert p["grid"] * p["threads"] // p["group"] >= min(rows, p["grid"] * p["threads"] // p["group"])
     elif path == B.PATH_CTA:
         assert p["threads"] * p["vpt"] >= nv and p["grid"] == rows
@@ -141,7 +141,10 @@ def test_dispatch_follows_width_rule():
     assert plan(4096, 16391) == B.PATH_CTA
     assert plan(4096, 2048, "f16") == B.PATH_WARP  # whole vectors, 256 per row: still a warp
     assert plan(4096, 1100) == B.PATH_WARP         # 275 whole vectors
-    assert B.plan(1 << 24, 1 << 40, 4096, 2047, 2047, "bf16", num_sms=152)["path"] == B.PATH_CTA  # edges
+    assert B.plan(1 << 24, 1 << 40, 4096, 2047, 2047, "bf16", num_sms=152)["path"] == B.PATH_WARP  # 16-bit edges
+    assert B.plan(1 << 24, 1 << 40, 8192, 2055, 2055, "f16", num_sms=152)["path"] == B.PATH_WARP
+    assert plan(4096, 2047) == B.PATH_CTA            # ragged fp32 rows past 1024: a block per row
+    assert B.plan(1 << 24, 1 << 40, 8192, 2305, 2305, "f16", num_sms=152)["path"] == B.PATH_CTA  # > 288 vectors
     assert plan(4096, 16384) == B.PATH_CTA           # 512 x 8 keeps two 64 KB rows per SM
     assert plan(512, 131072, "bf16") == B.PATH_CLUSTER   # long 16-bit rows: a cluster, registers
     assert plan(512, 65536) == B.PATH_STREAM             # long fp32 rows: a cluster streaming them twice
