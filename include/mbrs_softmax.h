@@ -105,7 +105,11 @@ typedef enum {
 
 /*
  * softmax_fwd -- the fused row softmax described above.
- *   in, out     device pointers (element-aligned); may be NULL only if rows == 0
+ *   in, out     element-aligned pointers to memory the device addresses
+ *               directly: device memory, or host memory that is page-locked
+ *               and mapped (cudaHostAlloc, cudaHostRegister), or pageable host
+ *               memory on a device that reaches it through the host's page
+ *               tables (a coherent CPU-GPU link); may be NULL only if rows == 0
  *   rows        number of rows (>= 0); rows == 0 returns SOFTMAX_OK and launches nothing
  *   cols        valid columns per row (>= 1)
  *   row_stride  distance between row starts in elements (>= cols), both buffers
@@ -158,7 +162,16 @@ int softmax_fwd_masked(const void *in, void *out, int64_t rows, int64_t cols, in
  *   workspace          device memory the caller owns (256-byte aligned),
  *                      workspace_bytes long: three slots of at least one row
  *                      each; softmax_host_workspace_bytes(rows, cols,
- *                      row_stride, dtype, 0) gives the recommended size
+ *                      row_stride, dtype, 0) gives the recommended size.
+ *                      workspace == NULL with workspace_bytes == 0 selects
+ *                      the zero-copy mode: the kernels read in_host and write
+ *                      out_host in place, each element crossing the CPU-GPU
+ *                      link once in each direction inside them.  Both ranges
+ *                      must be memory the device reaches at the same address
+ *                      (page-locked and mapped, or pageable on a device that
+ *                      uses the host's page tables, as over NVLink-C2C); the
+ *                      call checks the first and last byte of each range and
+ *                      returns SOFTMAX_ERR_ARG without launching otherwise
  *   stream             the call is ordered after the work already queued on
  *                      stream, and work queued on stream afterwards waits for
  *                      it; it returns without waiting (synchronise stream
@@ -168,9 +181,11 @@ int softmax_fwd_masked(const void *in, void *out, int64_t rows, int64_t cols, in
  * softmax of another and the device-to-host copy of a third are in flight at
  * once.  Only the rows' cols elements are copied (pitched copies): padding
  * between host rows is neither read nor written.  Calls on one device are serialised by a lock while they are queued.
- * Other arguments, layout, aliasing and status codes as softmax_fwd
- * (SOFTMAX_ERR_ARG for a workspace too small).  Allocates nothing on the
- * device; the streams and events are created once per device.
+ * In the zero-copy mode the call is softmax_fwd on the host pointers (one
+ * kernel, same paths and ordering on `stream`).  Other arguments, layout,
+ * aliasing and status codes as softmax_fwd (SOFTMAX_ERR_ARG for a workspace
+ * too small).  Allocates nothing on the device; the streams and events are
+ * created once per device.
  */
 int softmax_fwd_host(const void *in_host, void *out_host, int64_t rows, int64_t cols, int64_t row_stride,
                      int dtype, void *workspace, int64_t workspace_bytes, cudaStream_t stream);

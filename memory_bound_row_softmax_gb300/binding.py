@@ -251,12 +251,14 @@ def host_workspace_bytes(rows: int, cols: int, row_stride: int, dtype, chunk_byt
     return n
 
 
-def softmax_fwd_host(x, out=None, workspace=None, stream=None):
+def softmax_fwd_host(x, out=None, workspace=None, stream=None, zero_copy: bool = False):
     """Row softmax of a 2-D CPU tensor (pinned for overlapping copies),
     written to ``out`` (a CPU tensor, default a new pinned one) through the
     library's chunked copy / softmax / copy pipeline on the current CUDA
     device.  ``workspace`` (a CUDA tensor) defaults to a new one of
-    softmax_host_workspace_bytes.  Synchronises ``stream`` before returning."""
+    softmax_host_workspace_bytes.  ``zero_copy=True`` passes no workspace:
+    the kernels read and write the host buffers in place (they must be memory
+    the device reaches directly).  Synchronises ``stream`` before returning."""
     import torch
     if not isinstance(x, torch.Tensor) or x.is_cuda or x.dim() != 2:
         raise TypeError("softmax_fwd_host needs a 2-D CPU tensor")
@@ -269,13 +271,17 @@ def softmax_fwd_host(x, out=None, workspace=None, stream=None):
         out = torch.empty_strided((rows, cols), (row_stride, 1), dtype=x.dtype, pin_memory=True)
     elif out.shape != x.shape or out.dtype != x.dtype or out.is_cuda or (rows > 1 and out.stride(0) != row_stride):
         raise ValueError("out must be a CPU tensor with x's shape, dtype and row stride")
-    if workspace is None:
-        workspace = torch.empty(max(host_workspace_bytes(rows, cols, row_stride, code), 1), dtype=torch.uint8,
-                                device="cuda")
+    if zero_copy:
+        ws_ptr, ws_bytes = None, 0
+    else:
+        if workspace is None:
+            workspace = torch.empty(max(host_workspace_bytes(rows, cols, row_stride, code), 1), dtype=torch.uint8,
+                                    device="cuda")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     s = stream if stream is not None else torch.cuda.current_stream()
     handle = s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
-    st = lib().softmax_fwd_host(x.data_ptr(), out.data_ptr(), rows, cols, row_stride, code, workspace.data_ptr(),
-                                workspace.numel() * workspace.element_size(), handle)
+    st = lib().softmax_fwd_host(x.data_ptr(), out.data_ptr(), rows, cols, row_stride, code, ws_ptr, ws_bytes,
+                                handle)
     if st != OK:
         raise SoftmaxError(st, "softmax_fwd_host")
     torch.cuda.current_stream().synchronize() if stream is None else s.synchronize()

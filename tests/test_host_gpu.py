@@ -1,6 +1,7 @@
 """softmax_fwd_host: host buffers through the library's chunked copy / softmax /
 copy pipeline, against the oracle -- one chunk and many, in place, padded
-strides, page-locked and pageable memory, and the stream ordering."""
+strides, page-locked and pageable memory, and the stream ordering -- and the
+zero-copy mode, in which the kernels work on the host buffers in place."""
 import numpy as np
 import pytest
 import torch
@@ -97,3 +98,61 @@ def test_workspace_too_small_is_refused():
     h = torch.zeros(4, 100, pin_memory=True)
     ws = torch.empty(256, dtype=torch.uint8, device="cuda")
     assert B.lib().softmax_fwd_host(h.data_ptr(), h.data_ptr(), 4, 100, 100, 0, ws.data_ptr(), 256, 0) == B.ERR_ARG
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("rows,cols", [(1, 7), (37, 1000), (4096, 2048), (300, 40000), (512, 131072)])
+def test_zero_copy_on_page_locked_memory(dtype, rows, cols):
+    if rows * cols > 20_000_000:
+        rows = 128
+    x = W.make_random(rows, cols, dtype, seed=rows * 3 + cols, sigma=2.0)
+    h = host_tensor(x, dtype, True)
+    y = B.softmax_fwd_host(h, zero_copy=True)
+    check(y, x, dtype, cols)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_zero_copy_in_place_strided(dtype):
+    rows, cols, stride = 700, 3001, 3009
+    x = W.make_random(rows, cols, dtype, seed=13, row_stride=stride, sigma=2.0)
+    full = host_tensor(x, dtype, True)
+    view = full[:, :cols]
+    B.softmax_fwd_host(view, out=view, zero_copy=True)
+    check(full, x, dtype, cols)
+    pad = full.view(torch.int32 if dtype == "f32" else torch.int16).numpy()[:, cols:]
+    want = W.bits_view(np.ascontiguousarray(x), dtype)[:, cols:].view(np.int32 if dtype == "f32" else np.int16)
+    assert (pad == want).all()  # the padding columns are never written
+
+
+def test_zero_copy_on_pageable_memory_runs_or_is_refused():
+    # pageable memory: run in place where the device reaches it through the
+    # host's page tables (a coherent CPU-GPU link), refused before any launch
+    # elsewhere -- either way never a fault
+    rows, cols = 300, 5000
+    x = W.make_random(rows, cols, "f32", seed=14, sigma=2.0)
+    a_in = np.ascontiguousarray(x)
+    a_out = np.full_like(a_in, 7.0)
+    st = B.lib().softmax_fwd_host(a_in.ctypes.data, a_out.ctypes.data, rows, cols, cols, 0, None, 0,
+                                  torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    if st == B.ERR_ARG:
+        assert (a_out == 7.0).all()
+    else:
+        assert st == B.OK
+        ref = oracle.softmax(x, "f32", cols=cols, threads=8)
+        assert np.abs(a_out.astype(np.float64) - ref).max() <= TOL["f32"]
+
+
+def test_zero_copy_needs_both_ranges_reachable():
+    # a device buffer for in and a pinned one for out is fine; a NULL
+    # workspace with a non-zero size is an error, as before
+    rows, cols = 64, 1000
+    x = W.make_random(rows, cols, "f32", seed=15)
+    d = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    out = torch.empty(rows, cols, pin_memory=True)
+    st = B.lib().softmax_fwd_host(d.data_ptr(), out.data_ptr(), rows, cols, cols, 0, None, 0,
+                                  torch.cuda.current_stream().cuda_stream)
+    assert st == B.OK
+    torch.cuda.synchronize()
+    check(out, x, "f32", cols)
+    assert B.lib().softmax_fwd_host(d.data_ptr(), out.data_ptr(), rows, cols, cols, 0, None, 64, None) == B.ERR_NULL
