@@ -793,7 +793,7 @@ def main(argv=None):
                     help="warm-up and timed launches only (the command profiled with ncu)")
     ap.add_argument("--no-attention", action="store_true", help="leave out the attention forward block")
     ap.add_argument("--attention", default="",
-                    help="a4k | a16k | a4k_small: time only the fused attention forward on that workload")
+                    help="a4k | a16k | a4k_small | a4k_wave: time only the fused attention forward on that workload")
     ap.add_argument("--json-out", default="")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch in plain stream order (no programmatic dependent launch)")

@@ -62,7 +62,9 @@ constexpr int kTiles = 2;     // query tiles per block, one softmax warpgroup ea
 constexpr int kRowsPerBlock = kTiles * kBlockM;
 constexpr int kThreads = 320;  // warps 0-7 softmax, 8 TMA, 9 MMA
 constexpr int kWarpTma = 8, kWarpMma = 9;
-constexpr int kSlots = 5;  // K / V ring: load n (K_{n/2} or V_{n/2}) goes to slot n mod kSlots
+// K / V ring: load n (K_{n/2} or V_{n/2}) goes to slot n mod kSlots (measured:
+// 3 slots run as fast as 5 or faster -- the K/V tiles come from L2)
+constexpr int kSlots = 3;
 constexpr uint32_t kTileBytes = kBlockN * kHeadDim * 2;  // one 128 x 128 tile of 16-bit elements
 constexpr uint32_t kHalfBytes = kTileBytes / 2;          // its 64-column half: 128 rows of 128 bytes
 // shared memory, from a 1024-byte aligned base

@@ -332,6 +332,8 @@ ATTENTION_CONFIGS: dict[str, AttentionWorkload] = {
     "a16k": AttentionWorkload("attn_f16_b4_h32_n16384_d128_causal", 4, 32, 16384, 128, "f16", 7),
     # a small case of the same kernel for detailed profiler captures
     "a4k_small": AttentionWorkload("attn_f16_b1_h8_n4096_d128_causal", 1, 8, 4096, 128, "f16", 8),
+    # a profiler case of several full waves: 512 items on 152 persistent blocks
+    "a4k_wave": AttentionWorkload("attn_f16_b2_h16_n4096_d128_causal", 2, 16, 4096, 128, "f16", 9),
 }
 
 QKV_STREAMS = {"q": 0, "k": 1, "v": 2}

@@ -19,7 +19,7 @@ import random
 
 import pytest
 
-SLOTS = 5    # K/V ring slots
+SLOTS = 3    # K/V ring slots
 TILES = 2    # query tiles (softmax groups) per block
 
 
