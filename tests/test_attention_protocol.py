@@ -220,3 +220,23 @@ def test_model_catches_publishing_before_the_release():
     with pytest.raises(AssertionError):
         for trial in range(20):
             ns["run"]([0, 0, 0, 0], 100, True, seed=trial)
+
+
+def test_model_catches_releasing_q_before_the_first_p():
+    # releasing Q as soon as a one-tile item's S products are issued, before
+    # both softmax groups have written the item's first P, lets the producer
+    # publish ring entries while a group is still finishing the previous item
+    # (the release rule a draft with P in shared memory got wrong)
+    src = inspect.getsource(run)
+    good = "            mma(); commit(\"s0\"); mma(); commit(\"s1\"); commit(f\"empty{nb % SLOTS}\")\n"
+    bad = ("            mma(); commit(\"s0\"); mma(); commit(\"s1\"); commit(f\"empty{nb % SLOTS}\")\n"
+           "            if n_b == 1:\n                commit(\"q_empty\")\n")
+    rule = "                if j + 2 == n_b or (n_b == 1 and j == 0):\n"
+    assert good in src and rule in src
+    mutated = src.replace(good, bad).replace(rule, "                if j + 2 == n_b:\n")
+    ns = dict(globals())
+    exec(mutated, ns)
+    with pytest.raises(AssertionError):
+        for trial in range(40):
+            for skew in SKEWS:
+                ns["run"]([0, 0, 0, 0, 0, 0], 100, True, seed=trial, skew=skew)
