@@ -35,7 +35,8 @@
  * aliasing) is allowed; any other overlap of the two byte ranges is rejected.
  * The library allocates no device memory per call: every path keeps its
  * partial (max, sum) states on chip (registers, shared memory, or the
- * distributed shared memory of a thread-block cluster).  Calls are
+ * distributed shared memory of a thread-block cluster), except path 8 (out
+ * != in only), which keeps them in the output rows before it overwrites them.  Calls are
  * asynchronous on `stream`; nothing is synchronised.
  *
  * Errors: arguments are checked on the host before any launch and a status
@@ -98,9 +99,19 @@ typedef enum {
     SOFTMAX_PATH_STREAM = 6,  /* a cluster (<= 16 blocks) per row, each block streaming its slice
                                  of any length twice: pass 1 (max, sum), exchange through
                                  distributed shared memory, pass 2 re-read and write; no scratch */
-    SOFTMAX_PATH_PACKED = 7   /* narrow rows of a dense matrix (row_stride == cols) staged through
+    SOFTMAX_PATH_PACKED = 7,  /* narrow rows of a dense matrix (row_stride == cols) staged through
                                  shared memory many rows at a time as one contiguous span of
                                  whole 16-byte vectors; one thread per row */
+    SOFTMAX_PATH_GRID = 8     /* a few very long rows (rows * 16 < SMs, rows of 1 MiB or more) when
+                                 out != in: each row cut into chunks over the whole grid, in two
+                                 launches -- each chunk's (max, sum) written into a state region
+                                 at the start of its output row (8 bytes per chunk and a 32-bit
+                                 counter), then every block folds its row's states, re-reads its
+                                 chunk and writes it, the region's own outputs written by the
+                                 block of the row that counts itself last; nothing allocated.  The
+                                 counter is an atomic add on `out`: host memory takes it only
+                                 where the device performs atomics on host memory natively
+                                 (otherwise the automatic choice is path 6) */
 } softmax_path_t;
 
 /*
@@ -121,6 +132,9 @@ typedef enum {
  */
 int softmax_fwd(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride,
                 int dtype, cudaStream_t stream);
+/* (Path 8 uses the caller's `out` rows as the place where partial states
+ * meet before it overwrites them with the results; what `out` holds before
+ * the call never matters, as on every path.) */
 
 /*
  * softmax_fwd_masked -- the row softmax of scaled, causally masked scores.
@@ -212,9 +226,11 @@ int softmax_last_path(void);
  * threads / vpt / group override the launch shape where > 0 (threads per block,
  * 16-byte vectors per thread, and lanes per row / cluster size for paths 1 /
  * 3 and 6; for path 7 vpt is the rows each thread takes per staged span and
- * group must be 0 or 1).  A forced shape that cannot cover the row makes
+ * group must be 0 or 1; for path 8 group is the chunks per row, and threads x
+ * vpt one of 256 x 4, 256 x 8, 512 x 4, 1024 x 4).  A forced
+ * shape that cannot cover the row, or path 8 with in == out, makes
  * softmax_fwd return SOFTMAX_ERR_UNSUPPORTED.  Paths 4 and 5, and values
- * outside 0..7, return SOFTMAX_ERR_ARG and leave the setting unchanged.
+ * outside 0..8, return SOFTMAX_ERR_ARG and leave the setting unchanged.
  * Process-wide, not thread-safe.
  */
 int softmax_set_force_path(int path, int threads, int vpt, int group);
@@ -224,14 +240,14 @@ typedef struct {
     int path;              /* softmax_path_t actually chosen */
     int threads;           /* threads per block */
     int vpt;               /* 16-byte vectors per thread per tile (7: rows per lane group per span) */
-    int group;             /* lanes per row (1), cluster size (3, 6), else 1 */
-    int launches;          /* kernels per call (1) */
+    int group;             /* lanes per row (1), cluster size (3, 6), chunks per row (8), else 1 */
+    int launches;          /* kernels per call (1; 2 for path 8) */
     int vec_store;         /* 1 if out has in's 16-byte phase (vector stores) */
     int64_t grid;          /* blocks of the kernel */
     int64_t smem_bytes;    /* dynamic shared memory per block */
     int64_t scratch_bytes; /* device scratch the call needs: 0 on every path */
-    int64_t hbm_bytes;     /* bytes moved: 2 * rows * cols * elem (3x for STREAM, whose
-                              second read is usually served by L2) */
+    int64_t hbm_bytes;     /* bytes moved: 2 * rows * cols * elem (3x for STREAM and GRID,
+                              whose second read is usually served by L2) */
     int whole_vectors;     /* 1 if every row is whole 16-byte vectors (in and out 16-byte
                               aligned, row stride and width multiples of 16 bytes): the
                               kernels then run their variants without edge tests */
@@ -380,7 +396,7 @@ int softmax_autotune_clear(void);
  * softmax_plan_t.whole_vectors, 1.4.0 the autotune calls and softmax_fwd_masked,
  * 1.5.0 the PACKED path and softmax_fwd_host; 2.0.0 removes the RING path and
  * softmax_plan_t.stages, and softmax_fwd no longer takes the SPLIT path or any
- * scratch). */
+ * scratch; 2.1.0 the GRID path). */
 int softmax_abi_version(void);
 
 #ifdef __cplusplus

@@ -16,9 +16,9 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "
 OK, ERR_NULL, ERR_SHAPE, ERR_STRIDE, ERR_DTYPE, ERR_OVERLAP, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_ALIGN, \
     ERR_ARG, ERR_SCRATCH_LIMIT = range(12)
 PATH_AUTO, PATH_WARP, PATH_CTA, PATH_CLUSTER, PATH_SPLIT = range(5)  # PATH_SPLIT: softmax_fwd_noalloc only
-PATH_STREAM, PATH_PACKED = 6, 7
+PATH_STREAM, PATH_PACKED, PATH_GRID = 6, 7, 8
 PATH_NAMES = {PATH_WARP: "warp", PATH_CTA: "cta", PATH_CLUSTER: "cluster", PATH_SPLIT: "split",
-              PATH_STREAM: "stream", PATH_PACKED: "packed"}
+              PATH_STREAM: "stream", PATH_PACKED: "packed", PATH_GRID: "grid"}
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
 
 _i64, _u64, _int, _vp = ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p

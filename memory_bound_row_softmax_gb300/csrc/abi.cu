@@ -11,6 +11,8 @@
 //   rows a warp's registers hold            path 1, 2..32 lanes per row
 //   16-bit rows a cluster's registers hold  path 3, a cluster per row
 //   other rows a block's registers hold     path 2, a block per row
+//   a few very long rows, out != in         path 8, chunks over the whole grid,
+//                                           states in the output rows
 //   longer rows                             path 6, a cluster per row streaming
 //                                           its slices twice
 // Every path keeps its partial states on chip: no call allocates memory.
@@ -30,11 +32,12 @@ using namespace mbrs;
 
 namespace {
 
-constexpr int kAbiVersion = 20000;  // 2.0.0
+constexpr int kAbiVersion = 20100;  // 2.1.0
 constexpr int kVecBytes = 16;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDefaultWaitNs = 1000000000;  // 1 s
 constexpr int64_t kMaxGrid = 0x7fffffff;
+constexpr int64_t kGridMinRowBytes = 1 << 20;  // path 8 only for rows this long
 
 std::atomic<int> g_last_path{0};
 std::atomic<int> g_force_path{0}, g_force_threads{0}, g_force_vpt{0}, g_force_group{0};
@@ -44,7 +47,7 @@ std::atomic<int> g_overlap{1};
 
 struct Plan {
     int path = 0, threads = 0, vpt = 0, group = 1, launches = 0, vec_store = 0, whole = 0;
-    int64_t grid = 0, smem = 0, hbm = 0;
+    int64_t grid = 0, smem = 0, hbm = 0, chunks = 0, chunk_vecs = 0;
 };
 
 // A launch shape asked for: path 0 = automatic; threads / vpt / group 0 =
@@ -186,6 +189,12 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             // ring at every such width measured (8192 x 2816 fp16: block 14.4
             // us, ring 17.1; 4096 x 2816 fp32: 14.0 against 19.5)
             path = SOFTMAX_PATH_CTA;
+        } else if (rows * 16 < sms && in != out && cols * es >= kGridMinRowBytes) {
+            // a few rows of 1 MiB or more: no cluster can spread them over
+            // more than 16 SMs each, so their chunks go over the whole grid,
+            // their states meeting in the output rows (fp32 1 x 4e6: 34.6 us
+            // on the streaming cluster, 13.2 in three launches)
+            path = SOFTMAX_PATH_GRID;
         } else {
             // longer rows: a cluster streaming its slices twice, about one
             // 1024-vector tile per block.  Measured against a TMA-fed ring and
@@ -344,10 +353,53 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             p->hbm = 3 * rows * cols * es;
             break;
         }
+        case SOFTMAX_PATH_GRID: {
+            // about two 512-thread blocks per SM over all rows, the row cut
+            // into that many equal chunks, the last taking the rest (forced:
+            // up to `group` chunks of 3 vectors or more).  Measured on one
+            // GB300 (us): fp32 1 x 4e6 10.9 (256-thread blocks, four per SM:
+            // 12.3; 1024 x 4, one per SM: 11.7); fp32 3 x 1e6 9.7 (12.3);
+            // bf16 1 x 2^22 8.5 (9.4).  The row's state region (8 bytes per
+            // chunk and a counter) must fit in the row.
+            if (in == out || nv < 3) return SOFTMAX_ERR_UNSUPPORTED;
+            const int th = fth > 0 ? fth : kGridThreads, vp = fvpt > 0 ? fvpt : kGridVpt;
+            if (!grid_shape_ok(th, vp)) return SOFTMAX_ERR_UNSUPPORTED;
+            const int64_t want = fgrp > 0 ? fgrp : std::max<int64_t>(1, 2 * (int64_t)sms / rows);
+            const int64_t chunk_vecs = std::max<int64_t>(3, nv / want);
+            const int64_t k = std::max<int64_t>(1, std::min<int64_t>(want, nv / chunk_vecs));
+            if (8 * k + 8 > cols * es || rows > kMaxGrid / k) return SOFTMAX_ERR_UNSUPPORTED;
+            p->threads = th;
+            p->vpt = vp;
+            p->group = (int)k;
+            p->chunks = k;
+            p->chunk_vecs = chunk_vecs;
+            p->grid = std::min<int64_t>(rows * k, (int64_t)sms * (2048 / th));
+            p->launches = 2;
+            p->hbm = 3 * rows * cols * es;
+            break;
+        }
         default:
             return SOFTMAX_ERR_UNSUPPORTED;
     }
     return SOFTMAX_OK;
+}
+
+// The grid path counts the blocks of a row with a 32-bit atomic add on a word
+// of `out`: fine in device or managed memory, and in host memory when the
+// device performs atomics on host memory natively (a coherent CPU-GPU link).
+bool grid_atomics_ok(const void *out) {
+    int dev = 0, native = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&native, cudaDevAttrHostNativeAtomicSupported, dev) != cudaSuccess)
+        return false;
+    if (native) return true;
+    cudaPointerAttributes pa;
+    std::memset(&pa, 0, sizeof(pa));
+    if (cudaPointerGetAttributes(&pa, out) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return pa.type == cudaMemoryTypeDevice || pa.type == cudaMemoryTypeManaged;
 }
 
 int run(const Plan &p, const LaunchArgs &a) {
@@ -362,6 +414,10 @@ int run(const Plan &p, const LaunchArgs &a) {
             e = launch_stream(a, p.threads, p.vpt, p.group, g_wait_ns.load(), g_starve.load());
             break;
         case SOFTMAX_PATH_PACKED: e = launch_packed(a, kPackedThreads * p.vpt, p.grid); break;
+        case SOFTMAX_PATH_GRID:
+            if (!grid_atomics_ok(a.out)) return SOFTMAX_ERR_UNSUPPORTED;
+            e = launch_grid(a, p.threads, p.vpt, p.chunks, p.chunk_vecs, p.grid);
+            break;
         default: return SOFTMAX_ERR_UNSUPPORTED;
     }
     if (e == cudaErrorInvalidValue) return SOFTMAX_ERR_UNSUPPORTED;
@@ -455,9 +511,10 @@ Shape call_shape(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t 
 
 // Candidate shapes for rows of up to nv vectors: the automatic choice first,
 // the shared-memory staged path for narrow dense rows, then every lane-group /
-// block / cluster shape that can hold the row and the streaming cluster at
-// three block sizes.
-std::vector<Shape> tune_candidates(int64_t nv, int es, bool packed_ok) {
+// block / cluster shape that can hold the row, the streaming cluster at
+// three block sizes and, for rows longer than a block with out != in, the
+// grid-wide path.
+std::vector<Shape> tune_candidates(int64_t nv, int es, bool packed_ok, bool grid_ok) {
     std::vector<Shape> c;
     c.push_back(Shape{});
     if (packed_ok) c.push_back(Shape{SOFTMAX_PATH_PACKED, 0, 1, 0});
@@ -478,6 +535,7 @@ std::vector<Shape> tune_candidates(int64_t nv, int es, bool packed_ok) {
                 c.push_back(Shape{SOFTMAX_PATH_CLUSTER, t, 8, 0});
         for (int t = 256; t <= 1024; t *= 2) c.push_back(Shape{SOFTMAX_PATH_STREAM, t, 4, 0});
     }
+    if (nv > 512 * 10 && grid_ok) c.push_back(Shape{SOFTMAX_PATH_GRID, 0, 0, 0});
     return c;
 }
 
@@ -488,7 +546,7 @@ std::vector<Shape> candidates_for(uint64_t in, uint64_t out, int64_t cols, int64
     const int64_t nv = uniform ? cdiv(head + cols, V) : cdiv(cols + V - 1, V);
     const bool packed_ok = row_stride == cols && (in % kVecBytes) == (out % kVecBytes) &&
                            packed_smem_bytes(kPackedThreads, cols, es) <= kPackedMaxSmem;
-    return tune_candidates(nv, es, packed_ok);
+    return tune_candidates(nv, es, packed_ok, in != out);
 }
 
 void fill_public_plan(const Plan &p, softmax_plan_t *plan) {
@@ -591,10 +649,18 @@ int softmax_fwd(const void *in, void *out, int64_t rows, int64_t cols, int64_t r
     st = device_sms(&sms);
     if (st != SOFTMAX_OK) return st;
     Plan p;
-    st = make_plan(ia, oa, rows, cols, row_stride, dtype, sms, call_shape(ia, oa, rows, cols, row_stride, dtype), &p);
+    const Shape want = call_shape(ia, oa, rows, cols, row_stride, dtype);
+    st = make_plan(ia, oa, rows, cols, row_stride, dtype, sms, want, &p);
     if (st != SOFTMAX_OK) return st;
     LaunchArgs a{in, out, rows, cols, row_stride, dtype, p.vec_store, stream, g_overlap.load(), p.whole};
     st = run(p, a);
+    if (st == SOFTMAX_ERR_UNSUPPORTED && p.path == SOFTMAX_PATH_GRID && want.path != SOFTMAX_PATH_GRID) {
+        // the grid path's counter cannot live in this `out` (host memory
+        // without native atomics): the streaming cluster instead
+        st = make_plan(ia, oa, rows, cols, row_stride, dtype, sms, Shape{SOFTMAX_PATH_STREAM, 0, 0, 0}, &p);
+        if (st != SOFTMAX_OK) return st;
+        st = run(p, a);
+    }
     if (st == SOFTMAX_OK) g_last_path.store(p.path);
     return st;
 }
@@ -777,7 +843,7 @@ const char *softmax_status_string(int status) {
 int softmax_last_path(void) { return g_last_path.load(); }
 
 int softmax_set_force_path(int path, int threads, int vpt, int group) {
-    if (path < SOFTMAX_PATH_AUTO || path > SOFTMAX_PATH_PACKED || path == SOFTMAX_PATH_SPLIT || path == 5)
+    if (path < SOFTMAX_PATH_AUTO || path > SOFTMAX_PATH_GRID || path == SOFTMAX_PATH_SPLIT || path == 5)
         return SOFTMAX_ERR_ARG;
     g_force_path.store(path);
     g_force_threads.store(threads > 0 ? threads : 0);

@@ -370,6 +370,141 @@ __global__ void __launch_bounds__(THREADS)
 }
 
 // ---------------------------------------------------------------------------
+// path 8: a few very long rows over the whole grid, the per-chunk states kept
+// in the output row itself (out != in; two launches, nothing allocated)
+// ---------------------------------------------------------------------------
+// Chunk k (of `chunks`) of a row covers vectors [k chunk_vecs, (k + 1)
+// chunk_vecs), the last chunk also the rest of the row.  The row's state
+// region is the start of its output row, from its first 4-byte aligned byte:
+// one 8-byte slot per chunk (the chunk's (s, l) as the bit patterns of two
+// floats), then a 32-bit counter.  The planner keeps the region inside the
+// row.
+//
+// k_grid_stats: each block streams a chunk into its state, writes the slot,
+// and the block of chunk 0 zeroes the counter.
+// k_grid_apply (after k_grid_stats has completed, griddepcontrol.wait):
+// each block reads every slot of its row, folds them into the row's state,
+// counts itself on the counter (fence, then atomicAdd) and writes its chunk
+// but the vectors that cover the region.  The block that counts last knows
+// every block of the row has read the slots: it writes the region's vectors
+// (fence, then re-read from `in`).  No block waits on another.
+template <typename T>
+struct GridStates {
+    uint32_t *w;  // the region: slot k = w[2k], w[2k + 1]; the counter = w[2 chunks]
+    __device__ __forceinline__ explicit GridStates(T *out_row)
+        : w(reinterpret_cast<uint32_t *>((reinterpret_cast<uintptr_t>(out_row) + 3) & ~(uintptr_t)3)) {}
+    __device__ __forceinline__ void put(int64_t k, float2 st) const {
+        w[2 * k] = __float_as_uint(st.x);
+        w[2 * k + 1] = __float_as_uint(st.y);
+    }
+    // through L2 (the slots were written by the previous launch)
+    __device__ __forceinline__ float2 get(int64_t k) const {
+        return make_float2(__uint_as_float(__ldcg(w + 2 * k)), __uint_as_float(__ldcg(w + 2 * k + 1)));
+    }
+    __device__ __forceinline__ unsigned int *counter(int64_t chunks) const { return w + 2 * chunks; }
+    // vectors [0, r) of the row view `rv` (the input's vector geometry) cover
+    // the region's columns
+    __device__ __forceinline__ int64_t region_vecs(const RowView<T> &rv, const T *out_row, int64_t chunks) const {
+        const int64_t bytes = (int64_t)(reinterpret_cast<uintptr_t>(w) - reinterpret_cast<uintptr_t>(out_row)) +
+                              8 * chunks + 4;
+        const int64_t n = (bytes + (int64_t)sizeof(T) - 1) / (int64_t)sizeof(T);
+        return (rv.head + n + Elem<T>::kVec - 1) / Elem<T>::kVec;
+    }
+};
+
+__device__ __forceinline__ void grid_chunk(int64_t k, int64_t chunks, int64_t chunk_vecs, int64_t nvec,
+                                           int64_t &c0, int64_t &c1) {
+    c0 = min(k * chunk_vecs, nvec);
+    c1 = k == chunks - 1 ? nvec : min(c0 + chunk_vecs, nvec);
+}
+
+template <typename T, int THREADS, int VPT>
+__global__ void __launch_bounds__(THREADS) k_grid_stats(const T *in, T *out, int64_t rows, int64_t cols,
+                                                        int64_t stride, int64_t chunks, int64_t chunk_vecs) {
+    prefetch_first_chunk(in, rows, cols, stride, chunks, chunk_vecs);
+    pdl_enter();
+    constexpr int NW = THREADS / 32;
+    constexpr int64_t kTile = (int64_t)THREADS * VPT;
+    __shared__ float2 red[2][NW];
+    int parity = 0;
+    const int64_t units = rows * chunks;
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x, parity ^= 1) {
+        const int64_t row = u / chunks, k = u - row * chunks;
+        RowView<T> rv(in + row * stride, out + row * stride, cols, false);
+        int64_t c0, c1;
+        grid_chunk(k, chunks, chunk_vecs, rv.nvec, c0, c1);
+        float m = -INFINITY, l = 0.f;
+        for (int64_t t0 = c0; t0 < c1; t0 += kTile) {
+            Tile<T, VPT> tile;
+            tile.load(rv, t0 + threadIdx.x, THREADS, c1);
+            const float2 st = tile.stats();
+            const float M = fmaxf(m, st.x);
+            l = rescale(l, m, M) + rescale(st.y, st.x, M);
+            m = M;
+        }
+        block_merge<NW>(m, l, red[parity]);
+        if (threadIdx.x == 0) {
+            const GridStates<T> gs(out + row * stride);
+            gs.put(k, make_float2(m, l));
+            if (k == 0) *gs.counter(chunks) = 0u;
+        }
+    }
+}
+
+template <typename T, int THREADS, int VPT>
+__global__ void __launch_bounds__(THREADS, VPT == 4 ? 1024 / THREADS : 1)
+    k_grid_apply(const T *in, T *out, int64_t rows, int64_t cols, int64_t stride, int64_t chunks,
+                 int64_t chunk_vecs, int vec_store) {
+    prefetch_first_chunk(in, rows, cols, stride, chunks, chunk_vecs);
+    pdl_enter();
+    constexpr int NW = THREADS / 32;
+    constexpr int64_t kTile = (int64_t)THREADS * VPT;
+    __shared__ float2 red[2][NW];
+    __shared__ int last_flag[2];
+    int parity = 0;
+    const int64_t units = rows * chunks;
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x, parity ^= 1) {
+        const int64_t row = u / chunks, k = u - row * chunks;
+        T *orow = out + row * stride;
+        RowView<T> rv(in + row * stride, orow, cols, vec_store != 0);
+        const GridStates<T> gs(orow);
+        int64_t c0, c1;
+        grid_chunk(k, chunks, chunk_vecs, rv.nvec, c0, c1);
+        const int64_t r = gs.region_vecs(rv, orow, chunks);
+        const int64_t s0 = max(c0, r);  // the chunk's first vector past the region
+        Tile<T, VPT> tile;
+        if (s0 < c1) tile.load(rv, s0 + threadIdx.x, THREADS, c1);  // in flight while the slots are read
+        float m = -INFINITY, l = 0.f;
+        for (int64_t j = threadIdx.x; j < chunks; j += THREADS) {
+            const float2 st = gs.get(j);
+            const float M = fmaxf(m, st.x);
+            l = rescale(l, m, M) + rescale(st.y, st.x, M);
+            m = M;
+        }
+        block_merge<NW>(m, l, red[parity]);  // every thread's slot reads have returned
+        if (threadIdx.x == 0) {
+            __threadfence();
+            const bool last = atomicAdd(gs.counter(chunks), 1u) == (unsigned int)(chunks - 1);
+            if (last) __threadfence();
+            last_flag[parity] = last;
+        }
+        __syncthreads();
+        const float shift = m;  // the row's S
+        const float inv = m == -INFINITY ? __int_as_float(0x7fc00000) : 1.f / l;
+        // the chunk past the region, then (the last block only, once every
+        // block of the row has read the slots) the region's vectors
+        const int passes = last_flag[parity] ? 2 : 1;
+        for (int pass = 0; pass < passes; ++pass) {
+            const int64_t a = pass == 0 ? s0 : 0, b = pass == 0 ? c1 : r;
+            for (int64_t t0 = a; t0 < b; t0 += kTile) {
+                if (pass != 0 || t0 != s0) tile.load(rv, t0 + threadIdx.x, THREADS, b);
+                tile.shift_store(rv, t0 + threadIdx.x, THREADS, b, shift, inv);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // path 7: narrow dense rows staged through shared memory
 // ---------------------------------------------------------------------------
 // Rows of a dense matrix (row stride == cols) too narrow and too misaligned

@@ -128,6 +128,17 @@ cudaError_t launch_stream(const LaunchArgs &a, int threads, int vpt, int csize, 
 // read this device's error word after synchronising `stream`, then clear it
 cudaError_t read_clear_error_word(cudaStream_t stream, unsigned int *word);
 
+// path 8: a few very long rows over the whole grid, their per-chunk states in
+// the output row itself (k_grid.cu): two launches of `threads` threads x `vpt`
+// vectors (grid_shape_ok; kGridThreads x kGridVpt by default); a.in must
+// differ from a.out; `chunks` slots of 8 bytes and a 4-byte counter, from the
+// row's first 4-byte aligned byte, must fit in the row (8 chunks + 8 <= row
+// bytes)
+constexpr int kGridThreads = 512, kGridVpt = 4;
+bool grid_shape_ok(int threads, int vpt);
+cudaError_t launch_grid(const LaunchArgs &a, int threads, int vpt, int64_t chunks, int64_t chunk_vecs,
+                        int64_t grid);
+
 // softmax_fwd_noalloc: the split path with its per-chunk states in a fixed
 // device array of kNoAllocMaxStates float2 (k_noalloc.cu); rows * chunks must
 // not exceed it.  Launch shape: 256 threads, 4 vectors per thread.

@@ -46,7 +46,7 @@ def test_status_strings():
     for s in range(11):
         assert B.status_string(s) and B.status_string(s) != "unknown status"
     assert B.status_string(99) == "unknown status"
-    assert B.abi_version() == 20000
+    assert B.abi_version() == 20100
 
 
 @pytest.mark.parametrize("args,expect", [
@@ -105,12 +105,17 @@ def test_plans_cover_every_row(rows, cols, stride, dt, in_off):
     elif path == B.PATH_PACKED:  # dense narrow rows, one thread each, 128 rows per staged span
         assert stride == cols and cols <= 48 and p["threads"] == 128 and p["grid"] == -(-rows // 128)
         assert p["smem_bytes"] >= 128 * cols * 4
+    elif path == B.PATH_GRID:  # a few rows of 1 MiB or more, spread over the grid (out != in)
+        assert rows * 16 < 152 and cols * es >= 1 << 20
+        assert p["group"] == max(1, min(2 * 152 // rows, nv // max(3, nv // max(1, 2 * 152 // rows))))
+        assert p["threads"] == 512 and p["grid"] == min(rows * p["group"], 152 * 4)
     else:  # any slice length; enough blocks to fill the GPU (or 16 per row)
         assert path == B.PATH_STREAM
         assert 1 <= p["group"] <= 16 and p["grid"] == rows * p["group"]
         assert rows * p["group"] >= min(152, rows * 16)
-    assert p["scratch_bytes"] == 0 and p["launches"] == 1  # one kernel, nothing allocated
-    mult = 3 if path == B.PATH_STREAM else 2
+    assert p["scratch_bytes"] == 0  # nothing allocated
+    assert p["launches"] == (2 if path == B.PATH_GRID else 1)
+    mult = 3 if path in (B.PATH_STREAM, B.PATH_GRID) else 2
     assert p["hbm_bytes"] == mult * rows * cols * es
 
 
@@ -152,7 +157,10 @@ def test_dispatch_follows_width_rule():
     assert plan(512, 131079, "bf16") == B.PATH_CLUSTER   # long misaligned rows, enough of them
     assert plan(4, 131072, "bf16") == B.PATH_STREAM      # too few rows to fill the GPU: 16 blocks each
     assert plan(64, 1 << 22) == B.PATH_STREAM            # too long to hold on chip: stream it twice
-    assert plan(9, 1 << 22) == B.PATH_STREAM             # ... also when 16 blocks per row cannot fill the GPU
+    assert plan(9, 1 << 22) == B.PATH_GRID               # 9 rows of 16 MiB: chunks over the whole grid
+    assert B.plan(1 << 24, 1 << 24, 9, 1 << 22, 1 << 22, "f32", num_sms=152)["path"] == B.PATH_STREAM  # in place
+    assert plan(9, 1 << 18) == B.PATH_GRID               # 1 MiB rows
+    assert plan(9, (1 << 18) - 1) == B.PATH_STREAM       # ... but not shorter ones
 
 
 def test_few_long_rows_take_one_tile_per_block():
@@ -160,23 +168,65 @@ def test_few_long_rows_take_one_tile_per_block():
     # holds about one 4-vector tile of its slice
     p = B.plan(1 << 24, 1 << 40, 9, 262144, 262144, "bf16", num_sms=152)
     assert (p["path"], p["group"], p["threads"]) == (B.PATH_STREAM, 16, 512)
-    p = B.plan(1 << 24, 1 << 40, 3, 1_000_000, 1_000_000, "f32", num_sms=152)
+    p = B.plan(1 << 24, 1 << 24, 3, 1_000_000, 1_000_000, "f32", num_sms=152)   # in place
     assert (p["path"], p["group"], p["threads"]) == (B.PATH_STREAM, 16, 1024)
     p = B.plan(1 << 24, 1 << 40, 1, 40000, 40000, "f32", num_sms=152)
     assert (p["path"], p["group"], p["threads"]) == (B.PATH_STREAM, 10, 256)
+
+
+def test_few_very_long_rows_spread_over_the_grid():
+    # out != in and rows of 1 MiB or more: about two 512-thread blocks per SM
+    # over all rows, each row in equal chunks, the states kept in the output row
+    p = B.plan(1 << 24, 1 << 40, 3, 1_000_000, 1_000_000, "f32", num_sms=152)
+    assert (p["path"], p["threads"], p["vpt"], p["launches"]) == (B.PATH_GRID, 512, 4, 2)
+    assert p["group"] == 101 and p["grid"] == 303 and p["scratch_bytes"] == 0
+    p = B.plan(1 << 24, 1 << 40, 1, 4_000_000, 4_000_000, "f32", num_sms=152)
+    assert p["path"] == B.PATH_GRID and p["group"] == 304 and p["grid"] == 304
+    p = B.plan(1 << 24, 1 << 40, 1, 1 << 26, 1 << 26, "bf16", num_sms=152)
+    assert p["path"] == B.PATH_GRID and p["group"] == 304 and p["grid"] == 304
+    try:
+        B.set_force_path(B.PATH_GRID, group=7)   # forced: any chunk count, chunks of 3 vectors or more
+        p = B.plan(1 << 24, 1 << 40, 5, 100, 100, "f32", num_sms=152)
+        assert (p["path"], p["group"], p["grid"]) == (B.PATH_GRID, 7, 35)
+        p = B.plan(1 << 24, 1 << 40, 5, 9, 9, "f32", num_sms=152)         # 3 vectors: one chunk
+        assert (p["path"], p["group"]) == (B.PATH_GRID, 1)
+        for cols in (1, 8):                        # fewer than 3 vectors: no room for the states
+            with pytest.raises(B.SoftmaxError) as e:
+                B.plan(1 << 24, 1 << 40, 5, cols, cols, "f32", num_sms=152)
+            assert e.value.status == B.ERR_UNSUPPORTED
+        B.set_force_path(B.PATH_GRID, group=300)   # at most 2048 threads per SM
+        p = B.plan(1 << 24, 1 << 40, 5, 100000, 100000, "f32", num_sms=152)
+        assert (p["group"], p["grid"]) == (300, 152 * 4)
+        B.set_force_path(B.PATH_GRID, 1024, 4, 300)
+        p = B.plan(1 << 24, 1 << 40, 5, 100000, 100000, "f32", num_sms=152)
+        assert (p["threads"], p["vpt"], p["group"], p["grid"]) == (1024, 4, 300, 152 * 2)
+        for shape in ((128, 4), (256, 2), (512, 8)):   # not instantiated
+            B.set_force_path(B.PATH_GRID, *shape)
+            with pytest.raises(B.SoftmaxError):
+                B.plan(1 << 24, 1 << 40, 5, 100000, 100000, "f32", num_sms=152)
+        B.set_force_path(B.PATH_GRID, group=1 << 20)   # chunks of 3 vectors: the state region still fits
+        p = B.plan(1 << 24, 1 << 40, 5, 100000, 100000, "f32", num_sms=152)
+        assert p["group"] == 25000 // 3 and 8 * p["group"] + 8 <= 400000
+        with pytest.raises(B.SoftmaxError) as e:   # the states need an output row apart from the input
+            B.plan(1 << 24, 1 << 24, 5, 100, 100, "f32", num_sms=152)
+        assert e.value.status == B.ERR_UNSUPPORTED
+    finally:
+        B.set_force_path(0)
 
 
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 def test_no_automatic_plan_takes_scratch(dt):
     # softmax_fwd allocates nothing: every automatic plan, over rows from 1 to
     # 2^21 and widths from 1 to 2^24, has scratch_bytes == 0 and one kernel
+    # (two for the grid-wide path, whose states live in the output)
     for rows in (1, 2, 3, 5, 9, 10, 64, 1000, 1 << 21):
         for cols in (1, 39, 1000, 2055, 20000, 40961, 131072, 1_000_000, 1 << 24):
             if rows * cols > 1 << 34:
                 continue
             for off in (0, 4):
                 p = B.plan((1 << 24) + off, (1 << 46) + off, rows, cols, cols, dt, num_sms=152)
-                assert p["scratch_bytes"] == 0 and p["launches"] == 1 and p["path"] != B.PATH_SPLIT
+                assert p["scratch_bytes"] == 0 and p["path"] != B.PATH_SPLIT
+                assert p["launches"] == (2 if p["path"] == B.PATH_GRID else 1)
 
 
 def test_forced_paths_and_rejections():
@@ -253,6 +303,8 @@ def _check_plan_covers(p, rows, cols, stride, dt, in_off, out_off):
     elif path == B.PATH_PACKED:
         assert stride == cols and p["group"] == 1 and p["smem_bytes"] <= 48 * 1024
         assert p["grid"] * 128 * p["vpt"] >= rows
+    elif path == B.PATH_GRID:
+        assert p["group"] >= 1 and nv // p["group"] >= 3 and 1 <= p["grid"] <= rows * p["group"]
     else:
         assert path == B.PATH_STREAM
         assert 1 <= p["group"] <= 16 and p["grid"] == rows * p["group"]

@@ -37,7 +37,9 @@ def test_candidates_follow_the_row_length():
     assert B.PATH_CLUSTER not in _paths(medium)                          # fp32 slices would spill
     assert B.PATH_CLUSTER in _paths(B.tune_candidates(A_IN, A_OUT, 64, 16384, 16384, "f16"))
     long_ = B.tune_candidates(A_IN, A_OUT, 64, 1 << 20, 1 << 20, "f32")
-    assert _paths(long_) == {0, B.PATH_STREAM}                           # nothing else holds the row
+    assert _paths(long_) == {0, B.PATH_STREAM, B.PATH_GRID}              # nothing else holds the row
+    in_place = B.tune_candidates(A_IN, A_IN, 64, 1 << 20, 1 << 20, "f32")
+    assert _paths(in_place) == {0, B.PATH_STREAM}                        # the grid path keeps states in out
     bf16 = B.tune_candidates(A_IN, A_OUT, 512, 131072, 131072, "bf16")
     assert (B.PATH_CLUSTER, 256, 8, 0) in bf16                           # register-held slices
 

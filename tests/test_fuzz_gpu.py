@@ -13,7 +13,8 @@ from gpu_harness import DeviceCase, compare
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [0, 0, 0, B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_STREAM, B.PATH_STREAM, B.PATH_PACKED]
+PATHS = [0, 0, 0, B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_STREAM, B.PATH_STREAM, B.PATH_PACKED,
+         B.PATH_GRID]
 
 
 def draw_cases(n: int, seed: int = 20261202):
@@ -50,7 +51,8 @@ def test_fuzz(case):
     st = dc.run(cols, path=path)
     if path and st == B.ERR_UNSUPPORTED:
         # a forced path that cannot take this shape (cluster: 16-bit rows
-        # only; packed: dense narrow rows; warp / block: short rows)
+        # only; packed: dense narrow rows; warp / block: short rows; grid:
+        # out != in and three vectors or more)
         pytest.skip(f"path {path} refuses this shape")
     assert st == B.OK, B.status_string(st)
     assert B.check_device_error() == B.OK

@@ -143,6 +143,29 @@ def test_zero_copy_on_pageable_memory_runs_or_is_refused():
         assert np.abs(a_out.astype(np.float64) - ref).max() <= TOL["f32"]
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("pinned", [True, False])
+def test_zero_copy_few_very_long_rows(dtype, pinned):
+    # rows * 16 < SMs and 1 MiB rows: the grid path, whose chunk states and
+    # block counter live in the host output rows (atomics on host memory where
+    # the device performs them natively, else the streaming cluster); pageable
+    # memory runs where the device reaches it, else it is refused
+    rows, cols = 2, 700_001
+    x = W.make_random(rows, cols, dtype, seed=16, sigma=2.0)
+    h = host_tensor(x, dtype, pinned)
+    out = torch.full_like(h, 3.0)
+    st = B.lib().softmax_fwd_host(h.data_ptr(), out.data_ptr(), rows, cols, cols, B.DTYPE_CODES[dtype], None, 0,
+                                  torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    if st == B.ERR_ARG and not pinned:
+        assert (out == 3.0).all()
+        return
+    assert st == B.OK
+    assert B.last_path() in (B.PATH_GRID, B.PATH_STREAM)
+    assert B.check_device_error() == B.OK
+    check(out, x, dtype, cols)
+
+
 def test_zero_copy_needs_both_ranges_reachable():
     # a device buffer for in and a pinned one for out is fine; a NULL
     # workspace with a non-zero size is an error, as before

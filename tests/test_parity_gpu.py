@@ -55,7 +55,7 @@ WIDTHS = [1, 2, 3, 5, 7, 8, 9, 16, 31, 33, 63, 100, 255, 257, 1000, 1023, 1024, 
 def test_auto_widths(dtype, cols):
     rows = 5 if cols > 10000 else 7
     res = run_and_compare(rnd(rows, cols, dtype, seed=cols), dtype)
-    assert res["path"] in (B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_STREAM, B.PATH_PACKED)
+    assert res["path"] in (B.PATH_WARP, B.PATH_CTA, B.PATH_CLUSTER, B.PATH_STREAM, B.PATH_PACKED, B.PATH_GRID)
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -77,6 +77,7 @@ FORCED = {
     B.PATH_CLUSTER: [1, 100, 2048, 9000, 16391, 65536, 131079, 262151],
     B.PATH_STREAM: [1, 100, 4103, 65536, 262147],
     B.PATH_PACKED: [1, 7, 39, 90],
+    B.PATH_GRID: [17, 100, 4103, 65536, 262147],
 }
 
 
@@ -142,6 +143,52 @@ def test_stream_whole_rows(dtype, rows, cols):
     # cluster size
     res = run_and_compare(rnd(rows, cols, dtype, seed=rows + cols), dtype, path=B.PATH_STREAM)
     assert res["path"] == B.PATH_STREAM
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("group", [1, 2, 3, 7, 64, 1000, 5000])
+@pytest.mark.parametrize("in_off,out_off", [(1, 1), (3, 0)])
+def test_grid_chunk_counts(dtype, group, in_off, out_off):
+    # 70001 columns in `group` chunks (down to 3 vectors each), misaligned
+    # rows, out at in's 16-byte phase or not: every chunk's state passes
+    # through the state region at the start of the output row
+    res = run_and_compare(rnd(3, 70001, dtype, seed=group + in_off), dtype, in_off=in_off, out_off=out_off,
+                          path=B.PATH_GRID, group=group)
+    assert res["path"] == B.PATH_GRID
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("threads,vpt", [(256, 4), (256, 8), (512, 4), (1024, 4)])
+@pytest.mark.parametrize("group", [1, 5, 40, 700])
+def test_grid_block_shapes(dtype, threads, vpt, group):
+    # every block shape, chunks of one to many tiles, the state region over
+    # one chunk or several (700 chunks of 3-25 vectors)
+    res = run_and_compare(rnd(4, 70001, dtype, seed=threads + vpt + group), dtype, in_off=3, out_off=3,
+                          path=B.PATH_GRID, threads=threads, vpt=vpt, group=group)
+    assert res["path"] == B.PATH_GRID
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("rows,cols,in_off,out_off", [(1, 4_000_000, 0, 0), (3, 1_000_000, 0, 0),
+                                                      (9, 524288, 0, 0), (2, 3_000_001, 3, 1), (5, 777_777, 2, 2)])
+def test_grid_rows(dtype, rows, cols, in_off, out_off):
+    # a few rows of 1 MiB or more with out != in: the automatic choice
+    x = rnd(rows, cols, dtype, seed=rows * 31 + cols)
+    res = run_and_compare(x, dtype, in_off=in_off, out_off=out_off)
+    es = 4 if dtype == "f32" else 2
+    assert res["path"] == (B.PATH_GRID if cols * es >= 1 << 20 else B.PATH_STREAM)
+    # in place the same rows stream through a cluster instead
+    res = run_and_compare(x, dtype, inplace=True, in_off=in_off)
+    assert res["path"] == B.PATH_STREAM
+
+
+def test_grid_refuses_in_place_and_writes_nothing():
+    x = rnd(3, 70001, "f32", seed=5)
+    c = DeviceCase(x, "f32", inplace=True)
+    before = c.result(70001).copy()
+    assert c.run(70001, path=B.PATH_GRID) == B.ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert np.array_equal(c.result(70001).view(np.uint32), before.view(np.uint32))
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -236,7 +283,7 @@ def _result_bits(x, dtype, path):
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("path,cols", [(B.PATH_WARP, 33), (B.PATH_WARP, 1000), (B.PATH_CTA, 3000),
                                        (B.PATH_CLUSTER, 20000), (B.PATH_CLUSTER, 65536), (B.PATH_STREAM, 20000),
-                                       (B.PATH_STREAM, 65536)])
+                                       (B.PATH_STREAM, 65536), (B.PATH_GRID, 20000), (B.PATH_GRID, 65536)])
 def test_special_values(dtype, path, cols):
     skip_fp32_cluster(path, dtype)
     x = special_rows(dtype, cols)
@@ -386,6 +433,43 @@ def test_launch_overlap_orders_against_neighbours(dtype, path, cols):
             for _ in range(4):
                 assert B.softmax_fwd_ptr(z.data_ptr(), z.data_ptr(), rows, cols, cols, code, stream) == B.OK
             chains[overlap] = z
+        torch.cuda.synchronize()
+        assert B.check_device_error() == B.OK
+    finally:
+        B.set_launch_overlap(True)
+        B.set_force_path(0)
+    for i in range(k):
+        compare(outs[i].cpu().numpy().view(W.storage_dtype(dtype)), xs[i], dtype, cols)
+    assert torch.equal(chains[True], chains[False])
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_grid_launches_order_against_neighbours(dtype):
+    """The grid path's three launches, back to back with the overlap on: each
+    call's input is rewritten right before it and right after it, and a chain
+    of calls ping-pongs between two buffers (the path does not run in place),
+    matching the same chain in plain stream order bit for bit."""
+    rows, cols, k = 3, 300_007, 4
+    xs = [rnd(rows, cols, dtype, 950 + i) for i in range(k)]
+    srcs = [_bits_tensor(x, dtype) for x in xs]
+    buf = torch.empty_like(srcs[0])
+    outs = [torch.empty_like(buf) for _ in range(k)]
+    code = W.DTYPES.index(dtype)
+    stream = torch.cuda.current_stream().cuda_stream
+    B.set_force_path(B.PATH_GRID)
+    try:
+        B.set_launch_overlap(True)
+        for i in range(k):
+            buf.copy_(srcs[i])
+            assert B.softmax_fwd_ptr(buf.data_ptr(), outs[i].data_ptr(), rows, cols, cols, code, stream) == B.OK
+        chains = {}
+        for overlap in (True, False):
+            B.set_launch_overlap(overlap)
+            z = [srcs[0].clone(), torch.empty_like(srcs[0])]
+            for j in range(4):
+                a, b = z[j % 2], z[1 - j % 2]
+                assert B.softmax_fwd_ptr(a.data_ptr(), b.data_ptr(), rows, cols, cols, code, stream) == B.OK
+            chains[overlap] = z[0]
         torch.cuda.synchronize()
         assert B.check_device_error() == B.OK
     finally:
