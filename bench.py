@@ -617,14 +617,31 @@ def per_shape(args, peaks, l2, dev) -> dict:
                     raise B.SoftmaxError(st, "softmax_fwd_masked")
 
             mmed, _, _ = time_steps(launch_masked, sets, 200, 50)
+            masked_path = B.last_path()
             kept = sum(min(w.cols, (r % w.causal_period) + 1) for r in range(w.rows))
             mbytes = (kept + w.rows * w.cols) * w.elem_bytes  # kept entries read, every entry written
-            table[w.name + "_masked"] = {
-                "path": "masked " + B.PATH_NAMES.get(B.last_path(), "?"), "us_per_call": round(mmed * 1e3, 2),
+            entry = {
+                "path": "masked " + B.PATH_NAMES.get(masked_path, "?"), "us_per_call": round(mmed * 1e3, 2),
                 "algorithmic_bytes": mbytes, "gbs": round(mbytes / (mmed / 1e3) / 1e9, 1),
                 "frac_of_measured_hbm": round(mbytes / (mmed / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                 "time_vs_unmasked": round(mmed / med, 3),
             }
+            if masked_path == B.PATH_CTA:
+                # the same access pattern with no arithmetic, one block of the
+                # masked call's size per row: kept entries copied, the rest zeroed
+                pthreads = B.plan(sets[0][0].data_ptr(), sets[0][1].data_ptr(), w.rows, w.cols, w.stride,
+                                  w.dtype)["threads"]
+
+                def launch_pattern(a, b, w=w, code=code, pthreads=pthreads):
+                    st = B.masked_copy_ptr(a.data_ptr(), b.data_ptr(), w.rows, w.cols, w.stride, code, 0,
+                                           w.causal_period, pthreads, torch.cuda.current_stream().cuda_stream)
+                    if st != 0:
+                        raise B.SoftmaxError(st, "softmax_masked_copy")
+
+                pmed, _, _ = time_steps(launch_pattern, sets, 200, 50)
+                entry["pattern_copy_us"] = round(pmed * 1e3, 2)
+                entry["time_vs_pattern_copy"] = round(mmed / pmed, 3)
+            table[w.name + "_masked"] = entry
         del sets, csets, xd
         torch.cuda.empty_cache()
     return table

@@ -166,6 +166,22 @@ int softmax_fwd_masked(const void *in, void *out, int64_t rows, int64_t cols, in
                        cudaStream_t stream);
 
 /*
+ * softmax_masked_copy -- a diagnostic: the memory traffic of the matching
+ * softmax_fwd_masked call with no arithmetic.  Each row's kept columns (the
+ * same rule: c <= (r mod rows_per_seq) + causal_offset) are copied from in to
+ * out bit for bit and its other columns are set to zero bits, one block of
+ * `threads` threads per row (0 = 256; else a power of two from 32 to 1024).
+ * Timed beside softmax_fwd_masked it gives the time the masked call's access
+ * pattern takes on its own, as a same-bytes device-to-device copy does for
+ * softmax_fwd.  Rows of whole 16-byte vectors only (in and out 16-byte
+ * aligned, row_stride and cols multiples of 16 bytes; else
+ * SOFTMAX_ERR_UNSUPPORTED); other arguments and status codes as
+ * softmax_fwd_masked.  Allocates nothing.
+ */
+int softmax_masked_copy(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride, int dtype,
+                        int64_t causal_offset, int64_t rows_per_seq, int threads, cudaStream_t stream);
+
+/*
  * softmax_fwd_host -- the same softmax for a matrix in host memory, written
  * back to host memory.  (The pages have no counterpart: they time device
  * buffers only; this is the call whose end-to-end throughput includes the
@@ -396,7 +412,7 @@ int softmax_autotune_clear(void);
  * softmax_plan_t.whole_vectors, 1.4.0 the autotune calls and softmax_fwd_masked,
  * 1.5.0 the PACKED path and softmax_fwd_host; 2.0.0 removes the RING path and
  * softmax_plan_t.stages, and softmax_fwd no longer takes the SPLIT path or any
- * scratch; 2.1.0 the GRID path). */
+ * scratch; 2.1.0 the GRID path; 2.2.0 softmax_masked_copy). */
 int softmax_abi_version(void);
 
 #ifdef __cplusplus

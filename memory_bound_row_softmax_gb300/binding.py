@@ -71,6 +71,7 @@ SIGNATURES = {
     "softmax_abi_version": (_int, []),
     "softmax_fwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp]),
     "softmax_fwd_masked": (_int, [_vp, _vp, _i64, _i64, _i64, _int, ctypes.c_float, _i64, _i64, _vp]),
+    "softmax_masked_copy": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _i64, _i64, _int, _vp]),
     "softmax_attention_fwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, ctypes.c_float, _vp]),
     "softmax_attention_fwd_counter": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, ctypes.c_float,
                                              _vp, _vp]),
@@ -137,6 +138,14 @@ def softmax_fwd_masked_ptr(in_ptr: int, out_ptr: int, rows: int, cols: int, row_
     """Raw call of the scaled, causally masked softmax (status out)."""
     return lib().softmax_fwd_masked(in_ptr, out_ptr, rows, cols, row_stride, dtype, scale, causal_offset,
                                     rows_per_seq, stream)
+
+
+def masked_copy_ptr(in_ptr: int, out_ptr: int, rows: int, cols: int, row_stride: int, dtype: int,
+                    causal_offset: int, rows_per_seq: int = 0, threads: int = 0, stream: int = 0) -> int:
+    """Raw call of the diagnostic softmax_masked_copy: the masked call's
+    traffic (kept entries copied, the rest zeroed) with no arithmetic."""
+    return lib().softmax_masked_copy(in_ptr, out_ptr, rows, cols, row_stride, dtype, causal_offset, rows_per_seq,
+                                     threads, stream)
 
 
 def _prepare(x, out, what: str):

@@ -20,7 +20,7 @@ LIB = os.path.join(BUILD, "libmbrs_softmax.so")
 ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["abi.cu", "k_warp.cu", "k_warp_whole.cu", "k_cta.cu", "k_cta_whole.cu", "k_cluster.cu", "k_grid.cu",
+SOURCES = ["abi.cu", "k_warp.cu", "k_warp_whole.cu", "k_cta.cu", "k_cta_whole.cu", "k_cluster.cu", "k_grid.cu", "k_pattern_copy.cu",
            "k_noalloc.cu", "k_masked_warp.cu", "k_masked_warp_whole.cu", "k_masked.cu", "k_masked_whole.cu",
            "k_packed.cu", "k_attention.cu", "attention_abi.cu"]
 HEADERS = ["common.cuh", "kernels.cuh", "launch.h", "warp_launch.cuh", "cta_launch.cuh", "attention.cuh",

@@ -32,7 +32,7 @@ using namespace mbrs;
 
 namespace {
 
-constexpr int kAbiVersion = 20100;  // 2.1.0
+constexpr int kAbiVersion = 20200;  // 2.2.0
 constexpr int kVecBytes = 16;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDefaultWaitNs = 1000000000;  // 1 s
@@ -703,6 +703,28 @@ int softmax_fwd_masked(const void *in, void *out, int64_t rows, int64_t cols, in
     if (e != cudaSuccess) return SOFTMAX_ERR_CUDA;
     g_last_path.store(p.path);
     return SOFTMAX_OK;
+}
+
+int softmax_masked_copy(const void *in, void *out, int64_t rows, int64_t cols, int64_t row_stride, int dtype,
+                        int64_t causal_offset, int64_t rows_per_seq, int threads, cudaStream_t stream) {
+    int64_t ext = 0;
+    const uint64_t ia = (uint64_t)(uintptr_t)in, oa = (uint64_t)(uintptr_t)out;
+    int st = check_args(ia, oa, rows, cols, row_stride, dtype, &ext);
+    if (st != SOFTMAX_OK || rows == 0) return st;
+    if (rows_per_seq < 0) return SOFTMAX_ERR_ARG;
+    if (threads == 0) threads = 256;
+    if (threads < 32 || threads > 1024 || (threads & (threads - 1)) != 0) return SOFTMAX_ERR_ARG;
+    const int es = elem_bytes(dtype);
+    if (ia % kVecBytes != 0 || oa % kVecBytes != 0 || (row_stride * es) % kVecBytes != 0 ||
+        (cols * es) % kVecBytes != 0)
+        return SOFTMAX_ERR_UNSUPPORTED;  // rows of whole 16-byte vectors only
+    LaunchArgs a{in, out, rows, cols, row_stride, dtype, 1, stream, g_overlap.load(), 1};
+    const int64_t lim = (int64_t)1 << 62;
+    a.mask.off = std::max(-lim, std::min(causal_offset, cols));
+    a.mask.period = rows_per_seq;
+    const cudaError_t e = launch_masked_copy(a, threads, std::min<int64_t>(rows, kMaxGrid));
+    if (e == cudaErrorInvalidValue) return SOFTMAX_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? SOFTMAX_OK : SOFTMAX_ERR_CUDA;
 }
 
 int64_t softmax_host_workspace_bytes(int64_t rows, int64_t cols, int64_t row_stride, int dtype,

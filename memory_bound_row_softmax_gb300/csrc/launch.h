@@ -135,6 +135,10 @@ cudaError_t read_clear_error_word(cudaStream_t stream, unsigned int *word);
 // row's first 4-byte aligned byte, must fit in the row (8 chunks + 8 <= row
 // bytes)
 constexpr int kGridThreads = 512, kGridVpt = 4;
+
+// softmax_masked_copy (k_pattern_copy.cu): a.mask's kept entries of each row
+// copied, the rest zero-filled; rows of whole 16-byte vectors (a.whole).
+cudaError_t launch_masked_copy(const LaunchArgs &a, int threads, int64_t grid);
 bool grid_shape_ok(int threads, int vpt);
 cudaError_t launch_grid(const LaunchArgs &a, int threads, int vpt, int64_t chunks, int64_t chunk_vecs,
                         int64_t grid);

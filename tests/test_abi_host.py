@@ -46,7 +46,7 @@ def test_status_strings():
     for s in range(11):
         assert B.status_string(s) and B.status_string(s) != "unknown status"
     assert B.status_string(99) == "unknown status"
-    assert B.abi_version() == 20100
+    assert B.abi_version() == 20200
 
 
 @pytest.mark.parametrize("args,expect", [
@@ -261,6 +261,18 @@ def test_masked_argument_checks_need_no_gpu():
     assert B.softmax_fwd_masked_ptr(p, q, 0, 8, 8, 0, 1.0, 0, 0) == B.OK      # no rows: nothing to do
     assert B.softmax_fwd_masked_ptr(p, q, 4, 8, 7, 0, 1.0, 0, 0) == B.ERR_STRIDE
     assert B.softmax_fwd_masked_ptr(p, p + 4, 4, 8, 8, 0, 1.0, 0, 0) == B.ERR_OVERLAP
+
+
+def test_masked_copy_argument_checks_need_no_gpu():
+    p, q = 1 << 24, 1 << 40
+    assert B.masked_copy_ptr(p, q, 4, 8, 8, 0, 0, -1) == B.ERR_ARG             # rows_per_seq < 0
+    for threads in (16, 48, 2048):
+        assert B.masked_copy_ptr(p, q, 4, 8, 8, 0, 0, 0, threads) == B.ERR_ARG
+    assert B.masked_copy_ptr(p, q, 4, 6, 8, 0, 0, 0) == B.ERR_UNSUPPORTED      # 24-byte rows
+    assert B.masked_copy_ptr(p, q, 4, 8, 9, 0, 0, 0) == B.ERR_UNSUPPORTED      # 36-byte stride
+    assert B.masked_copy_ptr(p + 4, q + 4, 4, 8, 8, 0, 0, 0) == B.ERR_UNSUPPORTED
+    assert B.masked_copy_ptr(p, q, 0, 8, 8, 0, 0, 0) == B.OK                   # no rows: nothing to do
+    assert B.masked_copy_ptr(p, p + 4, 4, 8, 8, 0, 0, 0) == B.ERR_OVERLAP
 
 
 def test_host_workspace_sizes():

@@ -129,6 +129,25 @@ def test_the_fp16_causal_workload_at_full_size():
     assert np.abs(y[rows] - ref).max() <= TOL["f16"]
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("off,period,threads", [(0, 0, 64), (0, 150, 256), (-3, 100, 0), (5000, 0, 1024),
+                                                (-10000, 0, 32), (7, 64, 128)])
+def test_masked_copy_moves_the_masked_pattern(dtype, off, period, threads):
+    # the diagnostic softmax_masked_copy: kept entries bit for bit, the rest
+    # zero bits, padding and guards untouched (rows of whole 16-byte vectors)
+    rows, cols, stride = 300, 1024, 1032
+    x = W.make_random(rows, cols, dtype, seed=31 + threads, row_stride=stride, sigma=2.0)
+    case = DeviceCase(x, dtype)
+    st = B.masked_copy_ptr(case.in_ptr, case.out_ptr, rows, cols, stride, W.DTYPES.index(dtype), off, period,
+                           threads, torch.cuda.current_stream().cuda_stream)
+    assert st == B.OK, B.status_string(st)
+    y = case.result(cols)
+    xb = W.bits_view(np.ascontiguousarray(x), dtype)[:, :cols]
+    keep = np.array([kept(r, cols, off, period) for r in range(rows)])
+    live = np.arange(cols)[None, :] < keep[:, None]
+    assert (y[live] == xb[live]).all() and (y[~live] == 0).all()
+
+
 def test_rejects_bad_scale_and_period():
     d = torch.zeros(64, device="cuda")
     p = d.data_ptr()
