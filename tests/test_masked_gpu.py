@@ -126,7 +126,9 @@ def test_the_fp16_causal_workload_at_full_size():
     y = decode(case.result(w.cols), w.dtype)
     rows = list(range(0, w.rows, 97)) + [4095, 4096, w.rows - 1]
     ref = oracle.softmax(x, w.dtype, cols=w.cols, rows=rows, threads=8)
-    assert np.abs(y[rows] - ref).max() <= TOL["f16"]
+    err = float(np.abs(y[rows] - ref).max())
+    assert err <= TOL["f16"]
+    print(w.name + "_masked", {"max_abs_err": err, "rows_checked": len(rows)})
 
 
 @pytest.mark.parametrize("dtype", DTYPES)

@@ -321,13 +321,24 @@ def test_config_full_size(name):
     print(name, res)
 
 
+@pytest.mark.parametrize("name", sorted(W.EXTRA_SHAPES))
+def test_extra_shape_full_size(name):
+    # the shapes the benchmark times beside the pages' workloads (ragged
+    # 16-bit rows, a few very long rows), every element against the oracle
+    w = W.EXTRA_SHAPES[name]
+    x = W.make_input(w)
+    res = run_and_compare(x, w.dtype, w.cols)
+    print(w.name, B.PATH_NAMES[res["path"]], res)
+
+
 @pytest.mark.parametrize("cols", W.SWEEP_WIDTHS)
 def test_sweep_width_full_size(cols):
     w = W.sweep_workload(cols)
     x = W.make_input(w)
     rng = np.random.default_rng(cols)
     sample = np.unique(np.concatenate([[0, 1, 2, w.rows - 1], rng.integers(0, w.rows, 61)]))
-    run_and_compare(x, "f32", rows=sample)
+    res = run_and_compare(x, "f32", rows=sample)
+    print(w.name, res)
 
 
 def test_offsets_beyond_int32():
