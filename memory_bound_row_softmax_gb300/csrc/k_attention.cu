@@ -70,7 +70,8 @@ constexpr uint32_t kHalfBytes = kTileBytes / 2;          // its 64-column half: 
 // shared memory, from a 1024-byte aligned base
 constexpr uint32_t kOffQ = 0;                        // Q tile t at kOffQ + t kTileBytes
 constexpr uint32_t kOffRing = kTiles * kTileBytes;   // slot i at kOffRing + i kTileBytes
-constexpr uint32_t kOffBar = kOffRing + kSlots * kTileBytes;
+constexpr uint32_t kOffO = kOffRing + kSlots * kTileBytes;  // O_t staged for its TMA store at kOffO + t kTileBytes
+constexpr uint32_t kOffBar = kOffO + kTiles * kTileBytes;
 enum : int {
     kBarQ = 0,
     kBarFull = 1,                 // + slot: the load landed
@@ -81,7 +82,9 @@ enum : int {
     kBarDrain = kBarO + kTiles,
     kBarItem = kBarDrain + 1,    // the next ring entry of items is published
     kBarQEmpty = kBarItem + 1,   // the item's S products are done with Q
-    kNumBars = kBarQEmpty + 1
+    kBarStage = kBarQEmpty + 1,  // + tile: O_t's staging tile is free (its last store has read it)
+    kBarStaged = kBarStage + kTiles,  // + tile: O_t is staged (128 arrivals)
+    kNumBars = kBarStaged + kTiles
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
@@ -184,7 +187,8 @@ __device__ unsigned int g_work[kWorkSlots][2];
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, T *__restrict__ o, int n_ctx, int m_blocks,
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, int n_ctx,
+                    int m_blocks,
                     int heads_total, int group, unsigned int *work_ext, int work_slot, float kscale, int causal,
                     uint32_t wait_ns, int starve) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -205,7 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const auto tiles_b = [=](int mb) { return causal ? min(2 * mb + 2, n_all) : n_all; };
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), (i == kBarP || i == kBarP + 1) ? kBlockM : 1);
+        for (int i = 0; i < kNumBars; ++i)
+            mbar_init(bar(i), (i == kBarP || i == kBarP + 1 || i == kBarStaged || i == kBarStaged + 1) ? kBlockM : 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -213,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
+        tma_prefetch_desc(&to);
     }
     if (warp == kWarpMma) {
         tmem_alloc(base + kOffTmemSlot, kTmemCols);
@@ -409,8 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) mx[i] = s[i];
 #pragma unroll
-                for (int c = 4; c < kBlockN; ++c) mx[c & 3] = fmaxf(mx[c & 3], s[c]);
-                const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * kscale;
+                for (int c = 4; c < kBlockN; c += 8) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) mx[i] = max3(mx[i], s[c + i], s[c + 4 + i]);
+                }
+                const float m_tile = max3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * kscale;
                 float alpha = 1.f;
                 bool moved = false;
                 if (m_tile > m_run + kShiftSlack) {
@@ -422,20 +431,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // p = 2^(s kscale - m_run), rounded to T in pairs and written
                 // over S_t's first 64 columns, in quarters of 32 keys (this
                 // thread's S values are all in registers already)
-                float sum[4] = {0.f, 0.f, 0.f, 0.f};
+                // (the exponent arguments and the sums in packed fp32 pairs)
+                const uint64_t k2 = f2(kscale, kscale), nm2 = f2(-m_run, -m_run);
+                uint64_t sum2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const float p0 = ex2(fmaf(s[32 * h + 2 * c], kscale, -m_run));
-                        const float p1 = ex2(fmaf(s[32 * h + 2 * c + 1], kscale, -m_run));
-                        sum[c & 3] += p0 + p1;
+                        const float2 a = f2_split(fma_f2(f2(s[32 * h + 2 * c], s[32 * h + 2 * c + 1]), k2, nm2));
+                        const float p0 = ex2(a.x), p1 = ex2(a.y);
+                        sum2[c & 1] = add_f2(sum2[c & 1], f2(p0, p1));
                         pk[c] = pack2<T>(p0, p1);
                     }
                     tmem_st16(lane_addr + col_s(t) + 16 * h, pk);
                 }
-                l_run += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+                const float2 sa = f2_split(sum2[0]), sb = f2_split(sum2[1]);
+                l_run += (sa.x + sa.y) + (sb.x + sb.y);
                 if (__any_sync(0xffffffffu, moved)) {
                     // O_t += P_t V_{j-1} has completed (S_t of this tile was
                     // issued after it).  The whole warp takes part (TMEM
@@ -459,29 +471,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, wait_phase(bar(kBarO + t), k & 1, abort_flag, wait_ns));
             if (!ok) break;
             tc_fence_after();
+            // The epilogue: O_t / l into the staging tile (the TMA box layout:
+            // two 64-column halves of 128-byte rows, 16-byte chunks swizzled by
+            // the row), then one TMA store per half by thread 0 of the group.
+            // Thread 0 first lets the group know the previous item's store has
+            // read the tile; the group's writes reach the async proxy (fence)
+            // before it issues the store.  Rows past n_ctx are not stored.
             const float inv = 1.f / l_run;
-            T *orow = o + ((int64_t)it.bh * n_ctx + q) * kHeadDim;
+            const uint32_t stage = base + kOffO + (uint32_t)t * kTileBytes;
+            if (r == 0) {
+                bulk_wait_read_all();
+                mbar_arrive(bar(kBarStage + t));
+            }
+            ok = __all_sync(0xffffffffu, wait_phase(bar(kBarStage + t), k & 1, abort_flag, wait_ns));
+            if (!ok) break;
 #pragma unroll
-            for (int c = 0; c < kHeadDim / 32; ++c) {
+            for (int c = 0; c < kHeadDim / 32; ++c) {  // 32 columns of O at a time
                 float ov[32];
                 tmem_ld32(lane_addr + col_o(t) + c * 32, ov);
                 tmem_wait_ld();
-                if (q < n_ctx) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 w;
-                        w.x = pack2<T>(ov[8 * v + 0] * inv, ov[8 * v + 1] * inv);
-                        w.y = pack2<T>(ov[8 * v + 2] * inv, ov[8 * v + 3] * inv);
-                        w.z = pack2<T>(ov[8 * v + 4] * inv, ov[8 * v + 5] * inv);
-                        w.w = pack2<T>(ov[8 * v + 6] * inv, ov[8 * v + 7] * inv);
-                        *reinterpret_cast<uint4 *>(orow + c * 32 + v * 8) = w;
-                    }
+                for (int v = 0; v < 4; ++v) {  // 16-byte chunk 4c + v of the row
+                    uint4 w;
+                    w.x = pack2<T>(ov[8 * v + 0] * inv, ov[8 * v + 1] * inv);
+                    w.y = pack2<T>(ov[8 * v + 2] * inv, ov[8 * v + 3] * inv);
+                    w.z = pack2<T>(ov[8 * v + 4] * inv, ov[8 * v + 5] * inv);
+                    w.w = pack2<T>(ov[8 * v + 6] * inv, ov[8 * v + 7] * inv);
+                    const uint32_t chunk = (uint32_t)(4 * c + v);
+                    const uint32_t row = stage + (chunk >> 3) * kHalfBytes + (uint32_t)r * 128u;
+                    st_shared_v4(row + (((chunk & 7u) ^ (uint32_t)(r & 7)) << 4), w);
                 }
             }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kBarStaged + t));
+            bool staged = true;
+            if (r == 0) {
+                staged = wait_phase(bar(kBarStaged + t), k & 1, abort_flag, wait_ns);
+                if (staged) {
+                    const int32_t y = it.mb * kRowsPerBlock + t * kBlockM;
+                    tma_store_3d(&to, stage, 0, y, it.bh);
+                    tma_store_3d(&to, stage + kHalfBytes, 64, y, it.bh);
+                    bulk_commit();
+                }
+            }
+            ok = __all_sync(0xffffffffu, staged);
+            if (!ok) break;
             // this group's reads of O_t are done before it writes the next
             // item's first P_t (tcgen05.wait::ld above, fence before the
             // arrival that the next item's first PV product waits for)
         }
+        if (r == 0) bulk_wait_all();  // the stores are complete before the block exits
     }
 
     tc_fence_before();
@@ -547,9 +586,9 @@ cudaError_t go(const AttnArgs &a, int64_t wait_ns, int starve) {
         opted.fetch_or(bit, std::memory_order_acq_rel);
     }
     const int64_t bh = a.batch * a.heads;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, a.q, a.dtype, a.n_ctx, bh) || !make_map(&mk, a.k, a.dtype, a.n_ctx, bh) ||
-        !make_map(&mv, a.v, a.dtype, a.n_ctx, bh))
+        !make_map(&mv, a.v, a.dtype, a.n_ctx, bh) || !make_map(&mo, a.o, a.dtype, a.n_ctx, bh))
         return cudaErrorInvalidValue;
     const int64_t m_blocks = (a.n_ctx + kRowsPerBlock - 1) / kRowsPerBlock;
     const int group = attention_head_group(bh, a.n_ctx);
@@ -562,7 +601,7 @@ cudaError_t go(const AttnArgs &a, int64_t wait_ns, int starve) {
         a.counter ? 0 : (int)(launches.fetch_add(1, std::memory_order_relaxed) % kWorkSlots);
     const int64_t grid = std::min<int64_t>(std::max(a.sms, 1), bh * m_blocks);
     k_attention_fwd<T><<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(
-        mq, mk, mv, static_cast<T *>(a.o), (int)a.n_ctx, (int)m_blocks, (int)bh, group, a.counter, slot, kscale,
+        mq, mk, mv, mo, (int)a.n_ctx, (int)m_blocks, (int)bh, group, a.counter, slot, kscale,
         a.causal, limit, starve ? 1 : 0);
     return cudaGetLastError();
 }
