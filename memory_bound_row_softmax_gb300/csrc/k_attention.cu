@@ -77,7 +77,7 @@ enum : int {
     kBarFull = 1,                 // + slot: the load landed
     kBarEmpty = 1 + kSlots,       // + slot: its last MMA completed
     kBarS = 1 + 2 * kSlots,       // + tile: S_t is in TMEM
-    kBarP = kBarS + kTiles,       // + tile: P_t is in TMEM (128 arrivals)
+    kBarP = kBarS + kTiles,       // + tile: P_t is in TMEM (one arrival per warp of the group)
     kBarO = kBarP + kTiles,       // + tile: O_t is final
     kBarDrain = kBarO + kTiles,
     kBarItem = kBarDrain + 1,    // the next ring entry of items is published
@@ -210,7 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i)
-            mbar_init(bar(i), (i == kBarP || i == kBarP + 1 || i == kBarStaged || i == kBarStaged + 1) ? kBlockM : 1);
+            mbar_init(bar(i), (i == kBarP || i == kBarP + 1) ? kBlockM / 32
+                              : (i == kBarStaged || i == kBarStaged + 1) ? kBlockM : 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -463,9 +464,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st32(lane_addr + col_o(t) + c * 32, ov);
                     }
                 }
+                // one arrival per warp, once all its lanes' P (and O) stores
+                // have completed
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(kBarP + t));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarP + t));
             }
             if (!ok) break;
             ok = __all_sync(0xffffffffu, wait_phase(bar(kBarO + t), k & 1, abort_flag, wait_ns));
