@@ -318,10 +318,11 @@ int softmax_set_launch_overlap(int enable);
  * answers a deployment constraint, not a step of the method.)
  *
  * The split path cuts every row into chunks spread over all SMs, which suits
- * a few very long rows (one fp32 row of 4 M elements: about 3x faster than
- * softmax_fwd's streaming cluster, which can give a row at most 16 SMs).  Its
- * two passes meet in a global array of per-chunk (s, l) states: scratch
- * memory.  Some callers cannot obtain scratch: code running under an
+ * a few very long rows.  Its two passes meet in a global array of per-chunk
+ * (s, l) states: scratch memory.  (softmax_fwd spreads such rows the same way
+ * without scratch when out != in, keeping the states in the output rows: path
+ * 8; in place it can give a row at most 16 SMs, path 6 -- one fp32 row of
+ * 4 M elements: 11.1 us here against 34.8 us.)  Some callers cannot obtain scratch: code running under an
  * allocator that a host framework owns exclusively, real-time loops where an
  * allocation's latency or failure is not acceptable, or processes that must
  * not grow their device footprint after start-up.  This entry point keeps the
@@ -334,11 +335,10 @@ int softmax_set_launch_overlap(int enable);
  *     be at most SOFTMAX_NOALLOC_MAX_STATES; larger calls return
  *     SOFTMAX_ERR_SCRATCH_LIMIT before any launch (each row needs at least one
  *     state; chunks per row are reduced to fit).
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.  The cached address belongs
- *     to the device's primary context: after cudaDeviceReset on that device,
- *     do not call this entry point there again in the same process.
+ *   - Every call looks up the array's device address in the current
+ *     device's context (cudaGetSymbolAddress); the first lookup may load the
+ *     library's device code, so make the first call on a device before any
+ *     stream capture.
  *   - Every call on a device shares the array and leaves its states there.
  *     Nothing in it needs to start at zero: the second pass reads only states
  *     the first pass of the same call wrote.  Calls whose kernels overlap on

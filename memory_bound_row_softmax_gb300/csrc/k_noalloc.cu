@@ -1,15 +1,14 @@
 // k_noalloc.cu -- the split (two-pass) path with its per-chunk states in a
 // fixed device array instead of memory allocated per call.
 //
-// Why it exists: softmax_fwd takes the split path's scratch from a stream-
-// ordered memory pool.  Some callers cannot allocate device memory at all:
-// code running under an allocator that a host framework owns exclusively,
-// real-time loops where an allocation's latency or failure is not acceptable,
-// or code that must not grow the process's device footprint after start-up.
-// softmax_fwd_noalloc serves them: the scratch is the array below, which every
-// GPU that loads this library holds from load until process exit.
-#include <mutex>
-
+// Why it exists: the split spreads a few very long rows over the whole GPU,
+// and its two passes meet in per-chunk states.  softmax_fwd keeps such states
+// in the output rows (path 8), which it cannot do in place; callers that call
+// in place and cannot allocate device memory at all (code under an allocator
+// a host framework owns exclusively, real-time loops, processes that must not
+// grow their device footprint) get softmax_fwd_noalloc: its scratch is the
+// array below, which every GPU that loads this library holds from load until
+// process exit.
 #include "kernels.cuh"
 #include "launch.h"
 
@@ -20,23 +19,16 @@ namespace mbrs {
 static __device__ __align__(256) float2 g_noalloc_states[kNoAllocMaxStates];
 
 namespace {
-constexpr int kMaxDevices = 64;
 
-// Device address of g_noalloc_states on `device` (which must be current).  In
+// Device address of g_noalloc_states in the current device's context.  In
 // host code the array's name is only a host-side stand-in, so the address
-// comes from cudaGetSymbolAddress, once per device, and is cached.
-cudaError_t states_address(int device, float2 **ptr) {
-    static std::mutex mu;
-    static float2 *addr[kMaxDevices] = {};
-    if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[device]) {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_states);
-        if (e != cudaSuccess) return e;
-        addr[device] = static_cast<float2 *>(p);
-    }
-    *ptr = addr[device];
+// comes from cudaGetSymbolAddress, looked up on every call (so that a context
+// re-created after cudaDeviceReset is never handed a stale address).
+cudaError_t states_address(float2 **ptr) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_states);
+    if (e != cudaSuccess) return e;
+    *ptr = static_cast<float2 *>(p);
     return cudaSuccess;
 }
 
@@ -54,10 +46,8 @@ cudaError_t go(const LaunchArgs &a, int64_t chunks, int64_t chunk_vecs, int64_t 
 
 cudaError_t launch_split_noalloc(const LaunchArgs &a, int64_t chunks, int64_t chunk_vecs, int64_t grid) {
     if (chunks < 1 || a.rows > kNoAllocMaxStates / chunks) return cudaErrorInvalidValue;
-    int device = 0;
-    cudaError_t e = cudaGetDevice(&device);
     float2 *states = nullptr;
-    if (e == cudaSuccess) e = states_address(device, &states);
+    const cudaError_t e = states_address(&states);
     if (e != cudaSuccess) return e;
     switch (a.dtype) {
         case 0: return go<float>(a, chunks, chunk_vecs, grid, states);
