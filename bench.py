@@ -641,6 +641,13 @@ def per_shape(args, peaks, l2, dev) -> dict:
                 pmed, _, _ = time_steps(launch_pattern, sets, 200, 50)
                 entry["pattern_copy_us"] = round(pmed * 1e3, 2)
                 entry["time_vs_pattern_copy"] = round(mmed / pmed, 3)
+
+                # the writes alone: the whole output zero-filled (torch's fill)
+                def launch_zero(a, b):
+                    b.zero_()
+
+                zmed, _, _ = time_steps(launch_zero, sets, 200, 50)
+                entry["zero_fill_out_us"] = round(zmed * 1e3, 2)
             table[w.name + "_masked"] = entry
         del sets, csets, xd
         torch.cuda.empty_cache()
