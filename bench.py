@@ -512,6 +512,7 @@ def cpu_baseline(x, w, seconds: float = 4.0) -> dict:
     oracle.softmax(x[:n1], w.dtype, cols=w.cols, threads=1)
     el1 = time.perf_counter() - t0
     one = {"value": round(2 * n1 * w.cols * w.elem_bytes / el1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+           "elements_per_s": round(n1 * w.cols / el1), "wall_ms": round(el1 * 1e3, 1),
            "sample": f"rows 0..{n1 - 1} of {w.name} ({n1} of {w.rows} rows, {el1:.1f} s)"}
     t0 = time.perf_counter()
     reps = 0
@@ -522,7 +523,8 @@ def cpu_baseline(x, w, seconds: float = 4.0) -> dict:
         if el >= seconds:
             break
     return {"value": round(w.algorithmic_bytes * reps / el / 1e9, 3), "unit": "GB/s", "cores": cores,
-            "kind": "oracle",
+            "kind": "oracle", "elements_per_s": round(reps * w.rows * w.cols / el),
+            "wall_ms_per_pass": round(el / reps * 1e3, 1),
             "sample": f"{reps} full pass(es) over all {w.rows} rows of {w.name} ({el:.1f} s wall, "
                       f"double-precision C, rows split over {cores} threads = os.cpu_count() of this "
                       f"process, which may be a container's share of the host)",

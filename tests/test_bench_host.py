@@ -25,3 +25,15 @@ def test_attention_cpu_baseline_counts_the_kept_pairs():
     assert r["kind"] == "oracle" and r["unit"] == "TFLOP/s" and r["value"] > 0
     # queries 280..299 keep 281..300 keys each
     assert f"({sum(range(281, 301))} query-key pairs" in r["sample"]
+
+
+def test_cpu_baseline_reports_both_legs():
+    # the oracle on one thread over a bounded sample, then row-partitioned over
+    # every core this process sees: GB/s, elements/s and wall time for each
+    w = W.CONFIGS["c1"]
+    x = W.make_input(w)
+    r = bench.cpu_baseline(x, w, seconds=0.05)
+    assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["value"] > 0 and r["cores"] >= 1
+    assert r["elements_per_s"] > 0 and r["wall_ms_per_pass"] > 0
+    one = r["single_thread"]
+    assert one["cores"] == 1 and one["value"] > 0 and one["elements_per_s"] > 0 and one["wall_ms"] > 0
