@@ -452,10 +452,11 @@ int plan_noalloc(uint64_t in, int64_t rows, int64_t cols, int64_t row_stride, in
 // ---------------------------------------------------------------------------
 struct TuneKey {
     int device = 0, dtype = 0, in_phase = 0, out_phase = 0, rows_log2 = 0;
+    bool in_place = false;  // tuning runs out of place; in-place calls never match
     int64_t cols = 0, row_stride = 0;
     bool operator==(const TuneKey &o) const {
         return device == o.device && dtype == o.dtype && in_phase == o.in_phase && out_phase == o.out_phase &&
-               rows_log2 == o.rows_log2 && cols == o.cols && row_stride == o.row_stride;
+               rows_log2 == o.rows_log2 && in_place == o.in_place && cols == o.cols && row_stride == o.row_stride;
     }
 };
 
@@ -475,6 +476,7 @@ TuneKey tune_key(int device, uint64_t in, uint64_t out, int64_t rows, int64_t co
     k.in_phase = (int)(in % kVecBytes);
     k.out_phase = (int)(out % kVecBytes);
     k.rows_log2 = floor_log2(rows);
+    k.in_place = in == out;
     k.cols = cols;
     k.row_stride = row_stride;
     return k;
@@ -507,6 +509,21 @@ Shape call_shape(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t 
     for (const auto &e : g_tuned)
         if (e.first == k) return e.second;
     return f;
+}
+
+// The plan of a call: a forced shape, else the tuned one for its key, else
+// the automatic choice.  A tuned shape this call cannot take (rows of another
+// count in the same power-of-two bucket) gives way to the automatic choice.
+int plan_call(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row_stride, int dtype, int sms,
+              Plan *p, Shape *used) {
+    Shape want = call_shape(in, out, rows, cols, row_stride, dtype);
+    int st = make_plan(in, out, rows, cols, row_stride, dtype, sms, want, p);
+    if (st == SOFTMAX_ERR_UNSUPPORTED && want.path != SOFTMAX_PATH_AUTO && forced_shape().path == SOFTMAX_PATH_AUTO) {
+        want = Shape{};
+        st = make_plan(in, out, rows, cols, row_stride, dtype, sms, want, p);
+    }
+    if (used) *used = want;
+    return st;
 }
 
 // Candidate shapes for rows of up to nv vectors: the automatic choice first,
@@ -649,12 +666,11 @@ int softmax_fwd(const void *in, void *out, int64_t rows, int64_t cols, int64_t r
     st = device_sms(&sms);
     if (st != SOFTMAX_OK) return st;
     Plan p;
-    const Shape want = call_shape(ia, oa, rows, cols, row_stride, dtype);
-    st = make_plan(ia, oa, rows, cols, row_stride, dtype, sms, want, &p);
+    st = plan_call(ia, oa, rows, cols, row_stride, dtype, sms, &p, nullptr);
     if (st != SOFTMAX_OK) return st;
     LaunchArgs a{in, out, rows, cols, row_stride, dtype, p.vec_store, stream, g_overlap.load(), p.whole};
     st = run(p, a);
-    if (st == SOFTMAX_ERR_UNSUPPORTED && p.path == SOFTMAX_PATH_GRID && want.path != SOFTMAX_PATH_GRID) {
+    if (st == SOFTMAX_ERR_UNSUPPORTED && p.path == SOFTMAX_PATH_GRID && forced_shape().path != SOFTMAX_PATH_GRID) {
         // the grid path's counter cannot live in this `out` (host memory
         // without native atomics): the streaming cluster instead
         st = make_plan(ia, oa, rows, cols, row_stride, dtype, sms, Shape{SOFTMAX_PATH_STREAM, 0, 0, 0}, &p);
@@ -801,7 +817,7 @@ int softmax_fwd_host(const void *in_host, void *out_host, int64_t rows, int64_t 
         }
         const uint64_t sa = (uint64_t)(uintptr_t)slot;
         Plan p;
-        st = make_plan(sa, sa, n, cols, cols, dtype, sms, call_shape(sa, sa, n, cols, cols, dtype), &p);
+        st = plan_call(sa, sa, n, cols, cols, dtype, sms, &p, nullptr);
         if (st != SOFTMAX_OK) break;
         LaunchArgs a{slot, slot, n, cols, cols, dtype, p.vec_store, hp.s[j], g_overlap.load(), p.whole};
         st = run(p, a);  // in place in the slot
@@ -887,8 +903,7 @@ int softmax_plan(uint64_t in_addr, uint64_t out_addr, int64_t rows, int64_t cols
         if (st != SOFTMAX_OK) return st;
     }
     Plan p;
-    st = make_plan(in_addr, out_addr, rows, cols, row_stride, dtype, sms,
-                   call_shape(in_addr, out_addr, rows, cols, row_stride, dtype), &p);
+    st = plan_call(in_addr, out_addr, rows, cols, row_stride, dtype, sms, &p, nullptr);
     if (st != SOFTMAX_OK) return st;
     fill_public_plan(p, plan);
     return SOFTMAX_OK;

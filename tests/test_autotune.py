@@ -128,3 +128,24 @@ def test_autotune_refuses_in_place(cuda_lib):
     d = torch.zeros(64 * 1000, device="cuda")
     st = B.lib().softmax_autotune(d.data_ptr(), d.data_ptr(), 64, 1000, 1000, 0, 0, 5, None)
     assert st == B.ERR_ARG and B.autotune_size() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("rows", [2, 3])
+def test_a_tuned_shape_never_breaks_other_calls_of_its_key(cuda_lib, rows):
+    # tuning runs out of place; a few very long rows may keep the grid path,
+    # which cannot run in place: in-place calls with the same sizes and
+    # phases keep the automatic choice, and a tuned shape that another row
+    # count of the same power-of-two bucket cannot take gives way to it
+    cols, dt = 400_003, "f32"
+    x = W.make_random(rows, cols, dt, seed=rows, sigma=2.0)
+    case = DeviceCase(x, dt)
+    stream = torch.cuda.current_stream().cuda_stream
+    r = B.autotune_ptr(case.in_ptr, case.out_ptr, rows, cols, cols, 0, stream, iters=5)
+    assert B.autotune_size() == 1 and r["best_us"] <= r["auto_us"]
+    res = run_and_compare(x, dt, inplace=True)
+    assert res["path"] == B.PATH_STREAM
+    res = run_and_compare(x, dt)
+    assert res["path"] == r["plan"]["path"]
+    # the planner agrees (host side, same key, in place)
+    assert B.plan(case.in_ptr, case.in_ptr, rows, cols, cols, dt)["path"] == B.PATH_STREAM
