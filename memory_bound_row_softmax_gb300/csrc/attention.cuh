@@ -41,23 +41,35 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // 32 consecutive columns of this thread's lane (shape 32x32b: thread i of the
-// warp reads lane base + i) into v[0..31].  Completes at tmem_wait_ld().
+// warp reads lane base + i) into v[0..31], the load's destination registers
+// themselves.  Completes at tmem_wait_ld(); tmem_fence_regs<32>(v) after the
+// wait keeps every use of v after it.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
-    uint32_t r[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
         "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-          "=r"(r[30]), "=r"(r[31])
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]),
+          "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]), "=f"(v[14]), "=f"(v[15]),
+          "=f"(v[16]), "=f"(v[17]), "=f"(v[18]), "=f"(v[19]), "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]),
+          "=f"(v[24]), "=f"(v[25]), "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31])
         : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// After tmem_wait_ld(): v[0..N) -- registers a tcgen05.ld filled -- pass
+// through empty volatile statements that the compiler must treat as writing
+// them.  A load's outputs look ready to the compiler at the load itself, so
+// without this it may place arithmetic on them (or copies of them) before the
+// wait, reading registers the load has not filled yet.
+template <int N>
+__device__ __forceinline__ void tmem_fence_regs(float *v) {
+    static_assert(N % 8 == 0, "whole groups of eight registers");
+#pragma unroll
+    for (int i = 0; i < N; i += 8) {
+        float *w = v + i;
+        asm volatile("" : "+f"(w[0]), "+f"(w[1]), "+f"(w[2]), "+f"(w[3]), "+f"(w[4]), "+f"(w[5]), "+f"(w[6]), "+f"(w[7]));
+    }
+}
 
 // v[0..31] into 32 consecutive columns of this thread's lane.  Completes at
 // tmem_wait_st().

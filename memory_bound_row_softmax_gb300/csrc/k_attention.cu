@@ -406,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kBlockN / 32; ++c)
                     tmem_ld32(lane_addr + col_s(t) + c * 32, s + c * 32);
                 tmem_wait_ld();
+                tmem_fence_regs<kBlockN>(s);
                 const int lim = q_lim - j * kBlockN;  // kept columns of this tile: [0, lim)
                 if (lim < kBlockN) {
 #pragma unroll
@@ -459,6 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float ov[32];
                         tmem_ld32(lane_addr + col_o(t) + c * 32, ov);
                         tmem_wait_ld();
+                        tmem_fence_regs<32>(ov);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) ov[i] *= alpha;
                         tmem_st32(lane_addr + col_o(t) + c * 32, ov);
@@ -494,6 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float ov[32];
                 tmem_ld32(lane_addr + col_o(t) + c * 32, ov);
                 tmem_wait_ld();
+                tmem_fence_regs<32>(ov);
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {  // 16-byte chunk 4c + v of the row
                     uint4 w;
