@@ -15,7 +15,8 @@
 //                                           states in the output rows
 //   longer rows                             path 6, a cluster per row streaming
 //                                           its slices twice
-// Every path keeps its partial states on chip: no call allocates memory.
+// Every path keeps its partial states on chip -- path 8 in the output rows it
+// is about to overwrite: no call allocates memory.
 #include <algorithm>
 #include <cmath>
 #include <atomic>
@@ -192,8 +193,8 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
         } else if (rows * 16 < sms && in != out && cols * es >= kGridMinRowBytes) {
             // a few rows of 1 MiB or more: no cluster can spread them over
             // more than 16 SMs each, so their chunks go over the whole grid,
-            // their states meeting in the output rows (fp32 1 x 4e6: 34.6 us
-            // on the streaming cluster, 13.2 in three launches)
+            // their states meeting in the output rows (fp32 1 x 4e6: 34.8 us
+            // on the streaming cluster, 10.9 here)
             path = SOFTMAX_PATH_GRID;
         } else {
             // longer rows: a cluster streaming its slices twice, about one
@@ -201,10 +202,9 @@ int make_plan(uint64_t in, uint64_t out, int64_t rows, int64_t cols, int64_t row
             // a TMA-staged cluster it won at every long width tried
             // (1525 x 32768 fp32: 58.8 us, ring 62.5, TMA cluster 64.2;
             // 381 x 131072: 60.4, ring 74.0; 300 x 40000: 18.7, ring 25.0).
-            // Also for a few very long rows (rows * 16 < SMs), which no
-            // cluster can spread over the whole GPU: a grid-wide split would
-            // need its states in global scratch (bf16 9 x 262144: 4.7 us
-            // here, 6.1 split; fp32 3 x 10^6: 12.3 against 10.1)
+            // Also for a few long rows (rows * 16 < SMs) in place or under
+            // 1 MiB, which path 8 does not take (bf16 9 x 262144: 4.7 us
+            // here, 7.2 on path 8)
             path = SOFTMAX_PATH_STREAM;
         }
     }

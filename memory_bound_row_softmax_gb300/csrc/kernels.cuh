@@ -15,6 +15,14 @@
 //                           distributed shared memory between the passes).
 //   path 7  k_packed_rows   narrow dense rows staged through shared memory,
 //                           one thread per row.
+//   path 8  k_grid_stats / k_grid_apply
+//                           a few very long rows cut into chunks over the
+//                           whole grid (out != in): the chunk states go into
+//                           the start of the output row, and the second
+//                           launch folds them, counts its blocks on an atomic
+//                           counter there and writes (two passes and an
+//                           atomic: page "Kernel Fusion", section "What
+//                           fusion cannot fix").
 //   k_split_stats / k_split_apply
 //                           rows cut into chunks spread over the whole grid;
 //                           pass 1 streams each chunk into a (max, sum) state
