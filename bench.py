@@ -740,7 +740,7 @@ def attention_block(peaks, dev, keys=("a4k", "a16k")) -> dict:
     out = {"call": "softmax_attention_fwd", "workloads": {}}
     for key in keys:
         w = W.ATTENTION_CONFIGS[key]
-        ms, nbytes = attention_time(w, dev, steps=20 if w.n_ctx <= 4096 else 5, warmup=3)
+        ms, nbytes = attention_time(w, dev, steps=20 if w.n_ctx <= 4096 else 10, warmup=3)
         tf = w.flops() / (ms / 1e3) / 1e12
         out["workloads"][w.name] = {
             "batch": w.batch, "heads": w.heads, "n_ctx": w.n_ctx, "head_dim": w.head_dim, "dtype": w.dtype,
