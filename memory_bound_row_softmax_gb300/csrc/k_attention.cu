@@ -23,9 +23,13 @@
 //   warps 0-3 / 4-7   -- softmax of tile A / B: thread r of the group owns
 //                        query row r of its tile, which is TMEM lane r, so the
 //                        row max and row sum are thread-local (no shuffles, no
-//                        shared-memory reduction).  At the end the same threads
-//                        read O from TMEM, divide by the normaliser and store
-//                        their row.
+//                        shared-memory reduction); the exponent arguments and
+//                        the sums run as packed fp32 pairs.  Each warp makes
+//                        one arrival on its group's P barrier per tile.  At
+//                        the end of an item the same threads read O from TMEM,
+//                        divide by the normaliser and write their rows into a
+//                        shared-memory staging tile, which thread 0 of the
+//                        group stores with TMA.
 // The two softmax groups take turns with the tensor core: while group A turns
 // S_A into P_A, the tensor core computes P_B V and the next S_B, and the
 // other way round.  Per key tile the MMA thread issues, in this order,
